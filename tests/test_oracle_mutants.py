@@ -1,0 +1,110 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each case copies oracle.c, plants one plausible mistake (a wrong index, a
+dropped term, a wrong sign, a transposed operand, a wrong rounding or
+threshold rule), builds it with the oracle's own flags, and runs the pin
+battery of test_oracle_pins.py against that build in a child process (a
+planted mistake may also crash).  The unmodified source must pass the same
+battery, so the harness itself is checked too.  Everything runs on the CPU.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+MUTANTS = {
+    "getblock_index": ("return ufr[(W + p - 1 - s) % W];", "return ufr[(W + p - s) % W];"),
+    "drop_own_input_last_step": ("float v = ring_func(op, this_buffer[k], x);",
+                                 "float v = this_buffer[k];"),
+    "sum_sign": ("return acc + x; /* sum and avg */", "return acc - x; /* sum and avg */"),
+    "max_operand": ("if (acc > x) return acc;", "if (acc > x) return x;"),
+    "max_signed_zero": ("(signbit(acc) && signbit(x))", "(signbit(acc) || signbit(x))"),
+    "segment_offset": ("*off = (int64_t)j * q + (j < r ? j : r);", "*off = (int64_t)j * q;"),
+    "bf16_round_half_up": ("u += 0x7FFFu + lsb;", "u += 0x8000u;"),
+    "bf16_widen_shift": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;"),
+    "avg_scale_dropped": ("if (op == ORACLE_AVG) v = v * scale;", ";"),
+    "fusion_threshold_strict": ("size + counts[t] * es <= threshold_bytes",
+                                "size + counts[t] * es < threshold_bytes"),
+    "allgather_block": ("int b = ufr[(p - s + W) % W];", "int b = ufr[(p + s) % W];"),
+    "ring_position_vs_user_rank": ("float x = load_elem(in[me], boff + k, dtype);",
+                                   "float x = load_elem(in[p], boff + k, dtype);"),
+    "buffer_to_self": ("float* next_buffer = nxt + (int64_t)((p + 1) % W) * maxlen;",
+                       "float* next_buffer = nxt + (int64_t)p * maxlen;"),
+    "pack_offset": ("memcpy((char*)fused[u] + offset * es, tensors[(int64_t)u * T + t],",
+                    "memcpy((char*)fused[u], tensors[(int64_t)u * T + t],"),
+    "last_step_early": ("} else if (s < W - 1) {", "} else if (s < W - 2) {"),
+}
+
+BATTERY = r"""
+import sys, traceback
+sys.path.insert(0, {root!r}); sys.path.insert(0, {here!r})
+import oracle
+import test_oracle_pins as P
+pins = [
+    (P.test_ring_schedule_matches_nccl_page_table, ()),
+    (P.test_ring_schedule_structure, (5,)),
+    (P.test_segments_golden, ()),
+    (P.test_ring_order_hand_derived, ()),
+    (P.test_brute_force_tiny, (3, 5)),
+    (P.test_brute_force_tiny, (4, 16)),
+    (P.test_integer_valued_sums_exact, (7,)),
+    (P.test_avg_power_of_two_exact, (3,)),
+    (P.test_max_matches_numpy, (4,)),
+    (P.test_max_signed_zero_and_nan, ()),
+    (P.test_bf16_rne_golden, ()),
+    (P.test_bf16_allreduce_accumulates_in_fp32, ()),
+    (P.test_allgather_of_reduce_scatter_is_allreduce, (3, 10, oracle.F32, "sum")),
+    (P.test_allgather_is_concatenation, (5,)),
+    (P.test_fuse_plan_golden, ()),
+    (P.test_pack_is_concatenation_and_unpack_inverts, ()),
+    (P.test_fusion_allreduce_integer_mean_exact, ()),
+]
+failed = []
+with oracle.using({so!r}):
+    for fn, args in pins:
+        try:
+            fn(*args)
+        except Exception:
+            failed.append(fn.__name__)
+print("FAILED_PINS", failed)
+sys.exit(0 if failed else 3)
+"""
+
+
+def _build(src_text, tmp_path):
+    src = tmp_path / "oracle.c"
+    so = tmp_path / "liboracle_variant.so"
+    src.write_text(src_text)
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", str(so), str(src), "-lm"], check=True)
+    return str(so)
+
+
+def _battery(so):
+    code = BATTERY.format(root=ROOT, here=HERE, so=so)
+    return subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                          timeout=600)
+
+
+def _source():
+    with open(os.path.join(ROOT, "oracle", "oracle.c")) as f:
+        return f.read()
+
+
+def test_unmodified_oracle_passes_battery(tmp_path):
+    r = _battery(_build(_source(), tmp_path))
+    assert r.returncode == 3, r.stdout + r.stderr
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    orig, repl = MUTANTS[name]
+    text = _source()
+    assert text.count(orig) == 1, f"mutation site for {name} not unique/present"
+    r = _battery(_build(text.replace(orig, repl), tmp_path))
+    assert r.returncode != 3, f"planted mistake {name} survived every pin:\n{r.stdout}"

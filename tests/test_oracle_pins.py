@@ -1,0 +1,380 @@
+"""Pins for the CPU oracle: what the pages and the mathematics fix, checked
+against the oracle without any GPU.  Each test names what it pins.
+
+Pins used (none retypes the oracle's own formulas):
+  * the 4-GPU schedule table printed on the NCCL reduce_scatter.cu page;
+  * hand-derived order-sensitive sums (tests/golden/ring_order_cancellation.txt);
+  * exact integer sums (integer-valued floats add exactly in any order);
+  * exact rational sums within the textbook reordering bound gamma_{W-1};
+  * numpy.maximum.reduce for max on NaN-free data, hand cases for +-0 and NaN;
+  * torch's CPU bf16 conversion and hand-derived ties for the bf16 cast;
+  * the identities of the "Distributed primitives" notes (AllReduce =
+    ReduceScatter + AllGather, every node holds the same aggregate);
+  * NCCL's single-GPU copy and empty-message cases;
+  * Horovod's fusion batching rule on hand-derived lists, numpy.concatenate
+    for the packed layout.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(20261202 + seed)
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+# ---------------------------------------------------------------- schedule
+
+def test_ring_schedule_matches_nccl_page_table():
+    rows = _golden_lines("nccl_ring_schedule_4gpu.txt")
+    table = np.array([[int(v) for v in r.split()[1:]] for r in rows])
+    got = oracle.ring_schedule(4, [1, 2, 0, 3])
+    assert np.array_equal(got, table)
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 5, 8, 16])
+def test_ring_schedule_structure(W):
+    # The page's description of the table: the last row is userFromRing, each
+    # earlier row is the next one shifted left by one, and each GPU's column
+    # visits every block exactly once.
+    perm = list(_rng(W).permutation(W))
+    tab = oracle.ring_schedule(W, perm)
+    assert list(tab[W - 1]) == perm
+    for s in range(W - 1):
+        assert list(tab[s]) == list(np.roll(tab[s + 1], -1))
+    for p in range(W):
+        assert sorted(tab[:, p]) == list(range(W))
+
+
+# ----------------------------------------------------------- segmentation
+
+def test_segments_golden():
+    for line in _golden_lines("segments_uneven.txt"):
+        head, tail = line.split(":")
+        n, W = (int(v) for v in head.split())
+        vals = [int(v) for v in tail.split()]
+        for j in range(W):
+            assert oracle.segment(n, W, j) == (vals[2 * j], vals[2 * j + 1]), (n, W, j)
+
+
+@pytest.mark.parametrize("n,W", [(0, 1), (1, 7), (1000, 3), (1 << 20, 4), (12345, 16), (5, 64)])
+def test_segments_cover_contiguously(n, W):
+    end = 0
+    lens = []
+    for j in range(W):
+        off, ln = oracle.segment(n, W, j)
+        assert off == end
+        end += ln
+        lens.append(ln)
+    assert end == n
+    assert max(lens) - min(lens) <= 1
+    assert lens == sorted(lens, reverse=True)
+
+
+# ------------------------------------------------------- fold order (pins)
+
+def test_ring_order_hand_derived():
+    x = [np.full(4, v, np.float32) for v in (1e8, 1.0, -1e8, 1.0)]
+    for line in _golden_lines("ring_order_cancellation.txt"):
+        ring_s, res_s = line.split(":")
+        ring = None if ring_s.strip() == "identity" else [int(v) for v in ring_s.split()]
+        want = [float(v) for v in res_s.split()]
+        segs = oracle.reduce_scatter(x, "sum", oracle.F32, ring)
+        assert [float(s[0]) for s in segs] == want, ring_s
+        ar = oracle.allreduce(x, "sum", oracle.F32, ring)
+        for u in range(4):
+            assert list(ar[u]) == want
+
+
+def _stepwise_ring_fold(vals, j, ring):
+    # Independent re-fold of one element of block j: follow the block through
+    # the ring positions after its owner, widening to float32 and adding one
+    # rank at a time with numpy scalars (fp32 IEEE adds).
+    W = len(vals)
+    k = ring.index(j)
+    acc = np.float32(vals[ring[(k + 1) % W]])
+    for t in range(2, W + 1):
+        acc = np.float32(acc + np.float32(vals[ring[(k + t) % W]]))
+    return acc
+
+
+@pytest.mark.parametrize("W", [2, 3, 4])
+@pytest.mark.parametrize("n", [1, 2, 5, 16])
+def test_brute_force_tiny(W, n):
+    rng = _rng(100 * W + n)
+    ring = list(rng.permutation(W))
+    # wide dynamic range so that different orders really give different bits
+    ins = [(rng.standard_normal(n) * 10.0 ** rng.integers(-3, 9, n)).astype(np.float32)
+           for _ in range(W)]
+    segs = oracle.reduce_scatter(ins, "sum", oracle.F32, ring)
+    for j in range(W):
+        off, ln = oracle.segment(n, W, j)
+        for k in range(ln):
+            want = _stepwise_ring_fold([ins[u][off + k] for u in range(W)], j, ring)
+            assert segs[j][k].tobytes() == want.tobytes()
+
+
+def test_order_is_actually_observable():
+    # Same multiset of values, different start rank: the results differ, so
+    # the tests above really pin the order and not just the multiset.
+    x = [np.full(4, v, np.float32) for v in (1e8, 1.0, -1e8, 1.0)]
+    segs = oracle.reduce_scatter(x, "sum")
+    assert len({float(s[0]) for s in segs}) > 1
+
+
+# ------------------------------------------------------------- sum values
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 7, 8, 16])
+def test_integer_valued_sums_exact(W):
+    rng = _rng(W)
+    n = 1000 + W
+    ins = [rng.integers(-1024, 1025, n).astype(np.float32) for _ in range(W)]
+    want = np.sum(np.stack([a.astype(np.int64) for a in ins]), axis=0)
+    ar = oracle.allreduce(ins, "sum")
+    for u in range(W):
+        assert np.array_equal(ar[u].astype(np.int64), want)
+
+
+@pytest.mark.parametrize("W", [2, 4, 8, 16])
+def test_sum_within_reordering_bound_of_exact(W):
+    rng = _rng(7 * W)
+    n = 300
+    ins = [rng.uniform(-1, 1, n).astype(np.float32) for _ in range(W)]
+    ar = oracle.allreduce(ins, "sum")[0]
+    u = Fraction(1, 1 << 24)
+    gamma = (W - 1) * u / (1 - (W - 1) * u)
+    for i in range(n):
+        exact = sum(Fraction(float(a[i])) for a in ins)
+        mag = sum(abs(Fraction(float(a[i]))) for a in ins)
+        assert abs(Fraction(float(ar[i])) - exact) <= gamma * mag
+
+
+@pytest.mark.parametrize("k", [0, 1, 2, 3, 4])
+def test_avg_power_of_two_exact(k):
+    W = 1 << k
+    rng = _rng(k)
+    ins = [(rng.integers(-512, 513, 333) * W).astype(np.float32) for _ in range(W)]
+    want = np.sum(np.stack([a.astype(np.int64) for a in ins]), axis=0) // W
+    for got in oracle.allreduce(ins, "avg"):
+        assert np.array_equal(got.astype(np.int64), want)
+    assert np.array_equal(np.concatenate(oracle.reduce_scatter(ins, "avg")).astype(np.int64), want)
+
+
+@pytest.mark.parametrize("W", [3, 5, 6])
+def test_avg_close_to_exact_mean(W):
+    rng = _rng(W + 40)
+    ins = [rng.uniform(-1, 1, 200).astype(np.float32) for _ in range(W)]
+    got = oracle.allreduce(ins, "avg")[0]
+    u = Fraction(1, 1 << 24)
+    gamma = (W + 1) * u / (1 - (W + 1) * u)  # W-1 adds, 1/W rounding, 1 multiply
+    for i in range(200):
+        exact = sum(Fraction(float(a[i])) for a in ins) / W
+        mag = sum(abs(Fraction(float(a[i]))) for a in ins) / W
+        assert abs(Fraction(float(got[i])) - exact) <= gamma * mag
+
+
+# ------------------------------------------------------------------- max
+
+@pytest.mark.parametrize("W", [2, 3, 4, 8, 16])
+def test_max_matches_numpy(W):
+    rng = _rng(W + 99)
+    n = 777
+    ins = [rng.standard_normal(n).astype(np.float32) for _ in range(W)]
+    want = np.maximum.reduce(ins)
+    for got in oracle.allreduce(ins, "max"):
+        assert np.array_equal(got, want)
+
+
+def test_max_signed_zero_and_nan():
+    pz, nz, nan = np.float32(0.0), np.float32(-0.0), np.float32(np.nan)
+    ins = [np.array([pz, nz, nz, 1.0, nan], np.float32),
+           np.array([nz, pz, nz, nan, 1.0], np.float32)]
+    got = oracle.allreduce(ins, "max")[0]
+    bits = got.view(np.uint32)
+    assert bits[0] == 0x00000000 and bits[1] == 0x00000000  # +0 wins either order
+    assert bits[2] == 0x80000000  # max(-0, -0) = -0
+    assert bits[3] == 0x7FC00000 and bits[4] == 0x7FC00000  # canonical quiet NaN
+
+
+# ------------------------------------------------------------------ bf16
+
+def test_bf16_rne_golden():
+    for line in _golden_lines("bf16_rne.txt"):
+        fb, hb = line.split()
+        f = np.array([int(fb, 16)], np.uint32).view(np.float32)
+        assert oracle.bf16_from_f32(f)[0] == int(hb, 16), line
+
+
+def test_bf16_matches_torch_cpu_conversion():
+    torch = pytest.importorskip("torch")
+    rng = _rng(5)
+    bits = rng.integers(0, 1 << 32, 200_000, dtype=np.uint64).astype(np.uint32)
+    # add exact ties and near-ties around many exponents
+    hi = rng.integers(0, 1 << 16, 20_000, dtype=np.uint64).astype(np.uint32) << 16
+    bits = np.concatenate([bits, hi | 0x8000, hi | 0x7FFF, hi | 0x8001])
+    f = bits.view(np.float32)
+    f = f[~np.isnan(f)]
+    want = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.bf16_from_f32(f)
+    assert np.array_equal(got, want)
+
+
+def test_bf16_nan_stays_nan():
+    f = np.array([0x7FC00000, 0xFFC00001, 0x7F800001, 0x7FBFFFFF], np.uint32).view(np.float32)
+    h = oracle.bf16_from_f32(f).astype(np.uint32)
+    assert all(((v & 0x7F80) == 0x7F80) and (v & 0x7F) != 0 and (v & 0x40) for v in h)
+
+
+def test_bf16_allreduce_accumulates_in_fp32():
+    # 256 + 1 + 1 is 258 in fp32, and 258 is a bf16 value; rounding to bf16
+    # after every hop would lose the ones (256 + 1 -> 256 in bf16).
+    def b(v):
+        return oracle.bf16_from_f32(np.full(4, v, np.float32))
+    ins = [b(256.0), b(1.0), b(1.0)]
+    out = oracle.allreduce(ins, "sum", oracle.BF16)
+    assert all(np.array_equal(o, b(258.0)) for o in out)
+
+
+# ------------------------------------------------- RS / AG / AR identities
+
+@pytest.mark.parametrize("W,n", [(2, 9), (3, 10), (4, 4096 + 3), (8, 1001), (16, 50)])
+@pytest.mark.parametrize("dtype", [oracle.F32, oracle.BF16])
+@pytest.mark.parametrize("op", ["sum", "max", "avg"])
+def test_allgather_of_reduce_scatter_is_allreduce(W, n, dtype, op):
+    rng = _rng(W * n)
+    vals = [rng.standard_normal(n).astype(np.float32) for _ in range(W)]
+    ins = vals if dtype == oracle.F32 else [oracle.bf16_from_f32(v) for v in vals]
+    ring = list(rng.permutation(W))
+    rs = oracle.reduce_scatter(ins, op, dtype, ring)
+    ag = oracle.allgather(rs, n, dtype, ring)
+    ar = oracle.allreduce(ins, op, dtype, ring)
+    for u in range(W):
+        assert ag[u].tobytes() == ar[u].tobytes()
+        assert ar[u].tobytes() == ar[0].tobytes()  # every rank holds the same
+    assert np.concatenate(rs).tobytes() == ar[0].tobytes()
+
+
+@pytest.mark.parametrize("W", [1, 2, 5, 8])
+def test_allgather_is_concatenation(W):
+    rng = _rng(W)
+    n = 37
+    segs = [rng.standard_normal(oracle.segment(n, W, j)[1]).astype(np.float32) for j in range(W)]
+    want = np.concatenate(segs)
+    for out in oracle.allgather(segs, n, oracle.F32, list(rng.permutation(W))):
+        assert out.tobytes() == want.tobytes()
+
+
+def test_single_rank_is_copy():
+    rng = _rng(1)
+    x = rng.standard_normal(100).astype(np.float32)
+    x[3] = np.nan
+    for op in ("sum", "max", "avg"):
+        assert oracle.reduce_scatter([x], op)[0].tobytes() == x.tobytes()
+        assert oracle.allreduce([x], op)[0].tobytes() == x.tobytes()
+
+
+def test_empty_message_is_noop():
+    ins = [np.empty(0, np.float32) for _ in range(4)]
+    assert all(s.size == 0 for s in oracle.reduce_scatter(ins))
+    assert all(s.size == 0 for s in oracle.allreduce(ins))
+
+
+def test_invalid_arguments_rejected():
+    x = [np.zeros(4, np.float32)] * 2
+    with pytest.raises(ValueError):
+        oracle.reduce_scatter(x, 7)
+    with pytest.raises(ValueError):
+        oracle.allreduce(x, "sum", oracle.F32, [0, 0])
+    with pytest.raises(ValueError):
+        oracle.segment(10, 0, 0)
+
+
+@pytest.mark.parametrize("W,n", [(4, 1 << 12), (8, 1000), (3, 17), (16, 4099)])
+@pytest.mark.parametrize("op", ["sum", "max", "avg"])
+@pytest.mark.parametrize("dtype", [oracle.F32, oracle.BF16])
+def test_sampled_equals_full(W, n, op, dtype):
+    rng = _rng(W + n)
+    vals = [rng.standard_normal(n).astype(np.float32) for _ in range(W)]
+    ins = vals if dtype == oracle.F32 else [oracle.bf16_from_f32(v) for v in vals]
+    full = oracle.allreduce(ins, op, dtype)[0]
+    idx = np.concatenate([[0, n - 1], rng.integers(0, n, 200)])
+    samp = np.stack([np.asarray(a)[idx] for a in ins], axis=1)
+    got = oracle.allreduce_sampled(samp, idx, n, op, dtype)
+    assert got.tobytes() == full[idx].tobytes()
+
+
+# ---------------------------------------------------------------- fusion
+
+def test_fuse_plan_golden():
+    for line in _golden_lines("horovod_fusion_batches.txt"):
+        thr, sizes, begin = (p.strip() for p in line.split(";"))
+        counts = [int(v) // 4 for v in sizes.split()]
+        assert oracle.fuse_plan(counts, oracle.F32, int(thr)) == [int(v) for v in begin.split()]
+
+
+def test_fuse_plan_greedy_properties():
+    rng = _rng(3)
+    counts = np.round(np.exp(rng.uniform(np.log(1024), np.log(4194304), 200))).astype(np.int64)
+    thr = 64 << 20
+    begin = oracle.fuse_plan(counts, oracle.F32, thr)
+    assert begin[0] == 0 and begin[-1] == 200
+    for b in range(len(begin) - 1):
+        size = int(counts[begin[b]:begin[b + 1]].sum()) * 4
+        assert size <= thr or begin[b + 1] - begin[b] == 1
+        if begin[b + 1] < 200:  # greedy: the next tensor would not have fit
+            assert size + int(counts[begin[b + 1]]) * 4 > thr
+
+
+def test_pack_is_concatenation_and_unpack_inverts():
+    rng = _rng(11)
+    W, counts = 3, [5, 1, 17, 2, 8]
+    tensors = [[rng.standard_normal(c).astype(np.float32) for c in counts] for _ in range(W)]
+    fused = oracle.fuse_pack(tensors, counts, W)
+    for u in range(W):
+        assert fused[u].tobytes() == np.concatenate(tensors[u]).tobytes()
+    back = oracle.fuse_unpack(fused, counts)
+    for u in range(W):
+        for t in range(len(counts)):
+            assert back[u][t].tobytes() == tensors[u][t].tobytes()
+
+
+def test_fusion_allreduce_integer_mean_exact():
+    rng = _rng(12)
+    W = 8
+    counts = [1000, 3, 4097, 250, 1, 60]
+    tensors = [[(rng.integers(-100, 101, c) * 8).astype(np.float32) for c in counts]
+               for _ in range(W)]
+    outs = oracle.fusion_allreduce(tensors, counts, "avg", oracle.F32, threshold_bytes=4 * 4100)
+    for t, c in enumerate(counts):
+        want = sum(tensors[u][t].astype(np.int64) for u in range(W)) // W
+        for u in range(W):
+            assert np.array_equal(outs[u][t].astype(np.int64), want)
+
+
+def test_fusion_allreduce_is_batchwise_allreduce_of_concatenation():
+    # The fused allreduce segments the whole batch, so its bits are those of
+    # an allreduce of the concatenated tensors of each batch.
+    rng = _rng(13)
+    W = 4
+    counts = [7, 300, 41, 1000, 5]
+    thr = 4 * 400
+    tensors = [[rng.standard_normal(c).astype(np.float32) for c in counts] for _ in range(W)]
+    outs = oracle.fusion_allreduce(tensors, counts, "avg", oracle.F32, thr)
+    begin = oracle.fuse_plan(counts, oracle.F32, thr)
+    for b in range(len(begin) - 1):
+        ts = range(begin[b], begin[b + 1])
+        cat = [np.concatenate([tensors[u][t] for t in ts]) for u in range(W)]
+        ar = oracle.allreduce(cat, "avg")
+        for u in range(W):
+            assert np.concatenate([outs[u][t] for t in ts]).tobytes() == ar[u].tobytes()
