@@ -1,0 +1,518 @@
+"""Benchmark of the virtual-rank collectives on one GB300 (or N replicas).
+
+Default workload (the one the headline metric is quoted on): allreduce, sum,
+W = 8 virtual ranks, fp32, n = 67,108,864 elements per rank (256 MiB),
+values normal(0, 1e-3).  One step = one allreduce through the library's C ABI
+(one kernel launch that reads the 8 inputs once and writes the 8 outputs).
+value = algorithmic bytes (2 * W * n * 4: every input read once, every output
+written once) / time, in GB/s (1e9 B/s); the inputs (2 GiB) are larger than
+L2, so no flush is needed between steps.
+
+The same JSON line also carries:
+  roofline      the dominant kernel's achieved GB/s (CUDA events around each
+                launch on the launching stream) against the measured HBM copy
+                peak, with DRAM traffic per launch from the committed ncu
+                summary when the kernel sources still match it;
+  e2e           the same metric with the inputs copied from pinned host memory
+                and the outputs copied back inside the timed region;
+  cpu_baseline  the CPU oracle, single-threaded, on a bounded sample of the
+                same workload (rank 0, N = 1 only);
+  ops           the other workloads and operations timed in the same run
+                (reduce-scatter, allgather, ring order, bf16 avg, fusion,
+                small messages) unless --no-extras.
+
+--impl reference times the CPU oracle itself as the reference arm.
+Multi-GPU (torchrun): every rank runs its own independent replica (weak
+scaling, no exchange between GPUs); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import collective_reduction_virtual_gb300 as vc  # noqa: E402
+from collective_reduction_virtual_gb300 import inputs as I  # noqa: E402
+
+METRIC = "reduce-scatter/allreduce HBM GB/s (bytes read+written), % of GB300 HBM peak"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = ["device_common.cuh", "reduce_kernels.cuh", "reduce_f32.cu", "reduce_bf16.cu",
+                  "copy_kernels.cu", "staged_kernels.cu", "api.cpp", "vcoll_internal.h"]
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend):
+    ws, rank, _ = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device="cpu") -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_rank_step: float, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job GB/s: bytes every rank moved, over the slowest rank's time."""
+    return bytes_per_rank_step * steps * world / max_seconds / 1e9
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "collective_reduction_virtual_gb300", "csrc")
+    for name in KERNEL_SOURCES:
+        p = os.path.join(csrc, name)
+        if os.path.exists(p):
+            with open(p, "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since it was captured."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons during the timed region
+    (NVML through ctypes; nvidia-smi as a fallback).  Read-only."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, period_s=0.002):
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            handle = ctypes.c_void_p()
+            uuid = None
+            try:
+                uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+            except Exception:
+                uuid = None
+            ok = False
+            if uuid:
+                u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+                ok = nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(handle)) == 0
+            if not ok:
+                ok = nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(handle)) == 0
+            if not ok:
+                raise OSError("no NVML handle")
+            self._nvml, self._handle = nv, handle
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:  # 1 = SM
+                self.max_mhz = mx.value
+        except OSError:
+            self._nvml = None
+
+    def _poll(self):
+        nv, h = self._nvml, self._handle
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        getr = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if getr(h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(self.period)
+
+    def _smi(self):
+        cmd = ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+               "--format=csv,noheader,nounits", "-lms", "100"]
+        try:
+            self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, text=True)
+        except OSError:
+            self._proc = None
+            return
+        for line in self._proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            try:
+                self.samples.append(int(float(parts[0])))
+                self.max_mhz = int(float(parts[1]))
+                self.reasons |= int(parts[2], 16)
+            except (ValueError, IndexError):
+                pass
+            if self._stop.is_set():
+                break
+
+    def __enter__(self):
+        self._thread = threading.Thread(target=self._poll if self._nvml else self._smi, daemon=True)
+        self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if not self._nvml and getattr(self, "_proc", None):
+            self._proc.terminate()
+        self._thread.join(timeout=2)
+
+    def summary(self):
+        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "samples": len(self.samples), "reasons": names,
+                "source": "nvml" if self._nvml else "nvidia-smi"}
+
+
+def timed_steps(step, steps, warmup, stream, per_launch=True):
+    """Run warmup untimed steps, then time `steps` steps with CUDA events on
+    `stream` (barrier + synchronize on both sides).  Returns (total seconds,
+    mean seconds per launch)."""
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        if per_launch:
+            ev[i][0].record(stream)
+        step()
+        if per_launch:
+            ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    total = t0.elapsed_time(t1) / 1e3
+    per = (sum(a.elapsed_time(b) for a, b in ev) / 1e3 / steps) if per_launch else total / steps
+    return total, per
+
+
+# ---------------------------------------------------------------- workloads
+
+def ar_w8_f32(n_override=None):
+    W, n = 8, n_override or (1 << 26)
+    return dict(name="allreduce sum, W=8 virtual ranks, fp32, n=%d per rank, normal(0,1e-3)" % n,
+                W=W, n=n, kind="gradient", workload=I.AR_W8_F32, op="sum", dtype=torch.float32,
+                es=4)
+
+
+def run_vcoll(args):
+    world, rank = init_dist("nccl" if int(os.environ.get("WORLD_SIZE", "1")) > 1 else "gloo")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    vc.lib()
+    stream = torch.cuda.current_stream()
+    cfg = ar_w8_f32(args.n)
+    W, n, es = cfg["W"], cfg["n"], cfg["es"]
+    # every replica draws its own inputs (seed offset by the process rank)
+    ins = [I.gradient(n, I.rank_seed(cfg["workload"], u) + 100_000 * rank, dev) for u in range(W)]
+    outs = [torch.empty_like(t) for t in ins]
+    alg_bytes = 2 * W * n * es
+
+    def step():
+        vc.allreduce(ins, outs, op="sum")
+
+    with ClockSampler() as clocks:
+        total, per_launch = timed_steps(step, args.steps, args.warmup, stream)
+    total_max = max_over_ranks(total, dev if world > 1 else "cpu")
+    value = aggregate_gbs(alg_bytes, args.steps, world, total_max)
+    achieved = alg_bytes / per_launch / 1e9
+    peak, peak_src = measured_peaks()
+    kernel_key = "vc_reduce_vec<float,8,OpSum,AR,tree> W=8 n=2^26"
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_max / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded normal(0,1e-3) gradients generated on the GPU)",
+        "config": {"workload": cfg["name"], "op": "allreduce", "reduction": "sum", "W": W,
+                   "n_per_rank": n, "elem": "fp32", "order": "fastest (pairwise tree)",
+                   "bytes_per_step": alg_bytes, "parallelism": f"replicas{world}",
+                   "l2": "inputs (2 GiB) larger than L2; no flush"},
+        "pct_of_peak": {"measured_copy_peak": round(100 * achieved / peak, 1),
+                        "nominal_8000": round(100 * achieved / NOMINAL_HBM_GBS, 1)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": committed_traffic(kernel_key), "kernel": kernel_key,
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_e2e:
+        line["e2e"] = e2e_measure(cfg, ins, outs, args, stream, world, dev)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+    if not args.no_extras:
+        line["ops"] = extras(args, stream, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e_measure(cfg, ins, outs, args, stream, world, dev):
+    """Host buffers in, host buffers out: pinned H2D of every input, the
+    allreduce, D2H of every output, all inside the timed region."""
+    W, n, es = cfg["W"], cfg["n"], cfg["es"]
+    h_in = [t.cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(n, dtype=cfg["dtype"], pin_memory=True) for _ in range(W)]
+    steps = max(1, min(args.steps, 10))
+
+    def step():
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        vc.allreduce(ins, outs, op="sum")
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    total, _ = timed_steps(step, steps, max(1, min(args.warmup, 2)), stream, per_launch=False)
+    total = max_over_ranks(total, dev if world > 1 else "cpu")
+    bi = W * n * es
+    return {"value": round(aggregate_gbs(2 * W * n * es, steps, world, total), 1), "unit": "GB/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bi, "steps": steps}
+
+
+def cpu_baseline(cfg, seconds):
+    """The CPU oracle (single-threaded ring simulation) on a bounded sample of
+    the same workload: W rank buffers of the first m elements."""
+    import oracle
+    W = cfg["W"]
+    m = 1 << 16
+    xs = [I.gradient(m, I.rank_seed(cfg["workload"], u)).numpy() for u in range(W)]
+    t = time.perf_counter()
+    oracle.allreduce(xs, "sum", oracle.F32)
+    dt = time.perf_counter() - t
+    m = int(min(1 << 24, max(1 << 16, m * seconds / max(dt, 1e-6))))
+    xs = [I.gradient(m, I.rank_seed(cfg["workload"], u)).numpy() for u in range(W)]
+    t = time.perf_counter()
+    oracle.allreduce(xs, "sum", oracle.F32)
+    dt = time.perf_counter() - t
+    return {"value": round(2 * W * m * cfg["es"] / dt / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"allreduce sum of W={W} fp32 buffers of the first {m} elements "
+                      f"({dt:.1f} s single-threaded)"}
+
+
+# ------------------------------------------------------------------ extras
+
+def extras(args, stream, dev):
+    out = {}
+
+    def rate(fn, nbytes, steps=10, warmup=3):
+        total, per = timed_steps(fn, steps, warmup, stream)
+        return {"GBps": round(nbytes / per / 1e9, 1), "ms": round(per * 1e3, 4)}
+
+    # W=8 fp32 n=2^26: reduce-scatter, allgather, ring-order allreduce
+    W, n = 8, 1 << 26
+    ins = I.rank_buffers("gradient", W, n, I.AR_W8_F32, dev)
+    outs = [torch.empty_like(t) for t in ins]
+    segs = [torch.empty(vc.segment(n, W, j)[1], device=dev) for j in range(W)]
+    out["rs_sum_w8_f32_2^26"] = rate(lambda: vc.reduce_scatter(ins, segs, op="sum"),
+                                     (W + 1) * n * 4)
+    out["ag_w8_f32_2^26"] = rate(lambda: vc.allgather(segs, n, outs), (1 + W) * n * 4)
+    out["ar_ring_sum_w8_f32_2^26"] = rate(
+        lambda: vc.allreduce(ins, outs, op="sum", ring_order=True), 2 * W * n * 4)
+    del ins, outs, segs
+    torch.cuda.empty_cache()
+
+    # W=8 bf16 avg n=2^28 with outliers
+    W, n = 8, 1 << 28
+    ins = I.rank_buffers("outliers", W, n, I.AR_W8_BF16, dev)
+    outs = [torch.empty_like(t) for t in ins]
+    out["ar_avg_w8_bf16_2^28"] = rate(lambda: vc.allreduce(ins, outs, op="avg"), 2 * W * n * 2)
+    out["ar_ring_avg_w8_bf16_2^28"] = rate(
+        lambda: vc.allreduce(ins, outs, op="avg", ring_order=True), 2 * W * n * 2)
+    del ins, outs
+    torch.cuda.empty_cache()
+
+    # W=4 fp32 n=2^20 reduce-scatter: hot (L2-resident) and cold (L2 flushed)
+    W, n = 4, 1 << 20
+    ins = I.rank_buffers("uniform", W, n, I.RS_W4, dev)
+    segs = [torch.empty(vc.segment(n, W, j)[1], device=dev) for j in range(W)]
+    out["rs_sum_w4_f32_2^20_hot"] = rate(lambda: vc.reduce_scatter(ins, segs, op="sum"),
+                                         (W + 1) * n * 4, steps=50)
+    flush = torch.empty(2 * L2_BYTES // 4, device=dev)
+    times = []
+    for i in range(13):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        vc.reduce_scatter(ins, segs, op="sum")
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(a.elapsed_time(b) / 1e3)
+    per = statistics.median(times)
+    out["rs_sum_w4_f32_2^20_cold"] = {"GBps": round((W + 1) * n * 4 / per / 1e9, 1),
+                                      "ms": round(per * 1e3, 4), "l2": "flushed before each"}
+    del ins, segs, flush
+    torch.cuda.empty_cache()
+
+    # fusion: 200 fp32 tensors per rank, W=8, 64 MiB buffer, pack + AR avg + unpack
+    W = 8
+    counts = [int(c) for c in I.fusion_counts()]
+    tens = I.fusion_tensors(counts, W, dev)
+    fouts = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+    fused = [torch.empty((64 << 20) // 4, device=dev) for _ in range(W)]
+    tot = sum(counts) * 4
+    out["fusion_w8_200tensors"] = rate(
+        lambda: vc.fusion_allreduce(tens, fouts, fused, op="avg"), 6 * W * tot, steps=5, warmup=2)
+    out["fusion_w8_200tensors"]["bytes_formula"] = "6*W*B_total (pack + AR + unpack)"
+    del tens, fouts, fused
+    torch.cuda.empty_cache()
+
+    # small messages: latency in a CUDA graph of 1000 launches
+    lat = {}
+    for W in (2, 8, 16):
+        for nbytes in (1 << 10, 1 << 15):
+            n = nbytes // 4
+            ins = I.rank_buffers("uniform", W, n, I.SWEEP, dev)
+            outs = [torch.empty_like(t) for t in ins]
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                vc.allreduce(ins, outs, op="sum", stream=s)
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(1000):
+                    vc.allreduce(ins, outs, op="sum", stream=s)
+            g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / 1000
+            lat[f"ar_sum_W{W}_{nbytes}B"] = {"us": round(us, 2),
+                                             "GBps": round(2 * W * nbytes / us / 1e3, 2)}
+            del g, ins, outs
+    out["small_message_graph_1000"] = lat
+    return out
+
+
+# ------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: same metric, unit and config; each
+    step allreduces a bounded sample of the workload on one host core."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    cfg = ar_w8_f32(args.n)
+    W = cfg["W"]
+    m = args.ref_elems
+    xs = [I.gradient(m, I.rank_seed(cfg["workload"], u)).numpy() for u in range(W)]
+    for _ in range(args.warmup):
+        oracle.allreduce(xs, "sum", oracle.F32)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.allreduce(xs, "sum", oracle.F32)
+    dt = time.perf_counter() - t
+    value = 2 * W * m * 4 * args.steps / dt / 1e9
+    sample = f"allreduce sum of W={W} fp32 buffers of the first {m} elements per step"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded normal(0,1e-3) gradients)",
+            "config": {"workload": cfg["name"], "op": "allreduce", "reduction": "sum", "W": W,
+                       "n_per_rank": cfg["n"], "elem": "fp32", "order": "ring",
+                       "parallelism": "host, 1 core"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["vcoll", "reference"], default="vcoll")
+    ap.add_argument("--n", type=int, default=None, help="elements per rank (default 2^26)")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-elems", type=int, default=1 << 22)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "vcoll":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_vcoll(args)
+
+
+if __name__ == "__main__":
+    main()

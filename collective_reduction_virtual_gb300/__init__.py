@@ -1,0 +1,279 @@
+"""vcoll: virtual-rank collectives (reduce-scatter, allgather, allreduce,
+tensor-fusion pack/unpack) on one GB300 GPU.
+
+This module is a thin ctypes binding over ``libvcoll.so`` (C ABI in
+``include/vcoll.h``).  It only marshals arguments -- device pointers from
+``torch.Tensor.data_ptr()`` and the current CUDA stream -- every step of every
+collective runs in the library's CUDA kernels.  There is no CPU fallback: if
+the library is not built, every call raises.
+
+Two layers, same names as the C ABI:
+
+* ``vcoll_reduce_scatter(in_ptrs, out_ptrs, W, n, dtype, op, flags, stream)``
+  and friends take integer device pointers and return the status code
+  (``VcollError`` is raised by the tensor layer, not here);
+* ``reduce_scatter(ins, outs=None, op="sum", ring_order=False)`` and friends
+  take lists of CUDA tensors (one per virtual rank) and raise ``VcollError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libvcoll.so")
+
+F32, BF16 = 0, 1
+SUM, MAX, AVG = 0, 1, 2
+FLAG_RING_ORDER, FLAG_STAGED, FLAG_DIRECT = 0x1, 0x2, 0x4
+MAX_RANKS = 64
+OK, ERR_INVALID_ARG, ERR_INVALID_TYPE, ERR_INVALID_OP, ERR_UNSUPPORTED, ERR_CUDA = range(6)
+OPS = {"sum": SUM, "max": MAX, "avg": AVG}
+DEFAULT_FUSION_THRESHOLD = 64 * 1024 * 1024  # Horovod's tensor_fusion_threshold default
+
+_lock = threading.Lock()
+_lib = None
+
+
+class VcollError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"vcoll error {status}: {message}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    "libvcoll.so is not built; run `python -c \"import __graft_entry__ as g; "
+                    "g.build()\"` or `python collective_reduction_virtual_gb300/build.py`")
+            L = ctypes.CDLL(LIB_PATH)
+            PP = ctypes.POINTER(ctypes.c_void_p)
+            I, I64, U, P = ctypes.c_int, ctypes.c_int64, ctypes.c_uint, ctypes.c_void_p
+            I64P, IP = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int)
+            for name in ("vcoll_reduce_scatter", "vcoll_allgather", "vcoll_allreduce"):
+                getattr(L, name).argtypes = [PP, PP, I, I64, I, I, U, P]
+                getattr(L, name).restype = I
+            L.vcoll_fuse_plan.argtypes = [I64P, I, I, I64, IP, IP]
+            L.vcoll_fuse_plan.restype = I
+            L.vcoll_fuse_pack.argtypes = [PP, I64P, I, PP, I, I, P]
+            L.vcoll_fuse_pack.restype = I
+            L.vcoll_fuse_unpack.argtypes = [PP, I64P, I, PP, I, I, P]
+            L.vcoll_fuse_unpack.restype = I
+            L.vcoll_segment.argtypes = [I64, I, I, I64P, I64P]
+            L.vcoll_segment.restype = I
+            L.vcoll_status_string.argtypes = [I]
+            L.vcoll_status_string.restype = ctypes.c_char_p
+            L.vcoll_last_error.argtypes = []
+            L.vcoll_last_error.restype = ctypes.c_char_p
+            L.vcoll_version.argtypes = []
+            L.vcoll_version.restype = I
+            _lib = L
+    return _lib
+
+
+def _ptr_array(ptrs):
+    arr = (ctypes.c_void_p * max(1, len(ptrs)))()
+    for i, p in enumerate(ptrs):
+        arr[i] = int(p) if p else None
+    return arr
+
+
+def _i64_array(vals):
+    return (ctypes.c_int64 * max(1, len(vals)))(*[int(v) for v in vals])
+
+
+def last_error() -> str:
+    return lib().vcoll_last_error().decode()
+
+
+def status_string(status: int) -> str:
+    return lib().vcoll_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return lib().vcoll_version()
+
+
+# ----------------------------------------------------------- raw C ABI layer
+
+def vcoll_reduce_scatter(in_ptrs, out_ptrs, W, n, dtype, op, flags=0, stream=0) -> int:
+    return lib().vcoll_reduce_scatter(_ptr_array(in_ptrs), _ptr_array(out_ptrs), W, n, dtype, op,
+                                      flags, stream or None)
+
+
+def vcoll_allgather(in_ptrs, out_ptrs, W, n, dtype, op=SUM, flags=0, stream=0) -> int:
+    return lib().vcoll_allgather(_ptr_array(in_ptrs), _ptr_array(out_ptrs), W, n, dtype, op,
+                                 flags, stream or None)
+
+
+def vcoll_allreduce(in_ptrs, out_ptrs, W, n, dtype, op, flags=0, stream=0) -> int:
+    return lib().vcoll_allreduce(_ptr_array(in_ptrs), _ptr_array(out_ptrs), W, n, dtype, op,
+                                 flags, stream or None)
+
+
+def vcoll_fuse_pack(tensor_ptrs, counts, T, fused_ptrs, W, dtype, stream=0) -> int:
+    return lib().vcoll_fuse_pack(_ptr_array(tensor_ptrs), _i64_array(counts), T,
+                                 _ptr_array(fused_ptrs), W, dtype, stream or None)
+
+
+def vcoll_fuse_unpack(fused_ptrs, counts, T, tensor_ptrs, W, dtype, stream=0) -> int:
+    return lib().vcoll_fuse_unpack(_ptr_array(fused_ptrs), _i64_array(counts), T,
+                                   _ptr_array(tensor_ptrs), W, dtype, stream or None)
+
+
+def vcoll_fuse_plan(counts, dtype=F32, threshold_bytes=DEFAULT_FUSION_THRESHOLD):
+    """Returns (status, batch_begin list)."""
+    T = len(counts)
+    begin = (ctypes.c_int * (T + 1))()
+    nb = ctypes.c_int()
+    rc = lib().vcoll_fuse_plan(_i64_array(counts), T, dtype, int(threshold_bytes), begin,
+                               ctypes.byref(nb))
+    return rc, (list(begin[: nb.value + 1]) if rc == OK else [])
+
+
+def vcoll_segment(n, W, j):
+    """Returns (status, offset, length)."""
+    off, ln = ctypes.c_int64(), ctypes.c_int64()
+    rc = lib().vcoll_segment(int(n), int(W), int(j), ctypes.byref(off), ctypes.byref(ln))
+    return rc, off.value, ln.value
+
+
+# -------------------------------------------------------------- tensor layer
+
+def _check(rc: int):
+    if rc != OK:
+        raise VcollError(rc, last_error() or status_string(rc))
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise VcollError(ERR_INVALID_TYPE, f"unsupported dtype {t.dtype}")
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _check_tensors(ts, what):
+    for i, t in enumerate(ts):
+        if not t.is_cuda:
+            raise VcollError(ERR_INVALID_ARG, f"{what}[{i}] is not a CUDA tensor")
+        if not t.is_contiguous():
+            raise VcollError(ERR_INVALID_ARG, f"{what}[{i}] is not contiguous")
+
+
+def segment(n: int, W: int, j: int) -> tuple[int, int]:
+    rc, off, ln = vcoll_segment(n, W, j)
+    _check(rc)
+    return off, ln
+
+
+def reduce_scatter(ins, outs=None, op="sum", ring_order=False, stream=None, flags=0):
+    """ins: W CUDA tensors of n elements.  Returns W segment tensors."""
+    torch = _torch()
+    W, n = len(ins), ins[0].numel()
+    _check_tensors(ins, "ins")
+    if outs is None:
+        outs = [torch.empty(segment(n, W, j)[1], dtype=ins[0].dtype, device=ins[0].device)
+                for j in range(W)]
+    _check_tensors(outs, "outs")
+    fl = flags | (FLAG_RING_ORDER if ring_order else 0)
+    _check(vcoll_reduce_scatter([t.data_ptr() for t in ins], [t.data_ptr() for t in outs], W, n,
+                                _dtype_code(ins[0]), OPS[op] if isinstance(op, str) else op, fl,
+                                _stream_handle(stream)))
+    return outs
+
+
+def allgather(segs, n: int, outs=None, stream=None, flags=0):
+    """segs[j]: segment j (len_j elements).  Returns W tensors of n elements."""
+    torch = _torch()
+    W = len(segs)
+    _check_tensors(segs, "segs")
+    if outs is None:
+        outs = [torch.empty(n, dtype=segs[0].dtype, device=segs[0].device) for _ in range(W)]
+    _check_tensors(outs, "outs")
+    _check(vcoll_allgather([t.data_ptr() for t in segs], [t.data_ptr() for t in outs], W, n,
+                           _dtype_code(segs[0]), SUM, flags, _stream_handle(stream)))
+    return outs
+
+
+def allreduce(ins, outs=None, op="sum", ring_order=False, stream=None, flags=0):
+    """ins: W CUDA tensors of n elements; outs defaults to new tensors
+    (pass ``outs=ins`` for in place).  Returns outs."""
+    torch = _torch()
+    W, n = len(ins), ins[0].numel()
+    _check_tensors(ins, "ins")
+    if outs is None:
+        outs = [torch.empty_like(t) for t in ins]
+    _check_tensors(outs, "outs")
+    fl = flags | (FLAG_RING_ORDER if ring_order else 0)
+    _check(vcoll_allreduce([t.data_ptr() for t in ins], [t.data_ptr() for t in outs], W, n,
+                           _dtype_code(ins[0]), OPS[op] if isinstance(op, str) else op, fl,
+                           _stream_handle(stream)))
+    return outs
+
+
+def fuse_plan(counts, dtype=F32, threshold_bytes=DEFAULT_FUSION_THRESHOLD) -> list[int]:
+    rc, begin = vcoll_fuse_plan(list(counts), dtype, threshold_bytes)
+    _check(rc)
+    return begin
+
+
+def fuse_pack(tensors, fused, stream=None):
+    """tensors[u][t] -> fused[u] (back to back, no padding)."""
+    W, T = len(tensors), len(tensors[0])
+    counts = [tensors[0][t].numel() for t in range(T)]
+    flat = [tensors[u][t] for u in range(W) for t in range(T)]
+    _check_tensors(flat, "tensors")
+    _check_tensors(fused, "fused")
+    _check(vcoll_fuse_pack([t.data_ptr() for t in flat], counts, T, [f.data_ptr() for f in fused],
+                           W, _dtype_code(fused[0]), _stream_handle(stream)))
+    return fused
+
+
+def fuse_unpack(fused, tensors, stream=None):
+    """fused[u] -> tensors[u][t]."""
+    W, T = len(tensors), len(tensors[0])
+    counts = [tensors[0][t].numel() for t in range(T)]
+    flat = [tensors[u][t] for u in range(W) for t in range(T)]
+    _check_tensors(flat, "tensors")
+    _check_tensors(fused, "fused")
+    _check(vcoll_fuse_unpack([f.data_ptr() for f in fused], counts, T, [t.data_ptr() for t in flat],
+                             W, _dtype_code(fused[0]), _stream_handle(stream)))
+    return tensors
+
+
+def fusion_allreduce(tensors, outs, fused, op="avg", ring_order=False,
+                     threshold_bytes=DEFAULT_FUSION_THRESHOLD, stream=None):
+    """Horovod-style tensor fusion: plan greedy batches, then per batch pack
+    the tensors of every rank into its fusion buffer ``fused[u]`` (at least
+    the largest batch), allreduce the buffers in place, and unpack into
+    ``outs[u][t]``.  Three library launches per batch."""
+    W, T = len(tensors), len(tensors[0])
+    counts = [tensors[0][t].numel() for t in range(T)]
+    dt = _dtype_code(fused[0])
+    begin = fuse_plan(counts, dt, threshold_bytes)
+    for b in range(len(begin) - 1):
+        t0, t1 = begin[b], begin[b + 1]
+        nb = sum(counts[t0:t1])
+        bufs = [f[:nb] for f in fused]
+        fuse_pack([tensors[u][t0:t1] for u in range(W)], bufs, stream)
+        allreduce(bufs, bufs, op, ring_order, stream)
+        fuse_unpack(bufs, [outs[u][t0:t1] for u in range(W)], stream)
+    return outs

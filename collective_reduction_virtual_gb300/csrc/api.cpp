@@ -1,0 +1,488 @@
+// Host side of the C ABI declared in include/vcoll.h: argument validation,
+// segment / alignment / aliasing analysis, kernel selection and launch.
+//
+// Error conventions follow the early NCCL page (ncclReduceScatter: an unknown
+// datatype is ncclInvalidType, an unknown op ncclInvalidOperation, an empty
+// message succeeds without work, a single GPU is a plain device copy) and
+// Horovod's Status-with-message reporting (operations.cc): every failure
+// returns a code and leaves a thread-local message.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "vcoll_internal.h"
+
+using namespace vcoll;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(VCOLL_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int elem_size(int dtype) {
+  if (dtype == VCOLL_F32) return 4;
+  if (dtype == VCOLL_BF16) return 2;
+  return 0;
+}
+
+// ------------------------------------------------------------ device info
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sms[kMaxDevices];  // 0 = not queried yet
+
+struct OccEntry {
+  int dev;
+  const void* fn;
+  int threads;
+  size_t smem;
+  int blocks;
+};
+std::vector<OccEntry> g_occ;
+
+int current_device(int* dev, int* sms) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices) return fail(VCOLL_ERR_UNSUPPORTED, "device %d", *dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sms[*dev] == 0) {
+    int v = 0;
+    e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, *dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    g_sms[*dev] = v;
+  }
+  *sms = g_sms[*dev];
+  return VCOLL_OK;
+}
+
+int resident_blocks(int dev, const void* fn, int threads, size_t smem, int* blocks) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const OccEntry& o : g_occ)
+    if (o.dev == dev && o.fn == fn && o.threads == threads && o.smem == smem) {
+      *blocks = o.blocks;
+      return VCOLL_OK;
+    }
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  }
+  int b = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  if (b < 1) b = 1;
+  g_occ.push_back({dev, fn, threads, smem, b});
+  *blocks = b;
+  return VCOLL_OK;
+}
+
+// ------------------------------------------------------- buffer analysis
+
+void segment_of(int64_t n, int W, int j, int64_t* off, int64_t* len) {
+  const int64_t q = n / W, r = n % W;
+  *off = (int64_t)j * q + (j < r ? j : r);
+  *len = q + (j < r ? 1 : 0);
+}
+
+// One buffer of a call: bytes [addr, addr + nbytes) hold the elements
+// [lo, lo + nbytes / es) of the index space, so element i sits at
+// base + i * es with base = addr - lo * es (mod 2^64).
+struct Buf {
+  uint64_t addr;
+  uint64_t nbytes;
+  uint64_t base;
+  bool out;
+};
+
+bool overlaps(const Buf& x, const Buf& y) {
+  return x.nbytes && y.nbytes && x.addr < y.addr + y.nbytes && y.addr < x.addr + x.nbytes;
+}
+
+// Outputs must not overlap each other; an input may overlap an output only
+// when both map every element index to the same address (then the thread
+// that owns the index reads it before writing it).  Returns VCOLL_OK or
+// INVALID_ARG.  *vec / *phase: whether all buffers share one 16-byte phase.
+int analyse(const std::vector<Buf>& bufs, int es, int* vec, int* phase) {
+  for (size_t i = 0; i < bufs.size(); ++i) {
+    for (size_t k = 0; k < i; ++k) {
+      const Buf& a = bufs[i];
+      const Buf& b = bufs[k];
+      if (!overlaps(a, b)) continue;
+      if (a.out && b.out) return fail(VCOLL_ERR_INVALID_ARG, "two output buffers overlap");
+      if (a.out != b.out && a.base != b.base)
+        return fail(VCOLL_ERR_INVALID_ARG,
+                    "an input overlaps an output at a different element offset "
+                    "(only exact in-place aliasing is allowed)");
+    }
+  }
+  uint64_t ph = bufs.empty() ? 0 : (bufs[0].base & 15);
+  int same = 1;
+  for (const Buf& b : bufs)
+    if ((b.base & 15) != ph) same = 0;
+  *vec = same;
+  *phase = same ? (int)(ph / es) : 0;
+  return VCOLL_OK;
+}
+
+// No two of the given byte ranges may overlap (sort + sweep).
+int check_disjoint(std::vector<Buf> bufs) {
+  std::sort(bufs.begin(), bufs.end(), [](const Buf& a, const Buf& b) { return a.addr < b.addr; });
+  uint64_t end = 0;
+  bool any = false;
+  for (const Buf& b : bufs) {
+    if (!b.nbytes) continue;
+    if (any && b.addr < end) return fail(VCOLL_ERR_INVALID_ARG, "two buffers overlap");
+    end = std::max(end, b.addr + b.nbytes);
+    any = true;
+  }
+  return VCOLL_OK;
+}
+
+int check_ptrs(const void* const* p, int W, const char* what, int es, const int64_t* lens) {
+  if (!p) return fail(VCOLL_ERR_INVALID_ARG, "%s array is NULL", what);
+  for (int u = 0; u < W; ++u) {
+    if (lens[u] == 0) continue;
+    if (!p[u]) return fail(VCOLL_ERR_INVALID_ARG, "%s[%d] is NULL", what, u);
+    if ((uint64_t)p[u] % es)
+      return fail(VCOLL_ERR_INVALID_ARG, "%s[%d] is not aligned to the element size", what, u);
+  }
+  return VCOLL_OK;
+}
+
+int check_common(int W, int64_t n, int dtype, int op) {
+  if (W < 1 || W > VCOLL_MAX_RANKS)
+    return fail(VCOLL_ERR_INVALID_ARG, "W = %d outside [1, %d]", W, VCOLL_MAX_RANKS);
+  if (n < 0) return fail(VCOLL_ERR_INVALID_ARG, "n = %lld < 0", (long long)n);
+  if (!elem_size(dtype)) return fail(VCOLL_ERR_INVALID_TYPE, "unknown dtype %d", dtype);
+  if (op != VCOLL_SUM && op != VCOLL_MAX && op != VCOLL_AVG)
+    return fail(VCOLL_ERR_INVALID_OP, "unknown op %d", op);
+  return VCOLL_OK;
+}
+
+constexpr int64_t kSmallBytes = 32 * 1024;  // latency-bound path (MLX PR #3901: <= 32 KB)
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Tiles per segment: enough for the longest aligned body, at least one (tile
+// 0 also does the unaligned head and tail).
+int64_t tiles_per_segment(int64_t n, int W, int nseg, int V, int phase, int64_t tile_elems) {
+  int64_t tps = 1;
+  for (int j = 0; j < nseg; ++j) {
+    int64_t a, len;
+    if (nseg == 1) {
+      a = 0;
+      len = n;
+    } else {
+      segment_of(n, W, j, &a, &len);
+    }
+    const int64_t b = a + len;
+    int64_t up = a + ((V - ((a + phase) % V)) % V);
+    const int64_t av = std::min(up, b);
+    const int64_t dn = b - ((b + phase) % V);
+    const int64_t bv = std::max(dn, av);
+    tps = std::max(tps, ceil_div(bv - av, tile_elems));
+  }
+  return tps;
+}
+
+int launch(const void* fn, int64_t num_tiles, int threads, size_t smem, bool small, void* params,
+           void* stream) {
+  int64_t grid = num_tiles;
+  if (!small) {
+    int dev = 0, sms = 0, blocks = 0;
+    int rc = current_device(&dev, &sms);
+    if (rc) return rc;
+    rc = resident_blocks(dev, fn, threads, smem, &blocks);
+    if (rc) return rc;
+    grid = std::min<int64_t>(num_tiles, (int64_t)sms * blocks);
+  }
+  grid = std::max<int64_t>(1, std::min<int64_t>(grid, 0x7FFFFFFF));
+  void* args[] = {params};
+  cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(threads), args, smem,
+                                   (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return VCOLL_OK;
+}
+
+int copy_d2d(void* dst, const void* src, int64_t bytes, void* stream) {
+  if (dst == src || bytes == 0) return VCOLL_OK;
+  cudaError_t e = cudaMemcpyAsync(dst, src, (size_t)bytes, cudaMemcpyDeviceToDevice,
+                                  (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  return VCOLL_OK;
+}
+
+int reduce_common(int kind, const void* const* in, void* const* out, int W, int64_t n, int dtype,
+                  int op, unsigned flags, void* stream) {
+  g_err[0] = 0;
+  int rc = check_common(W, n, dtype, op);
+  if (rc) return rc;
+  if ((flags & VCOLL_FLAG_STAGED) && (flags & VCOLL_FLAG_DIRECT))
+    return fail(VCOLL_ERR_INVALID_ARG, "VCOLL_FLAG_STAGED and VCOLL_FLAG_DIRECT both set");
+  if (flags & ~(VCOLL_FLAG_RING_ORDER | VCOLL_FLAG_STAGED | VCOLL_FLAG_DIRECT))
+    return fail(VCOLL_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+  const int es = elem_size(dtype);
+  int64_t in_len[VCOLL_MAX_RANKS], out_len[VCOLL_MAX_RANKS], seg_off[VCOLL_MAX_RANKS];
+  for (int u = 0; u < W; ++u) {
+    segment_of(n, W, u, &seg_off[u], &out_len[u]);
+    in_len[u] = n;
+    if (kind == KIND_AR) out_len[u] = n;
+  }
+  if ((rc = check_ptrs(in, W, "in", es, in_len))) return rc;
+  if ((rc = check_ptrs((const void* const*)out, W, "out", es, out_len))) return rc;
+  if (n == 0) return VCOLL_OK;
+
+  std::vector<Buf> bufs;
+  for (int u = 0; u < W; ++u) {
+    bufs.push_back({(uint64_t)in[u], (uint64_t)(n * es), (uint64_t)in[u], false});
+    const uint64_t lo = kind == KIND_AR ? 0 : (uint64_t)seg_off[u];
+    bufs.push_back({(uint64_t)out[u], (uint64_t)(out_len[u] * es),
+                    (uint64_t)out[u] - lo * (uint64_t)es, true});
+  }
+  int vec, phase;
+  if ((rc = analyse(bufs, es, &vec, &phase))) return rc;
+
+  if (W == 1) return copy_d2d(out[0], in[0], n * es, stream);
+
+  const bool ring = (flags & VCOLL_FLAG_RING_ORDER) && op != VCOLL_MAX && W > 2;
+  const int W_t = (W == 2 || W == 4 || W == 8 || W == 16) ? W : 0;
+  const int nseg = (kind == KIND_RS || ring) ? W : 1;
+  const bool small = n * es <= kSmallBytes;
+  const int threads = small ? 128 : 256;
+  const int V = vec ? 16 / es : 1;
+
+  if (flags & VCOLL_FLAG_STAGED)
+    return fail(VCOLL_ERR_UNSUPPORTED, "the staged variant is not built in this library");
+
+  const void* fn = dtype == VCOLL_F32 ? reduce_kernel_f32(op, kind, W_t, ring, vec)
+                                      : reduce_kernel_bf16(op, kind, W_t, ring, vec);
+  ReduceParams prm;
+  memset(&prm, 0, sizeof(prm));
+  for (int u = 0; u < W; ++u) {
+    prm.in[u] = in[u];
+    prm.out[u] = out[u];
+  }
+  prm.n = n;
+  prm.q = n / W;
+  prm.r = n % W;
+  prm.W = W;
+  prm.nseg = nseg;
+  prm.phase = phase;
+  prm.ring = ring ? 1 : 0;
+  prm.scale = op == VCOLL_AVG ? 1.0f / (float)W : 1.0f;
+  prm.do_scale = op == VCOLL_AVG ? 1 : 0;
+  prm.tile_elems = vec ? (int64_t)threads * unroll_for(W_t) * V : (int64_t)threads * 4;
+  prm.tiles_per_seg = tiles_per_segment(n, W, nseg, V, phase, prm.tile_elems);
+  prm.num_tiles = prm.tiles_per_seg * nseg;
+  return launch(fn, prm.num_tiles, threads, 0, small, &prm, stream);
+}
+
+}  // namespace
+
+// ======================================================================
+extern "C" {
+
+int vcoll_reduce_scatter(const void* const* in, void* const* out, int W, int64_t n, int dtype,
+                         int op, unsigned flags, void* stream) {
+  return reduce_common(KIND_RS, in, out, W, n, dtype, op, flags, stream);
+}
+
+int vcoll_allreduce(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,
+                    unsigned flags, void* stream) {
+  return reduce_common(KIND_AR, in, out, W, n, dtype, op, flags, stream);
+}
+
+int vcoll_allgather(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,
+                    unsigned flags, void* stream) {
+  g_err[0] = 0;
+  int rc = check_common(W, n, dtype, op);
+  if (rc) return rc;
+  if (flags & ~(VCOLL_FLAG_RING_ORDER | VCOLL_FLAG_STAGED | VCOLL_FLAG_DIRECT))
+    return fail(VCOLL_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+  const int es = elem_size(dtype);
+  int64_t in_len[VCOLL_MAX_RANKS], out_len[VCOLL_MAX_RANKS], seg_off[VCOLL_MAX_RANKS];
+  for (int u = 0; u < W; ++u) {
+    segment_of(n, W, u, &seg_off[u], &in_len[u]);
+    out_len[u] = n;
+  }
+  if ((rc = check_ptrs(in, W, "in", es, in_len))) return rc;
+  if ((rc = check_ptrs((const void* const*)out, W, "out", es, out_len))) return rc;
+  if (n == 0) return VCOLL_OK;
+  std::vector<Buf> bufs;
+  for (int u = 0; u < W; ++u) {
+    bufs.push_back({(uint64_t)in[u], (uint64_t)(in_len[u] * es),
+                    (uint64_t)in[u] - (uint64_t)seg_off[u] * es, false});
+    bufs.push_back({(uint64_t)out[u], (uint64_t)(n * es), (uint64_t)out[u], true});
+  }
+  int vec, phase;
+  if ((rc = analyse(bufs, es, &vec, &phase))) return rc;
+  if (W == 1) return copy_d2d(out[0], in[0], n * es, stream);
+
+  const bool small = n * es <= kSmallBytes;
+  const int threads = small ? 128 : 256;
+  const int V = vec ? 16 / es : 1;
+  GatherParams prm;
+  memset(&prm, 0, sizeof(prm));
+  for (int u = 0; u < W; ++u) {
+    prm.in[u] = in[u];
+    prm.out[u] = out[u];
+  }
+  prm.n = n;
+  prm.q = n / W;
+  prm.r = n % W;
+  prm.W = W;
+  prm.phase = phase;
+  prm.tile_elems = (int64_t)threads * 4 * V;
+  prm.tiles_per_seg = tiles_per_segment(n, W, W, V, phase, prm.tile_elems);
+  prm.num_tiles = prm.tiles_per_seg * W;
+  return launch(gather_kernel(es, vec), prm.num_tiles, threads, 0, small, &prm, stream);
+}
+
+int vcoll_fuse_plan(const int64_t* counts, int T, int dtype, int64_t threshold_bytes,
+                    int* batch_begin, int* nbatches) {
+  g_err[0] = 0;
+  const int es = elem_size(dtype);
+  if (!es) return fail(VCOLL_ERR_INVALID_TYPE, "unknown dtype %d", dtype);
+  if (T < 0 || (T > 0 && !counts) || !batch_begin || !nbatches || threshold_bytes < 0)
+    return fail(VCOLL_ERR_INVALID_ARG, "invalid fuse_plan arguments");
+  for (int t = 0; t < T; ++t)
+    if (counts[t] < 0) return fail(VCOLL_ERR_INVALID_ARG, "counts[%d] < 0", t);
+  int nb = 0;
+  int t = 0;
+  while (t < T) {
+    batch_begin[nb++] = t;
+    int64_t bytes = counts[t] * es;
+    for (++t; t < T && bytes + counts[t] * es <= threshold_bytes; ++t) bytes += counts[t] * es;
+  }
+  batch_begin[nb] = T;
+  *nbatches = nb;
+  return VCOLL_OK;
+}
+
+static int fuse_common(const void* const* tensors, const int64_t* counts, int T,
+                       const void* const* fused, int W, int dtype, int unpack, void* stream) {
+  g_err[0] = 0;
+  const int es = elem_size(dtype);
+  if (!es) return fail(VCOLL_ERR_INVALID_TYPE, "unknown dtype %d", dtype);
+  if (W < 1 || W > VCOLL_MAX_RANKS)
+    return fail(VCOLL_ERR_INVALID_ARG, "W = %d outside [1, %d]", W, VCOLL_MAX_RANKS);
+  if (T < 0 || (T > 0 && (!counts || !tensors)) || !fused)
+    return fail(VCOLL_ERR_INVALID_ARG, "invalid fuse arguments");
+  int64_t total = 0;
+  for (int t = 0; t < T; ++t) {
+    if (counts[t] < 0) return fail(VCOLL_ERR_INVALID_ARG, "counts[%d] < 0", t);
+    total += counts[t];
+  }
+  std::vector<Buf> bufs;
+  for (int u = 0; u < W; ++u) {
+    if (total && !fused[u]) return fail(VCOLL_ERR_INVALID_ARG, "fused[%d] is NULL", u);
+    if ((uint64_t)fused[u] % es)
+      return fail(VCOLL_ERR_INVALID_ARG, "fused[%d] is not aligned to the element size", u);
+    bufs.push_back({(uint64_t)fused[u], (uint64_t)(total * es), 0, true});
+    for (int t = 0; t < T; ++t) {
+      const void* p = tensors[(int64_t)u * T + t];
+      if (!counts[t]) continue;
+      if (!p) return fail(VCOLL_ERR_INVALID_ARG, "tensors[%d] is NULL", u * T + t);
+      if ((uint64_t)p % es)
+        return fail(VCOLL_ERR_INVALID_ARG, "tensors[%d] is not aligned to the element size",
+                    u * T + t);
+      bufs.push_back({(uint64_t)p, (uint64_t)(counts[t] * es), 1, true});
+    }
+  }
+  int rc = check_disjoint(bufs);
+  if (rc) return rc;
+  if (total == 0) return VCOLL_OK;
+
+  const int chunk = std::min(kFuseMaxTensors, kFuseMaxCopies / W);
+  const int threads = 256;
+  const int64_t tile_elems = (int64_t)threads * 4 * (16 / es);
+  int64_t offset = 0;
+  for (int t0 = 0; t0 < T; t0 += chunk) {
+    const int nt = std::min(chunk, T - t0);
+    FuseParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.T = nt;
+    prm.W = W;
+    prm.unpack = unpack;
+    prm.tile_elems = tile_elems;
+    int64_t tiles = 0;
+    int64_t bytes = 0;
+    for (int t = 0; t < nt; ++t) {
+      prm.count[t] = counts[t0 + t];
+      prm.offset[t] = offset;
+      prm.tile_begin[t] = tiles;
+      tiles += ceil_div(counts[t0 + t], tile_elems);
+      offset += counts[t0 + t];
+      bytes += counts[t0 + t] * es;
+    }
+    prm.tile_begin[nt] = tiles;
+    for (int u = 0; u < W; ++u) {
+      prm.fused[u] = (void*)fused[u];
+      for (int t = 0; t < nt; ++t) prm.tensor[u * nt + t] = (void*)tensors[(int64_t)u * T + t0 + t];
+    }
+    if (tiles == 0) continue;
+    rc = launch(fuse_kernel(es), tiles, threads, 0, bytes <= kSmallBytes, &prm, stream);
+    if (rc) return rc;
+  }
+  return VCOLL_OK;
+}
+
+int vcoll_fuse_pack(const void* const* tensors, const int64_t* counts, int T, void* const* fused,
+                    int W, int dtype, void* stream) {
+  return fuse_common(tensors, counts, T, (const void* const*)fused, W, dtype, 0, stream);
+}
+
+int vcoll_fuse_unpack(const void* const* fused, const int64_t* counts, int T,
+                      void* const* tensors, int W, int dtype, void* stream) {
+  return fuse_common((const void* const*)tensors, counts, T, fused, W, dtype, 1, stream);
+}
+
+int vcoll_segment(int64_t n, int W, int j, int64_t* off, int64_t* len) {
+  g_err[0] = 0;
+  if (n < 0 || W < 1 || W > VCOLL_MAX_RANKS || j < 0 || j >= W || !off || !len)
+    return fail(VCOLL_ERR_INVALID_ARG, "invalid segment arguments");
+  segment_of(n, W, j, off, len);
+  return VCOLL_OK;
+}
+
+const char* vcoll_status_string(int status) {
+  switch (status) {
+    case VCOLL_OK:
+      return "success";
+    case VCOLL_ERR_INVALID_ARG:
+      return "invalid argument";
+    case VCOLL_ERR_INVALID_TYPE:
+      return "invalid data type";
+    case VCOLL_ERR_INVALID_OP:
+      return "invalid reduction operation";
+    case VCOLL_ERR_UNSUPPORTED:
+      return "unsupported request";
+    case VCOLL_ERR_CUDA:
+      return "CUDA error";
+    default:
+      return "unknown status";
+  }
+}
+
+const char* vcoll_last_error(void) { return g_err; }
+
+int vcoll_version(void) { return 100; }
+
+}  // extern "C"

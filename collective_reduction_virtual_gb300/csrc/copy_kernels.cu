@@ -1,0 +1,203 @@
+// Bit-copy kernels: allgather and tensor-fusion pack / unpack.
+//
+// Allgather ("Distributed primitives": AllGather propagates the reduced
+// segments so that every node holds their concatenation): each tile reads a
+// piece of segment j once and writes it to all W outputs.
+//
+// Fusion (Horovod PerformOperation: copy each tensor to buffer + offset with
+// offset += size, no padding; SINGA Communicator::fusedSynch likewise): one
+// launch moves up to kFuseMaxTensors tensors of every rank.  Tensor offsets
+// in the fused buffer are arbitrary element multiples, so source and
+// destination usually sit at different 16-byte phases; the copy then stores
+// aligned 16-byte vectors and assembles each from the two aligned source
+// vectors that cover it (a funnel shift), keeping both sides at full width.
+#include "device_common.cuh"
+#include "vcoll_internal.h"
+
+namespace vcoll {
+
+// ------------------------------------------------------------- allgather
+
+template <int ES, bool VEC>
+__global__ void __launch_bounds__(256) vc_gather(const __grid_constant__ GatherParams p) {
+  using B = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
+  constexpr int V = VEC ? 16 / ES : 1;
+  constexpr int U = 4;
+  const int W = p.W;
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    const int j = (int)(tile / p.tiles_per_seg);
+    const int64_t k = tile - (int64_t)j * p.tiles_per_seg;
+    int64_t a, b, av, bv;
+    segment_bounds(p.n, p.q, p.r, W, j, a, b);
+    if (VEC) {
+      aligned_body<V>(a, b, p.phase, av, bv);
+    } else {
+      av = a;
+      bv = b;
+    }
+    const int64_t e0 = av + k * p.tile_elems;
+    const int64_t e1 = e0 + p.tile_elems < bv ? e0 + p.tile_elems : bv;
+    const char* src = (const char*)p.in[j] - a * ES;  // element i of segment j at src + i*ES
+    if (VEC) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t e = e0 + ((int64_t)u * nthr + tid) * V;
+        if (e < e1) v[u] = ld_stream(src + e * ES);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t e = e0 + ((int64_t)u * nthr + tid) * V;
+        if (e < e1)
+          for (int r = 0; r < W; ++r) st_stream((char*)p.out[r] + e * ES, v[u]);
+      }
+      if (k == 0) {
+        // head [a, av) and tail [bv, b): fewer than V elements each
+        int64_t i = -1;
+        if (tid < av - a) i = a + tid;
+        if (tid >= 32 && tid - 32 < b - bv) i = bv + (tid - 32);
+        if (i >= 0) {
+          const B x = ld1<B>(src + i * ES);
+          for (int r = 0; r < W; ++r) st1((char*)p.out[r] + i * ES, x);
+        }
+      }
+    } else {
+      for (int64_t e = e0 + tid; e < e1; e += nthr) {
+        const B x = ld1<B>(src + e * ES);
+        for (int r = 0; r < W; ++r) st1((char*)p.out[r] + e * ES, x);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ fusion
+
+// out = bytes [sh, sh + 16) of the 32 bytes lo:hi (sh in 1..15).
+__device__ __forceinline__ uint4 funnel16(const uint4& lo, const uint4& hi, int sh) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  const int bs = (sh & 3) * 8;
+  uint4 o;
+  switch (sh >> 2) {
+    case 0:
+      o = make_uint4(__funnelshift_r(w[0], w[1], bs), __funnelshift_r(w[1], w[2], bs),
+                     __funnelshift_r(w[2], w[3], bs), __funnelshift_r(w[3], w[4], bs));
+      break;
+    case 1:
+      o = make_uint4(__funnelshift_r(w[1], w[2], bs), __funnelshift_r(w[2], w[3], bs),
+                     __funnelshift_r(w[3], w[4], bs), __funnelshift_r(w[4], w[5], bs));
+      break;
+    case 2:
+      o = make_uint4(__funnelshift_r(w[2], w[3], bs), __funnelshift_r(w[3], w[4], bs),
+                     __funnelshift_r(w[4], w[5], bs), __funnelshift_r(w[5], w[6], bs));
+      break;
+    default:
+      o = make_uint4(__funnelshift_r(w[3], w[4], bs), __funnelshift_r(w[4], w[5], bs),
+                     __funnelshift_r(w[5], w[6], bs), __funnelshift_r(w[6], w[7], bs));
+      break;
+  }
+  return o;
+}
+
+// Block-cooperative copy of nbytes (a multiple of ES) from src to dst, both
+// ES-aligned.  Destination-aligned 16-byte stores; the body loads either one
+// aligned source vector (same phase) or the two aligned vectors covering the
+// shifted source bytes.  Both of those lie in 16-byte blocks that hold at
+// least one byte of the source range, so no access leaves the source's pages.
+template <int ES>
+__device__ __forceinline__ void copy_range(char* dst, const char* src, int64_t nbytes) {
+  using B = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
+  constexpr int U = 4;
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  const uint64_t d0 = (uint64_t)dst;
+  int64_t head = (int64_t)((16 - (d0 & 15)) & 15);
+  if (head > nbytes) head = nbytes;
+  const int64_t body = (nbytes - head) & ~(int64_t)15;
+  const int64_t tail0 = head + body;
+  // head and tail, one element per thread
+  {
+    int64_t off = -1;
+    if ((int64_t)tid * ES < head) off = (int64_t)tid * ES;
+    const int t2 = tid - 32;
+    if (t2 >= 0 && tail0 + (int64_t)t2 * ES < nbytes) off = tail0 + (int64_t)t2 * ES;
+    if (off >= 0) st1(dst + off, ld1<B>(src + off));
+  }
+  const int64_t nv = body >> 4;
+  char* vd = dst + head;
+  const char* vs = src + head;
+  const int sh = (int)((uint64_t)vs & 15);
+  if (sh == 0) {
+    for (int64_t base = 0; base < nv; base += (int64_t)U * nthr) {
+      uint4 x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = base + (int64_t)u * nthr + tid;
+        if (i < nv) x[u] = ld_stream(vs + i * 16);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = base + (int64_t)u * nthr + tid;
+        if (i < nv) st_stream(vd + i * 16, x[u]);
+      }
+    }
+  } else {
+    const char* as = vs - sh;  // aligned source base
+    for (int64_t base = 0; base < nv; base += (int64_t)U * nthr) {
+      uint4 lo[U], hi[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = base + (int64_t)u * nthr + tid;
+        if (i < nv) {
+          lo[u] = ld_stream(as + i * 16);
+          hi[u] = ld_stream(as + i * 16 + 16);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t i = base + (int64_t)u * nthr + tid;
+        if (i < nv) st_stream(vd + i * 16, funnel16(lo[u], hi[u], sh));
+      }
+    }
+  }
+}
+
+template <int ES>
+__global__ void __launch_bounds__(256) vc_fuse(const __grid_constant__ FuseParams p) {
+  const int64_t total = p.tile_begin[p.T];
+  for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    // tensor t with tile_begin[t] <= tile < tile_begin[t + 1]
+    int lo = 0, hi = p.T - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.tile_begin[mid] <= tile)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int t = lo;
+    const int64_t k = tile - p.tile_begin[t];
+    const int64_t e0 = k * p.tile_elems;
+    const int64_t e1 = e0 + p.tile_elems < p.count[t] ? e0 + p.tile_elems : p.count[t];
+    for (int u = 0; u < p.W; ++u) {
+      char* tens = (char*)p.tensor[u * p.T + t] + e0 * ES;
+      char* fus = (char*)p.fused[u] + (p.offset[t] + e0) * ES;
+      if (p.unpack)
+        copy_range<ES>(tens, fus, (e1 - e0) * ES);
+      else
+        copy_range<ES>(fus, tens, (e1 - e0) * ES);
+    }
+  }
+}
+
+const void* gather_kernel(int elem_size, int vec) {
+  if (elem_size == 4) return vec ? (const void*)&vc_gather<4, true> : (const void*)&vc_gather<4, false>;
+  return vec ? (const void*)&vc_gather<2, true> : (const void*)&vc_gather<2, false>;
+}
+
+const void* fuse_kernel(int elem_size) {
+  return elem_size == 4 ? (const void*)&vc_fuse<4> : (const void*)&vc_fuse<2>;
+}
+
+}  // namespace vcoll

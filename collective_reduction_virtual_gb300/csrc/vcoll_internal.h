@@ -1,0 +1,108 @@
+// Internal interface between the host entry points (api.cpp) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/vcoll.h"
+
+#ifdef __CUDACC__
+#define VCOLL_HD __host__ __device__
+#else
+#define VCOLL_HD
+#endif
+
+namespace vcoll {
+
+enum Kind : int { KIND_RS = 0, KIND_AR = 1 };
+
+// Parameters of one reduce-scatter / allreduce launch.  The whole struct is a
+// __grid_constant__ kernel parameter (about 1.1 KB).
+//
+// Index space: element i in [0, n) of every rank.  Segment j is
+// [j*q + min(j, r), ... + q + (j < r)).  nseg == W splits the work by segment
+// (ring order, and always for reduce-scatter); nseg == 1 treats [0, n) as one
+// range (allreduce in the fastest order).
+//
+// Vector path: element i is 16-byte aligned in every buffer iff
+// (i + phase) % V == 0, V = 16 / elemsize.  Segment bodies are processed in
+// tiles of tile_elems elements (tiles_per_seg per segment); the unaligned head
+// and tail of each segment (< V elements each) are done by tile 0.
+struct ReduceParams {
+  const void* in[VCOLL_MAX_RANKS];
+  void* out[VCOLL_MAX_RANKS];
+  int64_t n;
+  int64_t q;
+  int64_t r;
+  int64_t tiles_per_seg;
+  int64_t num_tiles;
+  int64_t tile_elems;
+  int W;
+  int nseg;
+  int phase;
+  int ring;      // 1: ring order (start rank (j+1) mod W); 0: fastest order
+  float scale;   // fl32(1/W) for avg
+  int do_scale;
+};
+
+// Parameters of one allgather launch.  in[j] holds segment j.
+struct GatherParams {
+  const void* in[VCOLL_MAX_RANKS];
+  void* out[VCOLL_MAX_RANKS];
+  int64_t n;
+  int64_t q;
+  int64_t r;
+  int64_t tiles_per_seg;
+  int64_t num_tiles;
+  int64_t tile_elems;
+  int W;
+  int phase;
+};
+
+// Fusion pack / unpack.  One launch copies up to kFuseMaxTensors tensors of
+// every rank.  Copy e = u * T + t moves count[t] elements between
+// tensor[e] and fused[u] + offset[t].  Work is tiled per tensor:
+// tile_begin[t] is the first tile of tensor t (tile_begin[T] = total), each
+// tile covers tile_elems elements of that tensor on all W ranks.
+constexpr int kFuseMaxTensors = 64;
+constexpr int kFuseMaxCopies = 1024;  // W * T per launch
+struct FuseParams {
+  void* tensor[kFuseMaxCopies];
+  void* fused[VCOLL_MAX_RANKS];
+  int64_t count[kFuseMaxTensors];
+  int64_t offset[kFuseMaxTensors];
+  int64_t tile_begin[kFuseMaxTensors + 1];
+  int64_t tile_elems;
+  int T;
+  int W;
+  int unpack;  // 0: tensors -> fused, 1: fused -> tensors
+};
+
+// Kernel selection (function pointers for cudaLaunchKernel).  W_t is the
+// compile-time rank count (2, 4, 8, 16) or 0 for the runtime-W kernels; vec
+// selects the 16-byte vector path.
+const void* reduce_kernel_f32(int op, int kind, int W_t, int ring, int vec);
+const void* reduce_kernel_bf16(int op, int kind, int W_t, int ring, int vec);
+const void* staged_kernel_f32(int op, int kind, int W_t, int ring);
+const void* staged_kernel_bf16(int op, int kind, int W_t, int ring);
+const void* gather_kernel(int elem_size, int vec);
+const void* fuse_kernel(int elem_size);
+
+// Vectors (16 B) per thread per tile of the direct kernels, by W_t.
+VCOLL_HD constexpr int unroll_for(int W_t) {
+  return W_t == 2 ? 8 : W_t == 4 ? 4 : W_t == 8 ? 2 : W_t == 16 ? 1 : 2;
+}
+
+// Staged kernel geometry (shared with the host for launch configuration).
+constexpr int kStagedConsumerWarps = 8;
+constexpr int kStagedThreads = (kStagedConsumerWarps + 1) * 32;
+constexpr int kStagedStages = 4;
+// bytes of one rank's slice of one tile; the stage holds W of them
+VCOLL_HD constexpr int staged_slice_bytes(int W_t) {
+  return W_t == 2 ? 16384 : W_t == 4 ? 8192 : W_t == 8 ? 4096 : 2048;
+}
+VCOLL_HD constexpr int staged_smem_bytes(int W_t) {
+  return kStagedStages * W_t * staged_slice_bytes(W_t) + 256;
+}
+
+}  // namespace vcoll

@@ -1,0 +1,160 @@
+/*
+ * vcoll.h -- C ABI of the virtual-rank collective library for one GB300 GPU.
+ *
+ * A "virtual rank" is one device buffer.  W ranks live in the HBM of the
+ * current CUDA device; the collectives combine them element by element inside
+ * single kernel launches.  There is no second GPU, peer access or NCCL.
+ *
+ * Common conventions for every entry point below
+ * ------------------------------------------------
+ *  - Pointer arrays (`in`, `out`, `tensors`, `fused`) are HOST arrays of
+ *    DEVICE pointers on the current device.  Each device pointer must be
+ *    aligned to the element size.  Any 16-byte phase works; when all buffers
+ *    of one call share the same phase the 16-byte vector path runs, otherwise
+ *    an element-wise path gives the same bits more slowly.
+ *  - `n` counts elements per rank (int64).  Segment j of an n-element buffer
+ *    is [off_j, off_j + len_j) with q = n / W, r = n % W,
+ *    off_j = j*q + min(j, r), len_j = q + (j < r): contiguous, the first r
+ *    segments one element longer (vcoll_segment computes it).  When W divides
+ *    n this is NCCL's layout (block j at j * recvcount).
+ *  - Ownership: the caller owns every buffer; the library allocates no device
+ *    memory and keeps no pointer after the call returns.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Work is enqueued asynchronously on it; nothing
+ *    synchronises the host.
+ *  - Errors: every call returns a vcoll_status_t.  Argument errors are found
+ *    on the host before anything is enqueued.  vcoll_last_error() returns a
+ *    thread-local message for the last failure on the calling thread.
+ *  - Types: VCOLL_F32 and VCOLL_BF16.  Arithmetic is fp32 for both; bf16
+ *    inputs are widened exactly and outputs rounded to nearest even once.
+ *  - Ops: VCOLL_SUM, VCOLL_MAX, VCOLL_AVG (sum times fl32(1/W), applied once
+ *    to the finished sum).  max: a NaN operand gives the canonical quiet NaN;
+ *    +0 wins over -0; otherwise the larger value.
+ *  - Order: with VCOLL_FLAG_RING_ORDER each element of segment j is folded
+ *    in ring order -- starting at rank (j+1) mod W, accumulator first, ending
+ *    at rank j -- which reproduces the early NCCL ring bit for bit.  Without
+ *    it the library uses its fastest order (a pairwise tree for W in
+ *    {4, 8, 16}); results then differ from ring order only by float
+ *    reassociation.  max is the same in every order.
+ *  - Special cases: n == 0 returns VCOLL_OK without enqueuing anything;
+ *    W == 1 is a device-to-device copy (nothing when in and out coincide).
+ *
+ * Sources: early NCCL "src/reduce_scatter.cu" (pytorch mirror) for the ring
+ * schedule (GetBlock, ReduceScatterKernel) and the error conventions
+ * (ncclInvalidType / ncclInvalidOperation, recvcount == 0, nDev == 1);
+ * "Distributed primitives" notes for all-reduce / all-gather /
+ * reduce-scatter semantics and ring allreduce = reduce-scatter + allgather;
+ * Horovod "horovod/common/operations.cc" (PerformOperation, fusion batching in
+ * BackgroundThreadLoop) and Apache SINGA "src/io/communicator.cc"
+ * (Communicator::fusedSynch) for tensor fusion; MLX PR #3901 ("Add scatter
+ * reduce for JACCL") for the latency-bound path at <= 32 KB and the in-place
+ * read-before-write rule.
+ */
+#ifndef VCOLL_H_
+#define VCOLL_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VCOLL_MAX_RANKS 64
+
+typedef enum { VCOLL_F32 = 0, VCOLL_BF16 = 1 } vcoll_dtype_t;
+
+typedef enum { VCOLL_SUM = 0, VCOLL_MAX = 1, VCOLL_AVG = 2 } vcoll_op_t;
+
+typedef enum {
+  VCOLL_OK = 0,
+  VCOLL_ERR_INVALID_ARG = 1,  /* null pointer, W out of [1, 64], n < 0, misaligned
+                                 pointer, or an overlap other than the allowed
+                                 in-place forms */
+  VCOLL_ERR_INVALID_TYPE = 2, /* dtype not a vcoll_dtype_t (ncclInvalidType) */
+  VCOLL_ERR_INVALID_OP = 3,   /* op not a vcoll_op_t (ncclInvalidOperation) */
+  VCOLL_ERR_UNSUPPORTED = 4,  /* a valid request this build does not handle */
+  VCOLL_ERR_CUDA = 5          /* a CUDA runtime call or launch failed */
+} vcoll_status_t;
+
+/* Fold each segment in ring order (bit-exact with the NCCL ring). */
+#define VCOLL_FLAG_RING_ORDER 0x1u
+/* Force the variant that stages the W input tiles through shared memory with
+ * bulk asynchronous copies (TMA), or the variant that loads straight into
+ * registers.  Without either flag the library picks by message size.  Both
+ * give identical bits. */
+#define VCOLL_FLAG_STAGED 0x2u
+#define VCOLL_FLAG_DIRECT 0x4u
+
+/*
+ * Reduce-scatter ("Distributed primitives", section 3; NCCL
+ * ncclReduceScatter).  in[u]: n elements of rank u.  out[j]: receives the
+ * len_j elements of segment j of the element-wise reduction of all W inputs.
+ * In place: out[j] == (char*)in[j] + off_j * elemsize (NCCL's convention) or
+ * any out/in pair with the same element mapping; other overlaps are
+ * rejected.
+ */
+int vcoll_reduce_scatter(const void* const* in, void* const* out, int W, int64_t n, int dtype,
+                         int op, unsigned flags, void* stream);
+
+/*
+ * Allgather ("Distributed primitives", section 2; ring allreduce's second
+ * half).  in[j]: the len_j elements of segment j.  out[u]: receives all n
+ * elements (segment j at off_j) on every rank u.  op is checked but unused.
+ * In place: in[j] == (char*)out[u] + off_j * elemsize for some u.
+ */
+int vcoll_allgather(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,
+                    unsigned flags, void* stream);
+
+/*
+ * Allreduce ("Distributed primitives", section 1 and ring allreduce =
+ * reduce-scatter + allgather; Horovod / SINGA ncclAllReduce call sites).
+ * in[u]: n elements; out[u]: n elements, all W outputs receive the same
+ * result.  One kernel pass reads the W inputs once and writes the W outputs
+ * from registers; its bits equal reduce-scatter followed by allgather.
+ * In place: out[u] == in[u] (Horovod's in-place fusion-buffer allreduce).
+ */
+int vcoll_allreduce(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,
+                    unsigned flags, void* stream);
+
+/*
+ * Tensor-fusion batching (Horovod BackgroundThreadLoop): greedy in tensor
+ * order; a batch starts with the next tensor (even one above the threshold)
+ * and takes the following tensors while the fused byte size stays
+ * <= threshold_bytes.  counts[T] (host) are element counts; batch_begin
+ * (host, T + 1 ints) receives the first tensor of each batch followed by T;
+ * *nbatches the number of batches.  Host only, no GPU work.
+ */
+int vcoll_fuse_plan(const int64_t* counts, int T, int dtype, int64_t threshold_bytes,
+                    int* batch_begin, int* nbatches);
+
+/*
+ * Fusion pack (Horovod PerformOperation "memcpy in fusion buffer"; SINGA
+ * fusedSynch): fused[u] receives tensors[u*T + t] for t = 0..T-1 back to back,
+ * no padding (tensor t at element offset counts[0] + ... + counts[t-1]).
+ * tensors: host array of W*T device pointers, rank-major.  counts: host.
+ * One kernel launch per 128 tensors; no buffer may overlap another.
+ */
+int vcoll_fuse_pack(const void* const* tensors, const int64_t* counts, int T, void* const* fused,
+                    int W, int dtype, void* stream);
+
+/* Fusion unpack: the inverse of vcoll_fuse_pack. */
+int vcoll_fuse_unpack(const void* const* fused, const int64_t* counts, int T,
+                      void* const* tensors, int W, int dtype, void* stream);
+
+/* Segment j of an n-element buffer over W ranks (host only). */
+int vcoll_segment(int64_t n, int W, int j, int64_t* off, int64_t* len);
+
+/* Static description of a status code. */
+const char* vcoll_status_string(int status);
+
+/* Thread-local detail of the last failing call on this thread ("" if none). */
+const char* vcoll_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int vcoll_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VCOLL_H_ */

@@ -1,0 +1,172 @@
+"""Host-only checks of the C ABI: the library builds and loads without a GPU,
+exports every entry point include/vcoll.h declares, and rejects bad
+arguments with the documented status codes before touching the device.
+No call here reaches a kernel launch."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vcoll.h")
+
+
+@pytest.fixture(scope="module")
+def v():
+    from collective_reduction_virtual_gb300 import build
+    build.build()
+    import collective_reduction_virtual_gb300 as vc
+    return vc
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vcoll_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_compiles_as_c():
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-x", "c", HEADER],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_library_exports_every_declared_symbol(v):
+    names = declared_functions()
+    assert len(names) >= 10
+    out = subprocess.run(["nm", "-D", "--defined-only", v.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (vcoll_[a-z_0-9]+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    lib = ctypes.CDLL(v.LIB_PATH)
+    for n in names:
+        assert getattr(lib, n)
+
+
+def test_build_targets_sm103a_only():
+    from collective_reduction_virtual_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert not any("fast-math" in f or "use_fast_math" in f for f in build.NVCC_FLAGS)
+
+
+def test_version_and_status_strings(v):
+    assert v.version() == 100
+    assert v.status_string(v.OK) == "success"
+    assert "operation" in v.status_string(v.ERR_INVALID_OP)
+    assert v.status_string(99) == "unknown status"
+
+
+FAKE_IN = [0x100000 * (u + 1) for u in range(8)]
+FAKE_OUT = [0x10000000 + 0x100000 * u for u in range(8)]
+
+
+@pytest.mark.parametrize("fn", ["vcoll_reduce_scatter", "vcoll_allreduce", "vcoll_allgather"])
+def test_argument_errors(v, fn):
+    f = getattr(v, fn)
+    # unknown op / dtype (NCCL: ncclInvalidOperation / ncclInvalidType)
+    assert f(FAKE_IN[:4], FAKE_OUT[:4], 4, 64, v.F32, 9, 0, 0) == v.ERR_INVALID_OP
+    assert f(FAKE_IN[:4], FAKE_OUT[:4], 4, 64, 7, v.SUM, 0, 0) == v.ERR_INVALID_TYPE
+    # rank count and size
+    assert f(FAKE_IN[:1], FAKE_OUT[:1], 0, 64, v.F32, v.SUM, 0, 0) == v.ERR_INVALID_ARG
+    assert f(FAKE_IN * 9, FAKE_OUT * 9, 65, 64, v.F32, v.SUM, 0, 0) == v.ERR_INVALID_ARG
+    assert f(FAKE_IN[:4], FAKE_OUT[:4], 4, -1, v.F32, v.SUM, 0, 0) == v.ERR_INVALID_ARG
+    # null and misaligned pointers
+    assert f([0] + FAKE_IN[1:4], FAKE_OUT[:4], 4, 64, v.F32, v.SUM, 0, 0) == v.ERR_INVALID_ARG
+    assert f(FAKE_IN[:4], FAKE_OUT[:3] + [0], 4, 64, v.F32, v.SUM, 0, 0) == v.ERR_INVALID_ARG
+    assert f([FAKE_IN[0] + 2] + FAKE_IN[1:4], FAKE_OUT[:4], 4, 64, v.F32, v.SUM, 0, 0) \
+        == v.ERR_INVALID_ARG
+    assert "aligned" in v.last_error()
+    # unknown flag bits, conflicting variant flags
+    assert f(FAKE_IN[:4], FAKE_OUT[:4], 4, 64, v.F32, v.SUM, 0x80, 0) == v.ERR_INVALID_ARG
+    # empty message: success, nothing enqueued, null pointers allowed
+    assert f([0] * 4, [0] * 4, 4, 0, v.F32, v.SUM, 0, 0) == v.OK
+
+
+def test_conflicting_variant_flags(v):
+    assert v.vcoll_allreduce(FAKE_IN[:4], FAKE_OUT[:4], 4, 64, v.F32, v.SUM,
+                             v.FLAG_STAGED | v.FLAG_DIRECT, 0) == v.ERR_INVALID_ARG
+
+
+def test_overlap_rules(v):
+    n, W = 1000, 4
+    # two outputs overlapping
+    outs = [FAKE_OUT[0], FAKE_OUT[0] + 64, FAKE_OUT[2], FAKE_OUT[3]]
+    assert v.vcoll_allreduce(FAKE_IN[:W], outs, W, n, v.F32, v.SUM, 0, 0) == v.ERR_INVALID_ARG
+    assert "output" in v.last_error()
+    # output overlapping an input at a shifted offset
+    outs = [FAKE_IN[1] + 4] + FAKE_OUT[1:W]
+    assert v.vcoll_allreduce(FAKE_IN[:W], outs, W, n, v.F32, v.SUM, 0, 0) == v.ERR_INVALID_ARG
+    # reduce-scatter: out[j] aliasing in[j] one element away from NCCL's
+    # in-place position in[j] + off_j must fail
+    offs = [oracle.segment(n, W, j)[0] for j in range(W)]
+    outs = [FAKE_IN[j] + 4 * offs[j] + 4 for j in range(W)]
+    assert v.vcoll_reduce_scatter(FAKE_IN[:W], outs, W, n, v.F32, v.SUM, 0, 0) \
+        == v.ERR_INVALID_ARG
+    # allgather: input overlapping an output away from its own segment
+    segs = [FAKE_OUT[0] + 8] + FAKE_IN[1:W]
+    assert v.vcoll_allgather(segs, FAKE_OUT[:W], W, n, v.F32, v.SUM, 0, 0) == v.ERR_INVALID_ARG
+
+
+def test_fuse_errors(v):
+    counts = [10, 20]
+    ptrs = [0x100000, 0x200000]
+    assert v.vcoll_fuse_pack(ptrs, counts, 2, [0x300000], 1, 9, 0) == v.ERR_INVALID_TYPE
+    assert v.vcoll_fuse_pack(ptrs, [10, -1], 2, [0x300000], 1, v.F32, 0) == v.ERR_INVALID_ARG
+    assert v.vcoll_fuse_pack([0x100000, 0], counts, 2, [0x300000], 1, v.F32, 0) \
+        == v.ERR_INVALID_ARG
+    # overlapping tensors
+    assert v.vcoll_fuse_pack([0x100000, 0x100010], counts, 2, [0x300000], 1, v.F32, 0) \
+        == v.ERR_INVALID_ARG
+    # fused buffer overlapping a tensor
+    assert v.vcoll_fuse_unpack([0x100004], counts, 2, ptrs, 1, v.F32, 0) == v.ERR_INVALID_ARG
+    # nothing to copy
+    assert v.vcoll_fuse_pack([0, 0], [0, 0], 2, [0], 1, v.F32, 0) == v.OK
+
+
+def test_segment_matches_oracle(v):
+    rng = np.random.default_rng(1)
+    for _ in range(200):
+        W = int(rng.integers(1, 65))
+        n = int(rng.integers(0, 10 ** 6))
+        j = int(rng.integers(0, W))
+        assert v.segment(n, W, j) == oracle.segment(n, W, j)
+    assert v.vcoll_segment(10, 0, 0)[0] == v.ERR_INVALID_ARG
+    assert v.vcoll_segment(10, 4, 4)[0] == v.ERR_INVALID_ARG
+
+
+def test_fuse_plan_matches_oracle(v):
+    rng = np.random.default_rng(2)
+    for trial in range(50):
+        T = int(rng.integers(0, 300))
+        counts = list(np.round(np.exp(rng.uniform(0, 16, T))).astype(np.int64))
+        thr = int(rng.integers(1, 1 << 28))
+        for dt in (v.F32, v.BF16):
+            assert v.fuse_plan(counts, dt, thr) == oracle.fuse_plan(counts, dt, thr)
+    assert v.vcoll_fuse_plan([1, 2], 5)[0] == v.ERR_INVALID_TYPE
+    assert v.vcoll_fuse_plan([1, -2], v.F32)[0] == v.ERR_INVALID_ARG
+
+
+def test_product_package_does_not_touch_oracle():
+    # the CUDA library and its binding never import, load or name the oracle
+    pkg = os.path.join(ROOT, "collective_reduction_virtual_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                hit = re.search(r"import\s+oracle|from\s+oracle|liboracle|oracle\.(c|so)\b|oracle/",
+                                text)
+                assert not hit, os.path.join(dirpath, f)
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import collective_reduction_virtual_gb300 as vc
+    monkeypatch.setattr(vc, "_lib", None)
+    monkeypatch.setattr(vc, "LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        vc.lib()

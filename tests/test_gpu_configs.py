@@ -1,0 +1,231 @@
+"""GPU parity at the full sizes of the five benchmark workloads, in the launch
+configurations the benchmark times.
+
+Full-size outputs are checked two ways: at sampled indices against the
+oracle, which computes each sampled output one by one through its ring
+simulation (bit-exact in ring order and for max, tolerance otherwise), and on
+every element through properties that hold at any size (all allreduce
+outputs identical; ring-order allreduce equals the concatenated ring-order
+reduce-scatter; the fastest order within the reordering bound of the ring
+order).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from collective_reduction_virtual_gb300 import inputs as I
+from parity import assert_bit_exact, assert_close_fast, fp32_bound, to_np, widen
+
+pytestmark = pytest.mark.gpu
+
+ODT = {torch.float32: oracle.F32, torch.bfloat16: oracle.BF16}
+
+
+@pytest.fixture(scope="module")
+def v():
+    from collective_reduction_virtual_gb300 import build
+    build.build()
+    import collective_reduction_virtual_gb300 as vc
+    return vc
+
+
+@pytest.fixture(autouse=True)
+def _free_memory():
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def sample_indices(n, W, m, seed):
+    rng = np.random.default_rng(seed)
+    idx = [rng.integers(0, n, m), np.arange(min(n, 2048)), np.arange(max(0, n - 2048), n)]
+    for j in range(W):
+        off, ln = oracle.segment(n, W, j)
+        idx.append(np.arange(max(0, off - 3), min(n, off + 4)))
+    return np.unique(np.concatenate(idx)).astype(np.int64)
+
+
+def gather(ins, idx):
+    it = torch.from_numpy(idx).cuda()
+    vals = torch.stack([t[it] for t in ins], dim=1).contiguous()
+    return to_np(vals)
+
+
+def sampled_allreduce_check(ins, outs, n, W, op, ring, seed, m=50_000):
+    idx = sample_indices(n, W, m, seed)
+    vals = gather(ins, idx)
+    want = oracle.allreduce_sampled(vals, idx, n, op, ODT[ins[0].dtype])
+    got = to_np(outs[0][torch.from_numpy(idx).cuda()])
+    if ring or op == "max":
+        assert_bit_exact(got, want, f"sampled {op} ring={ring}")
+    else:
+        s = np.abs(widen(vals)).sum(axis=1)
+        assert_close_fast(got, want, s, W, op, f"sampled {op}")
+
+
+def all_ranks_equal(outs):
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16) if o.dtype == torch.bfloat16 else o.view(torch.int32),
+                           outs[0].view(torch.int16) if o.dtype == torch.bfloat16
+                           else outs[0].view(torch.int32))
+
+
+def fast_within_bound_of_ring(ins, fast, ring, W, op):
+    # every element: |fast - ring| <= fp32 bound (+ one bf16 ulp), on the GPU
+    absum = torch.zeros_like(ins[0], dtype=torch.float64)
+    for t in ins:
+        absum += t.double().abs()
+    rel = max(1e-6, 2 * (W - 1) * 2.0 ** -24)
+    bound = rel * absum / (W if op == "avg" else 1)
+    diff = (fast.double() - ring.double()).abs()
+    if fast.dtype == torch.bfloat16:
+        mag = torch.maximum(fast.double().abs(), ring.double().abs())
+        bound = bound + mag * 2.0 ** -7  # one bf16 ulp is at most 2^-7 |x|
+    assert bool((diff <= bound).all()), float((diff - bound).max())
+
+
+# --------------------------------------------------- W=4 fp32, n=2^20 (RS+AR)
+
+def test_rs_w4_f32_full(v):
+    W, n = 4, 1 << 20
+    ins = I.rank_buffers("uniform", W, n, I.RS_W4, "cuda")
+    ins_np = [to_np(t) for t in ins]
+    rs_want = oracle.reduce_scatter(ins_np, "sum", oracle.F32)
+    ar_want = oracle.allreduce(ins_np, "sum", oracle.F32)
+    for ring in (True, False):
+        rs = v.reduce_scatter(ins, op="sum", ring_order=ring)
+        ar = v.allreduce(ins, op="sum", ring_order=ring)
+        for j in range(W):
+            off, ln = oracle.segment(n, W, j)
+            if ring:
+                assert_bit_exact(to_np(rs[j]), rs_want[j], "RS C1")
+            else:
+                s = sum(np.abs(a[off:off + ln].astype(np.float64)) for a in ins_np)
+                assert_close_fast(to_np(rs[j]), rs_want[j], s, W, "sum", "RS C1 fast")
+        for u in range(W):
+            if ring:
+                assert_bit_exact(to_np(ar[u]), ar_want[u], "AR C1")
+        all_ranks_equal(ar)
+
+
+# ---------------------------------------------- W=8 fp32, n=2^26 allreduce
+
+def test_ar_w8_f32_full(v):
+    W, n = 8, 1 << 26
+    ins = I.rank_buffers("gradient", W, n, I.AR_W8_F32, "cuda")
+    fast = v.allreduce(ins, op="sum")
+    all_ranks_equal(fast)
+    sampled_allreduce_check(ins, fast, n, W, "sum", False, 1)
+    ring = v.allreduce(ins, op="sum", ring_order=True)
+    all_ranks_equal(ring)
+    sampled_allreduce_check(ins, ring, n, W, "sum", True, 2)
+    fast_within_bound_of_ring(ins, fast[0], ring[0], W, "sum")
+    rs = v.reduce_scatter(ins, op="sum", ring_order=True)
+    assert torch.equal(torch.cat(rs).view(torch.int32), ring[0].view(torch.int32))
+    ag = v.allgather(rs, n)
+    for o in ag:
+        assert torch.equal(o.view(torch.int32), ring[0].view(torch.int32))
+    mx = v.allreduce(ins, op="max")
+    sampled_allreduce_check(ins, mx, n, W, "max", False, 3)
+
+
+# ------------------------------------- W=8 bf16 avg, n=2^28, outliers x100
+
+def test_ar_w8_bf16_avg_full(v):
+    W, n = 8, 1 << 28
+    ins = I.rank_buffers("outliers", W, n, I.AR_W8_BF16, "cuda")
+    fast = v.allreduce(ins, op="avg")
+    all_ranks_equal(fast)
+    sampled_allreduce_check(ins, fast, n, W, "avg", False, 4)
+    ring = [torch.empty_like(t) for t in ins]
+    v.allreduce(ins, ring, op="avg", ring_order=True)
+    sampled_allreduce_check(ins, ring, n, W, "avg", True, 5)
+    all_ranks_equal(ring)
+    for lo in range(0, n, 1 << 26):  # chunked to bound the float64 temporaries
+        fast_within_bound_of_ring([t[lo:lo + (1 << 26)] for t in ins], fast[0][lo:lo + (1 << 26)],
+                                  ring[0][lo:lo + (1 << 26)], W, "avg")
+
+
+# ------------------------------------------------- fusion, W=8, 200 tensors
+
+def test_fusion_w8_full(v):
+    W = 8
+    counts = [int(c) for c in I.fusion_counts()]
+    tens = I.fusion_tensors(counts, W, "cuda")
+    outs = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+    thr = 64 << 20
+    fused = [torch.empty(thr // 4, device="cuda") for _ in range(W)]
+    begin = oracle.fuse_plan(counts, oracle.F32, thr)
+    assert v.fuse_plan(counts, v.F32, thr) == begin
+    for ring in (True, False):
+        v.fusion_allreduce(tens, outs, fused, op="avg", ring_order=ring, threshold_bytes=thr)
+        rng = np.random.default_rng(6 + ring)
+        for b in range(len(begin) - 1):
+            ts = list(range(begin[b], begin[b + 1]))
+            offs = np.cumsum([0] + [counts[t] for t in ts])
+            nb = int(offs[-1])
+            idx = np.unique(np.concatenate([rng.integers(0, nb, 4000), offs[:-1],
+                                            np.maximum(offs[1:] - 1, 0)]))
+            tpos = np.searchsorted(offs, idx, side="right") - 1
+            vals = np.empty((idx.size, W), np.float32)
+            got = np.empty(idx.size, np.float32)
+            for t_local, t in enumerate(ts):
+                sel = np.nonzero(tpos == t_local)[0]
+                if sel.size == 0:
+                    continue
+                k = torch.from_numpy(idx[sel] - offs[t_local]).cuda()
+                for u in range(W):
+                    vals[sel, u] = tens[u][t][k].cpu().numpy()
+                got[sel] = outs[3][t][k].cpu().numpy()
+            want = oracle.allreduce_sampled(vals, idx, nb, "avg", oracle.F32)
+            if ring:
+                assert_bit_exact(got, want, f"fusion batch {b}")
+            else:
+                assert_close_fast(got, want, np.abs(vals.astype(np.float64)).sum(axis=1), W,
+                                  "avg", f"fusion batch {b}")
+        for t in range(0, len(counts), 17):
+            for u in range(1, W):
+                assert torch.equal(outs[u][t], outs[0][t])
+
+
+# ----------------------------------------------------------- size sweep
+
+SWEEP_BYTES = [1 << 10, 1 << 12, 1 << 15, 1 << 16, 1 << 20, 1 << 24, 1 << 28]
+
+
+@pytest.mark.parametrize("W", [2, 4, 8, 16])
+@pytest.mark.parametrize("nbytes", SWEEP_BYTES)
+def test_sweep(v, W, nbytes):
+    n = nbytes // 4
+    ins = I.rank_buffers("uniform", W, n, I.SWEEP, "cuda")
+    full = n * W <= (1 << 22)
+    ins_np = [to_np(t) for t in ins] if full else None
+    for op in ("sum", "max"):
+        ar = v.allreduce(ins, op=op)
+        rs = v.reduce_scatter(ins, op=op)
+        all_ranks_equal(ar)
+        if full:
+            want = oracle.allreduce(ins_np, op, oracle.F32)
+            s = sum(np.abs(a.astype(np.float64)) for a in ins_np)
+            assert_close_fast(to_np(ar[0]), want[0], s, W, op, f"sweep AR {op}")
+            assert_close_fast(to_np(torch.cat(rs)), want[0], s, W, op, f"sweep RS {op}")
+        else:
+            sampled_allreduce_check(ins, ar, n, W, op, False, 7, m=20_000)
+            sampled_allreduce_check(ins, [torch.cat(rs)], n, W, op, False, 8, m=20_000)
+    segs = v.reduce_scatter(ins, op="sum", ring_order=True)
+    ag = v.allgather(segs, n)
+    ring = v.allreduce(ins, op="sum", ring_order=True)
+    for o in ag:
+        assert torch.equal(o.view(torch.int32), ring[0].view(torch.int32))
+
+
+def test_sweep_largest_point(v):
+    # 1 GiB per rank, W = 16: 16 GiB in and 16 GiB out
+    W, n = 16, (1 << 30) // 4
+    ins = I.rank_buffers("uniform", W, n, I.SWEEP, "cuda")
+    ar = v.allreduce(ins, op="sum")
+    sampled_allreduce_check(ins, ar, n, W, "sum", False, 9, m=20_000)
+    del ar
+    rs = v.reduce_scatter(ins, op="max")
+    sampled_allreduce_check(ins, [torch.cat(rs)], n, W, "max", False, 10, m=20_000)

@@ -1,0 +1,298 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded bytes.
+
+Ring order, max and allgather must be bit-exact; the fastest order must stay
+within the tolerance derived in tests/parity.py.  Sizes span several tiles
+and ragged tails; edge cases cover n = 0, n < W, W = 1, uneven segments,
+misaligned pointers (shared and mixed 16-byte phases), in-place forms, guard
+bands around every output, and non-default streams.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import abs_sum, assert_bit_exact, assert_close_fast, to_np
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+ODT = {"f32": oracle.F32, "bf16": oracle.BF16}
+
+
+@pytest.fixture(scope="module")
+def v():
+    from collective_reduction_virtual_gb300 import build
+    build.build()
+    import collective_reduction_virtual_gb300 as vc
+    return vc
+
+
+def make_inputs(W, n, dtype, seed, dev="cuda", kind="normal"):
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    outs = []
+    for _ in range(W):
+        if kind == "normal":
+            x = torch.randn(n, generator=g, device=dev) * (10.0 ** torch.randint(
+                -3, 4, (n,), generator=g, device=dev).float())
+        else:
+            x = torch.rand(n, generator=g, device=dev) * 2 - 1
+        outs.append(x.to(DT[dtype]))
+    return outs
+
+
+SMALL_W = [1, 2, 3, 4, 5, 8, 16, 64]
+SMALL_N = [0, 1, 3, 17, 4099, 65541]
+
+
+@pytest.mark.parametrize("W", SMALL_W)
+@pytest.mark.parametrize("n", SMALL_N)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_allreduce_small(v, W, n, dtype):
+    ins = make_inputs(W, n, dtype, 1000 * W + n)
+    ins_np = [to_np(t) for t in ins]
+    for op in ("sum", "max", "avg"):
+        want = oracle.allreduce(ins_np, op, ODT[dtype])
+        for ring in (True, False):
+            outs = v.allreduce(ins, op=op, ring_order=ring)
+            got = [to_np(t) for t in outs]
+            if ring or op == "max":
+                for u in range(W):
+                    assert_bit_exact(got[u], want[u], f"AR {op} ring={ring} W={W} n={n}")
+            else:
+                s = abs_sum(ins_np)
+                for u in range(W):
+                    assert_close_fast(got[u], want[u], s, W, op, f"AR {op} W={W} n={n}")
+            for u in range(1, W):  # every rank holds the same bits
+                assert got[u].tobytes() == got[0].tobytes()
+
+
+@pytest.mark.parametrize("W", SMALL_W)
+@pytest.mark.parametrize("n", SMALL_N)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_reduce_scatter_small(v, W, n, dtype):
+    ins = make_inputs(W, n, dtype, 2000 * W + n)
+    ins_np = [to_np(t) for t in ins]
+    s = abs_sum(ins_np)
+    for op in ("sum", "max", "avg"):
+        want = oracle.reduce_scatter(ins_np, op, ODT[dtype])
+        for ring in (True, False):
+            outs = v.reduce_scatter(ins, op=op, ring_order=ring)
+            for j in range(W):
+                off, ln = oracle.segment(n, W, j)
+                g = to_np(outs[j])
+                assert g.size == ln
+                if ring or op == "max":
+                    assert_bit_exact(g, want[j], f"RS {op} ring={ring} W={W} n={n} seg {j}")
+                else:
+                    assert_close_fast(g, want[j], s[off:off + ln], W, op, f"RS {op} W={W} n={n}")
+
+
+@pytest.mark.parametrize("W", SMALL_W)
+@pytest.mark.parametrize("n", SMALL_N)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_allgather_small(v, W, n, dtype):
+    segs = [make_inputs(1, oracle.segment(n, W, j)[1], dtype, 3000 * W + n + j)[0]
+            for j in range(W)]
+    want = oracle.allgather([to_np(s) for s in segs], n, ODT[dtype])
+    outs = v.allgather(segs, n)
+    for u in range(W):
+        assert_bit_exact(to_np(outs[u]), want[u], f"AG W={W} n={n} rank {u}")
+
+
+def test_ring_order_is_observable_on_gpu(v):
+    # the hand-derived example: ring order gives 0 1 0 1, and the library's
+    # ring mode must reproduce it exactly
+    x = [torch.full((4,), val, device="cuda") for val in (1e8, 1.0, -1e8, 1.0)]
+    outs = v.reduce_scatter(x, op="sum", ring_order=True)
+    assert [float(o[0]) for o in outs] == [0.0, 1.0, 0.0, 1.0]
+    ar = v.allreduce(x, op="sum", ring_order=True)
+    assert all(o.tolist() == [0.0, 1.0, 0.0, 1.0] for o in ar)
+
+
+# ------------------------------------------------------- alignment & layout
+
+def _views(W, n, dtype, shifts, seed):
+    """W tensors of n elements placed at the given element shifts inside
+    larger allocations (to control 16-byte phases)."""
+    base = make_inputs(W, n + 16, dtype, seed)
+    return [b[s:s + n] for b, s in zip(base, shifts)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shift_kind", ["same", "mixed"])
+@pytest.mark.parametrize("W", [3, 4, 8])
+def test_misaligned_buffers(v, dtype, shift_kind, W):
+    n = 50_001
+    if shift_kind == "same":
+        shifts = [1] * W
+    else:
+        shifts = [(u * 3) % 8 for u in range(W)]
+    ins = _views(W, n, dtype, shifts, 77 + W)
+    ins_np = [to_np(t) for t in ins]
+    s = abs_sum(ins_np)
+    obase = [torch.empty(n + 16, dtype=DT[dtype], device="cuda") for _ in range(W)]
+    outs = [b[sh:sh + n] for b, sh in zip(obase, reversed(shifts))]
+    for op in ("sum", "avg", "max"):
+        want = oracle.allreduce(ins_np, op, ODT[dtype])
+        for ring in (True, False):
+            v.allreduce(ins, outs, op=op, ring_order=ring)
+            for u in range(W):
+                g = to_np(outs[u])
+                if ring or op == "max":
+                    assert_bit_exact(g, want[u], f"AR misaligned {shift_kind} {op}")
+                else:
+                    assert_close_fast(g, want[u], s, W, op, f"AR misaligned {shift_kind} {op}")
+        rs_want = oracle.reduce_scatter(ins_np, op, ODT[dtype])
+        rs_out = [b[1:1 + oracle.segment(n, W, j)[1]] for j, b in enumerate(obase)]
+        v.reduce_scatter(ins, rs_out, op=op, ring_order=True)
+        for j in range(W):
+            assert_bit_exact(to_np(rs_out[j]), rs_want[j], f"RS misaligned {shift_kind} {op}")
+    segs = [ins[j][:oracle.segment(n, W, j)[1]] for j in range(W)]
+    ag_want = oracle.allgather([to_np(t) for t in segs], n, ODT[dtype])
+    v.allgather(segs, n, outs)
+    for u in range(W):
+        assert_bit_exact(to_np(outs[u]), ag_want[u], f"AG misaligned {shift_kind}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_guard_bands_untouched(v, dtype):
+    W, n, G = 5, 12_345, 64
+    ins = make_inputs(W, n, dtype, 5)
+    fill = torch.tensor([-1], dtype=torch.int16 if dtype == "bf16" else torch.int32)
+    big = [torch.empty(n + 2 * G, dtype=DT[dtype], device="cuda") for _ in range(W)]
+    for b in big:
+        b.view(fill.dtype).fill_(-1)
+    for kind in ("ar", "rs", "ag"):
+        for b in big:
+            b.view(fill.dtype).fill_(-1)
+        if kind == "ar":
+            outs = [b[G:G + n] for b in big]
+            v.allreduce(ins, outs, op="sum")
+        elif kind == "rs":
+            outs = [b[G:G + oracle.segment(n, W, j)[1]] for j, b in enumerate(big)]
+            v.reduce_scatter(ins, outs, op="avg", ring_order=True)
+        else:
+            segs = [ins[j][:oracle.segment(n, W, j)[1]] for j in range(W)]
+            outs = [b[G:G + n] for b in big]
+            v.allgather(segs, n, outs)
+        torch.cuda.synchronize()
+        for b, o in zip(big, outs):
+            raw = b.view(fill.dtype).cpu()
+            end = G + o.numel()
+            assert bool((raw[:G] == -1).all()), f"{kind}: front guard written"
+            assert bool((raw[end:] == -1).all()), f"{kind}: back guard written"
+
+
+# ------------------------------------------------------------- in place
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("W", [2, 4, 7, 8, 16])
+def test_in_place(v, dtype, W):
+    n = 100_003
+    ins = make_inputs(W, n, dtype, 900 + W)
+    ins_np = [to_np(t) for t in ins]
+    want = oracle.allreduce(ins_np, "sum", ODT[dtype])
+    bufs = [t.clone() for t in ins]
+    v.allreduce(bufs, bufs, op="sum", ring_order=True)  # Horovod's in-place fusion allreduce
+    for u in range(W):
+        assert_bit_exact(to_np(bufs[u]), want[u], "AR in place")
+    # NCCL in-place reduce-scatter: out[j] = in[j] + off_j
+    bufs = [t.clone() for t in ins]
+    outs = []
+    for j in range(W):
+        off, ln = oracle.segment(n, W, j)
+        outs.append(bufs[j][off:off + ln])
+    rs_want = oracle.reduce_scatter(ins_np, "sum", ODT[dtype])
+    v.reduce_scatter(bufs, outs, op="sum", ring_order=True)
+    for j in range(W):
+        assert_bit_exact(to_np(outs[j]), rs_want[j], "RS in place")
+    # in-place allgather: segment j already sits at its place in out[j]
+    full = [torch.empty(n, dtype=DT[dtype], device="cuda") for _ in range(W)]
+    segs = []
+    for j in range(W):
+        off, ln = oracle.segment(n, W, j)
+        full[j][off:off + ln].copy_(outs[j])
+        segs.append(full[j][off:off + ln])
+    v.allgather(segs, n, full)
+    for u in range(W):
+        assert_bit_exact(to_np(full[u]), want[u], "AG in place")
+
+
+def test_non_default_stream(v):
+    W, n = 8, 1 << 20
+    ins = make_inputs(W, n, "f32", 31)
+    want = oracle.allreduce([to_np(t) for t in ins], "sum", oracle.F32)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        outs = [torch.empty_like(t) for t in ins]
+        v.allreduce(ins, outs, op="sum", ring_order=True, stream=s)
+    s.synchronize()
+    for u in range(W):
+        assert_bit_exact(to_np(outs[u]), want[u], "AR on side stream")
+
+
+def test_cuda_graph_capture(v):
+    # the small-message path is timed inside CUDA graphs: capture must work
+    W, n = 8, 4096
+    ins = make_inputs(W, n, "f32", 41)
+    outs = [torch.empty_like(t) for t in ins]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        v.allreduce(ins, outs, op="sum", ring_order=True, stream=s)  # warm the caches
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        v.allreduce(ins, outs, op="sum", ring_order=True, stream=s)
+    for o in outs:
+        o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    want = oracle.allreduce([to_np(t) for t in ins], "sum", oracle.F32)
+    for u in range(W):
+        assert_bit_exact(to_np(outs[u]), want[u], "AR graph replay")
+
+
+# ---------------------------------------------------------------- fusion
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fuse_pack_unpack(v, dtype):
+    W = 5
+    rng = np.random.default_rng(3)
+    counts = [int(c) for c in rng.integers(0, 5000, 150)] + [1, 2, 3, 0, 7]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    tens = [[torch.randn(c, generator=g, device="cuda").to(DT[dtype]) for c in counts]
+            for _ in range(W)]
+    total = sum(counts)
+    fused = [torch.empty(total + 3, dtype=DT[dtype], device="cuda")[1:1 + total]
+             for _ in range(W)]
+    v.fuse_pack(tens, fused)
+    want = oracle.fuse_pack([[to_np(t) for t in tens[u]] for u in range(W)], counts, W, ODT[dtype])
+    for u in range(W):
+        assert_bit_exact(to_np(fused[u]), want[u], f"pack rank {u}")
+    back = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+    v.fuse_unpack(fused, back)
+    for u in range(W):
+        for t in range(len(counts)):
+            assert to_np(back[u][t]).tobytes() == to_np(tens[u][t]).tobytes()
+
+
+def test_fusion_allreduce_small(v):
+    W = 8
+    counts = [1000, 3, 4097, 250, 1, 60, 12345, 7]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(9)
+    tens = [[torch.randn(c, generator=g, device="cuda") * 1e-3 for c in counts] for _ in range(W)]
+    thr = 4 * 5000
+    outs = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+    fused = [torch.empty(max(counts) + 5000, device="cuda") for _ in range(W)]
+    v.fusion_allreduce(tens, outs, fused, op="avg", ring_order=True, threshold_bytes=thr)
+    want = oracle.fusion_allreduce([[to_np(t) for t in tens[u]] for u in range(W)], counts, "avg",
+                                   oracle.F32, thr)
+    for u in range(W):
+        for t in range(len(counts)):
+            assert_bit_exact(to_np(outs[u][t]), want[u][t], f"fusion rank {u} tensor {t}")
