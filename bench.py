@@ -339,23 +339,24 @@ def e2e_measure(cfg, ins, outs, args, stream, world, dev):
 
 def cpu_baseline(cfg, seconds):
     """The CPU oracle (single-threaded ring simulation) on a bounded sample of
-    the same workload: W rank buffers of the first m elements."""
+    the same workload: W rank buffers of the first m elements, allreduced
+    repeatedly for about `seconds` of CPU time."""
     import oracle
     W = cfg["W"]
-    m = 1 << 16
+    m = min(cfg["n"], 1 << 22)
     xs = [I.gradient(m, I.rank_seed(cfg["workload"], u)).numpy() for u in range(W)]
     t = time.perf_counter()
     oracle.allreduce(xs, "sum", oracle.F32)
-    dt = time.perf_counter() - t
-    m = int(min(1 << 24, max(1 << 16, m * seconds / max(dt, 1e-6))))
-    xs = [I.gradient(m, I.rank_seed(cfg["workload"], u)).numpy() for u in range(W)]
+    one = time.perf_counter() - t
+    reps = max(1, int(round(seconds / max(one, 1e-6))))
     t = time.perf_counter()
-    oracle.allreduce(xs, "sum", oracle.F32)
+    for _ in range(reps):
+        oracle.allreduce(xs, "sum", oracle.F32)
     dt = time.perf_counter() - t
-    return {"value": round(2 * W * m * cfg["es"] / dt / 1e9, 3), "unit": "GB/s", "cores": 1,
+    return {"value": round(2 * W * m * cfg["es"] * reps / dt / 1e9, 3), "unit": "GB/s", "cores": 1,
             "kind": "oracle",
-            "sample": f"allreduce sum of W={W} fp32 buffers of the first {m} elements "
-                      f"({dt:.1f} s single-threaded)"}
+            "sample": f"{reps} allreduces (sum, ring order) of W={W} fp32 buffers holding the "
+                      f"first {m} elements of the workload ({dt:.1f} s on one host core)"}
 
 
 # ------------------------------------------------------------------ extras
@@ -377,6 +378,12 @@ def extras(args, stream, dev):
     out["ag_w8_f32_2^26"] = rate(lambda: vc.allgather(segs, n, outs), (1 + W) * n * 4)
     out["ar_ring_sum_w8_f32_2^26"] = rate(
         lambda: vc.allreduce(ins, outs, op="sum", ring_order=True), 2 * W * n * 4)
+    out["ar_sum_w8_f32_2^26_staged"] = rate(
+        lambda: vc.allreduce(ins, outs, op="sum", flags=vc.FLAG_STAGED), 2 * W * n * 4)
+    out["ar_sum_w8_f32_2^26_direct"] = rate(
+        lambda: vc.allreduce(ins, outs, op="sum", flags=vc.FLAG_DIRECT), 2 * W * n * 4)
+    out["rs_sum_w8_f32_2^26_staged"] = rate(
+        lambda: vc.reduce_scatter(ins, segs, op="sum", flags=vc.FLAG_STAGED), (W + 1) * n * 4)
     del ins, outs, segs
     torch.cuda.empty_cache()
 
@@ -387,6 +394,8 @@ def extras(args, stream, dev):
     out["ar_avg_w8_bf16_2^28"] = rate(lambda: vc.allreduce(ins, outs, op="avg"), 2 * W * n * 2)
     out["ar_ring_avg_w8_bf16_2^28"] = rate(
         lambda: vc.allreduce(ins, outs, op="avg", ring_order=True), 2 * W * n * 2)
+    out["ar_avg_w8_bf16_2^28_staged"] = rate(
+        lambda: vc.allreduce(ins, outs, op="avg", flags=vc.FLAG_STAGED), 2 * W * n * 2)
     del ins, outs
     torch.cuda.empty_cache()
 
@@ -394,8 +403,8 @@ def extras(args, stream, dev):
     W, n = 4, 1 << 20
     ins = I.rank_buffers("uniform", W, n, I.RS_W4, dev)
     segs = [torch.empty(vc.segment(n, W, j)[1], device=dev) for j in range(W)]
-    out["rs_sum_w4_f32_2^20_hot"] = rate(lambda: vc.reduce_scatter(ins, segs, op="sum"),
-                                         (W + 1) * n * 4, steps=50)
+    out["rs_sum_w4_f32_2^20_hot"] = graph_rate(
+        lambda s: vc.reduce_scatter(ins, segs, op="sum", stream=s), (W + 1) * n * 4, 200)
     flush = torch.empty(2 * L2_BYTES // 4, device=dev)
     times = []
     for i in range(13):
@@ -433,28 +442,37 @@ def extras(args, stream, dev):
             n = nbytes // 4
             ins = I.rank_buffers("uniform", W, n, I.SWEEP, dev)
             outs = [torch.empty_like(t) for t in ins]
-            s = torch.cuda.Stream()
-            s.wait_stream(torch.cuda.current_stream())
-            with torch.cuda.stream(s):
-                vc.allreduce(ins, outs, op="sum", stream=s)
-            s.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=s):
-                for _ in range(1000):
-                    vc.allreduce(ins, outs, op="sum", stream=s)
-            g.replay()
-            torch.cuda.synchronize()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            g.replay()
-            b.record()
-            torch.cuda.synchronize()
-            us = a.elapsed_time(b) * 1e3 / 1000
-            lat[f"ar_sum_W{W}_{nbytes}B"] = {"us": round(us, 2),
-                                             "GBps": round(2 * W * nbytes / us / 1e3, 2)}
-            del g, ins, outs
+            r = graph_rate(lambda s: vc.allreduce(ins, outs, op="sum", stream=s), 2 * W * nbytes,
+                           1000)
+            lat[f"ar_sum_W{W}_{nbytes}B"] = {"us": round(r["ms"] * 1e3, 2), "GBps": r["GBps"]}
+            del ins, outs
     out["small_message_graph_1000"] = lat
     return out
+
+
+def graph_rate(launch, nbytes, reps):
+    """Device time per launch of `reps` launches captured in one CUDA graph
+    (no host launch overhead between them)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        launch(s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(reps):
+            launch(s)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    per = a.elapsed_time(b) / 1e3 / reps
+    del g
+    return {"GBps": round(nbytes / per / 1e9, 2), "ms": round(per * 1e3, 5),
+            "timing": f"CUDA graph of {reps} launches"}
 
 
 # ------------------------------------------------------------- reference arm

@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
             L.vcoll_last_error.restype = ctypes.c_char_p
             L.vcoll_version.argtypes = []
             L.vcoll_version.restype = I
+            L.vcoll_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
+            L.vcoll_device_errors.restype = I
             _lib = L
     return _lib
 
@@ -97,6 +99,23 @@ def status_string(status: int) -> str:
 
 def version() -> int:
     return lib().vcoll_version()
+
+
+DEVICE_ERR_TIMEOUT = 0x1
+
+
+def vcoll_device_errors(clear: bool = False):
+    """Returns (status, flags): the current device's error word
+    (DEVICE_ERR_* bits raised by kernels); synchronises the device."""
+    f = ctypes.c_uint()
+    rc = lib().vcoll_device_errors(ctypes.byref(f), 1 if clear else 0)
+    return rc, f.value
+
+
+def device_errors(clear: bool = False) -> int:
+    rc, f = vcoll_device_errors(clear)
+    _check(rc)
+    return f
 
 
 # ----------------------------------------------------------- raw C ABI layer

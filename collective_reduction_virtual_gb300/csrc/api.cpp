@@ -268,11 +268,16 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   const int threads = small ? 128 : 256;
   const int V = vec ? 16 / es : 1;
 
-  if (flags & VCOLL_FLAG_STAGED)
-    return fail(VCOLL_ERR_UNSUPPORTED, "the staged variant is not built in this library");
-
-  const void* fn = dtype == VCOLL_F32 ? reduce_kernel_f32(op, kind, W_t, ring, vec)
-                                      : reduce_kernel_bf16(op, kind, W_t, ring, vec);
+  // The staged (TMA bulk copy) variant needs the 16-byte vector layout and a
+  // compile-time W; everything else runs the direct kernels (same bits).
+  const bool staged = (flags & VCOLL_FLAG_STAGED) && vec && W_t != 0 && !small;
+  const void* fn;
+  if (staged)
+    fn = dtype == VCOLL_F32 ? staged_kernel_f32(op, kind, W_t, ring)
+                            : staged_kernel_bf16(op, kind, W_t, ring);
+  else
+    fn = dtype == VCOLL_F32 ? reduce_kernel_f32(op, kind, W_t, ring, vec)
+                            : reduce_kernel_bf16(op, kind, W_t, ring, vec);
   ReduceParams prm;
   memset(&prm, 0, sizeof(prm));
   for (int u = 0; u < W; ++u) {
@@ -288,9 +293,15 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   prm.ring = ring ? 1 : 0;
   prm.scale = op == VCOLL_AVG ? 1.0f / (float)W : 1.0f;
   prm.do_scale = op == VCOLL_AVG ? 1 : 0;
-  prm.tile_elems = vec ? (int64_t)threads * unroll_for(W_t) * V : (int64_t)threads * 4;
+  if (staged)
+    prm.tile_elems = staged_slice_bytes(W_t) / es;
+  else
+    prm.tile_elems = vec ? (int64_t)threads * unroll_for(W_t) * V : (int64_t)threads * 4;
   prm.tiles_per_seg = tiles_per_segment(n, W, nseg, V, phase, prm.tile_elems);
   prm.num_tiles = prm.tiles_per_seg * nseg;
+  if (staged)
+    return launch(fn, prm.num_tiles, kStagedThreads, (size_t)staged_smem_bytes(W_t), false, &prm,
+                  stream);
   return launch(fn, prm.num_tiles, threads, 0, small, &prm, stream);
 }
 
@@ -452,6 +463,22 @@ int vcoll_fuse_pack(const void* const* tensors, const int64_t* counts, int T, vo
 int vcoll_fuse_unpack(const void* const* fused, const int64_t* counts, int T,
                       void* const* tensors, int W, int dtype, void* stream) {
   return fuse_common((const void* const*)tensors, counts, T, fused, W, dtype, 1, stream);
+}
+
+int vcoll_device_errors(unsigned* flags, int clear) {
+  g_err[0] = 0;
+  if (!flags) return fail(VCOLL_ERR_INVALID_ARG, "flags is NULL");
+  unsigned int* sym = device_error_symbol();
+  if (!sym) return fail(VCOLL_ERR_CUDA, "cannot resolve the device error word");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  e = cudaMemcpy(flags, sym, sizeof(unsigned), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
+  if (clear) {
+    e = cudaMemset(sym, 0, sizeof(unsigned));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+  }
+  return VCOLL_OK;
 }
 
 int vcoll_segment(int64_t n, int W, int j, int64_t* off, int64_t* len) {

@@ -1,0 +1,224 @@
+// Staged reduce-scatter / allreduce: the W input slices of each tile travel
+// HBM -> shared memory by bulk asynchronous copies (TMA, cp.async.bulk, no
+// multicast), through a ring of kStagedStages stages guarded by mbarriers.
+//
+// One producer warp (one elected lane) issues, per tile, W bulk copies of one
+// rank's slice each -- placed in fold order (ring: rank (j+1) mod W first) --
+// and arms the stage's "full" barrier with the expected byte count.  Eight
+// consumer warps wait on "full", fold the W slices from shared memory in fp32
+// (same fold and rounding as the direct kernels, so the bits are identical),
+// apply the avg scale and the output cast, store to global memory, and
+// release the stage on its "empty" barrier.  Up to kStagedStages * 32 KB of
+// input is in flight per SM without holding it in registers.
+//
+// Every wait is bounded: after kSpinLimit unsuccessful polls the waiting
+// thread records VCOLL_DEVICE_ERR_TIMEOUT in g_vcoll_device_error and the CTA
+// stops issuing work; the producer then waits, again bounded, for the copies
+// it has already issued before it returns.
+#include "device_common.cuh"
+#include "reduce_kernels.cuh"
+#include "vcoll_internal.h"
+
+namespace vcoll {
+
+__device__ unsigned int g_vcoll_device_error = 0;
+
+namespace {
+
+constexpr unsigned kSpinLimit = 1u << 24;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait for the phase with the given parity; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
+  for (unsigned i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  atomicOr(&g_vcoll_device_error, (unsigned)VCOLL_DEVICE_ERR_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, unsigned bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+}  // namespace
+
+template <typename T, int WT, class Op, int KIND, int RING>
+__global__ void __launch_bounds__(kStagedThreads, 1)
+    vc_reduce_staged(const __grid_constant__ ReduceParams p) {
+  using E = Elem<T>;
+  constexpr int V = E::kVec;
+  constexpr int SLICE = staged_slice_bytes(WT);
+  constexpr int STAGE = WT * SLICE;
+  constexpr int S = kStagedStages;
+  constexpr int TREE_W = RING ? 0 : WT;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
+  uint64_t* empty = full + S;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kStagedConsumerWarps);
+    }
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == kStagedConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++issued) {
+        const int s = issued % S;
+        if (issued >= S && !mbar_wait(&empty[s], ((issued / S) - 1) & 1)) {
+          abort_flag = 1;
+          break;
+        }
+        if (abort_flag) break;
+        const TileRange tr = tile_range<V>(p, tile);
+        const int64_t n_el = tr.e1 > tr.e0 ? tr.e1 - tr.e0 : 0;
+        const unsigned bytes = (unsigned)(n_el * E::kBytes);
+        mbar_arrive_expect_tx(&full[s], bytes * WT);
+        if (bytes) {
+          const int start = RING ? rotate(tr.j, 1, WT) : 0;
+          unsigned char* st = smem + s * STAGE;
+#pragma unroll
+          for (int t = 0; t < WT; ++t) {
+            const int src = RING ? rotate(start, t, WT) : t;
+            bulk_load(st + t * SLICE, (const char*)p.in[src] + tr.e0 * E::kBytes, bytes, &full[s]);
+          }
+        }
+      }
+      // wait (bounded) until every copy this CTA issued has landed
+      for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i)
+        mbar_wait(&full[i % S], (i / S) & 1);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  int it = 0;
+  for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+    const int s = it % S;
+    if (!mbar_wait(&full[s], (it / S) & 1)) {
+      abort_flag = 1;
+      break;
+    }
+    const TileRange tr = tile_range<V>(p, tile);
+    const int start = RING ? rotate(tr.j, 1, WT) : 0;
+    const int64_t nvec = tr.e1 > tr.e0 ? (tr.e1 - tr.e0) / V : 0;
+    const unsigned char* st = smem + s * STAGE;
+    for (int64_t vi = tid; vi < nvec; vi += kStagedConsumerWarps * 32) {
+      uint4 v[WT];
+#pragma unroll
+      for (int t = 0; t < WT; ++t)
+        v[t] = *reinterpret_cast<const uint4*>(st + t * SLICE + vi * 16);
+      float acc[V];
+      if (RING)
+        left_fold<T, Op, WT>(v, acc);
+      else
+        TreeFold<T, Op, WT, 0, WT>::run(v, acc);
+      if (p.do_scale) {
+#pragma unroll
+        for (int x = 0; x < V; ++x) acc[x] = __fmul_rn(acc[x], p.scale);
+      }
+      const uint4 o = E::narrow(acc);
+      const int64_t e = tr.e0 + vi * V;
+      if (KIND == KIND_AR) {
+#pragma unroll
+        for (int r = 0; r < WT; ++r) st_stream((char*)p.out[r] + e * E::kBytes, o);
+      } else {
+        st_stream((char*)p.out[tr.j] + (e - tr.a) * E::kBytes, o);
+      }
+    }
+    if (tr.first) head_tail<T, Op, KIND, TREE_W>(p, tr, WT, start);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (abort_flag) break;
+  }
+}
+
+namespace {
+template <typename T, class Op, int KIND>
+const void* pick_staged(int W_t, int ring) {
+  switch (W_t) {
+    case 2:
+      return (const void*)&vc_reduce_staged<T, 2, Op, KIND, 0>;
+    case 4:
+      return ring ? (const void*)&vc_reduce_staged<T, 4, Op, KIND, 1>
+                  : (const void*)&vc_reduce_staged<T, 4, Op, KIND, 0>;
+    case 8:
+      return ring ? (const void*)&vc_reduce_staged<T, 8, Op, KIND, 1>
+                  : (const void*)&vc_reduce_staged<T, 8, Op, KIND, 0>;
+    case 16:
+      return ring ? (const void*)&vc_reduce_staged<T, 16, Op, KIND, 1>
+                  : (const void*)&vc_reduce_staged<T, 16, Op, KIND, 0>;
+    default:
+      return nullptr;
+  }
+}
+
+template <typename T>
+const void* staged_table(int op, int kind, int W_t, int ring) {
+  if (op == VCOLL_MAX)  // order-independent: the tree instantiation serves both orders
+    return kind == KIND_AR ? pick_staged<T, OpMax, KIND_AR>(W_t, 0)
+                           : pick_staged<T, OpMax, KIND_RS>(W_t, 0);
+  return kind == KIND_AR ? pick_staged<T, OpSum, KIND_AR>(W_t, ring)
+                         : pick_staged<T, OpSum, KIND_RS>(W_t, ring);
+}
+}  // namespace
+
+const void* staged_kernel_f32(int op, int kind, int W_t, int ring) {
+  return staged_table<float>(op, kind, W_t, ring);
+}
+const void* staged_kernel_bf16(int op, int kind, int W_t, int ring) {
+  return staged_table<__nv_bfloat16>(op, kind, W_t, ring);
+}
+
+unsigned int* device_error_symbol() {
+  unsigned int* p = nullptr;
+  if (cudaGetSymbolAddress((void**)&p, g_vcoll_device_error) != cudaSuccess) return nullptr;
+  return p;
+}
+
+}  // namespace vcoll

@@ -86,6 +86,8 @@ const void* reduce_kernel_bf16(int op, int kind, int W_t, int ring, int vec);
 const void* staged_kernel_f32(int op, int kind, int W_t, int ring);
 const void* staged_kernel_bf16(int op, int kind, int W_t, int ring);
 const void* gather_kernel(int elem_size, int vec);
+// Device address of the per-device error word (VCOLL_DEVICE_ERR_* bits).
+unsigned int* device_error_symbol();
 const void* fuse_kernel(int elem_size);
 
 // Vectors (16 B) per thread per tile of the direct kernels, by W_t.

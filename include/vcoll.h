@@ -141,6 +141,16 @@ int vcoll_fuse_pack(const void* const* tensors, const int64_t* counts, int T, vo
 int vcoll_fuse_unpack(const void* const* fused, const int64_t* counts, int T,
                       void* const* tensors, int W, int dtype, void* stream);
 
+/* Device-side error bits, OR-ed into one word per device by the kernels.
+ * The staged kernels bound every wait on their shared-memory barriers; a wait
+ * that gives up records VCOLL_DEVICE_ERR_TIMEOUT and the kernel returns early
+ * (its outputs are then incomplete). */
+#define VCOLL_DEVICE_ERR_TIMEOUT 0x1u
+
+/* Reads the current device's error word into *flags (and resets it when
+ * clear != 0).  Synchronous: waits for all work on the device to finish. */
+int vcoll_device_errors(unsigned* flags, int clear);
+
 /* Segment j of an n-element buffer over W ranks (host only). */
 int vcoll_segment(int64_t n, int W, int j, int64_t* off, int64_t* len);
 

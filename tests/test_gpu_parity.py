@@ -296,3 +296,39 @@ def test_fusion_allreduce_small(v):
     for u in range(W):
         for t in range(len(counts)):
             assert_bit_exact(to_np(outs[u][t]), want[u][t], f"fusion rank {u} tensor {t}")
+
+
+# ------------------------------------------------- staged (TMA) variant
+
+@pytest.mark.parametrize("W", [2, 4, 8, 16])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("n", [40_000, 1_000_003, (1 << 22) + 12])
+def test_staged_matches_direct_and_oracle(v, W, dtype, n):
+    ins = make_inputs(W, n, dtype, 5000 * W + n)
+    ins_np = [to_np(t) for t in ins]
+    assert v.device_errors(clear=True) == 0
+    for op in ("sum", "avg", "max"):
+        want = oracle.allreduce(ins_np, op, ODT[dtype])
+        for ring in (True, False):
+            d = v.allreduce(ins, op=op, ring_order=ring, flags=v.FLAG_DIRECT)
+            s = v.allreduce(ins, op=op, ring_order=ring, flags=v.FLAG_STAGED)
+            for u in range(W):
+                assert to_np(s[u]).tobytes() == to_np(d[u]).tobytes(), f"AR staged {op} {ring}"
+            if ring or op == "max":
+                assert_bit_exact(to_np(s[0]), want[0], f"AR staged {op}")
+            rs_d = v.reduce_scatter(ins, op=op, ring_order=ring, flags=v.FLAG_DIRECT)
+            rs_s = v.reduce_scatter(ins, op=op, ring_order=ring, flags=v.FLAG_STAGED)
+            for j in range(W):
+                assert to_np(rs_s[j]).tobytes() == to_np(rs_d[j]).tobytes(), f"RS staged {op}"
+    assert v.device_errors(clear=True) == 0
+
+
+def test_staged_in_place_and_phase(v):
+    W, n = 8, 3_000_001
+    base = make_inputs(W, n + 8, "f32", 71)
+    ins = [b[2:2 + n] for b in base]  # shared non-zero 16-byte phase
+    want = oracle.allreduce([to_np(t) for t in ins], "sum", oracle.F32)
+    v.allreduce(ins, ins, op="sum", ring_order=True, flags=v.FLAG_STAGED)
+    for u in range(W):
+        assert_bit_exact(to_np(ins[u]), want[u], "staged in place")
+    assert v.device_errors(clear=True) == 0
