@@ -273,8 +273,10 @@ def run_vcoll(args):
     outs = [torch.empty_like(t) for t in ins]
     alg_bytes = 2 * W * n * es
 
+    vflags = {"auto": 0, "direct": vc.FLAG_DIRECT, "staged": vc.FLAG_STAGED}[args.variant]
+
     def step():
-        vc.allreduce(ins, outs, op="sum")
+        vc.allreduce(ins, outs, op="sum", flags=vflags)
 
     with ClockSampler() as clocks:
         total, per_launch = timed_steps(step, args.steps, args.warmup, stream)
@@ -291,6 +293,7 @@ def run_vcoll(args):
         "data": "synthetic (seeded normal(0,1e-3) gradients generated on the GPU)",
         "config": {"workload": cfg["name"], "op": "allreduce", "reduction": "sum", "W": W,
                    "n_per_rank": n, "elem": "fp32", "order": "fastest (pairwise tree)",
+                   "variant": args.variant,
                    "bytes_per_step": alg_bytes, "parallelism": f"replicas{world}",
                    "l2": "inputs (2 GiB) larger than L2; no flush"},
         "pct_of_peak": {"measured_copy_peak": round(100 * achieved / peak, 1),
@@ -518,6 +521,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["vcoll", "reference"], default="vcoll")
     ap.add_argument("--n", type=int, default=None, help="elements per rank (default 2^26)")
+    ap.add_argument("--variant", choices=["auto", "direct", "staged"], default="auto",
+                    help="kernel variant of the timed step (identical bits)")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

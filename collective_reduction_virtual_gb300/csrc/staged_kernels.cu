@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
   uint64_t* empty = full + S;
-  __shared__ int abort_flag;
+  __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
