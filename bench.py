@@ -259,6 +259,68 @@ def ar_w8_f32(n_override=None):
                 es=4)
 
 
+def build_workload(args, dev, rank):
+    """The timed step for --op (default: the W=8 fp32 2^26 allreduce).
+    Returns a dict with the step function, its algorithmic bytes and the
+    device buffers that the end-to-end measurement copies in and out."""
+    vflags = {"auto": 0, "direct": vc.FLAG_DIRECT, "staged": vc.FLAG_STAGED}[args.variant]
+    ring = args.order == "ring"
+    red = args.reduction
+    dt = torch.bfloat16 if args.dtype == "bf16" else torch.float32
+    es = 2 if args.dtype == "bf16" else 4
+    seed_off = 100_000 * rank  # every replica draws its own inputs
+    if args.op in ("fusion", "multi"):
+        W = args.W or 8
+        counts = [int(c) for c in I.fusion_counts()]
+        g = torch.Generator(device=dev)
+        tens = []
+        for u in range(W):
+            g.manual_seed(I.rank_seed(I.FUSION_W8, u) + seed_off)
+            tens.append([torch.randn(c, generator=g, device=dev).mul_(1e-3).to(dt) for c in counts])
+        outs = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+        B = sum(counts) * es
+        if args.op == "fusion":
+            fused = [torch.empty((64 << 20) // es, dtype=dt, device=dev) for _ in range(W)]
+            step = lambda: vc.fusion_allreduce(tens, outs, fused, op=red, ring_order=ring)  # noqa
+            nb = len(vc.fuse_plan(counts, 0 if es == 4 else 1)) - 1
+            bytes_, launches = 6 * W * B, 3 * nb
+            desc = "pack + in-place allreduce + unpack per 64 MiB batch (6*W*B)"
+        else:
+            step = lambda: vc.fusion_allreduce_direct(tens, outs, op=red, ring_order=ring)  # noqa
+            nb = len(vc.fuse_plan(counts, 0 if es == 4 else 1)) - 1
+            bytes_, launches = 2 * W * B, nb
+            desc = "one pass per 64 MiB batch straight from the tensors (2*W*B)"
+        return dict(name=f"tensor-fusion allreduce {red}, W={W}, 200 {args.dtype} tensors per "
+                         f"rank (log-uniform 1024..4194304 elements), {desc}",
+                    W=W, n=sum(counts), step=step, bytes=bytes_, launches=launches,
+                    ins=[t for row in tens for t in row], outs=[t for row in outs for t in row],
+                    es=es, reduction=red, dtype=args.dtype)
+    W = args.W or 8
+    n = args.n or (1 << 26)
+    kind = "outliers" if args.dtype == "bf16" else ("gradient" if W == 8 else "uniform")
+    make = {"uniform": I.uniform, "gradient": I.gradient, "outliers": I.outliers}[kind]
+    wl = {"gradient": I.AR_W8_F32, "outliers": I.AR_W8_BF16, "uniform": I.SWEEP}[kind]
+    ins = [make(n, I.rank_seed(wl, u) + seed_off, dev) for u in range(W)]
+    if args.op == "allreduce":
+        outs = [torch.empty_like(t) for t in ins]
+        step = lambda: vc.allreduce(ins, outs, op=red, ring_order=ring, flags=vflags)  # noqa
+        bytes_ = 2 * W * n * es
+    elif args.op == "reduce_scatter":
+        outs = [torch.empty(vc.segment(n, W, j)[1], dtype=dt, device=dev) for j in range(W)]
+        step = lambda: vc.reduce_scatter(ins, outs, op=red, ring_order=ring, flags=vflags)  # noqa
+        bytes_ = (W + 1) * n * es
+    else:  # allgather: the inputs are the W segments
+        ins = [t[:vc.segment(n, W, j)[1]].clone() for j, t in enumerate(ins)]
+        outs = [torch.empty(n, dtype=dt, device=dev) for _ in range(W)]
+        step = lambda: vc.allgather(ins, n, outs)  # noqa
+        bytes_ = (1 + W) * n * es
+    dist_name = {"gradient": "normal(0,1e-3)", "uniform": "uniform[-1,1]",
+                 "outliers": "normal(0,1e-2) with 1% outliers x100"}[kind]
+    return dict(name=f"{args.op} {red}, W={W} virtual ranks, {args.dtype}, n={n} per rank, "
+                     f"{dist_name}", W=W, n=n, step=step, bytes=bytes_, launches=1, ins=ins,
+                outs=outs, es=es, reduction=red, dtype=args.dtype)
+
+
 def run_vcoll(args):
     world, rank = init_dist("nccl" if int(os.environ.get("WORLD_SIZE", "1")) > 1 else "gloo")
     _, _, local = dist_env()
@@ -266,50 +328,50 @@ def run_vcoll(args):
     dev = torch.device("cuda", local)
     vc.lib()
     stream = torch.cuda.current_stream()
-    cfg = ar_w8_f32(args.n)
-    W, n, es = cfg["W"], cfg["n"], cfg["es"]
-    # every replica draws its own inputs (seed offset by the process rank)
-    ins = [I.gradient(n, I.rank_seed(cfg["workload"], u) + 100_000 * rank, dev) for u in range(W)]
-    outs = [torch.empty_like(t) for t in ins]
-    alg_bytes = 2 * W * n * es
-
-    vflags = {"auto": 0, "direct": vc.FLAG_DIRECT, "staged": vc.FLAG_STAGED}[args.variant]
-
-    def step():
-        vc.allreduce(ins, outs, op="sum", flags=vflags)
+    wl = build_workload(args, dev, rank)
+    W, n, alg_bytes = wl["W"], wl["n"], wl["bytes"]
 
     with ClockSampler() as clocks:
-        total, per_launch = timed_steps(step, args.steps, args.warmup, stream)
+        total, per_step = timed_steps(wl["step"], args.steps, args.warmup, stream)
     total_max = max_over_ranks(total, dev if world > 1 else "cpu")
     value = aggregate_gbs(alg_bytes, args.steps, world, total_max)
-    achieved = alg_bytes / per_launch / 1e9
+    achieved = alg_bytes / per_step / 1e9
     peak, peak_src = measured_peaks()
-    kernel_key = "vc_reduce_vec<float,8,OpSum,AR,tree> W=8 n=2^26"
+    default = args.op == "allreduce" and W == 8 and n == (1 << 26) and args.dtype == "f32"
+    kernel_key = None
+    if default and wl["reduction"] == "sum" and args.order == "fast":
+        kernel_key = ("vc_reduce_staged<float,8,OpSum,AR,tree> W=8 n=2^26"
+                      if args.variant == "staged" else
+                      "vc_reduce_vec<float,8,OpSum,AR,tree> W=8 n=2^26")
+    big = W * n * wl["es"] > 2 * L2_BYTES
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_max / args.steps * 1e3, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded normal(0,1e-3) gradients generated on the GPU)",
-        "config": {"workload": cfg["name"], "op": "allreduce", "reduction": "sum", "W": W,
-                   "n_per_rank": n, "elem": "fp32", "order": "fastest (pairwise tree)",
-                   "variant": args.variant,
-                   "bytes_per_step": alg_bytes, "parallelism": f"replicas{world}",
-                   "l2": "inputs (2 GiB) larger than L2; no flush"},
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
+        "data": "synthetic (seeded, generated on the GPU)",
+        "config": {"workload": wl["name"], "op": args.op, "reduction": wl["reduction"], "W": W,
+                   "n_per_rank": n, "elem": args.dtype,
+                   "order": "ring" if args.order == "ring" else "fastest (pairwise tree)",
+                   "variant": args.variant, "bytes_per_step": alg_bytes,
+                   "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2; no flush" if big else
+                         "inputs fit in L2: number is L2-warm"},
         "pct_of_peak": {"measured_copy_peak": round(100 * achieved / peak, 1),
                         "nominal_8000": round(100 * achieved / NOMINAL_HBM_GBS, 1)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": committed_traffic(kernel_key), "kernel": kernel_key,
-                     "algorithmic_bytes_per_launch": alg_bytes},
-        "gpu_launches": args.steps,
+                     "traffic": committed_traffic(kernel_key) if kernel_key else None,
+                     "kernel": kernel_key or args.op,
+                     "algorithmic_bytes_per_launch": alg_bytes // wl["launches"]},
+        "gpu_launches": args.steps * wl["launches"],
         "clocks": clocks.summary(),
     }
     if not args.no_e2e:
-        line["e2e"] = e2e_measure(cfg, ins, outs, args, stream, world, dev)
-    if rank == 0 and world == 1 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
-    if not args.no_extras:
+        line["e2e"] = e2e_measure(wl, args, stream, world, dev)
+    if rank == 0 and world == 1 and not args.no_cpu and default:
+        line["cpu_baseline"] = cpu_baseline(ar_w8_f32(), args.cpu_seconds)
+    if not args.no_extras and default:
         line["ops"] = extras(args, stream, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -318,26 +380,26 @@ def run_vcoll(args):
         dist.destroy_process_group()
 
 
-def e2e_measure(cfg, ins, outs, args, stream, world, dev):
+def e2e_measure(wl, args, stream, world, dev):
     """Host buffers in, host buffers out: pinned H2D of every input, the
-    allreduce, D2H of every output, all inside the timed region."""
-    W, n, es = cfg["W"], cfg["n"], cfg["es"]
-    h_in = [t.cpu().pin_memory() for t in ins]
-    h_out = [torch.empty(n, dtype=cfg["dtype"], pin_memory=True) for _ in range(W)]
+    collective, D2H of every output, all inside the timed region."""
+    h_in = [t.cpu().pin_memory() for t in wl["ins"]]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wl["outs"]]
     steps = max(1, min(args.steps, 10))
 
     def step():
-        for d, h in zip(ins, h_in):
+        for d, h in zip(wl["ins"], h_in):
             d.copy_(h, non_blocking=True)
-        vc.allreduce(ins, outs, op="sum")
-        for h, d in zip(h_out, outs):
+        wl["step"]()
+        for h, d in zip(h_out, wl["outs"]):
             h.copy_(d, non_blocking=True)
 
     total, _ = timed_steps(step, steps, max(1, min(args.warmup, 2)), stream, per_launch=False)
     total = max_over_ranks(total, dev if world > 1 else "cpu")
-    bi = W * n * es
-    return {"value": round(aggregate_gbs(2 * W * n * es, steps, world, total), 1), "unit": "GB/s",
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bi, "steps": steps}
+    bi = sum(t.numel() * t.element_size() for t in wl["ins"])
+    bo = sum(t.numel() * t.element_size() for t in wl["outs"])
+    return {"value": round(aggregate_gbs(wl["bytes"], steps, world, total), 1), "unit": "GB/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": steps}
 
 
 def cpu_baseline(cfg, seconds):
@@ -435,6 +497,10 @@ def extras(args, stream, dev):
     out["fusion_w8_200tensors"] = rate(
         lambda: vc.fusion_allreduce(tens, fouts, fused, op="avg"), 6 * W * tot, steps=5, warmup=2)
     out["fusion_w8_200tensors"]["bytes_formula"] = "6*W*B_total (pack + AR + unpack)"
+    out["fusion_w8_200tensors_direct"] = rate(
+        lambda: vc.fusion_allreduce_direct(tens, fouts, op="avg"), 2 * W * tot, steps=5, warmup=2)
+    out["fusion_w8_200tensors_direct"]["bytes_formula"] = \
+        "2*W*B_total (one pass, no fusion buffer); same bits as the pipeline"
     del tens, fouts, fused
     torch.cuda.empty_cache()
 
@@ -521,6 +587,12 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["vcoll", "reference"], default="vcoll")
     ap.add_argument("--n", type=int, default=None, help="elements per rank (default 2^26)")
+    ap.add_argument("--op", choices=["allreduce", "reduce_scatter", "allgather", "fusion", "multi"],
+                    default="allreduce")
+    ap.add_argument("--W", type=int, default=None, help="virtual ranks (default 8)")
+    ap.add_argument("--dtype", choices=["f32", "bf16"], default="f32")
+    ap.add_argument("--reduction", choices=["sum", "max", "avg"], default=None)
+    ap.add_argument("--order", choices=["fast", "ring"], default="fast")
     ap.add_argument("--variant", choices=["auto", "direct", "staged"], default="auto",
                     help="kernel variant of the timed step (identical bits)")
     ap.add_argument("--no-extras", action="store_true")
@@ -529,6 +601,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-elems", type=int, default=1 << 22)
     args = ap.parse_args(argv)
+    if args.reduction is None:
+        args.reduction = "avg" if args.op in ("fusion", "multi") else "sum"
     if args.warmup < 3 and args.impl == "vcoll":
         args.warmup = 3
     if args.impl == "reference":

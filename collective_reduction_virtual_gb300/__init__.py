@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
             L.vcoll_fuse_pack.restype = I
             L.vcoll_fuse_unpack.argtypes = [PP, I64P, I, PP, I, I, P]
             L.vcoll_fuse_unpack.restype = I
+            L.vcoll_allreduce_multi.argtypes = [PP, PP, I64P, I, I, I, I, U, P]
+            L.vcoll_allreduce_multi.restype = I
             L.vcoll_segment.argtypes = [I64, I, I, I64P, I64P]
             L.vcoll_segment.restype = I
             L.vcoll_status_string.argtypes = [I]
@@ -143,6 +145,11 @@ def vcoll_fuse_pack(tensor_ptrs, counts, T, fused_ptrs, W, dtype, stream=0) -> i
 def vcoll_fuse_unpack(fused_ptrs, counts, T, tensor_ptrs, W, dtype, stream=0) -> int:
     return lib().vcoll_fuse_unpack(_ptr_array(fused_ptrs), _i64_array(counts), T,
                                    _ptr_array(tensor_ptrs), W, dtype, stream or None)
+
+
+def vcoll_allreduce_multi(in_ptrs, out_ptrs, counts, T, W, dtype, op, flags=0, stream=0) -> int:
+    return lib().vcoll_allreduce_multi(_ptr_array(in_ptrs), _ptr_array(out_ptrs), _i64_array(counts),
+                                       T, W, dtype, op, flags, stream or None)
 
 
 def vcoll_fuse_plan(counts, dtype=F32, threshold_bytes=DEFAULT_FUSION_THRESHOLD):
@@ -276,6 +283,42 @@ def fuse_unpack(fused, tensors, stream=None):
     _check(vcoll_fuse_unpack([f.data_ptr() for f in fused], counts, T, [t.data_ptr() for t in flat],
                              W, _dtype_code(fused[0]), _stream_handle(stream)))
     return tensors
+
+
+def allreduce_multi(tensors, outs=None, op="sum", ring_order=False, stream=None, flags=0):
+    """tensors[u][t]: tensor t of rank u.  Allreduce of each rank's tensors
+    taken as one concatenated buffer, written to outs[u][t] (new tensors by
+    default; pass outs=tensors for in place).  One pass, no fusion buffer."""
+    torch = _torch()
+    W, T = len(tensors), len(tensors[0])
+    if outs is None:
+        outs = [[torch.empty_like(t) for t in tensors[u]] for u in range(W)]
+    counts = [tensors[0][t].numel() for t in range(T)]
+    flat_in = [tensors[u][t] for u in range(W) for t in range(T)]
+    flat_out = [outs[u][t] for u in range(W) for t in range(T)]
+    _check_tensors(flat_in, "tensors")
+    _check_tensors(flat_out, "outs")
+    dt = _dtype_code(flat_in[0]) if flat_in else F32
+    fl = flags | (FLAG_RING_ORDER if ring_order else 0)
+    _check(vcoll_allreduce_multi([t.data_ptr() for t in flat_in], [t.data_ptr() for t in flat_out],
+                                 counts, T, W, dt, OPS[op] if isinstance(op, str) else op, fl,
+                                 _stream_handle(stream)))
+    return outs
+
+
+def fusion_allreduce_direct(tensors, outs, op="avg", ring_order=False,
+                            threshold_bytes=DEFAULT_FUSION_THRESHOLD, stream=None):
+    """The same batches and bits as fusion_allreduce, one pass per batch
+    straight from the tensors to the outputs (no fusion buffer)."""
+    W, T = len(tensors), len(tensors[0])
+    counts = [tensors[0][t].numel() for t in range(T)]
+    dt = _dtype_code(tensors[0][0])
+    begin = fuse_plan(counts, dt, threshold_bytes)
+    for b in range(len(begin) - 1):
+        t0, t1 = begin[b], begin[b + 1]
+        allreduce_multi([tensors[u][t0:t1] for u in range(W)], [outs[u][t0:t1] for u in range(W)],
+                        op, ring_order, stream)
+    return outs
 
 
 def fusion_allreduce(tensors, outs, fused, op="avg", ring_order=False,

@@ -117,12 +117,19 @@ bool overlaps(const Buf& x, const Buf& y) {
 // when both map every element index to the same address (then the thread
 // that owns the index reads it before writing it).  Returns VCOLL_OK or
 // INVALID_ARG.  *vec / *phase: whether all buffers share one 16-byte phase.
-int analyse(const std::vector<Buf>& bufs, int es, int* vec, int* phase) {
-  for (size_t i = 0; i < bufs.size(); ++i) {
-    for (size_t k = 0; k < i; ++k) {
-      const Buf& a = bufs[i];
-      const Buf& b = bufs[k];
-      if (!overlaps(a, b)) continue;
+int check_aliasing(const std::vector<Buf>& bufs) {
+  // sorted by start address, each buffer only meets the ones that start
+  // before it ends
+  std::vector<const Buf*> v;
+  v.reserve(bufs.size());
+  for (const Buf& b : bufs)
+    if (b.nbytes) v.push_back(&b);
+  std::sort(v.begin(), v.end(), [](const Buf* a, const Buf* b) { return a->addr < b->addr; });
+  for (size_t i = 0; i < v.size(); ++i) {
+    const uint64_t end = v[i]->addr + v[i]->nbytes;
+    for (size_t k = i + 1; k < v.size() && v[k]->addr < end; ++k) {
+      const Buf& a = *v[i];
+      const Buf& b = *v[k];
       if (a.out && b.out) return fail(VCOLL_ERR_INVALID_ARG, "two output buffers overlap");
       if (a.out != b.out && a.base != b.base)
         return fail(VCOLL_ERR_INVALID_ARG,
@@ -130,6 +137,12 @@ int analyse(const std::vector<Buf>& bufs, int es, int* vec, int* phase) {
                     "(only exact in-place aliasing is allowed)");
     }
   }
+  return VCOLL_OK;
+}
+
+int analyse(const std::vector<Buf>& bufs, int es, int* vec, int* phase) {
+  int rc = check_aliasing(bufs);
+  if (rc) return rc;
   uint64_t ph = bufs.empty() ? 0 : (bufs[0].base & 15);
   int same = 1;
   for (const Buf& b : bufs)
@@ -463,6 +476,121 @@ int vcoll_fuse_pack(const void* const* tensors, const int64_t* counts, int T, vo
 int vcoll_fuse_unpack(const void* const* fused, const int64_t* counts, int T,
                       void* const* tensors, int W, int dtype, void* stream) {
   return fuse_common((const void* const*)tensors, counts, T, fused, W, dtype, 1, stream);
+}
+
+int vcoll_allreduce_multi(const void* const* in, void* const* out, const int64_t* counts, int T,
+                          int W, int dtype, int op, unsigned flags, void* stream) {
+  g_err[0] = 0;
+  int rc = check_common(W, 0, dtype, op);
+  if (rc) return rc;
+  if (flags & ~(VCOLL_FLAG_RING_ORDER | VCOLL_FLAG_STAGED | VCOLL_FLAG_DIRECT))
+    return fail(VCOLL_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+  if (T < 0 || (T > 0 && (!counts || !in || !out)))
+    return fail(VCOLL_ERR_INVALID_ARG, "invalid multi-tensor arguments");
+  const int es = elem_size(dtype);
+  std::vector<int64_t> off(T + 1, 0);
+  for (int t = 0; t < T; ++t) {
+    if (counts[t] < 0) return fail(VCOLL_ERR_INVALID_ARG, "counts[%d] < 0", t);
+    off[t + 1] = off[t] + counts[t];
+  }
+  const int64_t n = off[T];
+  std::vector<Buf> bufs;
+  bufs.reserve(2 * (size_t)W * T);
+  for (int u = 0; u < W; ++u)
+    for (int t = 0; t < T; ++t) {
+      if (!counts[t]) continue;
+      const int64_t e = (int64_t)u * T + t;
+      if (!in[e] || !out[e])
+        return fail(VCOLL_ERR_INVALID_ARG, "tensor %d of rank %d is NULL", t, u);
+      if ((uint64_t)in[e] % es || (uint64_t)out[e] % es)
+        return fail(VCOLL_ERR_INVALID_ARG, "tensor %d of rank %d is not element-aligned", t, u);
+      // base: address of fused element 0 under this tensor's mapping
+      const uint64_t sh = (uint64_t)off[t] * es;
+      bufs.push_back({(uint64_t)in[e], (uint64_t)(counts[t] * es), (uint64_t)in[e] - sh, false});
+      bufs.push_back({(uint64_t)out[e], (uint64_t)(counts[t] * es), (uint64_t)out[e] - sh, true});
+    }
+  if ((rc = check_aliasing(bufs))) return rc;
+  if (n == 0) return VCOLL_OK;
+  if (W == 1) {
+    for (int t = 0; t < T; ++t)
+      if ((rc = copy_d2d(out[t], in[t], counts[t] * es, stream))) return rc;
+    return VCOLL_OK;
+  }
+
+  const bool ring = (flags & VCOLL_FLAG_RING_ORDER) && op != VCOLL_MAX && W > 2;
+  const int W_t = (W == 2 || W == 4 || W == 8 || W == 16) ? W : 0;
+  const int nseg = ring ? W : 1;
+  const void* fn = dtype == VCOLL_F32 ? multi_kernel_f32(op, W_t, ring)
+                                      : multi_kernel_bf16(op, W_t, ring);
+  const int threads = 256;
+  const int V = 16 / es;
+  const int64_t tile_elems = (int64_t)threads * unroll_for(W_t) * V;
+  const int max_t = std::min(kMultiMaxTensors, kMultiMaxPtrs / W);
+
+  int t0 = 0;
+  while (t0 < T) {
+    MultiParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.W = W;
+    prm.scale = op == VCOLL_AVG ? 1.0f / (float)W : 1.0f;
+    prm.do_scale = op == VCOLL_AVG ? 1 : 0;
+    prm.tile_elems = tile_elems;
+    const int nt = std::min(max_t, T - t0);
+    prm.T = nt;
+    for (int u = 0; u < W; ++u)
+      for (int t = 0; t < nt; ++t) {
+        prm.in[u * nt + t] = in[(int64_t)u * T + t0 + t];
+        prm.out[u * nt + t] = out[(int64_t)u * T + t0 + t];
+      }
+    int np = 0;
+    int64_t tiles = 0;
+    int64_t bytes = 0;
+    for (int t = 0; t < nt; ++t) {
+      const int tg = t0 + t;
+      int64_t k = 0;
+      while (k < counts[tg]) {
+        // the segment holding fused index off[tg] + k, and where it ends
+        const int64_t i = off[tg] + k;
+        int j = 0;
+        int64_t seg_end = n;
+        if (nseg > 1) {
+          const int64_t q = n / W, r = n % W;
+          const int64_t big = r * (q + 1);
+          j = i < big ? (int)(i / (q + 1)) : (int)(r + (i - big) / q);
+          int64_t so, sl;
+          segment_of(n, W, j, &so, &sl);
+          seg_end = so + sl;
+        }
+        const int64_t len = std::min(counts[tg] - k, seg_end - i);
+        MultiPiece& pc = prm.piece[np++];
+        pc.k0 = k;
+        pc.len = len;
+        pc.tile_begin = tiles;
+        pc.t = t;
+        pc.start = ring ? (j + 1) % W : 0;
+        // one 16-byte phase for every rank's input and output at element k?
+        int ph = -1;
+        bool same = true;
+        for (int u = 0; u < W && same; ++u) {
+          const uint64_t a = (uint64_t)in[(int64_t)u * T + tg] + (uint64_t)k * es;
+          const uint64_t b = (uint64_t)out[(int64_t)u * T + tg] + (uint64_t)k * es;
+          const int pa = (int)(a & 15), pb = (int)(b & 15);
+          if (ph < 0) ph = pa;
+          same = (pa == ph) && (pb == ph);
+        }
+        pc.phase = same ? ph / es : -1;
+        tiles += std::max<int64_t>(1, ceil_div(len, tile_elems));
+        bytes += len * es;
+        k += len;
+      }
+    }
+    prm.npieces = np;
+    prm.num_tiles = tiles;
+    if (np > 0 && (rc = launch(fn, tiles, threads, 0, bytes <= kSmallBytes, &prm, stream)))
+      return rc;
+    t0 += nt;
+  }
+  return VCOLL_OK;
 }
 
 int vcoll_device_errors(unsigned* flags, int clear) {

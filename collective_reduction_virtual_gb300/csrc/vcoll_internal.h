@@ -78,6 +78,39 @@ struct FuseParams {
   int unpack;  // 0: tensors -> fused, 1: fused -> tensors
 };
 
+// Multi-tensor allreduce: per rank u, tensors in[u*T + t] (t < T) form one
+// virtual buffer (tensor t at fused offset off_t = counts[0..t) summed), and
+// the allreduce of the W virtual buffers lands in out[u*T + t] -- the bits of
+// pack -> in-place allreduce -> unpack, without the fusion buffer.  The host
+// cuts the fused index space into pieces, each inside one tensor and one
+// segment (so the fold's start rank is uniform per piece); a launch covers up
+// to kMultiMaxTensors tensors.
+constexpr int kMultiMaxTensors = 64;
+constexpr int kMultiMaxPtrs = 768;  // W * T per launch (inputs; the same for outputs)
+constexpr int kMultiMaxPieces = kMultiMaxTensors + VCOLL_MAX_RANKS;
+struct MultiPiece {
+  int64_t k0;          // first element of the piece inside tensor t
+  int64_t len;         // elements
+  int64_t tile_begin;  // first tile of the piece (pieces are tiled back to back)
+  int t;               // tensor index inside this launch
+  int start;           // first rank of the fold
+  int phase;           // piece-local element i is 16-byte aligned in every buffer
+                       // iff (i + phase) % V == 0; -1: phases differ, element-wise
+  int pad;
+};
+struct MultiParams {
+  const void* in[kMultiMaxPtrs];
+  void* out[kMultiMaxPtrs];
+  MultiPiece piece[kMultiMaxPieces];
+  int64_t num_tiles;
+  int64_t tile_elems;
+  int npieces;
+  int T;
+  int W;
+  float scale;
+  int do_scale;
+};
+
 // Kernel selection (function pointers for cudaLaunchKernel).  W_t is the
 // compile-time rank count (2, 4, 8, 16) or 0 for the runtime-W kernels; vec
 // selects the 16-byte vector path.
@@ -89,6 +122,8 @@ const void* gather_kernel(int elem_size, int vec);
 // Device address of the per-device error word (VCOLL_DEVICE_ERR_* bits).
 unsigned int* device_error_symbol();
 const void* fuse_kernel(int elem_size);
+const void* multi_kernel_f32(int op, int W_t, int ring);
+const void* multi_kernel_bf16(int op, int W_t, int ring);
 
 // Vectors (16 B) per thread per tile of the direct kernels, by W_t.
 VCOLL_HD constexpr int unroll_for(int W_t) {

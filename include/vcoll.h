@@ -132,7 +132,8 @@ int vcoll_fuse_plan(const int64_t* counts, int T, int dtype, int64_t threshold_b
  * fusedSynch): fused[u] receives tensors[u*T + t] for t = 0..T-1 back to back,
  * no padding (tensor t at element offset counts[0] + ... + counts[t-1]).
  * tensors: host array of W*T device pointers, rank-major.  counts: host.
- * One kernel launch per 128 tensors; no buffer may overlap another.
+ * One kernel launch per up to 64 tensors (fewer when W*T would exceed 1024);
+ * no buffer may overlap another.
  */
 int vcoll_fuse_pack(const void* const* tensors, const int64_t* counts, int T, void* const* fused,
                     int W, int dtype, void* stream);
@@ -140,6 +141,23 @@ int vcoll_fuse_pack(const void* const* tensors, const int64_t* counts, int T, vo
 /* Fusion unpack: the inverse of vcoll_fuse_pack. */
 int vcoll_fuse_unpack(const void* const* fused, const int64_t* counts, int T,
                       void* const* tensors, int W, int dtype, void* stream);
+
+/*
+ * Multi-tensor allreduce: Horovod's tensor fusion (PerformOperation: pack into
+ * the fusion buffer, ncclAllReduce it in place, unpack; SINGA fusedSynch)
+ * without the fusion buffer.  For each rank u the T tensors in[u*T + t] form
+ * one virtual buffer of n = counts[0] + ... + counts[T-1] elements (tensor t at
+ * offset counts[0] + ... + counts[t-1]); the allreduce of the W virtual
+ * buffers is written to out[u*T + t].  The result has the bits of
+ * vcoll_fuse_pack -> vcoll_allreduce (in place, same flags) ->
+ * vcoll_fuse_unpack of the same batch, but every byte moves once (2*W*n*elemsize
+ * instead of 6*W*n*elemsize).  Call it once per batch of vcoll_fuse_plan.
+ * in, out: host arrays of W*T device pointers, rank-major; counts: host.  In
+ * place: out[e] == in[e].  One launch per up to 64 tensors (fewer when W*T
+ * would exceed 768).
+ */
+int vcoll_allreduce_multi(const void* const* in, void* const* out, const int64_t* counts, int T,
+                          int W, int dtype, int op, unsigned flags, void* stream);
 
 /* Device-side error bits, OR-ed into one word per device by the kernels.
  * The staged kernels bound every wait on their shared-memory barriers; a wait

@@ -170,3 +170,23 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(vc, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="not built"):
         vc.lib()
+
+
+def test_allreduce_multi_argument_errors(v):
+    ins = [0x100000 * (i + 1) for i in range(4)]    # W=2, T=2
+    outs = [0x10000000 + 0x100000 * i for i in range(4)]
+    f = v.vcoll_allreduce_multi
+    assert f(ins, outs, [10, 20], 2, 2, v.F32, 9) == v.ERR_INVALID_OP
+    assert f(ins, outs, [10, 20], 2, 2, 5, v.SUM) == v.ERR_INVALID_TYPE
+    assert f(ins, outs, [10, -1], 2, 2, v.F32, v.SUM) == v.ERR_INVALID_ARG
+    assert f(ins, outs, [10, 20], 2, 0, v.F32, v.SUM) == v.ERR_INVALID_ARG
+    assert f([0] + ins[1:], outs, [10, 20], 2, 2, v.F32, v.SUM) == v.ERR_INVALID_ARG
+    assert f([ins[0] + 2] + ins[1:], outs, [10, 20], 2, 2, v.F32, v.SUM) == v.ERR_INVALID_ARG
+    # output of tensor 0 overlapping input of tensor 1 at a different fused offset
+    bad = [ins[1]] + outs[1:]
+    assert f(ins, bad, [10, 10], 2, 2, v.F32, v.SUM) == v.ERR_INVALID_ARG
+    # two outputs overlapping
+    bad = [outs[0], outs[0] + 8] + outs[2:]
+    assert f(ins, bad, [10, 20], 2, 2, v.F32, v.SUM) == v.ERR_INVALID_ARG
+    # empty tensors need no pointers
+    assert f([0] * 4, [0] * 4, [0, 0], 2, 2, v.F32, v.SUM) == v.OK

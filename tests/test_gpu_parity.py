@@ -332,3 +332,79 @@ def test_staged_in_place_and_phase(v):
     for u in range(W):
         assert_bit_exact(to_np(ins[u]), want[u], "staged in place")
     assert v.device_errors(clear=True) == 0
+
+
+# --------------------------------------- multi-tensor allreduce (no buffer)
+
+def _tensor_list(W, counts, dtype, seed, shift_pattern=None):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    out = []
+    for u in range(W):
+        row = []
+        for i, c in enumerate(counts):
+            sh = 0 if shift_pattern is None else shift_pattern(u, i)
+            base = (torch.randn(c + 8, generator=g, device="cuda") *
+                    (10.0 ** torch.randint(-2, 3, (c + 8,), generator=g, device="cuda").float()))
+            row.append(base.to(DT[dtype])[sh:sh + c])
+        out.append(row)
+    return out
+
+
+@pytest.mark.parametrize("W", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("layout", ["aligned", "shared_shift", "mixed"])
+def test_allreduce_multi_matches_pipeline_and_oracle(v, W, dtype, layout):
+    counts = [1000, 3, 0, 4097, 250, 1, 60, 12345, 7, 77]
+    pat = {"aligned": None, "shared_shift": lambda u, i: i % 4,
+           "mixed": lambda u, i: (u + i) % 5}[layout]
+    tens = _tensor_list(W, counts, dtype, 300 + W, pat)
+    tot = sum(counts)
+    fused = [torch.empty(tot, dtype=DT[dtype], device="cuda") for _ in range(W)]
+    for op in ("sum", "avg", "max"):
+        for ring in (True, False):
+            direct = v.allreduce_multi(tens, op=op, ring_order=ring)
+            outs = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+            v.fusion_allreduce(tens, outs, fused, op=op, ring_order=ring,
+                               threshold_bytes=1 << 40)
+            for u in range(W):
+                for t in range(len(counts)):
+                    assert to_np(direct[u][t]).tobytes() == to_np(outs[u][t]).tobytes(), \
+                        f"multi vs pipeline {op} ring={ring} rank {u} tensor {t}"
+            if ring or op == "max":
+                want = oracle.fusion_allreduce(
+                    [[to_np(t) for t in tens[u]] for u in range(W)], counts, op, ODT[dtype],
+                    threshold_bytes=1 << 40)
+                for u in range(W):
+                    for t in range(len(counts)):
+                        assert_bit_exact(to_np(direct[u][t]), want[u][t], f"multi {op} vs oracle")
+
+
+def test_allreduce_multi_in_place_and_many_tensors(v):
+    W = 8
+    rng = np.random.default_rng(5)
+    counts = [int(c) for c in rng.integers(1, 3000, 150)]  # > one launch of 64 tensors
+    tens = _tensor_list(W, counts, "f32", 17)
+    want = oracle.fusion_allreduce([[to_np(t) for t in tens[u]] for u in range(W)], counts, "sum",
+                                   oracle.F32, threshold_bytes=1 << 40)
+    v.allreduce_multi(tens, tens, op="sum", ring_order=True)
+    for u in range(W):
+        for t in range(len(counts)):
+            assert_bit_exact(to_np(tens[u][t]), want[u][t], "multi in place")
+
+
+def test_fusion_direct_equals_pipeline_full_workload(v):
+    # 200 fp32 tensors per rank, W = 8, 64 MiB batches: the one-pass path and
+    # the pack -> allreduce -> unpack path give the same bits everywhere
+    from collective_reduction_virtual_gb300 import inputs as I
+    W = 8
+    counts = [int(c) for c in I.fusion_counts()]
+    tens = I.fusion_tensors(counts, W, "cuda")
+    fused = [torch.empty((64 << 20) // 4, device="cuda") for _ in range(W)]
+    for ring in (True, False):
+        a = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+        b = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+        v.fusion_allreduce(tens, a, fused, op="avg", ring_order=ring)
+        v.fusion_allreduce_direct(tens, b, op="avg", ring_order=ring)
+        for u in range(W):
+            assert torch.equal(torch.cat(a[u]).view(torch.int32), torch.cat(b[u]).view(torch.int32))
