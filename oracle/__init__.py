@@ -28,8 +28,8 @@ import threading
 import numpy as np
 
 F32, BF16 = 0, 1
-SUM, MAX, AVG = 0, 1, 2
-OPS = {"sum": SUM, "max": MAX, "avg": AVG}
+SUM, MAX, AVG, MIN, PROD = 0, 1, 2, 3, 4
+OPS = {"sum": SUM, "max": MAX, "avg": AVG, "min": MIN, "prod": PROD}
 DTYPES = {"f32": F32, "float32": F32, "bf16": BF16, "bfloat16": BF16}
 NP_DTYPE = {F32: np.float32, BF16: np.uint16}
 MAX_RANKS = 64
@@ -66,6 +66,7 @@ def load(path: str) -> ctypes.CDLL:
     L.oracle_reduce_scatter.argtypes = [PP, PP, I, I64, I, I, IP]
     L.oracle_allgather.argtypes = [PP, PP, I, I64, I, IP]
     L.oracle_allreduce.argtypes = [PP, PP, I, I64, I, I, IP]
+    L.oracle_allgatherv.argtypes = [PP, I64P, PP, I, I, IP]
     L.oracle_allreduce_sampled.argtypes = [P, I64P, I64, I64, I, I, I, IP, P]
     L.oracle_bf16_from_f32.argtypes = [ctypes.c_float]
     L.oracle_bf16_from_f32.restype = ctypes.c_uint16
@@ -75,6 +76,7 @@ def load(path: str) -> ctypes.CDLL:
     L.oracle_fusion_allreduce.argtypes = [PP, PP, I64P, I, I, I, I, I64, PP]
     for name in ("oracle_segment", "oracle_ring_schedule", "oracle_reduce_scatter",
                  "oracle_allgather", "oracle_allreduce", "oracle_allreduce_sampled",
+                 "oracle_allgatherv",
                  "oracle_fuse_plan", "oracle_fuse_pack", "oracle_fuse_unpack",
                  "oracle_fusion_allreduce"):
         getattr(L, name).restype = I
@@ -173,6 +175,20 @@ def allgather(segs, n: int, dtype=F32, user_from_ring=None):
     outs = [np.empty(n, NP_DTYPE[dtype]) for _ in range(W)]
     _check(lib().oracle_allgather(_ptrs(segs), _ptrs(outs), W, n, dtype,
                                   _ring(user_from_ring, W)), "allgather")
+    return outs
+
+
+def allgatherv(pieces, dtype=F32, user_from_ring=None):
+    """Ring allgather with per-rank sizes: pieces[u] (any length) -> W arrays
+    holding all pieces in rank order."""
+    dtype = _code(DTYPES, dtype)
+    pieces = [_contig(a, dtype) for a in pieces]
+    W = len(pieces)
+    counts = np.array([a.size for a in pieces], dtype=np.int64)
+    outs = [np.empty(int(counts.sum()), NP_DTYPE[dtype]) for _ in range(W)]
+    rc = lib().oracle_allgatherv(_ptrs(pieces), counts.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                 _ptrs(outs), W, dtype, _ring(user_from_ring, W))
+    _check(rc, "allgatherv")
     return outs
 
 

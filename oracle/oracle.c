@@ -43,6 +43,9 @@
  *  - avg: the ring sum multiplied once by fl32(1/W) at the last step.
  *  - max: NaN in either operand gives the canonical quiet NaN; otherwise the
  *    larger operand, and +0 over -0 when they compare equal.
+ *  - min (NCCL FuncMin, body not on the page): the mirror image of max --
+ *    canonical quiet NaN, otherwise the smaller operand, -0 over +0 on a tie.
+ *  - prod (NCCL FuncProd): one IEEE fp32 multiply per hop, accumulator first.
  *  - bf16 output: IEEE round-to-nearest-even from fp32; NaN stays a quiet NaN.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no -ffast-math),
@@ -59,6 +62,8 @@
 #define ORACLE_SUM 0
 #define ORACLE_MAX 1
 #define ORACLE_AVG 2
+#define ORACLE_MIN 3
+#define ORACLE_PROD 4
 
 #define ORACLE_MAX_RANKS 64
 
@@ -128,7 +133,21 @@ static float ring_func(int op, float acc, float x) {
     if (acc == 0.0f) return (signbit(acc) && signbit(x)) ? -0.0f : 0.0f;
     return acc;
   }
+  if (op == ORACLE_MIN) {
+    if (isnan(acc) || isnan(x)) return canonical_qnan();
+    if (acc < x) return acc;
+    if (x < acc) return x;
+    /* equal: identical bits, except +0 == -0 where -0 wins */
+    if (acc == 0.0f) return (signbit(acc) || signbit(x)) ? -0.0f : 0.0f;
+    return acc;
+  }
+  if (op == ORACLE_PROD) return acc * x;
   return acc + x; /* sum and avg */
+}
+
+static int valid_op(int op) {
+  return op == ORACLE_SUM || op == ORACLE_MAX || op == ORACLE_AVG || op == ORACLE_MIN ||
+         op == ORACLE_PROD;
 }
 
 static int check_ring(int W, const int* user_from_ring, int* ufr) {
@@ -181,7 +200,7 @@ int oracle_reduce_scatter(const void* const* in, void* const* out, int W, int64_
   int ufr[ORACLE_MAX_RANKS];
   int es = elem_size(dtype);
   if (!in || !out || W < 1 || W > ORACLE_MAX_RANKS || n < 0 || !es) return -1;
-  if (op != ORACLE_SUM && op != ORACLE_MAX && op != ORACLE_AVG) return -1;
+  if (!valid_op(op)) return -1;
   if (check_ring(W, user_from_ring, ufr)) return -1;
   if (n == 0) return 0;
   if (W == 1) {
@@ -259,6 +278,39 @@ int oracle_allgather(const void* const* in, void* const* out, int W, int64_t n,
   return 0;
 }
 
+/* Allgather with per-rank sizes (Horovod's allgatherv path: every rank's
+ * tensor, first dimensions possibly different, concatenated in rank order on
+ * every rank).  in[u]: counts[u] elements; out[u]: the sum of all counts,
+ * rank j's piece at counts[0] + ... + counts[j-1].  Same ring propagation as
+ * oracle_allgather, with the displacements in place of the even segments. */
+int oracle_allgatherv(const void* const* in, const int64_t* counts, void* const* out, int W,
+                      int dtype, const int* user_from_ring) {
+  int ufr[ORACLE_MAX_RANKS];
+  int64_t disp[ORACLE_MAX_RANKS + 1];
+  int es = elem_size(dtype);
+  if (!in || !out || !counts || W < 1 || W > ORACLE_MAX_RANKS || !es) return -1;
+  if (check_ring(W, user_from_ring, ufr)) return -1;
+  disp[0] = 0;
+  for (int u = 0; u < W; ++u) {
+    if (counts[u] < 0) return -1;
+    disp[u + 1] = disp[u] + counts[u];
+  }
+  for (int s = 0; s < W; ++s) {
+    for (int p = 0; p < W; ++p) {
+      int me = ufr[p];
+      int b = ufr[(W + p - s) % W]; /* block held at step s */
+      char* dst = (char*)out[me] + disp[b] * es;
+      const char* src;
+      if (s == 0)
+        src = (const char*)in[me];
+      else
+        src = (const char*)out[ufr[(p - 1 + W) % W]] + disp[b] * es;
+      if (dst != src && counts[b]) memmove(dst, src, (size_t)counts[b] * es);
+    }
+  }
+  return 0;
+}
+
 /* ------------------------------------------------------------- allreduce */
 
 /* Ring allreduce = reduce-scatter followed by allgather.  in[u], out[u]: n
@@ -269,7 +321,7 @@ int oracle_allreduce(const void* const* in, void* const* out, int W, int64_t n,
   int ufr[ORACLE_MAX_RANKS];
   int es = elem_size(dtype);
   if (!in || !out || W < 1 || W > ORACLE_MAX_RANKS || n < 0 || !es) return -1;
-  if (op != ORACLE_SUM && op != ORACLE_MAX && op != ORACLE_AVG) return -1;
+  if (!valid_op(op)) return -1;
   if (check_ring(W, user_from_ring, ufr)) return -1;
   if (n == 0) return 0;
   void* seg[ORACLE_MAX_RANKS];

@@ -39,6 +39,13 @@ MUTANTS = {
     "pack_offset": ("memcpy((char*)fused[u] + offset * es, tensors[(int64_t)u * T + t],",
                     "memcpy((char*)fused[u], tensors[(int64_t)u * T + t],"),
     "last_step_early": ("} else if (s < W - 1) {", "} else if (s < W - 2) {"),
+    "min_operand": ("if (acc < x) return acc;", "if (acc < x) return x;"),
+    "min_signed_zero": ("(signbit(acc) || signbit(x)) ? -0.0f", "(signbit(acc) && signbit(x)) ? -0.0f"),
+    "prod_is_sum": ("if (op == ORACLE_PROD) return acc * x;", "if (op == ORACLE_PROD) return acc + x;"),
+    "allgatherv_block": ("int b = ufr[(W + p - s) % W]; /* block held at step s */",
+                         "int b = ufr[(W + p + s) % W]; /* block held at step s */"),
+    "allgatherv_displacement": ("char* dst = (char*)out[me] + disp[b] * es;",
+                                "char* dst = (char*)out[me] + disp[me] * es;"),
 }
 
 BATTERY = r"""
@@ -64,6 +71,11 @@ pins = [
     (P.test_fuse_plan_golden, ()),
     (P.test_pack_is_concatenation_and_unpack_inverts, ()),
     (P.test_fusion_allreduce_integer_mean_exact, ()),
+    (P.test_min_matches_numpy, (4,)),
+    (P.test_min_signed_zero_and_nan, ()),
+    (P.test_prod_ring_order_hand_derived, ()),
+    (P.test_prod_of_small_integers_exact, (3,)),
+    (P.test_allgatherv_is_concatenation, (3,)),
 ]
 failed = []
 with oracle.using({so!r}):

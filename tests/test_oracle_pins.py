@@ -378,3 +378,61 @@ def test_fusion_allreduce_is_batchwise_allreduce_of_concatenation():
         ar = oracle.allreduce(cat, "avg")
         for u in range(W):
             assert np.concatenate([outs[u][t] for t in ts]).tobytes() == ar[u].tobytes()
+
+
+# ------------------------------------------------------------ min and prod
+
+@pytest.mark.parametrize("W", [2, 3, 4, 8, 16])
+def test_min_matches_numpy(W):
+    rng = _rng(W + 199)
+    ins = [rng.standard_normal(555).astype(np.float32) for _ in range(W)]
+    want = np.minimum.reduce(ins)
+    for got in oracle.allreduce(ins, "min"):
+        assert np.array_equal(got, want)
+
+
+def test_min_signed_zero_and_nan():
+    pz, nz, nan = np.float32(0.0), np.float32(-0.0), np.float32(np.nan)
+    ins = [np.array([pz, nz, pz, 1.0, nan], np.float32),
+           np.array([nz, pz, pz, nan, 1.0], np.float32)]
+    bits = oracle.allreduce(ins, "min")[0].view(np.uint32)
+    assert bits[0] == 0x80000000 and bits[1] == 0x80000000  # -0 wins either order
+    assert bits[2] == 0x00000000
+    assert bits[3] == 0x7FC00000 and bits[4] == 0x7FC00000
+
+
+def test_prod_ring_order_hand_derived():
+    line = _golden_lines("ring_order_prod.txt")[0]
+    want = [float(v) for v in line.split()]
+    x = [np.full(4, v, np.float32) for v in (2.0 ** 100, 2.0 ** 100, 2.0 ** -100, 2.0 ** -100)]
+    got = [float(s[0]) for s in oracle.reduce_scatter(x, "prod")]
+    assert got == want
+
+
+@pytest.mark.parametrize("W", [2, 3, 5, 8])
+def test_prod_of_small_integers_exact(W):
+    rng = _rng(W + 300)
+    ins = [rng.choice(np.array([-2, -1, 1, 2, 3], np.float32), 400) for _ in range(W)]
+    want = np.prod(np.stack([a.astype(np.int64) for a in ins]), axis=0)
+    for got in oracle.allreduce(ins, "prod"):
+        assert np.array_equal(got.astype(np.int64), want)
+
+
+# ------------------------------------------------------------ allgatherv
+
+@pytest.mark.parametrize("W", [1, 2, 3, 7])
+def test_allgatherv_is_concatenation(W):
+    rng = _rng(W + 400)
+    pieces = [rng.standard_normal(int(rng.integers(0, 50))).astype(np.float32) for _ in range(W)]
+    want = np.concatenate(pieces)
+    for out in oracle.allgatherv(pieces, oracle.F32, list(rng.permutation(W))):
+        assert out.tobytes() == want.tobytes()
+
+
+def test_allgatherv_with_even_sizes_is_allgather():
+    rng = _rng(401)
+    n, W = 40, 4
+    segs = [rng.standard_normal(oracle.segment(n, W, j)[1]).astype(np.float32) for j in range(W)]
+    a = oracle.allgatherv(segs)
+    b = oracle.allgather(segs, n)
+    assert all(x.tobytes() == y.tobytes() for x, y in zip(a, b))
