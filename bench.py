@@ -286,10 +286,13 @@ def build_workload(args, dev, rank):
             bytes_, launches = 6 * W * B, 3 * nb
             desc = "pack + in-place allreduce + unpack per 64 MiB batch (6*W*B)"
         else:
-            step = lambda: vc.fusion_allreduce_direct(tens, outs, op=red, ring_order=ring)  # noqa
+            plan = vc.FusionPlan(tens, outs, op=red, ring_order=ring)
+            step = lambda: plan()  # noqa
             nb = len(vc.fuse_plan(counts, 0 if es == 4 else 1)) - 1
-            bytes_, launches = 2 * W * B, nb
-            desc = "one pass per 64 MiB batch straight from the tensors (2*W*B)"
+            launches = -(-len(counts) // min(64, 768 // W))
+            bytes_ = 2 * W * B
+            desc = ("64 MiB batches, read straight from the tensors and written straight to "
+                    "the outputs (2*W*B), batches planned and launched in C")
         return dict(name=f"tensor-fusion allreduce {red}, W={W}, 200 {args.dtype} tensors per "
                          f"rank (log-uniform 1024..4194304 elements), {desc}",
                     W=W, n=sum(counts), step=step, bytes=bytes_, launches=launches,
@@ -497,8 +500,8 @@ def extras(args, stream, dev):
     out["fusion_w8_200tensors"] = rate(
         lambda: vc.fusion_allreduce(tens, fouts, fused, op="avg"), 6 * W * tot, steps=5, warmup=2)
     out["fusion_w8_200tensors"]["bytes_formula"] = "6*W*B_total (pack + AR + unpack)"
-    out["fusion_w8_200tensors_direct"] = rate(
-        lambda: vc.fusion_allreduce_direct(tens, fouts, op="avg"), 2 * W * tot, steps=5, warmup=2)
+    plan = vc.FusionPlan(tens, fouts, op="avg")
+    out["fusion_w8_200tensors_direct"] = rate(lambda: plan(), 2 * W * tot, steps=10, warmup=3)
     out["fusion_w8_200tensors_direct"]["bytes_formula"] = \
         "2*W*B_total (one pass, no fusion buffer); same bits as the pipeline"
     del tens, fouts, fused

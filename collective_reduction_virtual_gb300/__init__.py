@@ -25,11 +25,11 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libvcoll.so")
 
 F32, BF16 = 0, 1
-SUM, MAX, AVG = 0, 1, 2
+SUM, MAX, AVG, MIN, PROD = 0, 1, 2, 3, 4
 FLAG_RING_ORDER, FLAG_STAGED, FLAG_DIRECT = 0x1, 0x2, 0x4
 MAX_RANKS = 64
 OK, ERR_INVALID_ARG, ERR_INVALID_TYPE, ERR_INVALID_OP, ERR_UNSUPPORTED, ERR_CUDA = range(6)
-OPS = {"sum": SUM, "max": MAX, "avg": AVG}
+OPS = {"sum": SUM, "max": MAX, "avg": AVG, "min": MIN, "prod": PROD}
 DEFAULT_FUSION_THRESHOLD = 64 * 1024 * 1024  # Horovod's tensor_fusion_threshold default
 
 _lock = threading.Lock()
@@ -64,8 +64,12 @@ def lib() -> ctypes.CDLL:
             L.vcoll_fuse_pack.restype = I
             L.vcoll_fuse_unpack.argtypes = [PP, I64P, I, PP, I, I, P]
             L.vcoll_fuse_unpack.restype = I
+            L.vcoll_allgatherv.argtypes = [PP, I64P, PP, I, I, P]
+            L.vcoll_allgatherv.restype = I
             L.vcoll_allreduce_multi.argtypes = [PP, PP, I64P, I, I, I, I, U, P]
             L.vcoll_allreduce_multi.restype = I
+            L.vcoll_fusion_allreduce.argtypes = [PP, PP, I64P, I, I, I, I, U, I64, IP, P]
+            L.vcoll_fusion_allreduce.restype = I
             L.vcoll_segment.argtypes = [I64, I, I, I64P, I64P]
             L.vcoll_segment.restype = I
             L.vcoll_status_string.argtypes = [I]
@@ -130,6 +134,11 @@ def vcoll_reduce_scatter(in_ptrs, out_ptrs, W, n, dtype, op, flags=0, stream=0) 
 def vcoll_allgather(in_ptrs, out_ptrs, W, n, dtype, op=SUM, flags=0, stream=0) -> int:
     return lib().vcoll_allgather(_ptr_array(in_ptrs), _ptr_array(out_ptrs), W, n, dtype, op,
                                  flags, stream or None)
+
+
+def vcoll_allgatherv(in_ptrs, counts, out_ptrs, W, dtype, stream=0) -> int:
+    return lib().vcoll_allgatherv(_ptr_array(in_ptrs), _i64_array(counts), _ptr_array(out_ptrs), W,
+                                  dtype, stream or None)
 
 
 def vcoll_allreduce(in_ptrs, out_ptrs, W, n, dtype, op, flags=0, stream=0) -> int:
@@ -239,6 +248,22 @@ def allgather(segs, n: int, outs=None, stream=None, flags=0):
     return outs
 
 
+def allgatherv(pieces, outs=None, stream=None):
+    """pieces[j]: rank j's tensor (any length).  Returns W tensors holding all
+    pieces concatenated in rank order."""
+    torch = _torch()
+    W = len(pieces)
+    _check_tensors(pieces, "pieces")
+    counts = [p.numel() for p in pieces]
+    if outs is None:
+        outs = [torch.empty(sum(counts), dtype=pieces[0].dtype, device=pieces[0].device)
+                for _ in range(W)]
+    _check_tensors(outs, "outs")
+    _check(vcoll_allgatherv([t.data_ptr() for t in pieces], counts, [t.data_ptr() for t in outs], W,
+                            _dtype_code(pieces[0]), _stream_handle(stream)))
+    return outs
+
+
 def allreduce(ins, outs=None, op="sum", ring_order=False, stream=None, flags=0):
     """ins: W CUDA tensors of n elements; outs defaults to new tensors
     (pass ``outs=ins`` for in place).  Returns outs."""
@@ -306,18 +331,52 @@ def allreduce_multi(tensors, outs=None, op="sum", ring_order=False, stream=None,
     return outs
 
 
+def vcoll_fusion_allreduce(in_ptrs, out_ptrs, counts, T, W, dtype, op, flags=0,
+                           threshold_bytes=DEFAULT_FUSION_THRESHOLD, stream=0):
+    """Returns (status, number of batches)."""
+    nb = ctypes.c_int()
+    rc = lib().vcoll_fusion_allreduce(_ptr_array(in_ptrs), _ptr_array(out_ptrs), _i64_array(counts),
+                                      T, W, dtype, op, flags, int(threshold_bytes),
+                                      ctypes.byref(nb), stream or None)
+    return rc, nb.value
+
+
+class FusionPlan:
+    """Device pointers of a fixed set of tensors marshalled once, so that
+    repeated fusion allreduces (one per training step) cost one C call."""
+
+    def __init__(self, tensors, outs, op="avg", ring_order=False,
+                 threshold_bytes=DEFAULT_FUSION_THRESHOLD, flags=0):
+        W, T = len(tensors), len(tensors[0])
+        flat_in = [tensors[u][t] for u in range(W) for t in range(T)]
+        flat_out = [outs[u][t] for u in range(W) for t in range(T)]
+        _check_tensors(flat_in, "tensors")
+        _check_tensors(flat_out, "outs")
+        self.W, self.T = W, T
+        self.counts = [tensors[0][t].numel() for t in range(T)]
+        self._in = _ptr_array([t.data_ptr() for t in flat_in])
+        self._out = _ptr_array([t.data_ptr() for t in flat_out])
+        self._counts = _i64_array(self.counts)
+        self.dtype = _dtype_code(flat_in[0])
+        self.op = OPS[op] if isinstance(op, str) else op
+        self.flags = flags | (FLAG_RING_ORDER if ring_order else 0)
+        self.threshold = int(threshold_bytes)
+        self._keep = (flat_in, flat_out)
+        self.nbatches = 0
+
+    def __call__(self, stream=None):
+        nb = ctypes.c_int()
+        _check(lib().vcoll_fusion_allreduce(self._in, self._out, self._counts, self.T, self.W,
+                                            self.dtype, self.op, self.flags, self.threshold,
+                                            ctypes.byref(nb), _stream_handle(stream) or None))
+        self.nbatches = nb.value
+
+
 def fusion_allreduce_direct(tensors, outs, op="avg", ring_order=False,
                             threshold_bytes=DEFAULT_FUSION_THRESHOLD, stream=None):
-    """The same batches and bits as fusion_allreduce, one pass per batch
-    straight from the tensors to the outputs (no fusion buffer)."""
-    W, T = len(tensors), len(tensors[0])
-    counts = [tensors[0][t].numel() for t in range(T)]
-    dt = _dtype_code(tensors[0][0])
-    begin = fuse_plan(counts, dt, threshold_bytes)
-    for b in range(len(begin) - 1):
-        t0, t1 = begin[b], begin[b + 1]
-        allreduce_multi([tensors[u][t0:t1] for u in range(W)], [outs[u][t0:t1] for u in range(W)],
-                        op, ring_order, stream)
+    """The same batches and bits as fusion_allreduce, straight from the
+    tensors to the outputs (no fusion buffer), planned and launched in C."""
+    FusionPlan(tensors, outs, op, ring_order, threshold_bytes)(stream)
     return outs
 
 

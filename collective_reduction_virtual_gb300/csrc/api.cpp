@@ -182,7 +182,8 @@ int check_common(int W, int64_t n, int dtype, int op) {
     return fail(VCOLL_ERR_INVALID_ARG, "W = %d outside [1, %d]", W, VCOLL_MAX_RANKS);
   if (n < 0) return fail(VCOLL_ERR_INVALID_ARG, "n = %lld < 0", (long long)n);
   if (!elem_size(dtype)) return fail(VCOLL_ERR_INVALID_TYPE, "unknown dtype %d", dtype);
-  if (op != VCOLL_SUM && op != VCOLL_MAX && op != VCOLL_AVG)
+  if (op != VCOLL_SUM && op != VCOLL_MAX && op != VCOLL_AVG && op != VCOLL_MIN &&
+      op != VCOLL_PROD)
     return fail(VCOLL_ERR_INVALID_OP, "unknown op %d", op);
   return VCOLL_OK;
 }
@@ -274,7 +275,7 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
 
   if (W == 1) return copy_d2d(out[0], in[0], n * es, stream);
 
-  const bool ring = (flags & VCOLL_FLAG_RING_ORDER) && op != VCOLL_MAX && W > 2;
+  const bool ring = (flags & VCOLL_FLAG_RING_ORDER) && op != VCOLL_MAX && op != VCOLL_MIN && W > 2;
   const int W_t = (W == 2 || W == 4 || W == 8 || W == 16) ? W : 0;
   const int nseg = (kind == KIND_RS || ring) ? W : 1;
   const bool small = n * es <= kSmallBytes;
@@ -333,26 +334,26 @@ int vcoll_allreduce(const void* const* in, void* const* out, int W, int64_t n, i
   return reduce_common(KIND_AR, in, out, W, n, dtype, op, flags, stream);
 }
 
-int vcoll_allgather(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,
-                    unsigned flags, void* stream) {
-  g_err[0] = 0;
-  int rc = check_common(W, n, dtype, op);
-  if (rc) return rc;
-  if (flags & ~(VCOLL_FLAG_RING_ORDER | VCOLL_FLAG_STAGED | VCOLL_FLAG_DIRECT))
-    return fail(VCOLL_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+// Allgather of W pieces, piece j landing at [disp[j], disp[j+1]) of every
+// output (shared by allgather and allgatherv).
+static int gather_common(const void* const* in, void* const* out, int W, const int64_t* disp,
+                         int dtype, void* stream) {
   const int es = elem_size(dtype);
-  int64_t in_len[VCOLL_MAX_RANKS], out_len[VCOLL_MAX_RANKS], seg_off[VCOLL_MAX_RANKS];
+  const int64_t n = disp[W];
+  int64_t in_len[VCOLL_MAX_RANKS], out_len[VCOLL_MAX_RANKS];
   for (int u = 0; u < W; ++u) {
-    segment_of(n, W, u, &seg_off[u], &in_len[u]);
+    in_len[u] = disp[u + 1] - disp[u];
     out_len[u] = n;
   }
+  int rc;
   if ((rc = check_ptrs(in, W, "in", es, in_len))) return rc;
   if ((rc = check_ptrs((const void* const*)out, W, "out", es, out_len))) return rc;
   if (n == 0) return VCOLL_OK;
   std::vector<Buf> bufs;
   for (int u = 0; u < W; ++u) {
-    bufs.push_back({(uint64_t)in[u], (uint64_t)(in_len[u] * es),
-                    (uint64_t)in[u] - (uint64_t)seg_off[u] * es, false});
+    if (in_len[u])
+      bufs.push_back({(uint64_t)in[u], (uint64_t)(in_len[u] * es),
+                      (uint64_t)in[u] - (uint64_t)disp[u] * es, false});
     bufs.push_back({(uint64_t)out[u], (uint64_t)(n * es), (uint64_t)out[u], true});
   }
   int vec, phase;
@@ -368,15 +369,52 @@ int vcoll_allgather(const void* const* in, void* const* out, int W, int64_t n, i
     prm.in[u] = in[u];
     prm.out[u] = out[u];
   }
-  prm.n = n;
-  prm.q = n / W;
-  prm.r = n % W;
+  for (int u = 0; u <= W; ++u) prm.disp[u] = disp[u];
   prm.W = W;
   prm.phase = phase;
   prm.tile_elems = (int64_t)threads * 4 * V;
-  prm.tiles_per_seg = tiles_per_segment(n, W, W, V, phase, prm.tile_elems);
-  prm.num_tiles = prm.tiles_per_seg * W;
+  int64_t tps = 1;
+  for (int j = 0; j < W; ++j) {
+    const int64_t a = disp[j], b = disp[j + 1];
+    const int64_t up = a + ((V - ((a + phase) % V)) % V);
+    const int64_t av = std::min(up, b);
+    const int64_t bv = std::max(b - ((b + phase) % V), av);
+    tps = std::max(tps, ceil_div(bv - av, prm.tile_elems));
+  }
+  prm.tiles_per_seg = tps;
+  prm.num_tiles = tps * W;
   return launch(gather_kernel(es, vec), prm.num_tiles, threads, 0, small, &prm, stream);
+}
+
+int vcoll_allgather(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,
+                    unsigned flags, void* stream) {
+  g_err[0] = 0;
+  int rc = check_common(W, n, dtype, op);
+  if (rc) return rc;
+  if (flags & ~(VCOLL_FLAG_RING_ORDER | VCOLL_FLAG_STAGED | VCOLL_FLAG_DIRECT))
+    return fail(VCOLL_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+  int64_t disp[VCOLL_MAX_RANKS + 1];
+  for (int u = 0; u < W; ++u) {
+    int64_t len;
+    segment_of(n, W, u, &disp[u], &len);
+  }
+  disp[W] = n;
+  return gather_common(in, out, W, disp, dtype, stream);
+}
+
+int vcoll_allgatherv(const void* const* in, const int64_t* counts, void* const* out, int W,
+                     int dtype, void* stream) {
+  g_err[0] = 0;
+  int rc = check_common(W, 0, dtype, VCOLL_SUM);
+  if (rc) return rc;
+  if (!counts) return fail(VCOLL_ERR_INVALID_ARG, "counts is NULL");
+  int64_t disp[VCOLL_MAX_RANKS + 1];
+  disp[0] = 0;
+  for (int u = 0; u < W; ++u) {
+    if (counts[u] < 0) return fail(VCOLL_ERR_INVALID_ARG, "counts[%d] < 0", u);
+    disp[u + 1] = disp[u] + counts[u];
+  }
+  return gather_common(in, out, W, disp, dtype, stream);
 }
 
 int vcoll_fuse_plan(const int64_t* counts, int T, int dtype, int64_t threshold_bytes,
@@ -478,9 +516,13 @@ int vcoll_fuse_unpack(const void* const* fused, const int64_t* counts, int T,
   return fuse_common((const void* const*)tensors, counts, T, fused, W, dtype, 1, stream);
 }
 
-int vcoll_allreduce_multi(const void* const* in, void* const* out, const int64_t* counts, int T,
-                          int W, int dtype, int op, unsigned flags, void* stream) {
-  g_err[0] = 0;
+// Multi-tensor allreduce over consecutive batches of tensors: batch b is
+// tensors [batch_begin[b], batch_begin[b+1]), whose per-rank concatenation is
+// one virtual buffer segmented on its own (as its fusion buffer would be).
+// Pieces of different batches share launches; each carries its fold start.
+static int multi_run(const void* const* in, void* const* out, const int64_t* counts, int T, int W,
+                     int dtype, int op, unsigned flags, const std::vector<int>& batch_begin,
+                     void* stream) {
   int rc = check_common(W, 0, dtype, op);
   if (rc) return rc;
   if (flags & ~(VCOLL_FLAG_RING_ORDER | VCOLL_FLAG_STAGED | VCOLL_FLAG_DIRECT))
@@ -488,38 +530,47 @@ int vcoll_allreduce_multi(const void* const* in, void* const* out, const int64_t
   if (T < 0 || (T > 0 && (!counts || !in || !out)))
     return fail(VCOLL_ERR_INVALID_ARG, "invalid multi-tensor arguments");
   const int es = elem_size(dtype);
-  std::vector<int64_t> off(T + 1, 0);
-  for (int t = 0; t < T; ++t) {
-    if (counts[t] < 0) return fail(VCOLL_ERR_INVALID_ARG, "counts[%d] < 0", t);
-    off[t + 1] = off[t] + counts[t];
+  // per tensor: its offset inside its batch's virtual buffer, and that size
+  std::vector<int64_t> boff(T), bn(T);
+  int64_t total = 0;
+  for (size_t b = 0; b + 1 < batch_begin.size(); ++b) {
+    int64_t o = 0;
+    for (int t = batch_begin[b]; t < batch_begin[b + 1]; ++t) {
+      if (counts[t] < 0) return fail(VCOLL_ERR_INVALID_ARG, "counts[%d] < 0", t);
+      boff[t] = o;
+      o += counts[t];
+    }
+    for (int t = batch_begin[b]; t < batch_begin[b + 1]; ++t) bn[t] = o;
+    total += o;
   }
-  const int64_t n = off[T];
   std::vector<Buf> bufs;
   bufs.reserve(2 * (size_t)W * T);
-  for (int u = 0; u < W; ++u)
-    for (int t = 0; t < T; ++t) {
-      if (!counts[t]) continue;
-      const int64_t e = (int64_t)u * T + t;
-      if (!in[e] || !out[e])
-        return fail(VCOLL_ERR_INVALID_ARG, "tensor %d of rank %d is NULL", t, u);
-      if ((uint64_t)in[e] % es || (uint64_t)out[e] % es)
-        return fail(VCOLL_ERR_INVALID_ARG, "tensor %d of rank %d is not element-aligned", t, u);
-      // base: address of fused element 0 under this tensor's mapping
-      const uint64_t sh = (uint64_t)off[t] * es;
-      bufs.push_back({(uint64_t)in[e], (uint64_t)(counts[t] * es), (uint64_t)in[e] - sh, false});
-      bufs.push_back({(uint64_t)out[e], (uint64_t)(counts[t] * es), (uint64_t)out[e] - sh, true});
-    }
+  int64_t bbase = 0;  // distinct fused index space per batch for the aliasing check
+  for (size_t b = 0; b + 1 < batch_begin.size(); ++b) {
+    for (int u = 0; u < W; ++u)
+      for (int t = batch_begin[b]; t < batch_begin[b + 1]; ++t) {
+        if (!counts[t]) continue;
+        const int64_t e = (int64_t)u * T + t;
+        if (!in[e] || !out[e])
+          return fail(VCOLL_ERR_INVALID_ARG, "tensor %d of rank %d is NULL", t, u);
+        if ((uint64_t)in[e] % es || (uint64_t)out[e] % es)
+          return fail(VCOLL_ERR_INVALID_ARG, "tensor %d of rank %d is not element-aligned", t, u);
+        const uint64_t sh = (uint64_t)(bbase + boff[t]) * es;
+        bufs.push_back({(uint64_t)in[e], (uint64_t)(counts[t] * es), (uint64_t)in[e] - sh, false});
+        bufs.push_back({(uint64_t)out[e], (uint64_t)(counts[t] * es), (uint64_t)out[e] - sh, true});
+      }
+    bbase += bn[batch_begin[b]] + 1;
+  }
   if ((rc = check_aliasing(bufs))) return rc;
-  if (n == 0) return VCOLL_OK;
+  if (total == 0) return VCOLL_OK;
   if (W == 1) {
     for (int t = 0; t < T; ++t)
       if ((rc = copy_d2d(out[t], in[t], counts[t] * es, stream))) return rc;
     return VCOLL_OK;
   }
 
-  const bool ring = (flags & VCOLL_FLAG_RING_ORDER) && op != VCOLL_MAX && W > 2;
+  const bool ring = (flags & VCOLL_FLAG_RING_ORDER) && op != VCOLL_MAX && op != VCOLL_MIN && W > 2;
   const int W_t = (W == 2 || W == 4 || W == 8 || W == 16) ? W : 0;
-  const int nseg = ring ? W : 1;
   const void* fn = dtype == VCOLL_F32 ? multi_kernel_f32(op, W_t, ring)
                                       : multi_kernel_bf16(op, W_t, ring);
   const int threads = 256;
@@ -527,63 +578,80 @@ int vcoll_allreduce_multi(const void* const* in, void* const* out, const int64_t
   const int64_t tile_elems = (int64_t)threads * unroll_for(W_t) * V;
   const int max_t = std::min(kMultiMaxTensors, kMultiMaxPtrs / W);
 
+  // pieces of one tensor: pieces of a batch segment, each with its fold start
+  struct Cut {
+    int64_t k0, len;
+    int start;
+  };
+  auto cuts_of = [&](int tg, std::vector<Cut>& cuts) {
+    cuts.clear();
+    const int64_t n = bn[tg];
+    int64_t k = 0;
+    while (k < counts[tg]) {
+      const int64_t i = boff[tg] + k;
+      int j = 0;
+      int64_t seg_end = n;
+      if (ring) {
+        const int64_t q = n / W, r = n % W;
+        const int64_t big = r * (q + 1);
+        j = i < big ? (int)(i / (q + 1)) : (int)(r + (i - big) / q);
+        int64_t so, sl;
+        segment_of(n, W, j, &so, &sl);
+        seg_end = so + sl;
+      }
+      const int64_t len = std::min(counts[tg] - k, seg_end - i);
+      cuts.push_back({k, len, ring ? (j + 1) % W : 0});
+      k += len;
+    }
+  };
+
+  static_assert(kMultiMaxPieces >= VCOLL_MAX_RANKS, "a tensor has at most W pieces");
+  std::vector<Cut> cuts;
+  MultiParams prm;
   int t0 = 0;
   while (t0 < T) {
-    MultiParams prm;
     memset(&prm, 0, sizeof(prm));
     prm.W = W;
     prm.scale = op == VCOLL_AVG ? 1.0f / (float)W : 1.0f;
     prm.do_scale = op == VCOLL_AVG ? 1 : 0;
     prm.tile_elems = tile_elems;
-    const int nt = std::min(max_t, T - t0);
+    int nt = 0, np = 0;
+    int64_t tiles = 0, bytes = 0;
+    // take tensors while both the pointer table and the piece table have room
+    while (t0 + nt < T && nt < max_t) {
+      const int tg = t0 + nt;
+      cuts_of(tg, cuts);
+      if (np + (int)cuts.size() > kMultiMaxPieces) break;
+      for (const Cut& c : cuts) {
+        MultiPiece& pc = prm.piece[np++];
+        pc.k0 = c.k0;
+        pc.len = c.len;
+        pc.tile_begin = tiles;
+        pc.t = nt;
+        pc.start = c.start;
+        // one 16-byte phase for every rank's input and output at element k0?
+        int ph = -1;
+        bool same = true;
+        for (int u = 0; u < W && same; ++u) {
+          const uint64_t a = (uint64_t)in[(int64_t)u * T + tg] + (uint64_t)c.k0 * es;
+          const uint64_t o = (uint64_t)out[(int64_t)u * T + tg] + (uint64_t)c.k0 * es;
+          const int pa = (int)(a & 15), pb = (int)(o & 15);
+          if (ph < 0) ph = pa;
+          same = (pa == ph) && (pb == ph);
+        }
+        pc.phase = same ? ph / es : -1;
+        tiles += std::max<int64_t>(1, ceil_div(c.len, tile_elems));
+        bytes += c.len * es;
+      }
+      ++nt;
+    }
+    // pointer tables of the nt tensors taken (row stride nt)
     prm.T = nt;
     for (int u = 0; u < W; ++u)
       for (int t = 0; t < nt; ++t) {
         prm.in[u * nt + t] = in[(int64_t)u * T + t0 + t];
         prm.out[u * nt + t] = out[(int64_t)u * T + t0 + t];
       }
-    int np = 0;
-    int64_t tiles = 0;
-    int64_t bytes = 0;
-    for (int t = 0; t < nt; ++t) {
-      const int tg = t0 + t;
-      int64_t k = 0;
-      while (k < counts[tg]) {
-        // the segment holding fused index off[tg] + k, and where it ends
-        const int64_t i = off[tg] + k;
-        int j = 0;
-        int64_t seg_end = n;
-        if (nseg > 1) {
-          const int64_t q = n / W, r = n % W;
-          const int64_t big = r * (q + 1);
-          j = i < big ? (int)(i / (q + 1)) : (int)(r + (i - big) / q);
-          int64_t so, sl;
-          segment_of(n, W, j, &so, &sl);
-          seg_end = so + sl;
-        }
-        const int64_t len = std::min(counts[tg] - k, seg_end - i);
-        MultiPiece& pc = prm.piece[np++];
-        pc.k0 = k;
-        pc.len = len;
-        pc.tile_begin = tiles;
-        pc.t = t;
-        pc.start = ring ? (j + 1) % W : 0;
-        // one 16-byte phase for every rank's input and output at element k?
-        int ph = -1;
-        bool same = true;
-        for (int u = 0; u < W && same; ++u) {
-          const uint64_t a = (uint64_t)in[(int64_t)u * T + tg] + (uint64_t)k * es;
-          const uint64_t b = (uint64_t)out[(int64_t)u * T + tg] + (uint64_t)k * es;
-          const int pa = (int)(a & 15), pb = (int)(b & 15);
-          if (ph < 0) ph = pa;
-          same = (pa == ph) && (pb == ph);
-        }
-        pc.phase = same ? ph / es : -1;
-        tiles += std::max<int64_t>(1, ceil_div(len, tile_elems));
-        bytes += len * es;
-        k += len;
-      }
-    }
     prm.npieces = np;
     prm.num_tiles = tiles;
     if (np > 0 && (rc = launch(fn, tiles, threads, 0, bytes <= kSmallBytes, &prm, stream)))
@@ -591,6 +659,28 @@ int vcoll_allreduce_multi(const void* const* in, void* const* out, const int64_t
     t0 += nt;
   }
   return VCOLL_OK;
+}
+
+int vcoll_allreduce_multi(const void* const* in, void* const* out, const int64_t* counts, int T,
+                          int W, int dtype, int op, unsigned flags, void* stream) {
+  g_err[0] = 0;
+  if (T < 0) return fail(VCOLL_ERR_INVALID_ARG, "T = %d < 0", T);
+  std::vector<int> begin = {0, T};
+  return multi_run(in, out, counts, T, W, dtype, op, flags, begin, stream);
+}
+
+int vcoll_fusion_allreduce(const void* const* in, void* const* out, const int64_t* counts, int T,
+                           int W, int dtype, int op, unsigned flags, int64_t threshold_bytes,
+                           int* nbatches, void* stream) {
+  g_err[0] = 0;
+  if (T < 0) return fail(VCOLL_ERR_INVALID_ARG, "T = %d < 0", T);
+  std::vector<int> begin(T + 1);
+  int nb = 0;
+  int rc = vcoll_fuse_plan(counts, T, dtype, threshold_bytes, begin.data(), &nb);
+  if (rc) return rc;
+  begin.resize(nb + 1);
+  if (nbatches) *nbatches = nb;
+  return multi_run(in, out, counts, T, W, dtype, op, flags, begin, stream);
 }
 
 int vcoll_device_errors(unsigned* flags, int clear) {

@@ -30,7 +30,8 @@ __global__ void __launch_bounds__(256) vc_gather(const __grid_constant__ GatherP
     const int j = (int)(tile / p.tiles_per_seg);
     const int64_t k = tile - (int64_t)j * p.tiles_per_seg;
     int64_t a, b, av, bv;
-    segment_bounds(p.n, p.q, p.r, W, j, a, b);
+    a = p.disp[j];
+    b = p.disp[j + 1];
     if (VEC) {
       aligned_body<V>(a, b, p.phase, av, bv);
     } else {

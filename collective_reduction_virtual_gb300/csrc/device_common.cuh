@@ -27,6 +27,22 @@ struct OpMax {
   }
 };
 
+// min (NCCL FuncMin): the mirror image of OpMax -- canonical quiet NaN,
+// otherwise the smaller operand; equal operands give their bitwise OR, which
+// is -0 for +0 and -0.  Order-independent like max.
+struct OpMin {
+  static __device__ __forceinline__ float apply(float acc, float x) {
+    float r = acc < x ? acc : x;
+    r = acc == x ? __uint_as_float(__float_as_uint(acc) | __float_as_uint(x)) : r;
+    return (acc != acc || x != x) ? __uint_as_float(0x7FC00000u) : r;
+  }
+};
+
+// prod (NCCL FuncProd): one IEEE fp32 multiply, accumulator first.
+struct OpProd {
+  static __device__ __forceinline__ float apply(float acc, float x) { return __fmul_rn(acc, x); }
+};
+
 // ------------------------------------------------------------ element types
 template <typename T>
 struct Elem;

@@ -182,6 +182,8 @@ const void* pick_multi(int W_t, int ring) {
 template <typename T>
 const void* multi_table(int op, int W_t, int ring) {
   if (op == VCOLL_MAX) return pick_multi<T, OpMax>(W_t, 0);
+  if (op == VCOLL_MIN) return pick_multi<T, OpMin>(W_t, 0);
+  if (op == VCOLL_PROD) return pick_multi<T, OpProd>(W_t, ring);
   return pick_multi<T, OpSum>(W_t, ring);
 }
 }  // namespace

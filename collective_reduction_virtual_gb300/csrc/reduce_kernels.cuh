@@ -322,27 +322,34 @@ __global__ void __launch_bounds__(256) vc_reduce_elem(const __grid_constant__ Re
         return (const void*)&vc_reduce_vec_any<T, Op, KIND>;                                  \
     }                                                                                         \
   }                                                                                           \
-  /* max is order-independent: one (tree) instantiation serves both orders */                 \
-  template <int KIND>                                                                         \
+  /* max and min are order-independent: one (tree) instantiation, any order */                 \
+  template <class Op, int KIND>                                                                         \
   const void* pick_max(int W_t, int vec) {                                                    \
-    if (!vec) return (const void*)&vc_reduce_elem<T, OpMax, KIND>;                            \
+    if (!vec) return (const void*)&vc_reduce_elem<T, Op, KIND>;                            \
     switch (W_t) {                                                                            \
       case 2:                                                                                 \
-        return (const void*)&vc_reduce_vec<T, 2, OpMax, KIND, 0>;                             \
+        return (const void*)&vc_reduce_vec<T, 2, Op, KIND, 0>;                             \
       case 4:                                                                                 \
-        return (const void*)&vc_reduce_vec<T, 4, OpMax, KIND, 0>;                             \
+        return (const void*)&vc_reduce_vec<T, 4, Op, KIND, 0>;                             \
       case 8:                                                                                 \
-        return (const void*)&vc_reduce_vec<T, 8, OpMax, KIND, 0>;                             \
+        return (const void*)&vc_reduce_vec<T, 8, Op, KIND, 0>;                             \
       case 16:                                                                                \
-        return (const void*)&vc_reduce_vec<T, 16, OpMax, KIND, 0>;                            \
+        return (const void*)&vc_reduce_vec<T, 16, Op, KIND, 0>;                            \
       default:                                                                                \
-        return (const void*)&vc_reduce_vec_any<T, OpMax, KIND>;                               \
+        return (const void*)&vc_reduce_vec_any<T, Op, KIND>;                               \
     }                                                                                         \
   }                                                                                           \
   }                                                                                           \
   const void* FNAME(int op, int kind, int W_t, int ring, int vec) {                           \
     if (op == VCOLL_MAX)                                                                      \
-      return kind == KIND_AR ? pick_max<KIND_AR>(W_t, vec) : pick_max<KIND_RS>(W_t, vec);     \
+      return kind == KIND_AR ? pick_max<OpMax, KIND_AR>(W_t, vec)                             \
+                             : pick_max<OpMax, KIND_RS>(W_t, vec);                            \
+    if (op == VCOLL_MIN)                                                                      \
+      return kind == KIND_AR ? pick_max<OpMin, KIND_AR>(W_t, vec)                             \
+                             : pick_max<OpMin, KIND_RS>(W_t, vec);                            \
+    if (op == VCOLL_PROD)                                                                     \
+      return kind == KIND_AR ? pick<OpProd, KIND_AR>(W_t, ring, vec)                          \
+                             : pick<OpProd, KIND_RS>(W_t, ring, vec);                         \
     return kind == KIND_AR ? pick<OpSum, KIND_AR>(W_t, ring, vec)                             \
                            : pick<OpSum, KIND_RS>(W_t, ring, vec);                            \
   }                                                                                           \

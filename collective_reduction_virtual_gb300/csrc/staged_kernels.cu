@@ -203,6 +203,12 @@ const void* staged_table(int op, int kind, int W_t, int ring) {
   if (op == VCOLL_MAX)  // order-independent: the tree instantiation serves both orders
     return kind == KIND_AR ? pick_staged<T, OpMax, KIND_AR>(W_t, 0)
                            : pick_staged<T, OpMax, KIND_RS>(W_t, 0);
+  if (op == VCOLL_MIN)
+    return kind == KIND_AR ? pick_staged<T, OpMin, KIND_AR>(W_t, 0)
+                           : pick_staged<T, OpMin, KIND_RS>(W_t, 0);
+  if (op == VCOLL_PROD)
+    return kind == KIND_AR ? pick_staged<T, OpProd, KIND_AR>(W_t, ring)
+                           : pick_staged<T, OpProd, KIND_RS>(W_t, ring);
   return kind == KIND_AR ? pick_staged<T, OpSum, KIND_AR>(W_t, ring)
                          : pick_staged<T, OpSum, KIND_RS>(W_t, ring);
 }

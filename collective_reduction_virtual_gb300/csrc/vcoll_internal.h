@@ -45,13 +45,13 @@ struct ReduceParams {
   int do_scale;
 };
 
-// Parameters of one allgather launch.  in[j] holds segment j.
+// Parameters of one allgather launch.  in[j] holds piece j, which lands at
+// [disp[j], disp[j+1]) of every output (the even segments for allgather,
+// per-rank counts for allgatherv).
 struct GatherParams {
   const void* in[VCOLL_MAX_RANKS];
   void* out[VCOLL_MAX_RANKS];
-  int64_t n;
-  int64_t q;
-  int64_t r;
+  int64_t disp[VCOLL_MAX_RANKS + 1];
   int64_t tiles_per_seg;
   int64_t num_tiles;
   int64_t tile_elems;

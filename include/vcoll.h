@@ -28,14 +28,15 @@
  *  - Types: VCOLL_F32 and VCOLL_BF16.  Arithmetic is fp32 for both; bf16
  *    inputs are widened exactly and outputs rounded to nearest even once.
  *  - Ops: VCOLL_SUM, VCOLL_MAX, VCOLL_AVG (sum times fl32(1/W), applied once
- *    to the finished sum).  max: a NaN operand gives the canonical quiet NaN;
- *    +0 wins over -0; otherwise the larger value.
+ *    to the finished sum), VCOLL_MIN, VCOLL_PROD (one fp32 multiply per hop).
+ *    max: a NaN operand gives the canonical quiet NaN; +0 wins over -0;
+ *    otherwise the larger value.  min: the mirror image (-0 wins over +0).
  *  - Order: with VCOLL_FLAG_RING_ORDER each element of segment j is folded
  *    in ring order -- starting at rank (j+1) mod W, accumulator first, ending
  *    at rank j -- which reproduces the early NCCL ring bit for bit.  Without
  *    it the library uses its fastest order (a pairwise tree for W in
  *    {4, 8, 16}); results then differ from ring order only by float
- *    reassociation.  max is the same in every order.
+ *    reassociation.  max and min are the same in every order.
  *  - Special cases: n == 0 returns VCOLL_OK without enqueuing anything;
  *    W == 1 is a device-to-device copy (nothing when in and out coincide).
  *
@@ -63,7 +64,13 @@ extern "C" {
 
 typedef enum { VCOLL_F32 = 0, VCOLL_BF16 = 1 } vcoll_dtype_t;
 
-typedef enum { VCOLL_SUM = 0, VCOLL_MAX = 1, VCOLL_AVG = 2 } vcoll_op_t;
+typedef enum {
+  VCOLL_SUM = 0,
+  VCOLL_MAX = 1,
+  VCOLL_AVG = 2,
+  VCOLL_MIN = 3, /* NCCL FuncMin */
+  VCOLL_PROD = 4 /* NCCL FuncProd */
+} vcoll_op_t;
 
 typedef enum {
   VCOLL_OK = 0,
@@ -104,6 +111,17 @@ int vcoll_reduce_scatter(const void* const* in, void* const* out, int W, int64_t
  */
 int vcoll_allgather(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,
                     unsigned flags, void* stream);
+
+/*
+ * Allgather with per-rank sizes (Horovod's allgatherv path: every rank's
+ * tensor, first dimensions possibly different, concatenated in rank order on
+ * every rank).  in[j]: counts[j] elements (counts: host array of W).
+ * out[u]: receives counts[0] + ... + counts[W-1] elements, piece j at
+ * counts[0] + ... + counts[j-1].  In place: in[j] == (char*)out[u] + that
+ * offset * elemsize.
+ */
+int vcoll_allgatherv(const void* const* in, const int64_t* counts, void* const* out, int W,
+                     int dtype, void* stream);
 
 /*
  * Allreduce ("Distributed primitives", section 1 and ring allreduce =
@@ -158,6 +176,19 @@ int vcoll_fuse_unpack(const void* const* fused, const int64_t* counts, int T,
  */
 int vcoll_allreduce_multi(const void* const* in, void* const* out, const int64_t* counts, int T,
                           int W, int dtype, int op, unsigned flags, void* stream);
+
+/*
+ * Tensor-fusion allreduce, planned and executed in one call: the Horovod
+ * batches of vcoll_fuse_plan(counts, T, dtype, threshold_bytes) are each
+ * allreduced as in vcoll_allreduce_multi (each batch segmented on its own,
+ * exactly as its fusion buffer would be), with the pieces of all batches
+ * sharing kernel launches.  *nbatches (may be NULL) receives the batch count.
+ * Same arguments and aliasing rules as vcoll_allreduce_multi; the bits equal
+ * pack -> vcoll_allreduce -> unpack per batch.
+ */
+int vcoll_fusion_allreduce(const void* const* in, void* const* out, const int64_t* counts, int T,
+                           int W, int dtype, int op, unsigned flags, int64_t threshold_bytes,
+                           int* nbatches, void* stream);
 
 /* Device-side error bits, OR-ed into one word per device by the kernels.
  * The staged kernels bound every wait on their shared-memory barriers; a wait

@@ -4,6 +4,9 @@ Tolerances (the pages fix none numerically; these follow from the arithmetic):
 
 * ring order, max, allgather, fusion copies: bit-exact.  NaN compares equal to
   NaN (payloads of a sum of NaNs are not specified by IEEE 754).
+* prod in the fastest order: each multiply rounds relatively, so two orders
+  differ by at most 2 (W - 1) u |result| (inputs kept away from overflow and
+  underflow).
 * fp32 in the library's fastest order: the result and the ring-order oracle
   are two orderings of the same W - 1 fp32 additions; each is within
   gamma_{W-1} * sum_r |x_r| of the exact sum (Higham, Accuracy and Stability of
@@ -71,13 +74,18 @@ def assert_close_fast(got: np.ndarray, want: np.ndarray, abs_sum: np.ndarray, W:
                       what: str = ""):
     """Fastest-order result against the ring-order oracle (see module doc)."""
     assert got.shape == want.shape
-    if op == "max":
+    if op in ("max", "min"):
         return assert_bit_exact(got, want, what)
     gn, wn = _isnan(got), _isnan(want)
     assert np.array_equal(gn, wn), f"{what}: NaN positions differ"
     g, w = widen(got), widen(want)
     ok = gn | (g == w)
-    bound = fp32_bound(abs_sum, W, op)
+    if op == "prod":
+        # products: each of the W - 1 multiplies rounds relatively, so two
+        # orders differ by at most 2 (W - 1) u |result| (no overflow/underflow)
+        bound = 2 * (W - 1) * U32 * np.abs(w) * (1 + 4 * (W - 1) * U32)
+    else:
+        bound = fp32_bound(abs_sum, W, op)
     diff = np.abs(g - w)
     if got.dtype == np.float32:
         ok |= diff <= bound

@@ -190,3 +190,31 @@ def test_allreduce_multi_argument_errors(v):
     assert f(ins, bad, [10, 20], 2, 2, v.F32, v.SUM) == v.ERR_INVALID_ARG
     # empty tensors need no pointers
     assert f([0] * 4, [0] * 4, [0, 0], 2, 2, v.F32, v.SUM) == v.OK
+
+
+def test_new_ops_and_allgatherv_errors(v):
+    # min and prod are valid ops; 5 is not
+    assert v.vcoll_allreduce([0] * 4, [0] * 4, 4, 0, v.F32, v.MIN, 0, 0) == v.OK
+    assert v.vcoll_allreduce([0] * 4, [0] * 4, 4, 0, v.F32, v.PROD, 0, 0) == v.OK
+    assert v.vcoll_allreduce(FAKE_IN[:4], FAKE_OUT[:4], 4, 64, v.F32, 5, 0, 0) == v.ERR_INVALID_OP
+    f = v.vcoll_allgatherv
+    assert f(FAKE_IN[:2], [10, -1], FAKE_OUT[:2], 2, v.F32) == v.ERR_INVALID_ARG
+    assert f(FAKE_IN[:2], [10, 20], FAKE_OUT[:2], 2, 3) == v.ERR_INVALID_TYPE
+    assert f(FAKE_IN[:2], [10, 20], FAKE_OUT[:2], 0, v.F32) == v.ERR_INVALID_ARG
+    assert f([0, FAKE_IN[1]], [10, 20], FAKE_OUT[:2], 2, v.F32) == v.ERR_INVALID_ARG
+    # a zero-length piece needs no pointer; an empty total is a no-op
+    assert f([0, 0], [0, 0], [0, 0], 2, v.F32) == v.OK
+    # piece overlapping an output away from its own offset
+    assert f([FAKE_OUT[0] + 4, FAKE_IN[1]], [10, 20], FAKE_OUT[:2], 2, v.F32) == v.ERR_INVALID_ARG
+
+
+def test_fusion_allreduce_errors(v):
+    ins = [0x100000 * (i + 1) for i in range(4)]
+    outs = [0x10000000 + 0x100000 * i for i in range(4)]
+    f = v.vcoll_fusion_allreduce
+    assert f(ins, outs, [10, 20], 2, 2, v.F32, 9)[0] == v.ERR_INVALID_OP
+    assert f(ins, outs, [10, 20], 2, 2, 5, v.SUM)[0] == v.ERR_INVALID_TYPE
+    assert f(ins, outs, [10, -1], 2, 2, v.F32, v.SUM)[0] == v.ERR_INVALID_ARG
+    assert f(ins, outs, [10, 20], -1, 2, v.F32, v.SUM)[0] == v.ERR_INVALID_ARG
+    rc, nb = f([0] * 4, [0] * 4, [0, 0], 2, 2, v.F32, v.SUM, 0, 64)
+    assert rc == v.OK and nb == 1

@@ -408,3 +408,103 @@ def test_fusion_direct_equals_pipeline_full_workload(v):
         v.fusion_allreduce_direct(tens, b, op="avg", ring_order=ring)
         for u in range(W):
             assert torch.equal(torch.cat(a[u]).view(torch.int32), torch.cat(b[u]).view(torch.int32))
+
+
+# ------------------------------------------------------------ min and prod
+
+def _near_one(W, n, dtype, seed):
+    """sign * 2^U(-1, 1): products of up to 64 stay far from overflow."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    out = []
+    for _ in range(W):
+        mag = torch.pow(2.0, torch.rand(n, generator=g, device="cuda") * 2 - 1)
+        sgn = torch.where(torch.rand(n, generator=g, device="cuda") < 0.5, -1.0, 1.0)
+        out.append((mag * sgn).to(DT[dtype]))
+    return out
+
+
+@pytest.mark.parametrize("W", SMALL_W)
+@pytest.mark.parametrize("n", [1, 17, 4099, 65541])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_min_prod_small(v, W, n, dtype):
+    for op in ("min", "prod"):
+        ins = _near_one(W, n, dtype, 7000 * W + n) if op == "prod" else \
+            make_inputs(W, n, dtype, 7100 * W + n)
+        ins_np = [to_np(t) for t in ins]
+        want = oracle.allreduce(ins_np, op, ODT[dtype])
+        rs_want = oracle.reduce_scatter(ins_np, op, ODT[dtype])
+        for ring in (True, False):
+            got = v.allreduce(ins, op=op, ring_order=ring)
+            rs = v.reduce_scatter(ins, op=op, ring_order=ring)
+            for u in range(W):
+                if ring or op == "min":
+                    assert_bit_exact(to_np(got[u]), want[u], f"AR {op} ring={ring}")
+                    assert_bit_exact(to_np(rs[u]), rs_want[u], f"RS {op} ring={ring}")
+                else:
+                    assert_close_fast(to_np(got[u]), want[u], None, W, op, f"AR {op}")
+            if W in (2, 4, 8, 16) and n > 1000:
+                st = v.allreduce(ins, op=op, ring_order=ring, flags=v.FLAG_STAGED)
+                assert to_np(st[0]).tobytes() == to_np(got[0]).tobytes()
+        tens = [[t] for t in ins]
+        multi = v.allreduce_multi(tens, op=op, ring_order=True)
+        for u in range(W):
+            assert_bit_exact(to_np(multi[u][0]), want[u], f"multi {op}")
+
+
+def test_prod_ring_order_hand_derived_on_gpu(v):
+    x = [torch.full((4,), val, device="cuda") for val in (2.0 ** 100, 2.0 ** 100, 2.0 ** -100,
+                                                          2.0 ** -100)]
+    outs = v.reduce_scatter(x, op="prod", ring_order=True)
+    assert [float(o[0]) for o in outs] == [1.0, 0.0, 1.0, float("inf")]
+
+
+# ------------------------------------------------------------ allgatherv
+
+@pytest.mark.parametrize("W", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_allgatherv(v, W, dtype):
+    rng = np.random.default_rng(W)
+    counts = [int(c) for c in rng.integers(0, 20000, W)]
+    counts[0] = 0 if W > 1 else counts[0]
+    pieces = [make_inputs(1, c, dtype, 8000 + j)[0] for j, c in enumerate(counts)]
+    want = oracle.allgatherv([to_np(p) for p in pieces], ODT[dtype])
+    outs = v.allgatherv(pieces)
+    for u in range(W):
+        assert_bit_exact(to_np(outs[u]), want[u], f"AGV rank {u}")
+    # in place: each piece already sits at its offset in its own output
+    full = [torch.empty(sum(counts), dtype=DT[dtype], device="cuda") for _ in range(W)]
+    offs = np.cumsum([0] + counts)
+    views = []
+    for j in range(W):
+        full[j][offs[j]:offs[j + 1]].copy_(pieces[j])
+        views.append(full[j][offs[j]:offs[j + 1]])
+    v.allgatherv(views, full)
+    for u in range(W):
+        assert_bit_exact(to_np(full[u]), want[u], "AGV in place")
+
+
+@pytest.mark.parametrize("W", [3, 8, 16])
+@pytest.mark.parametrize("ring", [True, False])
+def test_fusion_allreduce_entry_many_batches(v, W, ring):
+    # many small batches: pieces of several batches share launches, and the
+    # piece table (not the pointer table) decides where a launch ends
+    rng = np.random.default_rng(W)
+    counts = [int(c) for c in rng.integers(1, 2500, 150)]
+    thr = 4 * 3000
+    tens = _tensor_list(W, counts, "f32", 900 + W)
+    a = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+    fused = [torch.empty(max(counts) + 3000, device="cuda") for _ in range(W)]
+    v.fusion_allreduce(tens, a, fused, op="avg", ring_order=ring, threshold_bytes=thr)
+    b = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+    plan = v.FusionPlan(tens, b, op="avg", ring_order=ring, threshold_bytes=thr)
+    plan()
+    assert plan.nbatches == len(v.fuse_plan(counts, v.F32, thr)) - 1
+    for u in range(W):
+        assert torch.equal(torch.cat(a[u]).view(torch.int32), torch.cat(b[u]).view(torch.int32))
+    if ring:
+        want = oracle.fusion_allreduce([[to_np(t) for t in tens[u]] for u in range(W)], counts,
+                                       "avg", oracle.F32, thr)
+        for u in (0, W - 1):
+            for t in range(len(counts)):
+                assert_bit_exact(to_np(b[u][t]), want[u][t], "fusion entry vs oracle")
