@@ -271,7 +271,7 @@ def build_workload(args, dev, rank):
     seed_off = 100_000 * rank  # every replica draws its own inputs
     if args.op in ("fusion", "multi"):
         W = args.W or 8
-        counts = [int(c) for c in I.fusion_counts()]
+        counts = [int(c) for c in I.fusion_counts()][:args.tensors]
         g = torch.Generator(device=dev)
         tens = []
         for u in range(W):
@@ -293,7 +293,7 @@ def build_workload(args, dev, rank):
             bytes_ = 2 * W * B
             desc = ("64 MiB batches, read straight from the tensors and written straight to "
                     "the outputs (2*W*B), batches planned and launched in C")
-        return dict(name=f"tensor-fusion allreduce {red}, W={W}, 200 {args.dtype} tensors per "
+        return dict(name=f"tensor-fusion allreduce {red}, W={W}, {len(counts)} {args.dtype} tensors per "
                          f"rank (log-uniform 1024..4194304 elements), {desc}",
                     W=W, n=sum(counts), step=step, bytes=bytes_, launches=launches,
                     ins=[t for row in tens for t in row], outs=[t for row in outs for t in row],
@@ -593,6 +593,7 @@ def main(argv=None):
     ap.add_argument("--op", choices=["allreduce", "reduce_scatter", "allgather", "fusion", "multi"],
                     default="allreduce")
     ap.add_argument("--W", type=int, default=None, help="virtual ranks (default 8)")
+    ap.add_argument("--tensors", type=int, default=200, help="tensors per rank for fusion/multi")
     ap.add_argument("--dtype", choices=["f32", "bf16"], default="f32")
     ap.add_argument("--reduction", choices=["sum", "max", "avg"], default=None)
     ap.add_argument("--order", choices=["fast", "ring"], default="fast")
