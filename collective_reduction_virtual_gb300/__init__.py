@@ -14,6 +14,8 @@ Two layers, same names as the C ABI:
   (``VcollError`` is raised by the tensor layer, not here);
 * ``reduce_scatter(ins, outs=None, op="sum", ring_order=False)`` and friends
   take lists of CUDA tensors (one per virtual rank) and raise ``VcollError``.
+  Pinned host tensors are accepted as well: the kernels then read and write
+  host memory directly over the CPU-GPU link (no staging copies).
 """
 from __future__ import annotations
 
@@ -207,8 +209,9 @@ def _stream_handle(stream) -> int:
 
 def _check_tensors(ts, what):
     for i, t in enumerate(ts):
-        if not t.is_cuda:
-            raise VcollError(ERR_INVALID_ARG, f"{what}[{i}] is not a CUDA tensor")
+        if not (t.is_cuda or t.is_pinned()):
+            raise VcollError(ERR_INVALID_ARG,
+                             f"{what}[{i}] is neither a CUDA tensor nor pinned host memory")
         if not t.is_contiguous():
             raise VcollError(ERR_INVALID_ARG, f"{what}[{i}] is not contiguous")
 

@@ -8,7 +8,11 @@
  * Common conventions for every entry point below
  * ------------------------------------------------
  *  - Pointer arrays (`in`, `out`, `tensors`, `fused`) are HOST arrays of
- *    DEVICE pointers on the current device.  Each device pointer must be
+ *    DEVICE pointers on the current device.  Pinned host memory
+ *    (cudaHostAlloc / cudaHostRegister) is accepted too: with unified
+ *    addressing its host pointer is a device pointer, and the kernels then
+ *    read and write it directly over the CPU-GPU link, which is faster than
+ *    staging copies in and out.  Each device pointer must be
  *    aligned to the element size.  Any 16-byte phase works; when all buffers
  *    of one call share the same phase the 16-byte vector path runs, otherwise
  *    an element-wise path gives the same bits more slowly.

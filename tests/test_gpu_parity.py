@@ -508,3 +508,33 @@ def test_fusion_allreduce_entry_many_batches(v, W, ring):
         for u in (0, W - 1):
             for t in range(len(counts)):
                 assert_bit_exact(to_np(b[u][t]), want[u][t], "fusion entry vs oracle")
+
+
+# ------------------------------------------------- pinned host buffers
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_pinned_host_buffers(v, dtype):
+    # the kernels read and write pinned host memory directly (unified
+    # addressing); the bits equal the device-buffer path
+    W, n = 8, 300_007
+    ins = make_inputs(W, n, dtype, 61)
+    h_in = [t.cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(n, dtype=DT[dtype], pin_memory=True) for _ in range(W)]
+    for op in ("sum", "avg", "max"):
+        for ring in (True, False):
+            d = v.allreduce(ins, op=op, ring_order=ring)
+            v.allreduce(h_in, h_out, op=op, ring_order=ring)
+            torch.cuda.synchronize()
+            for u in range(W):
+                assert to_np(h_out[u]).tobytes() == to_np(d[u]).tobytes()
+    segs = [torch.empty(v.segment(n, W, j)[1], dtype=DT[dtype], pin_memory=True) for j in range(W)]
+    v.reduce_scatter(h_in, segs, op="sum", ring_order=True)
+    torch.cuda.synchronize()
+    want = oracle.reduce_scatter([to_np(t) for t in ins], "sum", ODT[dtype])
+    for j in range(W):
+        assert_bit_exact(to_np(segs[j]), want[j], "RS on host buffers")
+    v.allgather(segs, n, h_out)
+    torch.cuda.synchronize()
+    ring = v.allreduce(ins, op="sum", ring_order=True)
+    for u in range(W):
+        assert to_np(h_out[u]).tobytes() == to_np(ring[u]).tobytes()
