@@ -497,7 +497,7 @@ static int fuse_common(const void* const* tensors, const int64_t* counts, int T,
     prm.tile_begin[nt] = tiles;
     for (int u = 0; u < W; ++u) {
       prm.fused[u] = (void*)fused[u];
-      for (int t = 0; t < nt; ++t) prm.tensor[u * nt + t] = (void*)tensors[(int64_t)u * T + t0 + t];
+      for (int t = 0; t < nt; ++t) prm.tensor[t * W + u] = (void*)tensors[(int64_t)u * T + t0 + t];
     }
     if (tiles == 0) continue;
     rc = launch(fuse_kernel(es), tiles, threads, 0, bytes <= kSmallBytes, &prm, stream);
@@ -645,12 +645,12 @@ static int multi_run(const void* const* in, void* const* out, const int64_t* cou
       }
       ++nt;
     }
-    // pointer tables of the nt tensors taken (row stride nt)
+    // pointer tables of the nt tensors taken, tensor-major (t * W + u)
     prm.T = nt;
     for (int u = 0; u < W; ++u)
       for (int t = 0; t < nt; ++t) {
-        prm.in[u * nt + t] = in[(int64_t)u * T + t0 + t];
-        prm.out[u * nt + t] = out[(int64_t)u * T + t0 + t];
+        prm.in[t * W + u] = in[(int64_t)u * T + t0 + t];
+        prm.out[t * W + u] = out[(int64_t)u * T + t0 + t];
       }
     prm.npieces = np;
     prm.num_tiles = tiles;

@@ -166,23 +166,27 @@ __device__ __forceinline__ void copy_range(char* dst, const char* src, int64_t n
 
 template <int ES>
 __global__ void __launch_bounds__(256) vc_fuse(const __grid_constant__ FuseParams p) {
-  const int64_t total = p.tile_begin[p.T];
+  // tile table in shared memory: the per-tile search stays on chip
+  __shared__ int64_t s_begin[kFuseMaxTensors + 1];
+  for (int i = threadIdx.x; i <= p.T; i += blockDim.x) s_begin[i] = p.tile_begin[i];
+  __syncthreads();
+  const int64_t total = s_begin[p.T];
   for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
     // tensor t with tile_begin[t] <= tile < tile_begin[t + 1]
     int lo = 0, hi = p.T - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.tile_begin[mid] <= tile)
+      if (s_begin[mid] <= tile)
         lo = mid;
       else
         hi = mid - 1;
     }
     const int t = lo;
-    const int64_t k = tile - p.tile_begin[t];
+    const int64_t k = tile - s_begin[t];
     const int64_t e0 = k * p.tile_elems;
     const int64_t e1 = e0 + p.tile_elems < p.count[t] ? e0 + p.tile_elems : p.count[t];
     for (int u = 0; u < p.W; ++u) {
-      char* tens = (char*)p.tensor[u * p.T + t] + e0 * ES;
+      char* tens = (char*)p.tensor[t * p.W + u] + e0 * ES;
       char* fus = (char*)p.fused[u] + (p.offset[t] + e0) * ES;
       if (p.unpack)
         copy_range<ES>(tens, fus, (e1 - e0) * ES);

@@ -14,11 +14,12 @@ namespace vcoll {
 
 namespace {
 
+// Pointer tables are tensor-major: the W pointers a tile needs are adjacent.
 __device__ __forceinline__ const char* in_ptr(const MultiParams& p, int rank, int t) {
-  return (const char*)p.in[rank * p.T + t];
+  return (const char*)p.in[t * p.W + rank];
 }
 __device__ __forceinline__ char* out_ptr(const MultiParams& p, int rank, int t) {
-  return (char*)p.out[rank * p.T + t];
+  return (char*)p.out[t * p.W + rank];
 }
 
 // Pairwise tree over ranks [LO, LO + CNT) for one element (matches TreeFold).
@@ -71,16 +72,22 @@ __global__ void __launch_bounds__(256, 2) vc_allreduce_multi(const __grid_consta
   const int W = WT > 0 ? WT : p.W;
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
+  // the piece table moves to shared memory once, so that finding a tile's
+  // piece is a short search in shared memory rather than a chain of
+  // dependent parameter-space loads
+  __shared__ MultiPiece s_piece[kMultiMaxPieces];
+  for (int i = tid; i < p.npieces; i += nthr) s_piece[i] = p.piece[i];
+  __syncthreads();
   for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
     int lo = 0, hi = p.npieces - 1;  // last piece with tile_begin <= tile
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.piece[mid].tile_begin <= tile)
+      if (s_piece[mid].tile_begin <= tile)
         lo = mid;
       else
         hi = mid - 1;
     }
-    const MultiPiece pc = p.piece[lo];
+    const MultiPiece pc = s_piece[lo];
     const int64_t k = tile - pc.tile_begin;
     const int t = pc.t;
     const int start = RING ? pc.start : 0;

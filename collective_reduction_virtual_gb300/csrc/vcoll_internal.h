@@ -60,8 +60,8 @@ struct GatherParams {
 };
 
 // Fusion pack / unpack.  One launch copies up to kFuseMaxTensors tensors of
-// every rank.  Copy e = u * T + t moves count[t] elements between
-// tensor[e] and fused[u] + offset[t].  Work is tiled per tensor:
+// every rank.  Copy (t, u) moves count[t] elements between tensor[t * W + u]
+// (tensor-major) and fused[u] + offset[t].  Work is tiled per tensor:
 // tile_begin[t] is the first tile of tensor t (tile_begin[T] = total), each
 // tile covers tile_elems elements of that tensor on all W ranks.
 constexpr int kFuseMaxTensors = 64;
@@ -99,6 +99,7 @@ struct MultiPiece {
   int pad;
 };
 struct MultiParams {
+  // tensor-major: in[t * W + u] is tensor t of rank u
   const void* in[kMultiMaxPtrs];
   void* out[kMultiMaxPtrs];
   MultiPiece piece[kMultiMaxPieces];
