@@ -319,7 +319,7 @@ def build_workload(args, dev, rank):
     else:  # allgather: the inputs are the W segments
         ins = [t[:vc.segment(n, W, j)[1]].clone() for j, t in enumerate(ins)]
         outs = [torch.empty(n, dtype=dt, device=dev) for _ in range(W)]
-        step = lambda: vc.allgather(ins, n, outs)  # noqa
+        step = lambda: vc.allgather(ins, n, outs, flags=vflags)  # noqa
         bytes_ = (1 + W) * n * es
         host_step = lambda hi, ho: vc.allgather(hi, n, ho)  # noqa
     dist_name = {"gradient": "normal(0,1e-3)", "uniform": "uniform[-1,1]",
@@ -466,6 +466,8 @@ def extras(args, stream, dev):
     out["rs_sum_w8_f32_2^26"] = rate(lambda: vc.reduce_scatter(ins, segs, op="sum"),
                                      (W + 1) * n * 4)
     out["ag_w8_f32_2^26"] = rate(lambda: vc.allgather(segs, n, outs), (1 + W) * n * 4)
+    out["ag_w8_f32_2^26_tma"] = rate(lambda: vc.allgather(segs, n, outs, flags=vc.FLAG_STAGED),
+                                     (1 + W) * n * 4)
     out["ar_ring_sum_w8_f32_2^26"] = rate(
         lambda: vc.allreduce(ins, outs, op="sum", ring_order=True), 2 * W * n * 4)
     out["ar_sum_w8_f32_2^26_staged"] = rate(

@@ -337,7 +337,7 @@ int vcoll_allreduce(const void* const* in, void* const* out, int W, int64_t n, i
 // Allgather of W pieces, piece j landing at [disp[j], disp[j+1]) of every
 // output (shared by allgather and allgatherv).
 static int gather_common(const void* const* in, void* const* out, int W, const int64_t* disp,
-                         int dtype, void* stream) {
+                         int dtype, unsigned flags, void* stream) {
   const int es = elem_size(dtype);
   const int64_t n = disp[W];
   int64_t in_len[VCOLL_MAX_RANKS], out_len[VCOLL_MAX_RANKS];
@@ -383,6 +383,22 @@ static int gather_common(const void* const* in, void* const* out, int W, const i
   }
   prm.tiles_per_seg = tps;
   prm.num_tiles = tps * W;
+  if ((flags & VCOLL_FLAG_STAGED) && vec && !small) {
+    // TMA variant: bulk loads into shared memory, W bulk stores per tile
+    prm.tile_elems = kGatherTmaTileBytes / es;
+    tps = 1;
+    for (int j = 0; j < W; ++j) {
+      const int64_t a = disp[j], b = disp[j + 1];
+      const int64_t up = a + ((V - ((a + phase) % V)) % V);
+      const int64_t av = std::min(up, b);
+      const int64_t bv = std::max(b - ((b + phase) % V), av);
+      tps = std::max(tps, ceil_div(bv - av, prm.tile_elems));
+    }
+    prm.tiles_per_seg = tps;
+    prm.num_tiles = tps * W;
+    return launch(gather_tma_kernel(es), prm.num_tiles, kGatherTmaThreads,
+                  (size_t)kGatherTmaStages * kGatherTmaTileBytes + 64, false, &prm, stream);
+  }
   return launch(gather_kernel(es, vec), prm.num_tiles, threads, 0, small, &prm, stream);
 }
 
@@ -399,7 +415,7 @@ int vcoll_allgather(const void* const* in, void* const* out, int W, int64_t n, i
     segment_of(n, W, u, &disp[u], &len);
   }
   disp[W] = n;
-  return gather_common(in, out, W, disp, dtype, stream);
+  return gather_common(in, out, W, disp, dtype, flags, stream);
 }
 
 int vcoll_allgatherv(const void* const* in, const int64_t* counts, void* const* out, int W,
@@ -414,7 +430,7 @@ int vcoll_allgatherv(const void* const* in, const int64_t* counts, void* const* 
     if (counts[u] < 0) return fail(VCOLL_ERR_INVALID_ARG, "counts[%d] < 0", u);
     disp[u + 1] = disp[u] + counts[u];
   }
-  return gather_common(in, out, W, disp, dtype, stream);
+  return gather_common(in, out, W, disp, dtype, 0, stream);
 }
 
 int vcoll_fuse_plan(const int64_t* counts, int T, int dtype, int64_t threshold_bytes,

@@ -75,6 +75,24 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
       : "memory");
 }
 
+__device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src, unsigned bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
+               "r"(smem_addr(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most N committed bulk groups may still be reading shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 }  // namespace
 
 template <typename T, int WT, class Op, int KIND, int RING>
@@ -213,6 +231,105 @@ const void* staged_table(int op, int kind, int W_t, int ring) {
                          : pick_staged<T, OpSum, KIND_RS>(W_t, ring);
 }
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// Allgather on the TMA engine: one thread per CTA moves each tile of segment j
+// HBM -> shared memory with one bulk copy, then shared memory -> the W
+// outputs with W bulk stores; kGatherStages tiles in flight.  Before a stage
+// is refilled, the stores that read it (kGatherStages - 1 groups ago) must
+// have finished reading.  The unaligned head and tail of each segment (< 16
+// bytes each) are copied by ordinary threads.
+constexpr int kGatherStages = kGatherTmaStages;
+constexpr int kGatherTileBytes = kGatherTmaTileBytes;
+
+template <int ES>
+__global__ void __launch_bounds__(kGatherTmaThreads, 1) vc_gather_tma(const __grid_constant__ GatherParams p) {
+  using B = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
+  constexpr int V = 16 / ES;
+  constexpr int S = kGatherStages;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kGatherTileBytes);
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int W = p.W;
+  // tile i of this CTA: its aligned body [e0, e1) inside segment j
+  auto range = [&](int64_t tile, int& j, int64_t& a, int64_t& b, int64_t& e0, int64_t& e1,
+                   int64_t& av, int64_t& bv) {
+    j = (int)(tile / p.tiles_per_seg);
+    const int64_t k = tile - (int64_t)j * p.tiles_per_seg;
+    a = p.disp[j];
+    b = p.disp[j + 1];
+    aligned_body<V>(a, b, p.phase, av, bv);
+    e0 = av + k * p.tile_elems;
+    e1 = e0 + p.tile_elems < bv ? e0 + p.tile_elems : bv;
+    if (e1 < e0) e1 = e0;
+  };
+  // unaligned heads and tails, element by element, by every thread
+  for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    int j;
+    int64_t a, b, e0, e1, av, bv;
+    range(tile, j, a, b, e0, e1, av, bv);
+    if (tile - (int64_t)j * p.tiles_per_seg != 0) continue;
+    const char* src = (const char*)p.in[j] - a * ES;
+    int64_t i = -1;
+    if (tid < av - a) i = a + tid;
+    if (tid >= 32 && tid - 32 < b - bv) i = bv + (tid - 32);
+    if (i >= 0) {
+      const B x = ld1<B>(src + i * ES);
+      for (int r = 0; r < W; ++r) st1((char*)p.out[r] + i * ES, x);
+    }
+  }
+  if (tid != 0) return;
+  // bodies: one thread drives the TMA engine
+  const int64_t n_mine = blockIdx.x < p.num_tiles
+                             ? (p.num_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x
+                             : 0;
+  auto issue = [&](int64_t i) {  // load tile i into stage i % S
+    int j;
+    int64_t a, b, e0, e1, av, bv;
+    range(blockIdx.x + i * gridDim.x, j, a, b, e0, e1, av, bv);
+    const int s = (int)(i % S);
+    const unsigned bytes = (unsigned)((e1 - e0) * ES);
+    mbar_arrive_expect_tx(&full[s], bytes);
+    if (bytes)
+      bulk_load(smem + s * kGatherTileBytes, (const char*)p.in[j] + (e0 - a) * ES, bytes, &full[s]);
+  };
+  for (int64_t i = 0; i < n_mine && i < S; ++i) issue(i);
+  int64_t issued = n_mine < S ? n_mine : S;
+  int64_t consumed = 0;
+  for (int64_t i = 0; i < n_mine; ++i) {
+    const int s = (int)(i % S);
+    if (!mbar_wait(&full[s], (unsigned)((i / S) & 1))) break;
+    consumed = i + 1;
+    int j;
+    int64_t a, b, e0, e1, av, bv;
+    range(blockIdx.x + i * gridDim.x, j, a, b, e0, e1, av, bv);
+    const unsigned bytes = (unsigned)((e1 - e0) * ES);
+    if (bytes) {
+      fence_proxy_async_smem();
+      for (int r = 0; r < W; ++r)
+        bulk_store((char*)p.out[r] + e0 * ES, smem + s * kGatherTileBytes, bytes);
+    }
+    bulk_commit();
+    // refill the stage used one tile ago once its stores have read it
+    if (i >= 1 && issued < n_mine) {
+      bulk_wait_read<1>();
+      issue(issued);
+      ++issued;
+    }
+  }
+  // after a timeout: wait (bounded) for the loads issued but not consumed
+  for (int64_t i = consumed; i < issued; ++i) mbar_wait(&full[i % S], (unsigned)((i / S) & 1));
+  bulk_wait_all();
+}
+
+const void* gather_tma_kernel(int elem_size) {
+  return elem_size == 4 ? (const void*)&vc_gather_tma<4> : (const void*)&vc_gather_tma<2>;
+}
 
 const void* staged_kernel_f32(int op, int kind, int W_t, int ring) {
   return staged_table<float>(op, kind, W_t, ring);

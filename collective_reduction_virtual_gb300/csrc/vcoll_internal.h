@@ -120,6 +120,10 @@ const void* reduce_kernel_bf16(int op, int kind, int W_t, int ring, int vec);
 const void* staged_kernel_f32(int op, int kind, int W_t, int ring);
 const void* staged_kernel_bf16(int op, int kind, int W_t, int ring);
 const void* gather_kernel(int elem_size, int vec);
+const void* gather_tma_kernel(int elem_size);
+constexpr int kGatherTmaThreads = 64;
+constexpr int kGatherTmaStages = 4;
+constexpr int kGatherTmaTileBytes = 32768;
 // Device address of the per-device error word (VCOLL_DEVICE_ERR_* bits).
 unsigned int* device_error_symbol();
 const void* fuse_kernel(int elem_size);

@@ -538,3 +538,34 @@ def test_pinned_host_buffers(v, dtype):
     ring = v.allreduce(ins, op="sum", ring_order=True)
     for u in range(W):
         assert to_np(h_out[u]).tobytes() == to_np(ring[u]).tobytes()
+
+
+@pytest.mark.parametrize("W", [2, 3, 8, 16])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("n", [100_003, (1 << 22) + 6, 3 << 22])
+def test_allgather_tma_matches_direct(v, W, dtype, n):
+    segs = [make_inputs(1, oracle.segment(n, W, j)[1], dtype, 9000 + W + j)[0] for j in range(W)]
+    d = v.allgather(segs, n, flags=v.FLAG_DIRECT)
+    assert v.device_errors(clear=True) == 0
+    t = v.allgather(segs, n, flags=v.FLAG_STAGED)
+    assert v.device_errors(clear=True) == 0
+    for u in range(W):
+        assert to_np(t[u]).tobytes() == to_np(d[u]).tobytes(), f"rank {u}"
+    if n < 200_000:
+        want = oracle.allgather([to_np(s) for s in segs], n, ODT[dtype])
+        for u in range(W):
+            assert_bit_exact(to_np(t[u]), want[u], "AG TMA vs oracle")
+    # shared non-zero phase: views one element into larger buffers
+    base = [torch.empty(n + 8, dtype=DT[dtype], device="cuda") for _ in range(W)]
+    outs = [b[1:1 + n] for b in base]
+    sbase = [torch.empty(s.numel() + 8, dtype=DT[dtype], device="cuda") for s in segs]
+    off = [oracle.segment(n, W, j)[0] for j in range(W)]
+    # segment j must share the outputs' phase: element off_j at offset 1 + off_j
+    sv = []
+    for j, (sb, s) in enumerate(zip(sbase, segs)):
+        sh = (1 + off[j]) % (4 if dtype == "f32" else 8)
+        sb[sh:sh + s.numel()].copy_(s)
+        sv.append(sb[sh:sh + s.numel()])
+    v.allgather(sv, n, outs, flags=v.FLAG_STAGED)
+    for u in range(W):
+        assert to_np(outs[u]).tobytes() == to_np(d[u]).tobytes(), f"phase rank {u}"
