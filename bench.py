@@ -52,8 +52,10 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = ["device_common.cuh", "reduce_kernels.cuh", "reduce_f32.cu", "reduce_bf16.cu",
-                  "copy_kernels.cu", "staged_kernels.cu", "api.cpp", "vcoll_internal.h"]
+# the device code of the timed kernels: DRAM traffic taken by ncu stays valid
+# while these files are unchanged
+KERNEL_SOURCES = ["device_common.cuh", "reduce_kernels.cuh", "reduce_f32.cu", "staged_kernels.cu",
+                  "vcoll_internal.h"]
 
 
 # ------------------------------------------------------------ distributed
