@@ -27,11 +27,12 @@ import threading
 
 import numpy as np
 
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
 SUM, MAX, AVG, MIN, PROD = 0, 1, 2, 3, 4
 OPS = {"sum": SUM, "max": MAX, "avg": AVG, "min": MIN, "prod": PROD}
-DTYPES = {"f32": F32, "float32": F32, "bf16": BF16, "bfloat16": BF16}
-NP_DTYPE = {F32: np.float32, BF16: np.uint16}
+DTYPES = {"f32": F32, "float32": F32, "bf16": BF16, "bfloat16": BF16, "f16": F16,
+          "float16": F16}
+NP_DTYPE = {F32: np.float32, BF16: np.uint16, F16: np.uint16}
 MAX_RANKS = 64
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -68,6 +69,12 @@ def load(path: str) -> ctypes.CDLL:
     L.oracle_allreduce.argtypes = [PP, PP, I, I64, I, I, IP]
     L.oracle_allgatherv.argtypes = [PP, I64P, PP, I, I, IP]
     L.oracle_allreduce_sampled.argtypes = [P, I64P, I64, I64, I, I, I, IP, P]
+    L.oracle_f16_from_f32.argtypes = [ctypes.c_float]
+    L.oracle_f16_from_f32.restype = ctypes.c_uint16
+    L.oracle_f32_from_f16.argtypes = [ctypes.c_uint16]
+    L.oracle_f32_from_f16.restype = ctypes.c_float
+    L.oracle_reduce_scatter_hop.argtypes = [PP, PP, I, I64, I, I, IP]
+    L.oracle_allreduce_wire.argtypes = [PP, PP, I, I64, I, I, IP]
     L.oracle_bf16_from_f32.argtypes = [ctypes.c_float]
     L.oracle_bf16_from_f32.restype = ctypes.c_uint16
     L.oracle_fuse_plan.argtypes = [I64P, I, I, I64, IP, IP]
@@ -76,7 +83,7 @@ def load(path: str) -> ctypes.CDLL:
     L.oracle_fusion_allreduce.argtypes = [PP, PP, I64P, I, I, I, I, I64, PP]
     for name in ("oracle_segment", "oracle_ring_schedule", "oracle_reduce_scatter",
                  "oracle_allgather", "oracle_allreduce", "oracle_allreduce_sampled",
-                 "oracle_allgatherv",
+                 "oracle_allgatherv", "oracle_reduce_scatter_hop", "oracle_allreduce_wire",
                  "oracle_fuse_plan", "oracle_fuse_pack", "oracle_fuse_unpack",
                  "oracle_fusion_allreduce"):
         getattr(L, name).restype = I
@@ -225,6 +232,45 @@ def bf16_from_f32(x) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32).ravel()
     f = lib().oracle_bf16_from_f32
     return np.array([f(float(v)) for v in x], dtype=np.uint16)
+
+
+def f16_from_f32(x) -> np.ndarray:
+    """Round-to-nearest-even fp32 -> IEEE binary16 bits, element by element."""
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    f = lib().oracle_f16_from_f32
+    return np.array([f(float(v)) for v in x], dtype=np.uint16)
+
+
+def f32_from_f16(h) -> np.ndarray:
+    """binary16 bits -> fp32 values (exact), element by element."""
+    h = np.ascontiguousarray(h, dtype=np.uint16).ravel()
+    f = lib().oracle_f32_from_f16
+    return np.array([f(int(v)) for v in h], dtype=np.float32)
+
+
+def reduce_scatter_hop(ins, op="sum", dtype=BF16, user_from_ring=None):
+    """Ring reduce-scatter whose buffers hold the element type: every hop
+    rounds to dtype (NCCL's T-typed ThisBuffer / NextBuffer)."""
+    dtype = _code(DTYPES, dtype)
+    ins = [_contig(a, dtype) for a in ins]
+    W, n = len(ins), int(ins[0].size)
+    outs = [np.empty(segment(n, W, j)[1], NP_DTYPE[dtype]) for j in range(W)]
+    rc = lib().oracle_reduce_scatter_hop(_ptrs(ins), _ptrs(outs), W, n, dtype, _code(OPS, op),
+                                         _ring(user_from_ring, W))
+    _check(rc, "reduce_scatter_hop")
+    return outs
+
+
+def allreduce_wire(ins, wire="f16", op="sum", user_from_ring=None):
+    """SINGA's reduced-precision allreduce: fp32 -> wire type, ring allreduce
+    in the wire type (rounding every hop), wire type -> fp32."""
+    ins = [_contig(a, F32) for a in ins]
+    W, n = len(ins), int(ins[0].size)
+    outs = [np.empty(n, np.float32) for _ in range(W)]
+    rc = lib().oracle_allreduce_wire(_ptrs(ins), _ptrs(outs), W, n, _code(DTYPES, wire),
+                                     _code(OPS, op), _ring(user_from_ring, W))
+    _check(rc, "allreduce_wire")
+    return outs
 
 
 def fuse_plan(counts, dtype=F32, threshold_bytes=64 * 1024 * 1024) -> list[int]:

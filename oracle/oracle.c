@@ -58,6 +58,7 @@
 
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
+#define ORACLE_F16 2
 
 #define ORACLE_SUM 0
 #define ORACLE_MAX 1
@@ -71,7 +72,7 @@
 
 static int elem_size(int dtype) {
   if (dtype == ORACLE_F32) return 4;
-  if (dtype == ORACLE_BF16) return 2;
+  if (dtype == ORACLE_BF16 || dtype == ORACLE_F16) return 2;
   return 0;
 }
 
@@ -96,6 +97,58 @@ uint16_t oracle_bf16_from_f32(float f) {
   return (uint16_t)(u >> 16);
 }
 
+/* IEEE binary16 from fp32, round to nearest even, with gradual underflow:
+ * rebias the exponent; below the normal range shift the 24-bit significand
+ * (implicit bit restored) into the 10-bit subnormal field; round on the bits
+ * shifted out (above half: up; exactly half: to even); a carry out of the
+ * significand moves into the exponent, up to infinity.  NaN stays a quiet
+ * NaN with its top payload bits. */
+uint16_t oracle_f16_from_f32(float f) {
+  uint32_t x;
+  memcpy(&x, &f, 4);
+  const uint32_t sign = (x >> 16) & 0x8000u;
+  const uint32_t exp = (x >> 23) & 0xFFu;
+  uint32_t man = x & 0x7FFFFFu;
+  if (exp == 0xFFu) return (uint16_t)(sign | (man ? 0x7E00u | (man >> 13) : 0x7C00u));
+  const int e = (int)exp - 127 + 15;
+  if (e >= 31) return (uint16_t)(sign | 0x7C00u);
+  if (e <= 0) {
+    if (e < -10) return (uint16_t)sign; /* below half the smallest subnormal */
+    man |= 0x800000u;
+    const int shift = 14 - e; /* 14..24 */
+    uint32_t r = man >> shift;
+    const uint32_t rem = man & ((1u << shift) - 1u);
+    const uint32_t half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (r & 1u))) ++r;
+    return (uint16_t)(sign | r);
+  }
+  uint32_t r = ((uint32_t)e << 10) | (man >> 13);
+  const uint32_t rem = man & 0x1FFFu;
+  if (rem > 0x1000u || (rem == 0x1000u && (r & 1u))) ++r;
+  return (uint16_t)(sign | r);
+}
+
+/* binary16 -> fp32, exact: normal numbers rebias the exponent, subnormals
+ * are scaled by 2^-24, infinities and NaNs keep their class. */
+float oracle_f32_from_f16(uint16_t h) {
+  const uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+  const uint32_t exp = (h >> 10) & 0x1Fu;
+  const uint32_t man = h & 0x3FFu;
+  float f;
+  if (exp == 0x1Fu) {
+    uint32_t u = sign | 0x7F800000u | (man << 13);
+    memcpy(&f, &u, 4);
+    return f;
+  }
+  if (exp == 0) {
+    f = ldexpf((float)man, -24);
+    return sign ? -f : f;
+  }
+  uint32_t u = sign | ((exp - 15 + 127) << 23) | (man << 13);
+  memcpy(&f, &u, 4);
+  return f;
+}
+
 static float load_elem(const void* base, int64_t k, int dtype) {
   if (dtype == ORACLE_F32) {
     float v;
@@ -104,6 +157,7 @@ static float load_elem(const void* base, int64_t k, int dtype) {
   }
   uint16_t h;
   memcpy(&h, (const char*)base + 2 * k, 2);
+  if (dtype == ORACLE_F16) return oracle_f32_from_f16(h);
   return widen_bf16(h);
 }
 
@@ -111,9 +165,17 @@ static void store_elem(void* base, int64_t k, int dtype, float v) {
   if (dtype == ORACLE_F32) {
     memcpy((char*)base + 4 * k, &v, 4);
   } else {
-    uint16_t h = oracle_bf16_from_f32(v);
+    uint16_t h = dtype == ORACLE_F16 ? oracle_f16_from_f32(v) : oracle_bf16_from_f32(v);
     memcpy((char*)base + 2 * k, &h, 2);
   }
+}
+
+/* The value a buffer of element type dtype holds after storing v (NCCL keeps
+ * the ring's intermediate buffers in the element type T). */
+static float round_to(float v, int dtype) {
+  if (dtype == ORACLE_F16) return oracle_f32_from_f16(oracle_f16_from_f32(v));
+  if (dtype == ORACLE_BF16) return widen_bf16(oracle_bf16_from_f32(v));
+  return v;
 }
 
 static float canonical_qnan(void) {
@@ -195,8 +257,24 @@ int oracle_ring_schedule(int W, const int* user_from_ring, int* table) {
  * step by step: cur[p] is the buffer ring position p received in the previous
  * step (ThisBuffer), nxt[p] what it receives in this step (the previous
  * position's NextBuffer). */
+/* hop != 0: every intermediate buffer is rounded to dtype after each FUNC,
+ * as in NCCL where ThisBuffer / NextBuffer hold values of the element type T
+ * (the fp32-accumulating reading is hop == 0). */
+static int ring_reduce_scatter(const void* const* in, void* const* out, int W, int64_t n,
+                               int dtype, int op, const int* user_from_ring, int hop);
+
 int oracle_reduce_scatter(const void* const* in, void* const* out, int W, int64_t n,
                           int dtype, int op, const int* user_from_ring) {
+  return ring_reduce_scatter(in, out, W, n, dtype, op, user_from_ring, 0);
+}
+
+int oracle_reduce_scatter_hop(const void* const* in, void* const* out, int W, int64_t n,
+                              int dtype, int op, const int* user_from_ring) {
+  return ring_reduce_scatter(in, out, W, n, dtype, op, user_from_ring, 1);
+}
+
+static int ring_reduce_scatter(const void* const* in, void* const* out, int W, int64_t n,
+                               int dtype, int op, const int* user_from_ring, int hop) {
   int ufr[ORACLE_MAX_RANKS];
   int es = elem_size(dtype);
   if (!in || !out || W < 1 || W > ORACLE_MAX_RANKS || n < 0 || !es) return -1;
@@ -231,9 +309,11 @@ int oracle_reduce_scatter(const void* const* in, void* const* out, int W, int64_
           next_buffer[k] = x; /* step 0: copy to the next position */
         } else if (s < W - 1) {
           next_buffer[k] = ring_func(op, this_buffer[k], x);
+          if (hop) next_buffer[k] = round_to(next_buffer[k], dtype);
         } else {
           /* step W-1: b == me, the finished block stays here */
           float v = ring_func(op, this_buffer[k], x);
+          if (hop) v = round_to(v, dtype);
           if (op == ORACLE_AVG) v = v * scale;
           store_elem(out[me], k, dtype, v);
         }
@@ -335,6 +415,43 @@ int oracle_allreduce(const void* const* in, void* const* out, int W, int64_t n,
   if (!rc) rc = oracle_reduce_scatter(in, seg, W, n, dtype, op, user_from_ring);
   if (!rc) rc = oracle_allgather((const void* const*)seg, out, W, n, dtype, user_from_ring);
   for (int u = 0; u < W; ++u) free(seg[u]);
+  return rc;
+}
+
+/* Reduced-precision "wire" allreduce (Apache SINGA, Communicator::synchHalf
+ * and fusedSynchHalf): fp32 inputs are converted to the wire type (float2half,
+ * here fp16 or bf16), allreduced in that type -- an NCCL ring whose buffers
+ * hold wire values, so every hop rounds to the wire type -- and converted back
+ * to fp32 (half2float).  in[u], out[u]: n fp32 elements. */
+int oracle_allreduce_wire(const void* const* in, void* const* out, int W, int64_t n, int wire,
+                          int op, const int* user_from_ring) {
+  if (!in || !out || W < 1 || W > ORACLE_MAX_RANKS || n < 0) return -1;
+  if (wire != ORACLE_F16 && wire != ORACLE_BF16) return -1;
+  if (!valid_op(op)) return -1;
+  void* win[ORACLE_MAX_RANKS];
+  void* seg[ORACLE_MAX_RANKS];
+  void* wout[ORACLE_MAX_RANKS];
+  int rc = 0;
+  for (int u = 0; u < W; ++u) {
+    int64_t off, len;
+    oracle_segment(n, W, u, &off, &len);
+    win[u] = malloc((size_t)(n ? n : 1) * 2);
+    wout[u] = malloc((size_t)(n ? n : 1) * 2);
+    seg[u] = malloc((size_t)(len ? len : 1) * 2);
+    if (!win[u] || !wout[u] || !seg[u]) rc = -2;
+  }
+  for (int u = 0; !rc && u < W; ++u)
+    for (int64_t i = 0; i < n; ++i) store_elem(win[u], i, wire, load_elem(in[u], i, ORACLE_F32));
+  if (!rc) rc = oracle_reduce_scatter_hop((const void* const*)win, seg, W, n, wire, op,
+                                          user_from_ring);
+  if (!rc) rc = oracle_allgather((const void* const*)seg, wout, W, n, wire, user_from_ring);
+  for (int u = 0; !rc && u < W; ++u)
+    for (int64_t i = 0; i < n; ++i) store_elem(out[u], i, ORACLE_F32, load_elem(wout[u], i, wire));
+  for (int u = 0; u < W; ++u) {
+    free(win[u]);
+    free(wout[u]);
+    free(seg[u]);
+  }
   return rc;
 }
 

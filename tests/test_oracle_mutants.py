@@ -42,6 +42,12 @@ MUTANTS = {
     "min_operand": ("if (acc < x) return acc;", "if (acc < x) return x;"),
     "min_signed_zero": ("(signbit(acc) || signbit(x)) ? -0.0f", "(signbit(acc) && signbit(x)) ? -0.0f"),
     "prod_is_sum": ("if (op == ORACLE_PROD) return acc * x;", "if (op == ORACLE_PROD) return acc + x;"),
+    "f16_round_half_up": ("if (rem > 0x1000u || (rem == 0x1000u && (r & 1u))) ++r;",
+                          "if (rem >= 0x1000u) ++r;"),
+    "f16_subnormal_shift": ("const int shift = 14 - e; /* 14..24 */",
+                            "const int shift = 13 - e; /* 14..24 */"),
+    "hop_rounding_dropped": ("if (hop) next_buffer[k] = round_to(next_buffer[k], dtype);", ";"),
+    "f16_widen_subnormal": ("f = ldexpf((float)man, -24);", "f = ldexpf((float)man, -25);"),
     "allgatherv_block": ("int b = ufr[(W + p - s) % W]; /* block held at step s */",
                          "int b = ufr[(W + p + s) % W]; /* block held at step s */"),
     "allgatherv_displacement": ("char* dst = (char*)out[me] + disp[b] * es;",
@@ -76,6 +82,10 @@ pins = [
     (P.test_prod_ring_order_hand_derived, ()),
     (P.test_prod_of_small_integers_exact, (3,)),
     (P.test_allgatherv_is_concatenation, (3,)),
+    (P.test_f16_rne_golden, ()),
+    (P.test_f16_widening_matches_numpy_for_all_patterns, ()),
+    (P.test_wire_hop_rounding_hand_derived, ()),
+    (P.test_wire_integer_sums_exact, ("f16", 3)),
 ]
 failed = []
 with oracle.using({so!r}):

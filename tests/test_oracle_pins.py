@@ -436,3 +436,83 @@ def test_allgatherv_with_even_sizes_is_allgather():
     a = oracle.allgatherv(segs)
     b = oracle.allgather(segs, n)
     assert all(x.tobytes() == y.tobytes() for x, y in zip(a, b))
+
+
+# ---------------------------------------- fp16 and the reduced-precision wire
+
+def test_f16_rne_golden():
+    for line in _golden_lines("f16_rne.txt"):
+        fb, hb = line.split()[:2]
+        f = np.array([int(fb, 16)], np.uint32).view(np.float32)
+        assert oracle.f16_from_f32(f)[0] == int(hb, 16), line
+
+
+def test_f16_matches_numpy_conversion():
+    rng = _rng(77)
+    bits = rng.integers(0, 1 << 32, 100_000, dtype=np.uint64).astype(np.uint32)
+    # concentrate on the binary16 range, subnormals and the overflow edge
+    mags = np.concatenate([rng.uniform(-30, 17, 100_000), rng.uniform(-26, -13, 50_000)])
+    vals = (np.sign(rng.standard_normal(mags.size)) * 2.0 ** mags).astype(np.float32)
+    hi = rng.integers(0, 1 << 19, 20_000, dtype=np.uint64).astype(np.uint32) << 13
+    ties = (hi | 0x1000) + (0x70 << 23)
+    f = np.concatenate([bits.view(np.float32), vals, ties.view(np.float32)])
+    f = f[~np.isnan(f)]
+    with np.errstate(over="ignore"):
+        want = f.astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.f16_from_f32(f), want)
+
+
+def test_f16_widening_matches_numpy_for_all_patterns():
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = oracle.f32_from_f16(h)
+    want = h.view(np.float16).astype(np.float32)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+
+
+def test_wire_hop_rounding_hand_derived():
+    for line in _golden_lines("wire_hop_rounding.txt"):
+        wire, xs, res = (p.strip() for p in line.split(";"))
+        x = [np.full(3, float(v), np.float32) for v in xs.split()]
+        want = [float(v) for v in res.split()]
+        got = oracle.allreduce_wire(x, wire, "sum")
+        for u in range(3):
+            assert list(got[u]) == want, wire
+
+
+@pytest.mark.parametrize("wire", ["f16", "bf16"])
+@pytest.mark.parametrize("W", [2, 3, 8])
+def test_wire_integer_sums_exact(wire, W):
+    # integers up to 256 are exact in both wire types and every partial sum
+    # here stays below 256
+    rng = _rng(W + 500)
+    ins = [rng.integers(-16, 17, 300).astype(np.float32) for _ in range(W)]
+    want = np.sum(np.stack([a.astype(np.int64) for a in ins]), axis=0)
+    for out in oracle.allreduce_wire(ins, wire, "sum"):
+        assert np.array_equal(out.astype(np.int64), want)
+
+
+@pytest.mark.parametrize("wire", ["f16", "bf16"])
+def test_wire_single_rank_is_round_trip(wire):
+    rng = _rng(501)
+    x = rng.standard_normal(1000).astype(np.float32)
+    conv = oracle.f16_from_f32 if wire == "f16" else oracle.bf16_from_f32
+    back = oracle.f32_from_f16 if wire == "f16" else \
+        (lambda h: (h.astype(np.uint32) << 16).view(np.float32))
+    got = oracle.allreduce_wire([x], wire, "sum")[0]
+    assert got.tobytes() == back(conv(x)).tobytes()
+
+
+def test_wire_within_hop_rounding_bound():
+    # each of the W-1 hops rounds relatively by at most u_wire, plus the
+    # input conversion: |wire result - exact| <= ((W-1) + 1) u_w sum|x| (+ tiny)
+    rng = _rng(502)
+    W = 8
+    ins = [rng.standard_normal(2000).astype(np.float32) for _ in range(W)]
+    exact = np.sum(np.stack(ins).astype(np.float64), axis=0)
+    mag = np.sum(np.abs(np.stack(ins).astype(np.float64)), axis=0)
+    for wire, u in (("f16", 2.0 ** -11), ("bf16", 2.0 ** -8)):
+        got = oracle.allreduce_wire(ins, wire, "sum")[0].astype(np.float64)
+        gam = W * u / (1 - W * u)
+        assert np.all(np.abs(got - exact) <= gam * mag + 2.0 ** -24)
