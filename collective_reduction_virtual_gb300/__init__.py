@@ -26,7 +26,7 @@ import threading
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libvcoll.so")
 
-F32, BF16 = 0, 1
+F32, BF16, F16 = 0, 1, 2
 SUM, MAX, AVG, MIN, PROD = 0, 1, 2, 3, 4
 FLAG_RING_ORDER, FLAG_STAGED, FLAG_DIRECT = 0x1, 0x2, 0x4
 MAX_RANKS = 64
@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             L.vcoll_fuse_pack.restype = I
             L.vcoll_fuse_unpack.argtypes = [PP, I64P, I, PP, I, I, P]
             L.vcoll_fuse_unpack.restype = I
+            L.vcoll_allreduce_wire.argtypes = [PP, PP, I, I64, I, I, U, P]
+            L.vcoll_allreduce_wire.restype = I
             L.vcoll_allgatherv.argtypes = [PP, I64P, PP, I, I, P]
             L.vcoll_allgatherv.restype = I
             L.vcoll_allreduce_multi.argtypes = [PP, PP, I64P, I, I, I, I, U, P]
@@ -136,6 +138,11 @@ def vcoll_reduce_scatter(in_ptrs, out_ptrs, W, n, dtype, op, flags=0, stream=0) 
 def vcoll_allgather(in_ptrs, out_ptrs, W, n, dtype, op=SUM, flags=0, stream=0) -> int:
     return lib().vcoll_allgather(_ptr_array(in_ptrs), _ptr_array(out_ptrs), W, n, dtype, op,
                                  flags, stream or None)
+
+
+def vcoll_allreduce_wire(in_ptrs, out_ptrs, W, n, wire, op, flags=0, stream=0) -> int:
+    return lib().vcoll_allreduce_wire(_ptr_array(in_ptrs), _ptr_array(out_ptrs), W, n, wire, op,
+                                      flags, stream or None)
 
 
 def vcoll_allgatherv(in_ptrs, counts, out_ptrs, W, dtype, stream=0) -> int:
@@ -280,6 +287,24 @@ def allreduce(ins, outs=None, op="sum", ring_order=False, stream=None, flags=0):
     _check(vcoll_allreduce([t.data_ptr() for t in ins], [t.data_ptr() for t in outs], W, n,
                            _dtype_code(ins[0]), OPS[op] if isinstance(op, str) else op, fl,
                            _stream_handle(stream)))
+    return outs
+
+
+def allreduce_wire(ins, outs=None, wire="f16", op="sum", ring_order=False, stream=None):
+    """SINGA's reduced-precision allreduce of W fp32 tensors: values travel
+    and accumulate in fp16 (or bf16), rounding every hop; fp32 results."""
+    torch = _torch()
+    W, n = len(ins), ins[0].numel()
+    _check_tensors(ins, "ins")
+    if any(t.dtype != torch.float32 for t in ins):
+        raise VcollError(ERR_INVALID_TYPE, "the wire allreduce takes fp32 tensors")
+    if outs is None:
+        outs = [torch.empty_like(t) for t in ins]
+    _check_tensors(outs, "outs")
+    wcode = {"f16": F16, "fp16": F16, "bf16": BF16}[wire] if isinstance(wire, str) else wire
+    _check(vcoll_allreduce_wire([t.data_ptr() for t in ins], [t.data_ptr() for t in outs], W, n,
+                                wcode, OPS[op] if isinstance(op, str) else op,
+                                FLAG_RING_ORDER if ring_order else 0, _stream_handle(stream)))
     return outs
 
 

@@ -243,8 +243,10 @@ int copy_d2d(void* dst, const void* src, int64_t bytes, void* stream) {
   return VCOLL_OK;
 }
 
+// wire >= 0: the reduced-precision allreduce (fp32 buffers, arithmetic rounded
+// to the 16-bit wire type every hop); -1: the plain collectives.
 int reduce_common(int kind, const void* const* in, void* const* out, int W, int64_t n, int dtype,
-                  int op, unsigned flags, void* stream) {
+                  int op, unsigned flags, void* stream, int wire = -1) {
   g_err[0] = 0;
   int rc = check_common(W, n, dtype, op);
   if (rc) return rc;
@@ -272,6 +274,36 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   }
   int vec, phase;
   if ((rc = analyse(bufs, es, &vec, &phase))) return rc;
+
+  if (wire >= 0) {
+    // every rank count, W = 1 included, goes through the kernel: even a single
+    // rank's values are rounded to the wire type and back
+    const bool ring = (flags & VCOLL_FLAG_RING_ORDER) && W > 2;
+    const int W_t = (W == 2 || W == 4 || W == 8 || W == 16) ? W : 0;
+    ReduceParams prm;
+    memset(&prm, 0, sizeof(prm));
+    for (int u = 0; u < W; ++u) {
+      prm.in[u] = in[u];
+      prm.out[u] = out[u];
+    }
+    prm.n = n;
+    prm.q = n / W;
+    prm.r = n % W;
+    prm.W = W;
+    prm.nseg = ring ? W : 1;
+    prm.phase = vec ? phase : -1;
+    prm.ring = ring ? 1 : 0;
+    prm.scale = op == VCOLL_AVG ? 1.0f / (float)W : 1.0f;
+    prm.do_scale = op == VCOLL_AVG ? 1 : 0;
+    const bool small = n * es <= kSmallBytes;
+    const int threads = small ? 128 : 256;
+    prm.tile_elems = (int64_t)threads * (vec ? 2 * 4 : 4);
+    prm.tiles_per_seg = vec ? tiles_per_segment(n, W, prm.nseg, 4, phase, prm.tile_elems)
+                            : tiles_per_segment(n, W, prm.nseg, 1, 0, prm.tile_elems);
+    prm.num_tiles = prm.tiles_per_seg * prm.nseg;
+    return launch(wire_kernel(wire, W_t, ring ? 1 : 0), prm.num_tiles, threads, 0, small, &prm,
+                  stream);
+  }
 
   if (W == 1) return copy_d2d(out[0], in[0], n * es, stream);
 
@@ -332,6 +364,20 @@ int vcoll_reduce_scatter(const void* const* in, void* const* out, int W, int64_t
 int vcoll_allreduce(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,
                     unsigned flags, void* stream) {
   return reduce_common(KIND_AR, in, out, W, n, dtype, op, flags, stream);
+}
+
+int vcoll_allreduce_wire(const void* const* in, void* const* out, int W, int64_t n, int wire, int op,
+                         unsigned flags, void* stream) {
+  g_err[0] = 0;
+  if (wire != VCOLL_F16 && wire != VCOLL_BF16)
+    return fail(VCOLL_ERR_INVALID_TYPE, "wire type %d is neither VCOLL_F16 nor VCOLL_BF16", wire);
+  if (op != VCOLL_SUM && op != VCOLL_AVG) {
+    if (op == VCOLL_MAX || op == VCOLL_MIN || op == VCOLL_PROD)
+      return fail(VCOLL_ERR_UNSUPPORTED, "the wire allreduce supports sum and avg");
+    return fail(VCOLL_ERR_INVALID_OP, "unknown op %d", op);
+  }
+  if (flags & (VCOLL_FLAG_STAGED | VCOLL_FLAG_DIRECT)) flags &= VCOLL_FLAG_RING_ORDER;
+  return reduce_common(KIND_AR, in, out, W, n, VCOLL_F32, op, flags, stream, wire);
 }
 
 // Allgather of W pieces, piece j landing at [disp[j], disp[j+1]) of every

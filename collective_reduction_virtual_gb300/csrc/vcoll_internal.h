@@ -121,6 +121,7 @@ const void* staged_kernel_f32(int op, int kind, int W_t, int ring);
 const void* staged_kernel_bf16(int op, int kind, int W_t, int ring);
 const void* gather_kernel(int elem_size, int vec);
 const void* gather_tma_kernel(int elem_size);
+const void* wire_kernel(int wire, int W_t, int ring);
 constexpr int kGatherTmaThreads = 64;
 constexpr int kGatherTmaStages = 4;
 constexpr int kGatherTmaTileBytes = 32768;

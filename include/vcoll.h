@@ -66,7 +66,11 @@ extern "C" {
 
 #define VCOLL_MAX_RANKS 64
 
-typedef enum { VCOLL_F32 = 0, VCOLL_BF16 = 1 } vcoll_dtype_t;
+typedef enum {
+  VCOLL_F32 = 0,
+  VCOLL_BF16 = 1,
+  VCOLL_F16 = 2 /* IEEE binary16: only as the wire type of vcoll_allreduce_wire */
+} vcoll_dtype_t;
 
 typedef enum {
   VCOLL_SUM = 0,
@@ -137,6 +141,21 @@ int vcoll_allgatherv(const void* const* in, const int64_t* counts, void* const* 
  */
 int vcoll_allreduce(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,
                     unsigned flags, void* stream);
+
+/*
+ * Reduced-precision ("wire") allreduce, Apache SINGA Communicator::synchHalf /
+ * fusedSynchHalf: fp32 inputs are converted to the 16-bit wire type (wire =
+ * VCOLL_F16 as SINGA's float2half, or VCOLL_BF16), allreduced in that type by
+ * the NCCL ring, whose buffers hold wire values so every hop rounds to the
+ * wire type, and converted back to fp32 (half2float).  One pass: each
+ * element is rounded, folded with a rounding after every op (ring order with
+ * VCOLL_FLAG_RING_ORDER, else a pairwise tree), and the widened result is
+ * written to the W fp32 outputs.  in[u], out[u]: n fp32 elements.  op: sum or
+ * avg (the rounded sum times fl32(1/W), rounded again); max/min/prod give
+ * VCOLL_ERR_UNSUPPORTED.  W == 1 is the round trip through the wire type.
+ */
+int vcoll_allreduce_wire(const void* const* in, void* const* out, int W, int64_t n, int wire, int op,
+                         unsigned flags, void* stream);
 
 /*
  * Tensor-fusion batching (Horovod BackgroundThreadLoop): greedy in tensor

@@ -218,3 +218,16 @@ def test_fusion_allreduce_errors(v):
     assert f(ins, outs, [10, 20], -1, 2, v.F32, v.SUM)[0] == v.ERR_INVALID_ARG
     rc, nb = f([0] * 4, [0] * 4, [0, 0], 2, 2, v.F32, v.SUM, 0, 64)
     assert rc == v.OK and nb == 1
+
+
+def test_allreduce_wire_errors(v):
+    f = v.vcoll_allreduce_wire
+    assert f(FAKE_IN[:4], FAKE_OUT[:4], 4, 64, v.F32, v.SUM) == v.ERR_INVALID_TYPE
+    assert f(FAKE_IN[:4], FAKE_OUT[:4], 4, 64, 7, v.SUM) == v.ERR_INVALID_TYPE
+    assert f(FAKE_IN[:4], FAKE_OUT[:4], 4, 64, v.F16, v.MAX) == v.ERR_UNSUPPORTED
+    assert f(FAKE_IN[:4], FAKE_OUT[:4], 4, 64, v.F16, 9) == v.ERR_INVALID_OP
+    assert f(FAKE_IN[:4], FAKE_OUT[:4], 0, 64, v.F16, v.SUM) == v.ERR_INVALID_ARG
+    assert f([0] * 4, [0] * 4, 4, 0, v.BF16, v.AVG) == v.OK
+    # fp16 is only a wire type: the plain collectives reject it
+    assert v.vcoll_allreduce(FAKE_IN[:4], FAKE_OUT[:4], 4, 64, v.F16, v.SUM, 0, 0) \
+        == v.ERR_INVALID_TYPE

@@ -569,3 +569,50 @@ def test_allgather_tma_matches_direct(v, W, dtype, n):
     v.allgather(sv, n, outs, flags=v.FLAG_STAGED)
     for u in range(W):
         assert to_np(outs[u]).tobytes() == to_np(d[u]).tobytes(), f"phase rank {u}"
+
+
+# ------------------------------------------- reduced-precision wire allreduce
+
+@pytest.mark.parametrize("wire", ["f16", "bf16"])
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("n", [1, 17, 4099, 100_003])
+def test_allreduce_wire(v, wire, W, n):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(W * 1000 + n)
+    ins = [torch.randn(n, generator=g, device="cuda") *
+           (10.0 ** torch.randint(-6, 3, (n,), generator=g, device="cuda").float())
+           for _ in range(W)]
+    ins_np = [to_np(t) for t in ins]
+    u = 2.0 ** -11 if wire == "f16" else 2.0 ** -8
+    for op in ("sum", "avg"):
+        want = oracle.allreduce_wire(ins_np, wire, op)
+        ring = v.allreduce_wire(ins, wire=wire, op=op, ring_order=True)
+        fast = v.allreduce_wire(ins, wire=wire, op=op)
+        for r in range(W):
+            assert_bit_exact(to_np(ring[r]), want[r], f"wire {wire} {op} ring")
+            # fastest order: both orders are W-1 roundings away from the same
+            # rounded inputs; the results differ by at most 2 (W-1) u_w sum|x|
+            # (+ the final scale's rounding for avg, + subnormal granularity)
+            s = abs_sum([(to_np(t)) for t in ins])
+            bound = 2 * (W + 1) * u * s / (W if op == "avg" else 1) + 2.0 ** -24
+            d = np.abs(to_np(fast[r]).astype(np.float64) - want[r].astype(np.float64))
+            ok = (d <= bound) | (np.isnan(to_np(fast[r])) & np.isnan(want[r]))
+            assert ok.all(), f"wire {wire} {op} fast: max excess {(d - bound).max()}"
+
+
+def test_allreduce_wire_hop_rounding_on_gpu(v):
+    for wire, xs, want in (("f16", (2048.0, 1.0, 1.0), [2050.0, 2048.0, 2048.0]),
+                           ("bf16", (256.0, 1.0, 1.0), [258.0, 256.0, 256.0])):
+        x = [torch.full((3,), val, device="cuda") for val in xs]
+        out = v.allreduce_wire(x, wire=wire, op="sum", ring_order=True)
+        assert all(o.tolist() == want for o in out), wire
+
+
+def test_allreduce_wire_misaligned(v):
+    W, n = 4, 50_001
+    base = [torch.randn(n + 8, device="cuda") for _ in range(W)]
+    ins = [b[(u * 3) % 4: (u * 3) % 4 + n] for u, b in enumerate(base)]
+    want = oracle.allreduce_wire([to_np(t) for t in ins], "f16", "sum")
+    got = v.allreduce_wire(ins, wire="f16", op="sum", ring_order=True)
+    for r in range(W):
+        assert_bit_exact(to_np(got[r]), want[r], "wire misaligned")
