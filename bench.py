@@ -476,6 +476,8 @@ def extras(args, stream, dev):
         lambda: vc.allreduce(ins, outs, op="sum", flags=vc.FLAG_STAGED), 2 * W * n * 4)
     out["ar_sum_w8_f32_2^26_direct"] = rate(
         lambda: vc.allreduce(ins, outs, op="sum", flags=vc.FLAG_DIRECT), 2 * W * n * 4)
+    out["ar_wire_f16_sum_w8_f32_2^26"] = rate(
+        lambda: vc.allreduce_wire(ins, outs, wire="f16", op="sum"), 2 * W * n * 4)
     out["rs_sum_w8_f32_2^26_staged"] = rate(
         lambda: vc.reduce_scatter(ins, segs, op="sum", flags=vc.FLAG_STAGED), (W + 1) * n * 4)
     del ins, outs, segs
