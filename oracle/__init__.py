@@ -75,6 +75,7 @@ def load(path: str) -> ctypes.CDLL:
     L.oracle_f32_from_f16.restype = ctypes.c_float
     L.oracle_reduce_scatter_hop.argtypes = [PP, PP, I, I64, I, I, IP]
     L.oracle_allreduce_wire.argtypes = [PP, PP, I, I64, I, I, IP]
+    L.oracle_sparse_allreduce.argtypes = [PP, PP, PP, I, I64, ctypes.c_float, I, I64P]
     L.oracle_bf16_from_f32.argtypes = [ctypes.c_float]
     L.oracle_bf16_from_f32.restype = ctypes.c_uint16
     L.oracle_fuse_plan.argtypes = [I64P, I, I, I64, IP, IP]
@@ -84,6 +85,7 @@ def load(path: str) -> ctypes.CDLL:
     for name in ("oracle_segment", "oracle_ring_schedule", "oracle_reduce_scatter",
                  "oracle_allgather", "oracle_allreduce", "oracle_allreduce_sampled",
                  "oracle_allgatherv", "oracle_reduce_scatter_hop", "oracle_allreduce_wire",
+                 "oracle_sparse_allreduce",
                  "oracle_fuse_plan", "oracle_fuse_pack", "oracle_fuse_unpack",
                  "oracle_fusion_allreduce"):
         getattr(L, name).restype = I
@@ -271,6 +273,25 @@ def allreduce_wire(ins, wire="f16", op="sum", user_from_ring=None):
                                      _code(OPS, op), _ring(user_from_ring, W))
     _check(rc, "allreduce_wire")
     return outs
+
+
+def sparse_allreduce(ins, threshold, topk=False, accum=None):
+    """SINGA's sparsified allreduce of W fp32 arrays (threshold or top-K).
+    accum: W fp32 arrays updated in place (error feedback), or None.
+    Returns (outputs, nnz per rank)."""
+    ins = [_contig(a, F32) for a in ins]
+    W, n = len(ins), int(ins[0].size)
+    outs = [np.empty(n, np.float32) for _ in range(W)]
+    nnz = np.zeros(W, np.int64)
+    if accum is not None:
+        for a in accum:
+            assert a.dtype == np.float32 and a.flags.c_contiguous and a.size == n
+    rc = lib().oracle_sparse_allreduce(_ptrs(ins), _ptrs(outs),
+                                       _ptrs(accum) if accum is not None else None, W, n,
+                                       float(threshold), 1 if topk else 0,
+                                       nnz.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
+    _check(rc, "sparse_allreduce")
+    return outs, nnz
 
 
 def fuse_plan(counts, dtype=F32, threshold_bytes=64 * 1024 * 1024) -> list[int]:

@@ -455,6 +455,116 @@ int oracle_allreduce_wire(const void* const* in, void* const* out, int W, int64_
   return rc;
 }
 
+/* ------------------------------------------------- sparsified allreduce */
+
+/* Total order on fp32 values as unsigned keys: larger value, larger key
+ * (negative values have their bits inverted, non-negative ones get the sign
+ * bit set).  -0 sorts just below +0; NaNs sort beyond the infinities. */
+static uint32_t order_key(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+typedef struct {
+  uint32_t key;
+  int64_t idx; /* 1-based, as SINGA's index arrays */
+  float val;
+} sparse_entry;
+
+/* "sort the values from large to small" with their indices; equal values
+ * keep index order (a stable sort) */
+static int by_value_desc(const void* a, const void* b) {
+  const sparse_entry* x = (const sparse_entry*)a;
+  const sparse_entry* y = (const sparse_entry*)b;
+  if (x->key != y->key) return x->key > y->key ? -1 : 1;
+  return x->idx < y->idx ? -1 : (x->idx > y->idx ? 1 : 0);
+}
+
+/* SINGA Communicator::valSparsAllReduce (topk == 0) and topKSparsAllReduce
+ * (topk != 0), over W virtual ranks.  Per rank u, in the page's order:
+ *   send = in[u]; with accumulation: send += accum[u], backup = send;
+ *   threshold: send[i] = |send[i]| > threshold ? send[i] : 0, the accumulation
+ *     becomes backup - send, and the (1-based index, value) list holds the
+ *     nonzero entries of send in index order (sparsindex, removezeroidx,
+ *     removezeroval);
+ *   top-K: K = ceil(threshold * num) in fp32; (index, value) pairs sorted by
+ *     value from large to small; the first K are sent; with accumulation it
+ *     becomes zero, then gets the K values scattered in (saxpyi), then
+ *     backup - itself.
+ * The lists are allgathered; every rank's result starts at zero and receives
+ * y[idx - 1] += 1.0 * val for the lists of ranks 0, 1, ..., W-1 in turn
+ * (cusparseSaxpyi, index base one).  in/out/accum: W arrays of n fp32;
+ * accum may be NULL (no error feedback).  nnz (may be NULL) gets each rank's
+ * list length. */
+int oracle_sparse_allreduce(const void* const* in, void* const* out, void* const* accum, int W,
+                            int64_t n, float threshold, int topk, int64_t* nnz) {
+  if (!in || !out || W < 1 || W > ORACLE_MAX_RANKS || n < 0) return -1;
+  sparse_entry* lists[ORACLE_MAX_RANKS];
+  int64_t len[ORACLE_MAX_RANKS];
+  float* send = (float*)malloc(sizeof(float) * (size_t)(n ? n : 1));
+  float* backup = (float*)malloc(sizeof(float) * (size_t)(n ? n : 1));
+  float* result = (float*)malloc(sizeof(float) * (size_t)(n ? n : 1));
+  int rc = (send && backup && result) ? 0 : -2;
+  for (int u = 0; u < W; ++u) lists[u] = NULL;
+  for (int u = 0; !rc && u < W; ++u) {
+    float* acc = accum ? (float*)accum[u] : NULL;
+    for (int64_t i = 0; i < n; ++i) send[i] = load_elem(in[u], i, ORACLE_F32);
+    if (acc) {
+      for (int64_t i = 0; i < n; ++i) send[i] = send[i] + acc[i];
+      for (int64_t i = 0; i < n; ++i) backup[i] = send[i];
+    }
+    lists[u] = (sparse_entry*)malloc(sizeof(sparse_entry) * (size_t)(n ? n : 1));
+    if (!lists[u]) {
+      rc = -2;
+      break;
+    }
+    if (!topk) {
+      for (int64_t i = 0; i < n; ++i) send[i] = fabsf(send[i]) > threshold ? send[i] : 0.0f;
+      if (acc)
+        for (int64_t i = 0; i < n; ++i) acc[i] = backup[i] - send[i];
+      int64_t m = 0;
+      for (int64_t i = 0; i < n; ++i)
+        if (send[i] != 0.0f) {
+          lists[u][m].idx = i + 1;
+          lists[u][m].val = send[i];
+          ++m;
+        }
+      len[u] = m;
+    } else {
+      for (int64_t i = 0; i < n; ++i) {
+        lists[u][i].idx = i + 1;
+        lists[u][i].val = send[i];
+        lists[u][i].key = order_key(send[i]);
+      }
+      qsort(lists[u], (size_t)n, sizeof(sparse_entry), by_value_desc);
+      int64_t K = (int64_t)ceilf(threshold * (float)n);
+      if (K > n) K = n;
+      if (K < 0) K = 0;
+      if (acc) {
+        for (int64_t i = 0; i < n; ++i) acc[i] = 0.0f;
+        for (int64_t k = 0; k < K; ++k) acc[lists[u][k].idx - 1] += 1.0f * lists[u][k].val;
+        for (int64_t i = 0; i < n; ++i) acc[i] = backup[i] - acc[i];
+      }
+      len[u] = K;
+    }
+    if (nnz) nnz[u] = len[u];
+  }
+  if (!rc) {
+    for (int64_t i = 0; i < n; ++i) result[i] = 0.0f;
+    for (int u = 0; u < W; ++u)
+      for (int64_t k = 0; k < len[u]; ++k)
+        result[lists[u][k].idx - 1] = 1.0f * lists[u][k].val + result[lists[u][k].idx - 1];
+    for (int u = 0; u < W; ++u)
+      for (int64_t i = 0; i < n; ++i) store_elem(out[u], i, ORACLE_F32, result[i]);
+  }
+  for (int u = 0; u < W; ++u) free(lists[u]);
+  free(send);
+  free(backup);
+  free(result);
+  return rc;
+}
+
 /* Allreduce at sampled indices.  vals[i*W + u] is user rank u's input at
  * index idx[i] of an n-element allreduce; result[i] receives the allreduce
  * output there.  Each sample is run through the same ring reduce-scatter on a

@@ -48,6 +48,18 @@ MUTANTS = {
                             "const int shift = 13 - e; /* 14..24 */"),
     "hop_rounding_dropped": ("if (hop) next_buffer[k] = round_to(next_buffer[k], dtype);", ";"),
     "f16_widen_subnormal": ("f = ldexpf((float)man, -24);", "f = ldexpf((float)man, -25);"),
+    "sparse_threshold_inclusive": ("send[i] = fabsf(send[i]) > threshold ? send[i] : 0.0f;",
+                                   "send[i] = fabsf(send[i]) >= threshold ? send[i] : 0.0f;"),
+    "sparse_sort_ascending": ("if (x->key != y->key) return x->key > y->key ? -1 : 1;",
+                              "if (x->key != y->key) return x->key < y->key ? -1 : 1;"),
+    "sparse_k_floor": ("int64_t K = (int64_t)ceilf(threshold * (float)n);",
+                       "int64_t K = (int64_t)floorf(threshold * (float)n);"),
+    "sparse_residual_sign": ("for (int64_t i = 0; i < n; ++i) acc[i] = backup[i] - send[i];",
+                             "for (int64_t i = 0; i < n; ++i) acc[i] = send[i] - backup[i];"),
+    "sparse_rank_order": ("    for (int u = 0; u < W; ++u)\n      for (int64_t k = 0; k < len[u]; ++k)",
+                          "    for (int u = W - 1; u >= 0; --u)\n      for (int64_t k = 0; k < len[u]; ++k)"),
+    "sparse_index_base": ("result[lists[u][k].idx - 1] = 1.0f * lists[u][k].val + result[lists[u][k].idx - 1];",
+                          "result[lists[u][k].idx % n] = 1.0f * lists[u][k].val + result[lists[u][k].idx % n];"),
     "allgatherv_block": ("int b = ufr[(W + p - s) % W]; /* block held at step s */",
                          "int b = ufr[(W + p + s) % W]; /* block held at step s */"),
     "allgatherv_displacement": ("char* dst = (char*)out[me] + disp[b] * es;",
@@ -86,6 +98,10 @@ pins = [
     (P.test_f16_widening_matches_numpy_for_all_patterns, ()),
     (P.test_wire_hop_rounding_hand_derived, ()),
     (P.test_wire_integer_sums_exact, ("f16", 3)),
+    (P.test_sparse_allreduce_hand_derived, ()),
+    (P.test_sparse_threshold_matches_dense_definition, (3, True)),
+    (P.test_sparse_topk_matches_sorted_selection, (2, 0.05)),
+    (P.test_sparse_topk_count_rounding, ()),
 ]
 failed = []
 with oracle.using({so!r}):

@@ -516,3 +516,87 @@ def test_wire_within_hop_rounding_bound():
         got = oracle.allreduce_wire(ins, wire, "sum")[0].astype(np.float64)
         gam = W * u / (1 - W * u)
         assert np.all(np.abs(got - exact) <= gam * mag + 2.0 ** -24)
+
+
+# ------------------------------------------------- sparsified allreduce
+
+def test_sparse_allreduce_hand_derived():
+    x = [np.array([3, -1, 0.5, 2], np.float32), np.array([1, 4, -2, 0.1], np.float32)]
+    for line in _golden_lines("singa_sparse_allreduce.txt"):
+        mode, thr, res, r0, r1 = (p.strip() for p in line.split(";"))
+        acc = [np.zeros(4, np.float32), np.zeros(4, np.float32)]
+        outs, nnz = oracle.sparse_allreduce(x, float(thr), mode == "topk", acc)
+        want = np.array([float(v) for v in res.split()], np.float32)
+        assert all(np.array_equal(o, want) for o in outs), mode
+        assert np.array_equal(acc[0], np.array([float(v) for v in r0.split()], np.float32))
+        assert np.array_equal(acc[1], np.array([float(v) for v in r1.split()], np.float32))
+    x = [np.array([v], np.float32) for v in (1.0, 1e8, -1e8)]
+    assert float(oracle.sparse_allreduce(x, 0.5)[0][0][0]) == 0.0
+
+
+def _keys(a):
+    u = a.view(np.uint32).astype(np.uint64)
+    return np.where(u & 0x80000000, (~u) & 0xFFFFFFFF, u | 0x80000000)
+
+
+def _dense_reference(xs, kept):
+    # zeros, then each rank's kept values in rank order (fp32 adds)
+    res = np.zeros(xs[0].size, np.float32)
+    for x, k in zip(xs, kept):
+        res = np.where(k, (res + x).astype(np.float32), res)
+    return res
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 8])
+@pytest.mark.parametrize("with_acc", [False, True])
+def test_sparse_threshold_matches_dense_definition(W, with_acc):
+    rng = _rng(600 + W)
+    n = 5000
+    xs = [(rng.standard_normal(n) * 10.0 ** rng.integers(-2, 2, n)).astype(np.float32)
+          for _ in range(W)]
+    acc = [(rng.standard_normal(n) * 0.1).astype(np.float32) for _ in range(W)] if with_acc \
+        else None
+    acc0 = [a.copy() for a in acc] if with_acc else None
+    thr = 0.7
+    outs, nnz = oracle.sparse_allreduce(xs, thr, False, acc)
+    eff = [(x + a).astype(np.float32) for x, a in zip(xs, acc0)] if with_acc else xs
+    kept = [(np.abs(e) > thr) & (e != 0) for e in eff]
+    want = _dense_reference(eff, kept)
+    for o in outs:
+        assert o.tobytes() == want.tobytes()
+    assert list(nnz) == [int(k.sum()) for k in kept]
+    if with_acc:
+        for a, e, k in zip(acc, eff, kept):
+            assert np.array_equal(a, np.where(k, np.float32(0), e))
+
+
+@pytest.mark.parametrize("W", [1, 2, 5])
+@pytest.mark.parametrize("frac", [0.0, 0.001, 0.05, 0.5, 1.0])
+def test_sparse_topk_matches_sorted_selection(W, frac):
+    rng = _rng(700 + W)
+    n = 3001
+    xs = [rng.standard_normal(n).astype(np.float32) for _ in range(W)]
+    xs[0][::7] = 0.25  # ties across the selection boundary for some fractions
+    acc = [np.zeros(n, np.float32) for _ in range(W)]
+    outs, nnz = oracle.sparse_allreduce(xs, frac, True, acc)
+    K = min(n, int(np.ceil(np.float32(frac) * np.float32(n))))
+    kept = []
+    for x in xs:
+        order = np.lexsort((np.arange(n), -_keys(x).astype(np.int64)))  # value desc, index asc
+        k = np.zeros(n, bool)
+        k[order[:K]] = True
+        kept.append(k)
+    want = _dense_reference(xs, kept)
+    for o in outs:
+        assert o.tobytes() == want.tobytes()
+    assert list(nnz) == [K] * W
+    for a, x, k in zip(acc, xs, kept):
+        assert np.array_equal(a, np.where(k, np.float32(0), x))
+
+
+def test_sparse_topk_count_rounding():
+    # K = ceil(threshold * n) in fp32, as the page computes it
+    for n, thr, K in ((10, 0.25, 3), (1000, 0.01, 10), (7, 1.0, 7), (100, 0.0, 0), (3, 0.34, 2)):
+        xs = [np.arange(n, dtype=np.float32)]
+        _, nnz = oracle.sparse_allreduce(xs, thr, True)
+        assert nnz[0] == K, (n, thr)
