@@ -66,6 +66,11 @@ def lib() -> ctypes.CDLL:
             L.vcoll_fuse_pack.restype = I
             L.vcoll_fuse_unpack.argtypes = [PP, I64P, I, PP, I, I, P]
             L.vcoll_fuse_unpack.restype = I
+            L.vcoll_sparse_workspace_bytes.argtypes = [I, I]
+            L.vcoll_sparse_workspace_bytes.restype = ctypes.c_size_t
+            L.vcoll_sparse_allreduce.argtypes = [PP, PP, PP, I, I64, ctypes.c_float, I, P, P,
+                                                 ctypes.c_size_t, P]
+            L.vcoll_sparse_allreduce.restype = I
             L.vcoll_allreduce_wire.argtypes = [PP, PP, I, I64, I, I, U, P]
             L.vcoll_allreduce_wire.restype = I
             L.vcoll_allgatherv.argtypes = [PP, I64P, PP, I, I, P]
@@ -143,6 +148,18 @@ def vcoll_allgather(in_ptrs, out_ptrs, W, n, dtype, op=SUM, flags=0, stream=0) -
 def vcoll_allreduce_wire(in_ptrs, out_ptrs, W, n, wire, op, flags=0, stream=0) -> int:
     return lib().vcoll_allreduce_wire(_ptr_array(in_ptrs), _ptr_array(out_ptrs), W, n, wire, op,
                                       flags, stream or None)
+
+
+def vcoll_sparse_workspace_bytes(W, topk) -> int:
+    return int(lib().vcoll_sparse_workspace_bytes(W, 1 if topk else 0))
+
+
+def vcoll_sparse_allreduce(in_ptrs, out_ptrs, acc_ptrs, W, n, threshold, topk, nnz_ptr=0,
+                           workspace=0, workspace_bytes=0, stream=0) -> int:
+    return lib().vcoll_sparse_allreduce(_ptr_array(in_ptrs), _ptr_array(out_ptrs),
+                                        _ptr_array(acc_ptrs) if acc_ptrs else None, W, n,
+                                        float(threshold), 1 if topk else 0, nnz_ptr or None,
+                                        workspace or None, workspace_bytes, stream or None)
 
 
 def vcoll_allgatherv(in_ptrs, counts, out_ptrs, W, dtype, stream=0) -> int:
@@ -306,6 +323,35 @@ def allreduce_wire(ins, outs=None, wire="f16", op="sum", ring_order=False, strea
                                 wcode, OPS[op] if isinstance(op, str) else op,
                                 FLAG_RING_ORDER if ring_order else 0, _stream_handle(stream)))
     return outs
+
+
+def sparse_allreduce(ins, outs=None, accum=None, threshold=0.0, topk=False, nnz=None,
+                     workspace=None, stream=None):
+    """SINGA's sparsified allreduce of W fp32 CUDA tensors (threshold mode, or
+    top-K with K = ceil(threshold * n)).  accum: W fp32 tensors updated in
+    place (error feedback) or None.  nnz: int64 CUDA tensor of W survivor
+    counts (optional).  workspace: a uint8 CUDA tensor of at least
+    sparse_workspace_bytes(W, topk) bytes; allocated here when omitted."""
+    torch = _torch()
+    W, n = len(ins), ins[0].numel()
+    _check_tensors(ins, "ins")
+    if outs is None:
+        outs = [torch.empty_like(t) for t in ins]
+    _check_tensors(outs, "outs")
+    need = vcoll_sparse_workspace_bytes(W, topk)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=ins[0].device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else 0
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(vcoll_sparse_allreduce([t.data_ptr() for t in ins], [t.data_ptr() for t in outs],
+                                  [t.data_ptr() for t in accum] if accum is not None else None,
+                                  W, n, threshold, topk, nnz.data_ptr() if nnz is not None else 0,
+                                  ws_ptr, ws_bytes, _stream_handle(stream)))
+    return outs
+
+
+def sparse_workspace_bytes(W, topk=True) -> int:
+    return vcoll_sparse_workspace_bytes(W, topk)
 
 
 def fuse_plan(counts, dtype=F32, threshold_bytes=DEFAULT_FUSION_THRESHOLD) -> list[int]:

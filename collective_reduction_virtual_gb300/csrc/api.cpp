@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -240,6 +241,44 @@ int copy_d2d(void* dst, const void* src, int64_t bytes, void* stream) {
   cudaError_t e = cudaMemcpyAsync(dst, src, (size_t)bytes, cudaMemcpyDeviceToDevice,
                                   (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  return VCOLL_OK;
+}
+
+// Launch sequence of the sparsified allreduce (shared by the entry points
+// that differ only in where the top-K workspace lives).
+int sparse_launch(SparseParams& prm, int topk, void* workspace, void* stream) {
+  int dev = 0, sms = 0, blocks = 0;
+  int rc = current_device(&dev, &sms);
+  if (rc) return rc;
+  const int W = prm.W;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (topk && prm.K > 0) {
+    prm.hist = (uint32_t*)workspace;
+    prm.state = (TopkState*)((char*)workspace + (size_t)W * kTopkBins * sizeof(uint32_t));
+    cudaError_t e = cudaMemsetAsync(prm.hist, 0, (size_t)W * kTopkBins * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    const int64_t gx = std::max<int64_t>(
+        1, std::min<int64_t>(prm.tiles_per_rank, ceil_div((int64_t)sms * 4, W)));
+    for (int pass = 0; pass < 3; ++pass) {
+      void* args[] = {&prm};
+      e = cudaLaunchKernel(topk_hist_kernel(pass), dim3((unsigned)gx, (unsigned)W), dim3(256), args,
+                           0, st);
+      if (e != cudaSuccess) return cuda_fail(e, "top-K histogram launch");
+      e = cudaLaunchKernel(topk_select_kernel(pass), dim3((unsigned)W), dim3(1024), args, 0, st);
+      if (e != cudaSuccess) return cuda_fail(e, "top-K select launch");
+    }
+    void* args[] = {&prm};
+    e = cudaLaunchKernel(topk_ties_kernel(), dim3((unsigned)W), dim3(1024), args, 0, st);
+    if (e != cudaSuccess) return cuda_fail(e, "top-K ties launch");
+  }
+  const void* fn = sparse_apply_kernel(topk);
+  if ((rc = resident_blocks(dev, fn, 256, 0, &blocks))) return rc;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(prm.num_tiles, (int64_t)sms * blocks));
+  void* args[] = {&prm};
+  cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(256), args, 0, st);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse apply launch");
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "sparse allreduce");
   return VCOLL_OK;
 }
 
@@ -747,6 +786,72 @@ int vcoll_fusion_allreduce(const void* const* in, void* const* out, const int64_
   begin.resize(nb + 1);
   if (nbatches) *nbatches = nb;
   return multi_run(in, out, counts, T, W, dtype, op, flags, begin, stream);
+}
+
+size_t vcoll_sparse_workspace_bytes(int W, int topk) {
+  if (W < 1 || W > VCOLL_MAX_RANKS || !topk) return 0;
+  return topk_workspace_bytes(W);
+}
+
+int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const* accum, int W,
+                           int64_t n, float threshold, int topk, int64_t* nnz, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  g_err[0] = 0;
+  int rc = check_common(W, n, VCOLL_F32, VCOLL_SUM);
+  if (rc) return rc;
+  if (topk && !(threshold >= 0.0f && threshold <= 1.0f))
+    return fail(VCOLL_ERR_INVALID_ARG, "top-K fraction %g outside [0, 1]", (double)threshold);
+  if (topk && n >= (int64_t)1 << 32)
+    return fail(VCOLL_ERR_UNSUPPORTED, "top-K needs n < 2^32 elements per rank");
+  int64_t lens[VCOLL_MAX_RANKS];
+  for (int u = 0; u < W; ++u) lens[u] = n;
+  if ((rc = check_ptrs(in, W, "in", 4, lens))) return rc;
+  if ((rc = check_ptrs((const void* const*)out, W, "out", 4, lens))) return rc;
+  if (accum && (rc = check_ptrs((const void* const*)accum, W, "accum", 4, lens))) return rc;
+  // the survivor counts are outputs: zero them first (also when n == 0)
+  if (nnz) {
+    if ((uint64_t)nnz % 8) return fail(VCOLL_ERR_INVALID_ARG, "nnz is not 8-byte aligned");
+    cudaError_t e = cudaMemsetAsync(nnz, 0, sizeof(int64_t) * W, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  }
+  if (n == 0) return VCOLL_OK;
+  std::vector<Buf> bufs;
+  for (int u = 0; u < W; ++u) {
+    bufs.push_back({(uint64_t)in[u], (uint64_t)(n * 4), (uint64_t)in[u], false});
+    bufs.push_back({(uint64_t)out[u], (uint64_t)(n * 4), (uint64_t)out[u], true});
+    if (accum) bufs.push_back({(uint64_t)accum[u], (uint64_t)(n * 4), (uint64_t)accum[u], true});
+  }
+  int vec, phase;
+  if ((rc = analyse(bufs, 4, &vec, &phase))) return rc;
+
+  int64_t K = 0;
+  if (topk) {
+    // K = ceil(threshold * num) in fp32, as SINGA computes nnzMax
+    const float kf = ceilf(threshold * (float)n);
+    K = kf >= (float)n ? n : (int64_t)kf;
+    if (!workspace || workspace_bytes < topk_workspace_bytes(W))
+      return fail(VCOLL_ERR_INVALID_ARG, "top-K needs a workspace of %zu bytes",
+                  topk_workspace_bytes(W));
+    if ((uint64_t)workspace % 16) return fail(VCOLL_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  }
+  SparseParams prm;
+  memset(&prm, 0, sizeof(prm));
+  for (int u = 0; u < W; ++u) {
+    prm.in[u] = in[u];
+    prm.out[u] = out[u];
+    prm.acc[u] = accum ? accum[u] : nullptr;
+  }
+  prm.nnz = nnz;
+  prm.n = n;
+  prm.W = W;
+  prm.K = K;
+  prm.phase = vec ? phase : -1;
+  prm.has_acc = accum ? 1 : 0;
+  prm.threshold = threshold;
+  prm.tile_elems = 4096;
+  prm.tiles_per_rank = ceil_div(n, prm.tile_elems);
+  prm.num_tiles = prm.tiles_per_rank;
+  return sparse_launch(prm, topk, workspace, stream);
 }
 
 int vcoll_device_errors(unsigned* flags, int clear) {

@@ -1,0 +1,351 @@
+// Sparsified allreduce with error feedback (Apache SINGA, Communicator::
+// valSparsAllReduce and topKSparsAllReduce).
+//
+// On the pages every rank compacts its surviving (index, value) pairs, the
+// lists are allgathered, and each rank scatters them into zeros with
+// cusparseSaxpyi, rank after rank.  With all W ranks in one GPU's memory the
+// same result is one rank-order fold per index over the entries that
+// survived, so the kernels never build the lists:
+//
+//   threshold: one pass -- x = in (+ accumulation); an entry survives when
+//     |x| > threshold (and x != 0, as the index array only holds nonzeros);
+//     the accumulation becomes x - (survivor ? x : 0); the output is zeros
+//     plus the survivors in rank order, written to every rank.
+//   top-K: the K entries of each rank with the largest values (ties: lower
+//     index first) are found exactly by a radix select on order-preserving
+//     32-bit keys -- three histogram passes over 11, 11 and 10 key bits, each
+//     followed by a one-CTA-per-rank selection of the digit that holds the
+//     K-th largest key; if keys equal to the K-th one straddle the cut, a
+//     scan in index order finds the last equal entry kept -- then the same
+//     apply pass as the threshold mode.
+//
+// The histograms (W x 2048 counters) and the per-rank selection state live in
+// a device workspace the caller provides.
+#include "device_common.cuh"
+#include "vcoll_internal.h"
+
+namespace vcoll {
+
+namespace {
+
+// larger value -> larger key; -0 just below +0; NaNs beyond the infinities
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// x = in (+ accumulation), one element
+__device__ __forceinline__ float load_x(const SparseParams& p, int r, int64_t i) {
+  float x = __uint_as_float(ld1<uint32_t>((const char*)p.in[r] + i * 4));
+  if (p.has_acc) x = __fadd_rn(x, __uint_as_float(ld1<uint32_t>((const char*)p.acc[r] + i * 4)));
+  return x;
+}
+
+// the same for a 16-byte vector of four elements
+__device__ __forceinline__ void load_x4(const SparseParams& p, int r, int64_t i, float (&x)[4]) {
+  const uint4 a = ld_stream((const char*)p.in[r] + i * 4);
+  x[0] = __uint_as_float(a.x);
+  x[1] = __uint_as_float(a.y);
+  x[2] = __uint_as_float(a.z);
+  x[3] = __uint_as_float(a.w);
+  if (p.has_acc) {
+    const uint4 b = ld_stream((const char*)p.acc[r] + i * 4);
+    x[0] = __fadd_rn(x[0], __uint_as_float(b.x));
+    x[1] = __fadd_rn(x[1], __uint_as_float(b.y));
+    x[2] = __fadd_rn(x[2], __uint_as_float(b.z));
+    x[3] = __fadd_rn(x[3], __uint_as_float(b.w));
+  }
+}
+
+// digit of pass P and whether the key matches the prefix fixed so far
+template <int P>
+__device__ __forceinline__ bool digit_of(uint32_t key, uint32_t prefix, uint32_t& d) {
+  if (P == 0) {
+    d = key >> 21;
+    return true;
+  }
+  if (P == 1) {
+    d = (key >> 10) & 0x7FFu;
+    return (key >> 21) == prefix;
+  }
+  d = key & 0x3FFu;
+  return (key >> 10) == prefix;
+}
+
+// shared-memory histogram add, lanes that share a bin combined first
+__device__ __forceinline__ void hist_add(uint32_t* h, bool valid, uint32_t d) {
+  const unsigned active = __ballot_sync(0xFFFFFFFFu, valid);
+  if (!valid) return;
+  const unsigned peers = __match_any_sync(active, d);
+  if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[d], (uint32_t)__popc(peers));
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- histogram
+// grid.y = rank; each CTA counts the digits of its tiles of that rank.
+template <int P>
+__global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ SparseParams p) {
+  __shared__ uint32_t h[kTopkBins];
+  const int r = blockIdx.y;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kTopkBins; i += blockDim.x) h[i] = 0;
+  const uint32_t prefix = p.state[r].prefix;
+  __syncthreads();
+  for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x) {
+    const int64_t t0 = tile * p.tile_elems;
+    const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
+    if (p.phase >= 0) {
+      int64_t av, bv;
+      aligned_body<4>(t0, t1, p.phase, av, bv);
+      // vectors [av, bv); the loop runs the same trip count on every lane of
+      // a warp so that the warp-wide combining stays converged
+      const int64_t nv = (bv - av) / 4;
+      for (int64_t base = 0; base < nv; base += blockDim.x) {
+        const int64_t v = base + tid;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        const bool in_range = v < nv;
+        if (in_range) load_x4(p, r, av + v * 4, x);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t d;
+          const bool m = digit_of<P>(order_key(x[q]), prefix, d) && in_range;
+          hist_add(h, m, d);
+        }
+      }
+      // head [t0, av) and tail [bv, t1): fewer than 4 elements each
+      int64_t i = -1;
+      if (tid < av - t0) i = t0 + tid;
+      if (tid >= 32 && tid - 32 < t1 - bv) i = bv + (tid - 32);
+      if (i >= 0) {
+        uint32_t d;
+        if (digit_of<P>(order_key(load_x(p, r, i)), prefix, d)) atomicAdd(&h[d], 1u);
+      }
+    } else {
+      for (int64_t base = t0; base < t1; base += blockDim.x) {
+        const int64_t i = base + tid;
+        uint32_t d = 0;
+        bool m = false;
+        if (i < t1) m = digit_of<P>(order_key(load_x(p, r, i)), prefix, d);
+        hist_add(h, m, d);
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < kTopkBins; i += blockDim.x)
+    if (h[i]) atomicAdd(&p.hist[(int64_t)r * kTopkBins + i], h[i]);
+}
+
+// ---------------------------------------------------------------- selection
+// One CTA of 1024 threads per rank: thread t owns bins 2047-2t and 2046-2t;
+// an inclusive scan from the top bin down finds the digit holding the
+// remaining-th largest key; the rank's histogram is cleared for the next pass.
+template <int P>
+__global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ SparseParams p) {
+  const int r = blockIdx.x;
+  const int t = threadIdx.x;
+  const int lane = t & 31, warp = t >> 5;
+  __shared__ unsigned long long warp_sum[32];
+  uint32_t* hist = p.hist + (int64_t)r * kTopkBins;
+  TopkState* st = p.state + r;
+  const int b0 = kTopkBins - 1 - 2 * t, b1 = b0 - 1;
+  const unsigned long long c0 = hist[b0], c1 = hist[b1];
+  unsigned long long s = c0 + c1;
+  // inclusive scan over threads (descending bins)
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, s, o);
+    if (lane >= o) s += y;
+  }
+  if (lane == 31) warp_sum[warp] = s;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long w = warp_sum[lane];
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sum[lane] = w;
+  }
+  __syncthreads();
+  const unsigned long long incl = s + (warp > 0 ? warp_sum[warp - 1] : 0ull);
+  const unsigned long long above = incl - c0 - c1;  // keys in bins > b0
+  const long long rem = P == 0 ? p.K : st->remaining;
+  const uint32_t prefix = P == 0 ? 0u : st->prefix;
+  __syncthreads();  // every thread has read the state before it changes
+  if (rem > 0 && (long long)above < rem && rem <= (long long)incl) {
+    int bin;
+    unsigned long long more;  // keys strictly above the chosen bin
+    if ((long long)(above + c0) >= rem) {
+      bin = b0;
+      more = above;
+    } else {
+      bin = b1;
+      more = above + c0;
+    }
+    const long long left = rem - (long long)more;
+    if (P == 0) {
+      st->prefix = (uint32_t)bin;
+      st->remaining = left;
+    } else if (P == 1) {
+      st->prefix = (prefix << 11) | (uint32_t)bin;
+      st->remaining = left;
+    } else {
+      st->T = (prefix << 10) | (uint32_t)bin;
+      st->need = left;
+      st->equal = (long long)(bin == b0 ? c0 : c1);
+      st->boundary = left == st->equal ? 0x7FFFFFFFFFFFFFFFll : -1;
+    }
+  }
+  hist[b0] = 0;
+  hist[b1] = 0;
+}
+
+// ---------------------------------------------------------------------- ties
+// One CTA per rank whose equal keys straddle the cut: the index of the
+// need-th entry equal to T, scanning in index order.
+__global__ void __launch_bounds__(1024) vc_topk_ties(const __grid_constant__ SparseParams p) {
+  const int r = blockIdx.x;
+  const int t = threadIdx.x;
+  const int lane = t & 31, warp = t >> 5;
+  __shared__ int wcount[32];
+  __shared__ long long found;
+  TopkState* st = p.state + r;
+  const long long need = st->need, equal = st->equal;
+  const uint32_t T = st->T;
+  if (p.K == 0 || need >= equal) return;  // every equal key kept (or none selected)
+  if (t == 0) found = -1;
+  long long seen = 0;
+  for (int64_t base = 0; base < p.n; base += blockDim.x) {
+    const int64_t i = base + t;
+    const bool eq = i < p.n && order_key(load_x(p, r, i)) == T;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, eq);
+    if (lane == 0) wcount[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < 32; ++w) {
+      if (w < warp) before += wcount[w];
+      total += wcount[w];
+    }
+    before += __popc(bal & ((1u << lane) - 1u));
+    if (eq && seen + before + 1 == need) found = i;
+    __syncthreads();
+    seen += total;
+    if (found >= 0) break;
+  }
+  if (t == 0) st->boundary = found;
+}
+
+// -------------------------------------------------------------------- apply
+// One pass: survivors, error feedback, rank-order sum written to every rank,
+// survivor counts per rank.
+template <int TOPK>
+__global__ void __launch_bounds__(256) vc_sparse_apply(const __grid_constant__ SparseParams p) {
+  __shared__ uint32_t s_T[VCOLL_MAX_RANKS];
+  __shared__ long long s_bound[VCOLL_MAX_RANKS];
+  __shared__ unsigned long long s_cnt[VCOLL_MAX_RANKS];
+  const int W = p.W;
+  const int tid = threadIdx.x;
+  for (int r = tid; r < W; r += blockDim.x) {
+    if (TOPK) {
+      s_T[r] = p.state[r].T;
+      s_bound[r] = p.state[r].boundary;
+    }
+    s_cnt[r] = 0;
+  }
+  __syncthreads();
+  auto keep = [&](int r, float x, int64_t i) -> bool {
+    if (TOPK) {
+      if (p.K == 0) return false;
+      const uint32_t k = order_key(x);
+      return k > s_T[r] || (k == s_T[r] && i <= s_bound[r]);
+    }
+    return fabsf(x) > p.threshold && x != 0.0f;
+  };
+  auto count = [&](int r, int c) {
+    // per-warp sum of this rank's survivors, one shared atomic per warp
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+    if ((tid & 31) == 0 && c) atomicAdd(&s_cnt[r], (unsigned long long)c);
+  };
+  for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    const int64_t t0 = tile * p.tile_elems;
+    const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
+    int64_t av = t0, bv = t0;
+    if (p.phase >= 0) aligned_body<4>(t0, t1, p.phase, av, bv);
+    const int64_t nv = (bv - av) / 4;
+    for (int64_t base = 0; base < nv; base += blockDim.x) {
+      const int64_t v = base + tid;
+      const bool in_range = v < nv;
+      const int64_t e = av + v * 4;
+      float res[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int r = 0; r < W; ++r) {
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        int c = 0;
+        if (in_range) {
+          load_x4(p, r, e, x);
+          float s[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const bool k = keep(r, x[q], e + q);
+            s[q] = k ? x[q] : 0.0f;
+            if (k) res[q] = __fadd_rn(x[q], res[q]);
+            c += k;
+          }
+          if (p.has_acc)
+            st_stream((char*)p.acc[r] + e * 4,
+                      make_uint4(__float_as_uint(__fsub_rn(x[0], s[0])),
+                                 __float_as_uint(__fsub_rn(x[1], s[1])),
+                                 __float_as_uint(__fsub_rn(x[2], s[2])),
+                                 __float_as_uint(__fsub_rn(x[3], s[3]))));
+        }
+        if (p.nnz) count(r, c);
+      }
+      if (in_range) {
+        const uint4 o = make_uint4(__float_as_uint(res[0]), __float_as_uint(res[1]),
+                                   __float_as_uint(res[2]), __float_as_uint(res[3]));
+        for (int r = 0; r < W; ++r) st_stream((char*)p.out[r] + e * 4, o);
+      }
+    }
+    // the elements outside whole vectors (all of the tile when the phases
+    // differ), one per thread
+    const int64_t head = av - t0, tail = t1 - bv;
+    for (int64_t base = 0; base < head + tail; base += blockDim.x) {
+      const int64_t j = base + tid;
+      const bool in_range = j < head + tail;
+      const int64_t i = j < head ? t0 + j : bv + (j - head);
+      float res = 0.0f;
+      for (int r = 0; r < W; ++r) {
+        int c = 0;
+        if (in_range) {
+          const float x = load_x(p, r, i);
+          const bool k = keep(r, x, i);
+          const float s = k ? x : 0.0f;
+          if (k) res = __fadd_rn(x, res);
+          c = k;
+          if (p.has_acc) st1((char*)p.acc[r] + i * 4, __float_as_uint(__fsub_rn(x, s)));
+        }
+        if (p.nnz) count(r, c);
+      }
+      if (in_range)
+        for (int r = 0; r < W; ++r) st1((char*)p.out[r] + i * 4, __float_as_uint(res));
+    }
+  }
+  __syncthreads();
+  if (p.nnz)
+    for (int r = tid; r < W; r += blockDim.x)
+      if (s_cnt[r]) atomicAdd((unsigned long long*)&p.nnz[r], s_cnt[r]);
+}
+
+const void* sparse_apply_kernel(int topk) {
+  return topk ? (const void*)&vc_sparse_apply<1> : (const void*)&vc_sparse_apply<0>;
+}
+const void* topk_hist_kernel(int pass) {
+  return pass == 0 ? (const void*)&vc_topk_hist<0>
+                   : pass == 1 ? (const void*)&vc_topk_hist<1> : (const void*)&vc_topk_hist<2>;
+}
+const void* topk_select_kernel(int pass) {
+  return pass == 0 ? (const void*)&vc_topk_select<0>
+                   : pass == 1 ? (const void*)&vc_topk_select<1> : (const void*)&vc_topk_select<2>;
+}
+const void* topk_ties_kernel() { return (const void*)&vc_topk_ties; }
+
+}  // namespace vcoll

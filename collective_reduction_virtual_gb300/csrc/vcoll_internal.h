@@ -112,6 +112,41 @@ struct MultiParams {
   int do_scale;
 };
 
+// Sparsified allreduce (SINGA valSparsAllReduce / topKSparsAllReduce).
+// Top-K keeps, per rank, the K entries with the largest values (ties: lower
+// index first), found by an exact radix select over order-preserving 32-bit
+// keys in three digit passes (11, 11 and 10 bits).  Per-rank selection state
+// and the digit histograms live in a device workspace.
+constexpr int kTopkBins = 2048;
+struct TopkState {
+  uint32_t prefix;    // key bits fixed by the passes so far
+  uint32_t T;         // after the last pass: the K-th largest key
+  int64_t remaining;  // entries still to take at or below the current prefix
+  int64_t need;       // entries equal to T that are kept
+  int64_t equal;      // entries equal to T
+  int64_t boundary;   // equal entries with index <= boundary are kept
+};
+struct SparseParams {
+  const void* in[VCOLL_MAX_RANKS];
+  void* out[VCOLL_MAX_RANKS];
+  void* acc[VCOLL_MAX_RANKS];  // error-feedback accumulations, or all NULL
+  int64_t* nnz;                // device, W counters (may be NULL)
+  uint32_t* hist;              // workspace: W x kTopkBins
+  TopkState* state;            // workspace: W entries
+  int64_t n;
+  int64_t tiles_per_rank;      // histogram passes: grid.y = rank
+  int64_t num_tiles;           // apply pass: tiles over [0, n)
+  int64_t tile_elems;
+  int64_t K;
+  int W;
+  int phase;                   // 16-byte phase shared by every buffer, or -1
+  int has_acc;
+  float threshold;
+};
+inline size_t topk_workspace_bytes(int W) {
+  return (size_t)W * kTopkBins * sizeof(uint32_t) + (size_t)W * sizeof(TopkState) + 256;
+}
+
 // Kernel selection (function pointers for cudaLaunchKernel).  W_t is the
 // compile-time rank count (2, 4, 8, 16) or 0 for the runtime-W kernels; vec
 // selects the 16-byte vector path.
@@ -122,6 +157,10 @@ const void* staged_kernel_bf16(int op, int kind, int W_t, int ring);
 const void* gather_kernel(int elem_size, int vec);
 const void* gather_tma_kernel(int elem_size);
 const void* wire_kernel(int wire, int W_t, int ring);
+const void* sparse_apply_kernel(int topk);
+const void* topk_hist_kernel(int pass);
+const void* topk_select_kernel(int pass);
+const void* topk_ties_kernel();
 constexpr int kGatherTmaThreads = 64;
 constexpr int kGatherTmaStages = 4;
 constexpr int kGatherTmaTileBytes = 32768;

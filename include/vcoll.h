@@ -58,6 +58,7 @@
 #ifndef VCOLL_H_
 #define VCOLL_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -212,6 +213,28 @@ int vcoll_allreduce_multi(const void* const* in, void* const* out, const int64_t
 int vcoll_fusion_allreduce(const void* const* in, void* const* out, const int64_t* counts, int T,
                            int W, int dtype, int op, unsigned flags, int64_t threshold_bytes,
                            int* nbatches, void* stream);
+
+/*
+ * Sparsified allreduce with error feedback (Apache SINGA
+ * Communicator::valSparsAllReduce, topK == false, and topKSparsAllReduce,
+ * topK == true), fp32.  Per rank u: x = in[u] (+ accum[u] when accum is not
+ * NULL).  threshold mode: the entries with |x| > threshold survive (and
+ * x != 0); top-K mode: the K = ceil(threshold * n) entries (threshold in
+ * [0, 1], computed in fp32 as SINGA does) with the largest values survive,
+ * ties broken toward the lower index.  With accum, accum[u] becomes x minus
+ * the survivors (zero where an entry survived, x elsewhere).  Every out[u]
+ * receives the sum of all ranks' survivors, added into zeros rank by rank --
+ * what the allgathered sparse lists scattered with cusparseSaxpyi give.
+ * nnz (device, W int64, may be NULL) receives each rank's survivor count.
+ * workspace: device memory of vcoll_sparse_workspace_bytes(W, topk) bytes
+ * (16-byte aligned; none needed in threshold mode), owned by the caller, not
+ * kept after the call; calls that share a workspace must not overlap.
+ * In place: out[u] == in[u].
+ */
+size_t vcoll_sparse_workspace_bytes(int W, int topk);
+int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const* accum, int W,
+                           int64_t n, float threshold, int topk, int64_t* nnz, void* workspace,
+                           size_t workspace_bytes, void* stream);
 
 /* Device-side error bits, OR-ed into one word per device by the kernels.
  * The staged kernels bound every wait on their shared-memory barriers; a wait

@@ -231,3 +231,20 @@ def test_allreduce_wire_errors(v):
     # fp16 is only a wire type: the plain collectives reject it
     assert v.vcoll_allreduce(FAKE_IN[:4], FAKE_OUT[:4], 4, 64, v.F16, v.SUM, 0, 0) \
         == v.ERR_INVALID_TYPE
+
+
+def test_sparse_allreduce_errors(v):
+    f = v.vcoll_sparse_allreduce
+    assert v.vcoll_sparse_workspace_bytes(8, 0) == 0
+    need = v.vcoll_sparse_workspace_bytes(8, 1)
+    assert need >= 8 * 2048 * 4
+    ins, outs = FAKE_IN[:4], FAKE_OUT[:4]
+    assert f(ins, outs, None, 0, 64, 0.5, 0) == v.ERR_INVALID_ARG
+    assert f(ins, outs, None, 4, -1, 0.5, 0) == v.ERR_INVALID_ARG
+    assert f(ins, outs, None, 4, 64, 1.5, 1) == v.ERR_INVALID_ARG        # fraction > 1
+    assert f(ins, outs, None, 4, 64, 0.5, 1, 0, 0, 0) == v.ERR_INVALID_ARG  # no workspace
+    assert f(ins, outs, None, 4, 64, 0.5, 1, 0, 0x100000, 16) == v.ERR_INVALID_ARG  # too small
+    assert f([ins[0] + 2] + ins[1:], outs, None, 4, 64, 0.5, 0) == v.ERR_INVALID_ARG
+    # accumulation overlapping an output
+    assert f(ins, outs, [outs[1]] + FAKE_OUT[4:7], 4, 64, 0.5, 0) == v.ERR_INVALID_ARG
+    assert f([0] * 4, [0] * 4, None, 4, 0, 0.5, 1) == v.OK

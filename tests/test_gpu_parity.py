@@ -617,3 +617,79 @@ def test_allreduce_wire_misaligned(v):
     got = v.allreduce_wire(ins, wire="f16", op="sum", ring_order=True)
     for r in range(W):
         assert_bit_exact(to_np(got[r]), want[r], "wire misaligned")
+
+
+# ----------------------------------------------- sparsified allreduce (SINGA)
+
+def _sparse_inputs(W, n, seed, ties=False):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    xs = []
+    for _ in range(W):
+        x = torch.randn(n, generator=g, device="cuda")
+        if ties:
+            x = torch.round(x * 4) / 4  # many equal values across the top-K cut
+        xs.append(x)
+    return xs
+
+
+def _check_sparse(v, ins, acc, thr, topk):
+    W = len(ins)
+    ins_np = [to_np(t) for t in ins]
+    acc_np = [to_np(a).copy() for a in acc] if acc is not None else None
+    want, want_nnz = oracle.sparse_allreduce(ins_np, thr, topk, acc_np)
+    nnz = torch.empty(W, dtype=torch.int64, device="cuda")
+    outs = v.sparse_allreduce(ins, accum=acc, threshold=thr, topk=topk, nnz=nnz)
+    torch.cuda.synchronize()
+    for u in range(W):
+        assert_bit_exact(to_np(outs[u]), want[u], f"sparse topk={topk} out {u}")
+        if acc is not None:
+            assert_bit_exact(to_np(acc[u]), acc_np[u], f"sparse topk={topk} accum {u}")
+    assert nnz.cpu().tolist() == list(want_nnz)
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("n", [1, 17, 4097, 100_003])
+@pytest.mark.parametrize("with_acc", [False, True])
+def test_sparse_threshold(v, W, n, with_acc):
+    ins = _sparse_inputs(W, n, 40 * W + n)
+    acc = [t * 0.3 for t in _sparse_inputs(W, n, 41 * W + n)] if with_acc else None
+    _check_sparse(v, ins, acc, 0.8, False)
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 8])
+@pytest.mark.parametrize("n", [1, 17, 4097, 100_003])
+@pytest.mark.parametrize("frac", [0.0, 0.001, 0.05, 0.5, 1.0])
+def test_sparse_topk(v, W, n, frac):
+    ins = _sparse_inputs(W, n, 50 * W + n)
+    acc = [t * 0.3 for t in _sparse_inputs(W, n, 51 * W + n)]
+    _check_sparse(v, ins, acc, frac, True)
+
+
+@pytest.mark.parametrize("frac", [0.01, 0.3, 0.77])
+def test_sparse_topk_ties_straddle_the_cut(v, frac):
+    W, n = 4, 50_001
+    ins = _sparse_inputs(W, n, 77, ties=True)
+    _check_sparse(v, ins, None, frac, True)
+    _check_sparse(v, ins, [torch.zeros(n, device="cuda") for _ in range(W)], frac, True)
+
+
+def test_sparse_misaligned_and_in_place(v):
+    W, n = 3, 30_001
+    base = _sparse_inputs(W, n + 4, 9)
+    ins = [b[u % 4: u % 4 + n] for u, b in enumerate(base)]  # mixed 16-byte phases
+    _check_sparse(v, ins, None, 0.9, False)
+    _check_sparse(v, ins, None, 0.02, True)
+    bufs = [t.clone() for t in _sparse_inputs(W, n, 10)]
+    want, _ = oracle.sparse_allreduce([to_np(t) for t in bufs], 0.05, True)
+    v.sparse_allreduce(bufs, bufs, threshold=0.05, topk=True)
+    for u in range(W):
+        assert_bit_exact(to_np(bufs[u]), want[u], "sparse in place")
+
+
+def test_sparse_topk_larger(v):
+    W, n = 8, 1 << 21
+    ins = _sparse_inputs(W, n, 123)
+    acc = [torch.zeros(n, device="cuda") for _ in range(W)]
+    _check_sparse(v, ins, acc, 0.01, True)
+    _check_sparse(v, ins, acc, 0.01, True)  # second step: the error feedback is nonzero now
