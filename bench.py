@@ -480,7 +480,18 @@ def extras(args, stream, dev):
         lambda: vc.allreduce_wire(ins, outs, wire="f16", op="sum"), 2 * W * n * 4)
     out["rs_sum_w8_f32_2^26_staged"] = rate(
         lambda: vc.reduce_scatter(ins, segs, op="sum", flags=vc.FLAG_STAGED), (W + 1) * n * 4)
-    del ins, outs, segs
+    # sparsified allreduce with error feedback (SINGA): threshold and top-1 %
+    acc = [torch.zeros_like(t) for t in ins]
+    nnz = torch.empty(W, dtype=torch.int64, device=dev)
+    ws = torch.empty(vc.sparse_workspace_bytes(W, True), dtype=torch.uint8, device=dev)
+    out["sparse_threshold_w8_f32_2^26"] = rate(
+        lambda: vc.sparse_allreduce(ins, outs, acc, 1e-3, False, nnz), 4 * W * n * 4)
+    out["sparse_topk1pct_w8_f32_2^26"] = rate(
+        lambda: vc.sparse_allreduce(ins, outs, acc, 0.01, True, nnz, ws), 4 * W * n * 4)
+    out["sparse_bytes_formula"] = ("4*W*n*4: read inputs and accumulations, write outputs and "
+                                   "accumulations (top-K also reads the inputs and accumulations "
+                                   "three more times for its radix select)")
+    del ins, outs, segs, acc
     torch.cuda.empty_cache()
 
     # W=8 bf16 avg n=2^28 with outliers
