@@ -252,9 +252,11 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, void* stream) {
   if (rc) return rc;
   const int W = prm.W;
   cudaStream_t st = (cudaStream_t)stream;
-  if (topk && prm.K > 0) {
+  if (topk) {
     prm.hist = (uint32_t*)workspace;
     prm.state = (TopkState*)((char*)workspace + (size_t)W * kTopkBins * sizeof(uint32_t));
+  }
+  if (topk && prm.K > 0) {
     cudaError_t e = cudaMemsetAsync(prm.hist, 0, (size_t)W * kTopkBins * sizeof(uint32_t), st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     const int64_t gx = std::max<int64_t>(

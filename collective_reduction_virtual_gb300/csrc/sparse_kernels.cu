@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(256) vc_sparse_apply(const __grid_constant__ S
   const int W = p.W;
   const int tid = threadIdx.x;
   for (int r = tid; r < W; r += blockDim.x) {
-    if (TOPK) {
+    if (TOPK && p.K > 0) {  // with K == 0 no selection ran and nothing survives
       s_T[r] = p.state[r].T;
       s_bound[r] = p.state[r].boundary;
     }
