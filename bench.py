@@ -54,8 +54,7 @@ L2_BYTES = 129 * 1024 * 1024
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 # the device code of the timed kernels: DRAM traffic taken by ncu stays valid
 # while these files are unchanged
-KERNEL_SOURCES = ["device_common.cuh", "reduce_kernels.cuh", "reduce_f32.cu", "staged_kernels.cu",
-                  "vcoll_internal.h"]
+KERNEL_SOURCES = ["device_common.cuh", "reduce_kernels.cuh", "reduce_f32.cu", "staged_kernels.cu"]
 
 
 # ------------------------------------------------------------ distributed
@@ -483,7 +482,7 @@ def extras(args, stream, dev):
     # sparsified allreduce with error feedback (SINGA): threshold and top-1 %
     acc = [torch.zeros_like(t) for t in ins]
     nnz = torch.empty(W, dtype=torch.int64, device=dev)
-    ws = torch.empty(vc.sparse_workspace_bytes(W, True), dtype=torch.uint8, device=dev)
+    ws = torch.empty(vc.sparse_workspace_bytes(W, n, True), dtype=torch.uint8, device=dev)
     out["sparse_threshold_w8_f32_2^26"] = rate(
         lambda: vc.sparse_allreduce(ins, outs, acc, 1e-3, False, nnz), 4 * W * n * 4)
     out["sparse_topk1pct_w8_f32_2^26"] = rate(

@@ -66,7 +66,7 @@ def lib() -> ctypes.CDLL:
             L.vcoll_fuse_pack.restype = I
             L.vcoll_fuse_unpack.argtypes = [PP, I64P, I, PP, I, I, P]
             L.vcoll_fuse_unpack.restype = I
-            L.vcoll_sparse_workspace_bytes.argtypes = [I, I]
+            L.vcoll_sparse_workspace_bytes.argtypes = [I, I64, I]
             L.vcoll_sparse_workspace_bytes.restype = ctypes.c_size_t
             L.vcoll_sparse_allreduce.argtypes = [PP, PP, PP, I, I64, ctypes.c_float, I, P, P,
                                                  ctypes.c_size_t, P]
@@ -150,8 +150,8 @@ def vcoll_allreduce_wire(in_ptrs, out_ptrs, W, n, wire, op, flags=0, stream=0) -
                                       flags, stream or None)
 
 
-def vcoll_sparse_workspace_bytes(W, topk) -> int:
-    return int(lib().vcoll_sparse_workspace_bytes(W, 1 if topk else 0))
+def vcoll_sparse_workspace_bytes(W, n, topk) -> int:
+    return int(lib().vcoll_sparse_workspace_bytes(W, n, 1 if topk else 0))
 
 
 def vcoll_sparse_allreduce(in_ptrs, out_ptrs, acc_ptrs, W, n, threshold, topk, nnz_ptr=0,
@@ -331,14 +331,14 @@ def sparse_allreduce(ins, outs=None, accum=None, threshold=0.0, topk=False, nnz=
     top-K with K = ceil(threshold * n)).  accum: W fp32 tensors updated in
     place (error feedback) or None.  nnz: int64 CUDA tensor of W survivor
     counts (optional).  workspace: a uint8 CUDA tensor of at least
-    sparse_workspace_bytes(W, topk) bytes; allocated here when omitted."""
+    sparse_workspace_bytes(W, n, topk) bytes; allocated here when omitted."""
     torch = _torch()
     W, n = len(ins), ins[0].numel()
     _check_tensors(ins, "ins")
     if outs is None:
         outs = [torch.empty_like(t) for t in ins]
     _check_tensors(outs, "outs")
-    need = vcoll_sparse_workspace_bytes(W, topk)
+    need = vcoll_sparse_workspace_bytes(W, n, topk)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=ins[0].device)
     ws_ptr = workspace.data_ptr() if workspace is not None else 0
@@ -350,8 +350,8 @@ def sparse_allreduce(ins, outs=None, accum=None, threshold=0.0, topk=False, nnz=
     return outs
 
 
-def sparse_workspace_bytes(W, topk=True) -> int:
-    return vcoll_sparse_workspace_bytes(W, topk)
+def sparse_workspace_bytes(W, n, topk=True) -> int:
+    return vcoll_sparse_workspace_bytes(W, n, topk)
 
 
 def fuse_plan(counts, dtype=F32, threshold_bytes=DEFAULT_FUSION_THRESHOLD) -> list[int]:

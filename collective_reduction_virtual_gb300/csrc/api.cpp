@@ -255,6 +255,7 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, void* stream) {
   if (topk) {
     prm.hist = (uint32_t*)workspace;
     prm.state = (TopkState*)((char*)workspace + (size_t)W * kTopkBins * sizeof(uint32_t));
+    prm.tilecnt = (uint32_t*)((char*)prm.state + (size_t)W * sizeof(TopkState));
   }
   if (topk && prm.K > 0) {
     cudaError_t e = cudaMemsetAsync(prm.hist, 0, (size_t)W * kTopkBins * sizeof(uint32_t), st);
@@ -270,8 +271,11 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, void* stream) {
       if (e != cudaSuccess) return cuda_fail(e, "top-K select launch");
     }
     void* args[] = {&prm};
-    e = cudaLaunchKernel(topk_ties_kernel(), dim3((unsigned)W), dim3(1024), args, 0, st);
-    if (e != cudaSuccess) return cuda_fail(e, "top-K ties launch");
+    e = cudaLaunchKernel(topk_tie_count_kernel(), dim3((unsigned)gx, (unsigned)W), dim3(256), args,
+                         0, st);
+    if (e != cudaSuccess) return cuda_fail(e, "top-K tie count launch");
+    e = cudaLaunchKernel(topk_tie_find_kernel(), dim3((unsigned)W), dim3(1024), args, 0, st);
+    if (e != cudaSuccess) return cuda_fail(e, "top-K tie find launch");
   }
   const void* fn = sparse_apply_kernel(topk);
   if ((rc = resident_blocks(dev, fn, 256, 0, &blocks))) return rc;
@@ -790,9 +794,9 @@ int vcoll_fusion_allreduce(const void* const* in, void* const* out, const int64_
   return multi_run(in, out, counts, T, W, dtype, op, flags, begin, stream);
 }
 
-size_t vcoll_sparse_workspace_bytes(int W, int topk) {
-  if (W < 1 || W > VCOLL_MAX_RANKS || !topk) return 0;
-  return topk_workspace_bytes(W);
+size_t vcoll_sparse_workspace_bytes(int W, int64_t n, int topk) {
+  if (W < 1 || W > VCOLL_MAX_RANKS || n < 0 || !topk) return 0;
+  return topk_workspace_bytes(W, n);
 }
 
 int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const* accum, int W,
@@ -831,9 +835,9 @@ int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const*
     // K = ceil(threshold * num) in fp32, as SINGA computes nnzMax
     const float kf = ceilf(threshold * (float)n);
     K = kf >= (float)n ? n : (int64_t)kf;
-    if (!workspace || workspace_bytes < topk_workspace_bytes(W))
+    if (!workspace || workspace_bytes < topk_workspace_bytes(W, n))
       return fail(VCOLL_ERR_INVALID_ARG, "top-K needs a workspace of %zu bytes",
-                  topk_workspace_bytes(W));
+                  topk_workspace_bytes(W, n));
     if ((uint64_t)workspace % 16) return fail(VCOLL_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
   }
   SparseParams prm;
@@ -850,7 +854,7 @@ int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const*
   prm.phase = vec ? phase : -1;
   prm.has_acc = accum ? 1 : 0;
   prm.threshold = threshold;
-  prm.tile_elems = 4096;
+  prm.tile_elems = kSparseTileElems;
   prm.tiles_per_rank = ceil_div(n, prm.tile_elems);
   prm.num_tiles = prm.tiles_per_rank;
   return sparse_launch(prm, topk, workspace, stream);

@@ -15,12 +15,13 @@
 //     index first) are found exactly by a radix select on order-preserving
 //     32-bit keys -- three histogram passes over 11, 11 and 10 key bits, each
 //     followed by a one-CTA-per-rank selection of the digit that holds the
-//     K-th largest key; if keys equal to the K-th one straddle the cut, a
-//     scan in index order finds the last equal entry kept -- then the same
-//     apply pass as the threshold mode.
+//     K-th largest key; if keys equal to the K-th one straddle the cut,
+//     per-tile counts of equal keys and a scan over them find the last equal
+//     entry kept in index order -- then the same apply pass as the threshold
+//     mode.
 //
-// The histograms (W x 2048 counters) and the per-rank selection state live in
-// a device workspace the caller provides.
+// The histograms (W x 2048 counters), the per-rank selection state and the
+// per-tile tie counts live in a device workspace the caller provides.
 #include "device_common.cuh"
 #include "vcoll_internal.h"
 
@@ -201,38 +202,99 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
 }
 
 // ---------------------------------------------------------------------- ties
-// One CTA per rank whose equal keys straddle the cut: the index of the
-// need-th entry equal to T, scanning in index order.
-__global__ void __launch_bounds__(1024) vc_topk_ties(const __grid_constant__ SparseParams p) {
+// Only for ranks whose keys equal to the K-th largest straddle the cut
+// (need < equal): (1) every tile counts its entries equal to T; (2) one CTA
+// per rank scans the tile counts to the tile holding the need-th equal entry
+// and then that tile in index order; the entry's index is the boundary.
+__global__ void __launch_bounds__(256) vc_topk_tie_count(const __grid_constant__ SparseParams p) {
+  const int r = blockIdx.y;
+  const TopkState* st = p.state + r;
+  if (p.K == 0 || st->need >= st->equal) return;  // uniform per CTA
+  const uint32_t T = st->T;
+  for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x) {
+    const int64_t t0 = tile * p.tile_elems;
+    const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
+    int c = 0;
+    for (int64_t base = t0; base < t1; base += blockDim.x) {
+      const int64_t i = base + threadIdx.x;
+      c += __syncthreads_count(i < t1 && order_key(load_x(p, r, i)) == T);
+    }
+    if (threadIdx.x == 0) p.tilecnt[(int64_t)r * p.tiles_per_rank + tile] = (uint32_t)c;
+  }
+}
+
+// block-wide exclusive scan of one int per thread (1024 threads); *total gets
+// the sum
+__device__ __forceinline__ long long block_excl_scan(long long v, long long* total) {
+  __shared__ long long ws[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long s = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xFFFFFFFFu, s, o);
+    if (lane >= o) s += y;
+  }
+  if (lane == 31) ws[warp] = s;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = ws[lane];
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += y;
+    }
+    ws[lane] = w;
+  }
+  __syncthreads();
+  const long long excl = s - v + (warp > 0 ? ws[warp - 1] : 0);
+  *total = ws[31];
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(1024) vc_topk_tie_find(const __grid_constant__ SparseParams p) {
   const int r = blockIdx.x;
-  const int t = threadIdx.x;
-  const int lane = t & 31, warp = t >> 5;
-  __shared__ int wcount[32];
-  __shared__ long long found;
   TopkState* st = p.state + r;
   const long long need = st->need, equal = st->equal;
+  if (p.K == 0 || need >= equal) return;
   const uint32_t T = st->T;
-  if (p.K == 0 || need >= equal) return;  // every equal key kept (or none selected)
-  if (t == 0) found = -1;
+  const uint32_t* cnt = p.tilecnt + (int64_t)r * p.tiles_per_rank;
+  __shared__ long long s_tile, s_before, s_found;
+  if (threadIdx.x == 0) {
+    s_tile = -1;
+    s_found = -1;
+  }
+  __syncthreads();
+  // the tile where the running count of equal entries reaches need
   long long seen = 0;
-  for (int64_t base = 0; base < p.n; base += blockDim.x) {
-    const int64_t i = base + t;
-    const bool eq = i < p.n && order_key(load_x(p, r, i)) == T;
-    const unsigned bal = __ballot_sync(0xFFFFFFFFu, eq);
-    if (lane == 0) wcount[warp] = __popc(bal);
-    __syncthreads();
-    int before = 0, total = 0;
-    for (int w = 0; w < 32; ++w) {
-      if (w < warp) before += wcount[w];
-      total += wcount[w];
+  for (int64_t base = 0; base < p.tiles_per_rank; base += blockDim.x) {
+    const int64_t k = base + threadIdx.x;
+    const long long c = k < p.tiles_per_rank ? cnt[k] : 0;
+    long long total;
+    const long long before = seen + block_excl_scan(c, &total);
+    if (c > 0 && before < need && need <= before + c) {
+      s_tile = k;
+      s_before = before;
     }
-    before += __popc(bal & ((1u << lane) - 1u));
-    if (eq && seen + before + 1 == need) found = i;
     __syncthreads();
     seen += total;
-    if (found >= 0) break;
+    if (s_tile >= 0) break;
   }
-  if (t == 0) st->boundary = found;
+  const int64_t tile = s_tile;
+  if (tile < 0) return;  // cannot happen when the histograms are consistent
+  // inside that tile, in index order
+  const int64_t t0 = tile * p.tile_elems;
+  const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
+  seen = s_before;
+  for (int64_t base = t0; base < t1; base += blockDim.x) {
+    const int64_t i = base + threadIdx.x;
+    const bool eq = i < t1 && order_key(load_x(p, r, i)) == T;
+    long long total;
+    const long long before = seen + block_excl_scan(eq ? 1 : 0, &total);
+    if (eq && before + 1 == need) s_found = i;
+    __syncthreads();
+    seen += total;
+    if (s_found >= 0) break;
+  }
+  if (threadIdx.x == 0) st->boundary = s_found;
 }
 
 // -------------------------------------------------------------------- apply
@@ -346,6 +408,7 @@ const void* topk_select_kernel(int pass) {
   return pass == 0 ? (const void*)&vc_topk_select<0>
                    : pass == 1 ? (const void*)&vc_topk_select<1> : (const void*)&vc_topk_select<2>;
 }
-const void* topk_ties_kernel() { return (const void*)&vc_topk_ties; }
+const void* topk_tie_count_kernel() { return (const void*)&vc_topk_tie_count; }
+const void* topk_tie_find_kernel() { return (const void*)&vc_topk_tie_find; }
 
 }  // namespace vcoll

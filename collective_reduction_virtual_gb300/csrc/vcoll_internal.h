@@ -133,6 +133,7 @@ struct SparseParams {
   int64_t* nnz;                // device, W counters (may be NULL)
   uint32_t* hist;              // workspace: W x kTopkBins
   TopkState* state;            // workspace: W entries
+  uint32_t* tilecnt;           // workspace: W x tiles_per_rank (tie counts)
   int64_t n;
   int64_t tiles_per_rank;      // histogram passes: grid.y = rank
   int64_t num_tiles;           // apply pass: tiles over [0, n)
@@ -143,8 +144,11 @@ struct SparseParams {
   int has_acc;
   float threshold;
 };
-inline size_t topk_workspace_bytes(int W) {
-  return (size_t)W * kTopkBins * sizeof(uint32_t) + (size_t)W * sizeof(TopkState) + 256;
+constexpr int64_t kSparseTileElems = 4096;
+inline size_t topk_workspace_bytes(int W, int64_t n) {
+  const int64_t tiles = (n + kSparseTileElems - 1) / kSparseTileElems;
+  return (size_t)W * kTopkBins * sizeof(uint32_t) + (size_t)W * sizeof(TopkState) +
+         (size_t)W * (size_t)(tiles > 0 ? tiles : 1) * sizeof(uint32_t) + 256;
 }
 
 // Kernel selection (function pointers for cudaLaunchKernel).  W_t is the
@@ -160,7 +164,8 @@ const void* wire_kernel(int wire, int W_t, int ring);
 const void* sparse_apply_kernel(int topk);
 const void* topk_hist_kernel(int pass);
 const void* topk_select_kernel(int pass);
-const void* topk_ties_kernel();
+const void* topk_tie_count_kernel();
+const void* topk_tie_find_kernel();
 constexpr int kGatherTmaThreads = 64;
 constexpr int kGatherTmaStages = 4;
 constexpr int kGatherTmaTileBytes = 32768;

@@ -226,12 +226,12 @@ int vcoll_fusion_allreduce(const void* const* in, void* const* out, const int64_
  * receives the sum of all ranks' survivors, added into zeros rank by rank --
  * what the allgathered sparse lists scattered with cusparseSaxpyi give.
  * nnz (device, W int64, may be NULL) receives each rank's survivor count.
- * workspace: device memory of vcoll_sparse_workspace_bytes(W, topk) bytes
+ * workspace: device memory of vcoll_sparse_workspace_bytes(W, n, topk) bytes
  * (16-byte aligned; none needed in threshold mode), owned by the caller, not
  * kept after the call; calls that share a workspace must not overlap.
  * In place: out[u] == in[u].
  */
-size_t vcoll_sparse_workspace_bytes(int W, int topk);
+size_t vcoll_sparse_workspace_bytes(int W, int64_t n, int topk);
 int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const* accum, int W,
                            int64_t n, float threshold, int topk, int64_t* nnz, void* workspace,
                            size_t workspace_bytes, void* stream);

@@ -235,8 +235,8 @@ def test_allreduce_wire_errors(v):
 
 def test_sparse_allreduce_errors(v):
     f = v.vcoll_sparse_allreduce
-    assert v.vcoll_sparse_workspace_bytes(8, 0) == 0
-    need = v.vcoll_sparse_workspace_bytes(8, 1)
+    assert v.vcoll_sparse_workspace_bytes(8, 64, 0) == 0
+    need = v.vcoll_sparse_workspace_bytes(8, 64, 1)
     assert need >= 8 * 2048 * 4
     ins, outs = FAKE_IN[:4], FAKE_OUT[:4]
     assert f(ins, outs, None, 0, 64, 0.5, 0) == v.ERR_INVALID_ARG
