@@ -264,8 +264,11 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, void* stream) {
         1, std::min<int64_t>(prm.tiles_per_rank, ceil_div((int64_t)sms * 4, W)));
     for (int pass = 0; pass < 3; ++pass) {
       void* args[] = {&prm};
-      e = cudaLaunchKernel(topk_hist_kernel(pass), dim3((unsigned)gx, (unsigned)W), dim3(256), args,
-                           0, st);
+      const void* hk = topk_hist_kernel(pass);
+      int hb = 0;  // also raises the kernel's dynamic shared memory limit once
+      if ((rc = resident_blocks(dev, hk, topk_hist_threads(), topk_hist_smem(), &hb))) return rc;
+      e = cudaLaunchKernel(hk, dim3((unsigned)gx, (unsigned)W), dim3(topk_hist_threads()), args,
+                           topk_hist_smem(), st);
       if (e != cudaSuccess) return cuda_fail(e, "top-K histogram launch");
       e = cudaLaunchKernel(topk_select_kernel(pass), dim3((unsigned)W), dim3(1024), args, 0, st);
       if (e != cudaSuccess) return cuda_fail(e, "top-K select launch");

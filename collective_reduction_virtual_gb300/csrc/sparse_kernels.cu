@@ -84,13 +84,19 @@ __device__ __forceinline__ void hist_add(uint32_t* h, bool valid, uint32_t d) {
 }  // namespace
 
 // ---------------------------------------------------------------- histogram
-// grid.y = rank; each CTA counts the digits of its tiles of that rank.
+// grid.y = rank; each CTA counts the digits of its tiles of that rank.  Every
+// warp has its own shared-memory histogram (float exponents put most keys in
+// a few dozen bins of the first digit: one shared histogram per CTA makes the
+// warps queue on the same counters); lanes that share a bin are combined with
+// one atomic.  The warp histograms are summed into the rank's global one.
+constexpr int kHistWarps = 8;
 template <int P>
-__global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ SparseParams p) {
-  __shared__ uint32_t h[kTopkBins];
+__global__ void __launch_bounds__(kHistWarps * 32) vc_topk_hist(const __grid_constant__ SparseParams p) {
+  extern __shared__ uint32_t hsm[];  // kHistWarps x kTopkBins
   const int r = blockIdx.y;
   const int tid = threadIdx.x;
-  for (int i = tid; i < kTopkBins; i += blockDim.x) h[i] = 0;
+  uint32_t* h = hsm + (tid >> 5) * kTopkBins;
+  for (int i = tid; i < kHistWarps * kTopkBins; i += blockDim.x) hsm[i] = 0;
   const uint32_t prefix = p.state[r].prefix;
   __syncthreads();
   for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x) {
@@ -133,8 +139,12 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
     }
   }
   __syncthreads();
-  for (int i = tid; i < kTopkBins; i += blockDim.x)
-    if (h[i]) atomicAdd(&p.hist[(int64_t)r * kTopkBins + i], h[i]);
+  for (int i = tid; i < kTopkBins; i += blockDim.x) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int w = 0; w < kHistWarps; ++w) c += hsm[w * kTopkBins + i];
+    if (c) atomicAdd(&p.hist[(int64_t)r * kTopkBins + i], c);
+  }
 }
 
 // ---------------------------------------------------------------- selection
@@ -207,19 +217,40 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
 // per rank scans the tile counts to the tile holding the need-th equal entry
 // and then that tile in index order; the entry's index is the boundary.
 __global__ void __launch_bounds__(256) vc_topk_tie_count(const __grid_constant__ SparseParams p) {
+  __shared__ int wc[8];
   const int r = blockIdx.y;
   const TopkState* st = p.state + r;
   if (p.K == 0 || st->need >= st->equal) return;  // uniform per CTA
   const uint32_t T = st->T;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x) {
     const int64_t t0 = tile * p.tile_elems;
     const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
     int c = 0;
-    for (int64_t base = t0; base < t1; base += blockDim.x) {
-      const int64_t i = base + threadIdx.x;
-      c += __syncthreads_count(i < t1 && order_key(load_x(p, r, i)) == T);
+    if (p.phase >= 0) {
+      int64_t av, bv;
+      aligned_body<4>(t0, t1, p.phase, av, bv);
+      const int64_t nv = (bv - av) / 4;
+      for (int64_t v = tid; v < nv; v += blockDim.x) {
+        float x[4];
+        load_x4(p, r, av + v * 4, x);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) c += order_key(x[q]) == T;
+      }
+      if (tid < av - t0) c += order_key(load_x(p, r, t0 + tid)) == T;
+      if (tid >= 32 && tid - 32 < t1 - bv) c += order_key(load_x(p, r, bv + (tid - 32))) == T;
+    } else {
+      for (int64_t i = t0 + tid; i < t1; i += blockDim.x) c += order_key(load_x(p, r, i)) == T;
     }
-    if (threadIdx.x == 0) p.tilecnt[(int64_t)r * p.tiles_per_rank + tile] = (uint32_t)c;
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+    if (lane == 0) wc[warp] = c;
+    __syncthreads();
+    if (tid == 0) {
+      int sum = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) sum += wc[w];
+      p.tilecnt[(int64_t)r * p.tiles_per_rank + tile] = (uint32_t)sum;
+    }
+    __syncthreads();
   }
 }
 
@@ -400,6 +431,8 @@ __global__ void __launch_bounds__(256) vc_sparse_apply(const __grid_constant__ S
 const void* sparse_apply_kernel(int topk) {
   return topk ? (const void*)&vc_sparse_apply<1> : (const void*)&vc_sparse_apply<0>;
 }
+int topk_hist_threads() { return kHistWarps * 32; }
+size_t topk_hist_smem() { return (size_t)kHistWarps * kTopkBins * sizeof(uint32_t); }
 const void* topk_hist_kernel(int pass) {
   return pass == 0 ? (const void*)&vc_topk_hist<0>
                    : pass == 1 ? (const void*)&vc_topk_hist<1> : (const void*)&vc_topk_hist<2>;

@@ -163,6 +163,8 @@ const void* gather_tma_kernel(int elem_size);
 const void* wire_kernel(int wire, int W_t, int ring);
 const void* sparse_apply_kernel(int topk);
 const void* topk_hist_kernel(int pass);
+int topk_hist_threads();
+size_t topk_hist_smem();
 const void* topk_select_kernel(int pass);
 const void* topk_tie_count_kernel();
 const void* topk_tie_find_kernel();
