@@ -262,18 +262,21 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     const int64_t gx = std::max<int64_t>(
         1, std::min<int64_t>(prm.tiles_per_rank, ceil_div((int64_t)sms * 4, W)));
-    for (int pass = 0; pass < 3; ++pass) {
-      void* args[] = {&prm};
-      const void* hk = topk_hist_kernel(pass);
-      int hb = 0;  // also raises the kernel's dynamic shared memory limit once
-      if ((rc = resident_blocks(dev, hk, topk_hist_threads(), topk_hist_smem(), &hb))) return rc;
-      e = cudaLaunchKernel(hk, dim3((unsigned)gx, (unsigned)W), dim3(topk_hist_threads()), args,
-                           topk_hist_smem(), st);
+    void* args[] = {&prm};
+    const dim3 hgrid((unsigned)gx, (unsigned)W), sgrid((unsigned)W);
+    // sample pass, lower bound, first digit (redone over all bins where the
+    // bound failed), second and third digits
+    const void* seq[][2] = {{topk_sample_kernel(), topk_select_low_kernel()},
+                            {topk_hist_kernel(0), topk_select_kernel(0)},
+                            {topk_redo_hist_kernel(), topk_redo_select_kernel()},
+                            {topk_hist_kernel(1), topk_select_kernel(1)},
+                            {topk_hist_kernel(2), topk_select_kernel(2)}};
+    for (auto& pair : seq) {
+      e = cudaLaunchKernel(pair[0], hgrid, dim3(256), args, 0, st);
       if (e != cudaSuccess) return cuda_fail(e, "top-K histogram launch");
-      e = cudaLaunchKernel(topk_select_kernel(pass), dim3((unsigned)W), dim3(1024), args, 0, st);
+      e = cudaLaunchKernel(pair[1], sgrid, dim3(1024), args, 0, st);
       if (e != cudaSuccess) return cuda_fail(e, "top-K select launch");
     }
-    void* args[] = {&prm};
     e = cudaLaunchKernel(topk_tie_count_kernel(), dim3((unsigned)gx, (unsigned)W), dim3(256), args,
                          0, st);
     if (e != cudaSuccess) return cuda_fail(e, "top-K tie count launch");

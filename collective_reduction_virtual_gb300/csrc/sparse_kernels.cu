@@ -84,22 +84,31 @@ __device__ __forceinline__ void hist_add(uint32_t* h, bool valid, uint32_t d) {
 }  // namespace
 
 // ---------------------------------------------------------------- histogram
-// grid.y = rank; each CTA counts the digits of its tiles of that rank.  Every
-// warp has its own shared-memory histogram (float exponents put most keys in
-// a few dozen bins of the first digit: one shared histogram per CTA makes the
-// warps queue on the same counters); lanes that share a bin are combined with
-// one atomic.  The warp histograms are summed into the rank's global one.
-constexpr int kHistWarps = 8;
-template <int P>
-__global__ void __launch_bounds__(kHistWarps * 32) vc_topk_hist(const __grid_constant__ SparseParams p) {
-  extern __shared__ uint32_t hsm[];  // kHistWarps x kTopkBins
+// grid.y = rank; each CTA counts the digits of its tiles of that rank into a
+// shared histogram (lanes sharing a bin combined into one atomic), then adds
+// it to the rank's global histogram.
+//
+// MODE 0: the first digit, bins >= state.low only (a lower bound from the
+//         sample pass: keys below it cannot be among the K largest when the
+//         counted bins hold at least K keys -- checked by the selection);
+// MODE 1, 2: the second and third digits, keys matching the prefix so far;
+// MODE 3: the first digit over a 1/16 sample (every 16th tile);
+// MODE 4: the first digit over all bins, only for ranks whose bound failed.
+template <int MODE>
+__global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ SparseParams p) {
+  constexpr int P = (MODE == 1 || MODE == 2) ? MODE : 0;
+  __shared__ uint32_t h[kTopkBins];
   const int r = blockIdx.y;
   const int tid = threadIdx.x;
-  uint32_t* h = hsm + (tid >> 5) * kTopkBins;
-  for (int i = tid; i < kHistWarps * kTopkBins; i += blockDim.x) hsm[i] = 0;
-  const uint32_t prefix = p.state[r].prefix;
+  const TopkState& st = p.state[r];
+  if (MODE == 4 && !st.redo) return;  // uniform per CTA
+  for (int i = tid; i < kTopkBins; i += blockDim.x) h[i] = 0;
+  const uint32_t prefix = st.prefix;
+  const uint32_t low = MODE == 0 ? st.low : 0u;
   __syncthreads();
-  for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x) {
+  const int64_t step = MODE == 3 ? 16 : 1;
+  for (int64_t tile = (int64_t)blockIdx.x * step; tile < p.tiles_per_rank;
+       tile += (int64_t)gridDim.x * step) {
     const int64_t t0 = tile * p.tile_elems;
     const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
     if (p.phase >= 0) {
@@ -116,7 +125,7 @@ __global__ void __launch_bounds__(kHistWarps * 32) vc_topk_hist(const __grid_con
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t d;
-          const bool m = digit_of<P>(order_key(x[q]), prefix, d) && in_range;
+          const bool m = digit_of<P>(order_key(x[q]), prefix, d) && d >= low && in_range;
           hist_add(h, m, d);
         }
       }
@@ -126,32 +135,35 @@ __global__ void __launch_bounds__(kHistWarps * 32) vc_topk_hist(const __grid_con
       if (tid >= 32 && tid - 32 < t1 - bv) i = bv + (tid - 32);
       if (i >= 0) {
         uint32_t d;
-        if (digit_of<P>(order_key(load_x(p, r, i)), prefix, d)) atomicAdd(&h[d], 1u);
+        if (digit_of<P>(order_key(load_x(p, r, i)), prefix, d) && d >= low) atomicAdd(&h[d], 1u);
       }
     } else {
       for (int64_t base = t0; base < t1; base += blockDim.x) {
         const int64_t i = base + tid;
         uint32_t d = 0;
         bool m = false;
-        if (i < t1) m = digit_of<P>(order_key(load_x(p, r, i)), prefix, d);
+        if (i < t1) m = digit_of<P>(order_key(load_x(p, r, i)), prefix, d) && d >= low;
         hist_add(h, m, d);
       }
     }
   }
   __syncthreads();
-  for (int i = tid; i < kTopkBins; i += blockDim.x) {
-    uint32_t c = 0;
-#pragma unroll
-    for (int w = 0; w < kHistWarps; ++w) c += hsm[w * kTopkBins + i];
-    if (c) atomicAdd(&p.hist[(int64_t)r * kTopkBins + i], c);
-  }
+  for (int i = tid; i < kTopkBins; i += blockDim.x)
+    if (h[i]) atomicAdd(&p.hist[(int64_t)r * kTopkBins + i], h[i]);
 }
 
 // ---------------------------------------------------------------- selection
 // One CTA of 1024 threads per rank: thread t owns bins 2047-2t and 2046-2t;
 // an inclusive scan from the top bin down finds the digit holding the
 // remaining-th largest key; the rank's histogram is cleared for the next pass.
-template <int P>
+//
+// MODE 0, 1, 2: after the histogram pass of that digit (MODE 0 flags a redo
+//   when the bins counted from state.low up hold fewer than K keys);
+// MODE 3: after the sample pass: state.low = the highest bin whose sampled
+//   suffix holds twice the keys K calls for (scaled to the sample) plus a
+//   margin, or 0 (count everything) when K is a large fraction of n;
+// MODE 4: after the redo pass, for ranks that needed it.
+template <int MODE>
 __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ SparseParams p) {
   const int r = blockIdx.x;
   const int t = threadIdx.x;
@@ -159,6 +171,7 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
   __shared__ unsigned long long warp_sum[32];
   uint32_t* hist = p.hist + (int64_t)r * kTopkBins;
   TopkState* st = p.state + r;
+  if (MODE == 4 && !st->redo) return;
   const int b0 = kTopkBins - 1 - 2 * t, b1 = b0 - 1;
   const unsigned long long c0 = hist[b0], c1 = hist[b1];
   unsigned long long s = c0 + c1;
@@ -180,10 +193,26 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
   __syncthreads();
   const unsigned long long incl = s + (warp > 0 ? warp_sum[warp - 1] : 0ull);
   const unsigned long long above = incl - c0 - c1;  // keys in bins > b0
-  const long long rem = P == 0 ? p.K : st->remaining;
+  const unsigned long long total = warp_sum[31];
+  constexpr int P = (MODE == 1 || MODE == 2) ? MODE : 0;
+  long long rem;
+  if (MODE == 3) {
+    // sampled keys wanted above the bound: twice K's share of the sample,
+    // plus a margin; no bound when K is a quarter of n or more
+    rem = 4 * p.K >= p.n ? -1 : 2 * ((p.K + 15) / 16) + 64;
+  } else {
+    rem = P == 0 ? p.K : st->remaining;
+  }
   const uint32_t prefix = P == 0 ? 0u : st->prefix;
   __syncthreads();  // every thread has read the state before it changes
-  if (rem > 0 && (long long)above < rem && rem <= (long long)incl) {
+  if (MODE == 3) {
+    if (t == 0 && (rem < 0 || (long long)total < rem)) st->low = 0;
+    if (rem >= 0 && (long long)total >= rem && (long long)above < rem && rem <= (long long)incl)
+      st->low = (uint32_t)((long long)(above + c0) >= rem ? b0 : b1);
+    if (t == 0) st->redo = 0;
+  } else if (MODE == 0 && (long long)total < rem) {
+    if (t == 0) st->redo = 1;  // the bound was too high: count every bin again
+  } else if (rem > 0 && (long long)above < rem && rem <= (long long)incl) {
     int bin;
     unsigned long long more;  // keys strictly above the chosen bin
     if ((long long)(above + c0) >= rem) {
@@ -197,6 +226,7 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
     if (P == 0) {
       st->prefix = (uint32_t)bin;
       st->remaining = left;
+      st->redo = 0;
     } else if (P == 1) {
       st->prefix = (prefix << 11) | (uint32_t)bin;
       st->remaining = left;
@@ -431,8 +461,10 @@ __global__ void __launch_bounds__(256) vc_sparse_apply(const __grid_constant__ S
 const void* sparse_apply_kernel(int topk) {
   return topk ? (const void*)&vc_sparse_apply<1> : (const void*)&vc_sparse_apply<0>;
 }
-int topk_hist_threads() { return kHistWarps * 32; }
-size_t topk_hist_smem() { return (size_t)kHistWarps * kTopkBins * sizeof(uint32_t); }
+const void* topk_sample_kernel() { return (const void*)&vc_topk_hist<3>; }
+const void* topk_select_low_kernel() { return (const void*)&vc_topk_select<3>; }
+const void* topk_redo_hist_kernel() { return (const void*)&vc_topk_hist<4>; }
+const void* topk_redo_select_kernel() { return (const void*)&vc_topk_select<4>; }
 const void* topk_hist_kernel(int pass) {
   return pass == 0 ? (const void*)&vc_topk_hist<0>
                    : pass == 1 ? (const void*)&vc_topk_hist<1> : (const void*)&vc_topk_hist<2>;

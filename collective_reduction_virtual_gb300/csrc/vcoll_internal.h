@@ -125,6 +125,8 @@ struct TopkState {
   int64_t need;       // entries equal to T that are kept
   int64_t equal;      // entries equal to T
   int64_t boundary;   // equal entries with index <= boundary are kept
+  uint32_t low;       // first-digit bins below this one are not counted
+  int redo;           // the first-digit pass must be repeated over all bins
 };
 struct SparseParams {
   const void* in[VCOLL_MAX_RANKS];
@@ -163,8 +165,10 @@ const void* gather_tma_kernel(int elem_size);
 const void* wire_kernel(int wire, int W_t, int ring);
 const void* sparse_apply_kernel(int topk);
 const void* topk_hist_kernel(int pass);
-int topk_hist_threads();
-size_t topk_hist_smem();
+const void* topk_sample_kernel();
+const void* topk_select_low_kernel();
+const void* topk_redo_hist_kernel();
+const void* topk_redo_select_kernel();
 const void* topk_select_kernel(int pass);
 const void* topk_tie_count_kernel();
 const void* topk_tie_find_kernel();

@@ -693,3 +693,16 @@ def test_sparse_topk_larger(v):
     acc = [torch.zeros(n, device="cuda") for _ in range(W)]
     _check_sparse(v, ins, acc, 0.01, True)
     _check_sparse(v, ins, acc, 0.01, True)  # second step: the error feedback is nonzero now
+
+
+def test_sparse_topk_sample_bound_redo(v):
+    # the sample pass reads every 16th tile of 4096 entries; large values only
+    # in those tiles make its lower bound far too high for the whole array,
+    # so the first-digit pass must be redone over all bins on the device
+    W, n = 2, 64 * 4096
+    ins = _sparse_inputs(W, n, 5)
+    for t in ins:
+        tiles = t.view(-1, 4096)
+        tiles[::16] = tiles[::16].abs() + 100.0
+    _check_sparse(v, ins, None, 0.01, True)
+    _check_sparse(v, ins, [torch.zeros(n, device="cuda") for _ in range(W)], 0.2, True)
