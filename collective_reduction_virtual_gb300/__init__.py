@@ -71,6 +71,9 @@ def lib() -> ctypes.CDLL:
             L.vcoll_sparse_allreduce.argtypes = [PP, PP, PP, I, I64, ctypes.c_float, I, P, P,
                                                  ctypes.c_size_t, P]
             L.vcoll_sparse_allreduce.restype = I
+            L.vcoll_sparse_allreduce_noalloc.argtypes = [PP, PP, PP, I, I64, ctypes.c_float, I, P,
+                                                         P]
+            L.vcoll_sparse_allreduce_noalloc.restype = I
             L.vcoll_allreduce_wire.argtypes = [PP, PP, I, I64, I, I, U, P]
             L.vcoll_allreduce_wire.restype = I
             L.vcoll_allgatherv.argtypes = [PP, I64P, PP, I, I, P]
@@ -160,6 +163,19 @@ def vcoll_sparse_allreduce(in_ptrs, out_ptrs, acc_ptrs, W, n, threshold, topk, n
                                         _ptr_array(acc_ptrs) if acc_ptrs else None, W, n,
                                         float(threshold), 1 if topk else 0, nnz_ptr or None,
                                         workspace or None, workspace_bytes, stream or None)
+
+
+def vcoll_sparse_allreduce_noalloc(in_ptrs, out_ptrs, acc_ptrs, W, n, threshold, topk, nnz_ptr=0,
+                                   stream=0) -> int:
+    """The sparsified allreduce with its top-K working memory in a fixed array
+    inside the library (for callers that must not allocate device memory)."""
+    return lib().vcoll_sparse_allreduce_noalloc(_ptr_array(in_ptrs), _ptr_array(out_ptrs),
+                                                _ptr_array(acc_ptrs) if acc_ptrs else None, W, n,
+                                                float(threshold), 1 if topk else 0,
+                                                nnz_ptr or None, stream or None)
+
+
+SPARSE_NOALLOC_BYTES = 1 << 20  # the fixed working memory of the no-allocation entry point
 
 
 def vcoll_allgatherv(in_ptrs, counts, out_ptrs, W, dtype, stream=0) -> int:

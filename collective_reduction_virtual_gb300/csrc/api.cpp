@@ -911,6 +911,16 @@ const char* vcoll_status_string(int status) {
 
 const char* vcoll_last_error(void) { return g_err; }
 
+}  // extern "C"
+
+namespace vcoll {
+// lets entry points defined in other translation units report a failure
+// through vcoll_last_error()
+int report_error(int status, const char* message) { return fail(status, "%s", message); }
+}  // namespace vcoll
+
+extern "C" {
+
 int vcoll_version(void) { return 100; }
 
 }  // extern "C"

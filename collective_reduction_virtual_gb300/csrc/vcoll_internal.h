@@ -153,6 +153,9 @@ inline size_t topk_workspace_bytes(int W, int64_t n) {
          (size_t)W * (size_t)(tiles > 0 ? tiles : 1) * sizeof(uint32_t) + 256;
 }
 
+// Sets the thread-local message vcoll_last_error() returns; returns status.
+int report_error(int status, const char* message);
+
 // Kernel selection (function pointers for cudaLaunchKernel).  W_t is the
 // compile-time rank count (2, 4, 8, 16) or 0 for the runtime-W kernels; vec
 // selects the 16-byte vector path.

@@ -236,6 +236,31 @@ int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const*
                            int64_t n, float threshold, int topk, int64_t* nnz, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/*
+ * vcoll_sparse_allreduce without a caller workspace, for code that may not
+ * allocate device memory (a framework that owns the whole device through its
+ * own pool, a callback that must not block on cudaMalloc, a loop that must
+ * have every resource in place before it starts).  The top-K working memory
+ * is a fixed array inside the library, 1 MiB (VCOLL_SPARSE_NOALLOC_BYTES) on
+ * every GPU that loads it, held until the process exits;
+ * the call allocates nothing.  Arguments and results are those of
+ * vcoll_sparse_allreduce; sizes whose working memory would not fit
+ * (vcoll_sparse_workspace_bytes(W, n, 1) > the maximum, about n <= 120 Mi
+ * elements at W = 8) return VCOLL_ERR_INVALID_ARG with an explanation.  The
+ * threshold mode needs no working memory and passes straight through.
+ * The first top-K call on a device looks up the array's device address with
+ * cudaGetSymbolAddress; make that first call before capturing a stream.
+ * All calls share the one array and it keeps the last call's contents (the
+ * call clears what must start at zero), so calls that may run at the same
+ * time on the GPU -- on different streams, or from different threads --
+ * race on it: order them on one stream.
+ * The pages have no counterpart of this entry point.
+ */
+#define VCOLL_SPARSE_NOALLOC_BYTES (1u << 20)
+int vcoll_sparse_allreduce_noalloc(const void* const* in, void* const* out, void* const* accum,
+                                   int W, int64_t n, float threshold, int topk, int64_t* nnz,
+                                   void* stream);
+
 /* Device-side error bits, OR-ed into one word per device by the kernels.
  * The staged kernels bound every wait on their shared-memory barriers; a wait
  * that gives up records VCOLL_DEVICE_ERR_TIMEOUT and the kernel returns early
