@@ -305,6 +305,27 @@ def build_workload(args, dev, rank):
     make = {"uniform": I.uniform, "gradient": I.gradient, "outliers": I.outliers}[kind]
     wl = {"gradient": I.AR_W8_F32, "outliers": I.AR_W8_BF16, "uniform": I.SWEEP}[kind]
     ins = [make(n, I.rank_seed(wl, u) + seed_off, dev) for u in range(W)]
+    if args.op in ("wire", "sparse", "sparse_topk"):
+        outs = [torch.empty_like(t) for t in ins]
+        if args.op == "wire":
+            step = lambda: vc.allreduce_wire(ins, outs, wire="f16", op=red,  # noqa
+                                             ring_order=ring)
+            bytes_ = 2 * W * n * 4
+            what = "fp16-wire allreduce"
+        else:
+            topk = args.op == "sparse_topk"
+            acc = [torch.zeros_like(t) for t in ins]
+            nnz = torch.empty(W, dtype=torch.int64, device=dev)
+            ws = torch.empty(max(1, vc.sparse_workspace_bytes(W, n, topk)), dtype=torch.uint8,
+                             device=dev)
+            frac = args.sparsity if topk else 1e-3
+            step = lambda: vc.sparse_allreduce(ins, outs, acc, frac, topk, nnz, ws)  # noqa
+            bytes_ = 4 * W * n * 4
+            what = (f"sparsified allreduce, top-{frac:g} of each rank" if topk else
+                    f"sparsified allreduce, threshold {frac:g}") + ", with error feedback"
+        return dict(name=f"{what}, W={W}, f32, n={n} per rank", W=W, n=n, step=step,
+                    bytes=bytes_, launches=1 if args.op != "sparse_topk" else 13, ins=ins,
+                    outs=outs, es=4, reduction=red, dtype="f32")
     if args.op == "allreduce":
         outs = [torch.empty_like(t) for t in ins]
         step = lambda: vc.allreduce(ins, outs, op=red, ring_order=ring, flags=vflags)  # noqa
@@ -628,8 +649,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["vcoll", "reference"], default="vcoll")
     ap.add_argument("--n", type=int, default=None, help="elements per rank (default 2^26)")
-    ap.add_argument("--op", choices=["allreduce", "reduce_scatter", "allgather", "fusion", "multi"],
-                    default="allreduce")
+    ap.add_argument("--op", choices=["allreduce", "reduce_scatter", "allgather", "fusion", "multi",
+                                     "wire", "sparse", "sparse_topk"], default="allreduce")
+    ap.add_argument("--sparsity", type=float, default=0.01, help="top-K fraction")
     ap.add_argument("--W", type=int, default=None, help="virtual ranks (default 8)")
     ap.add_argument("--tensors", type=int, default=200, help="tensors per rank for fusion/multi")
     ap.add_argument("--dtype", choices=["f32", "bf16"], default="f32")

@@ -90,6 +90,8 @@ def lib() -> ctypes.CDLL:
             L.vcoll_last_error.restype = ctypes.c_char_p
             L.vcoll_version.argtypes = []
             L.vcoll_version.restype = I
+            L.vcoll_selftest_wait_timeout.argtypes = [U, P]
+            L.vcoll_selftest_wait_timeout.restype = I
             L.vcoll_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
             L.vcoll_device_errors.restype = I
             _lib = L
@@ -128,6 +130,10 @@ def vcoll_device_errors(clear: bool = False):
     f = ctypes.c_uint()
     rc = lib().vcoll_device_errors(ctypes.byref(f), 1 if clear else 0)
     return rc, f.value
+
+
+def vcoll_selftest_wait_timeout(limit_us: int, stream=0) -> int:
+    return lib().vcoll_selftest_wait_timeout(int(limit_us), stream or None)
 
 
 def device_errors(clear: bool = False) -> int:

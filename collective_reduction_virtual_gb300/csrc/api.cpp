@@ -866,6 +866,18 @@ int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const*
   return sparse_launch(prm, topk, workspace, stream);
 }
 
+int vcoll_selftest_wait_timeout(unsigned limit_us, void* stream) {
+  g_err[0] = 0;
+  if (limit_us == 0 || limit_us > 1000000)
+    return fail(VCOLL_ERR_INVALID_ARG, "limit_us = %u outside [1, 1000000]", limit_us);
+  uint64_t limit_ns = (uint64_t)limit_us * 1000ull;
+  void* args[] = {&limit_ns};
+  cudaError_t e = cudaLaunchKernel(selftest_timeout_kernel(), dim3(1), dim3(32), args, 0,
+                                   (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return VCOLL_OK;
+}
+
 int vcoll_device_errors(unsigned* flags, int clear) {
   g_err[0] = 0;
   if (!flags) return fail(VCOLL_ERR_INVALID_ARG, "flags is NULL");

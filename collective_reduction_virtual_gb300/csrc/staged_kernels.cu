@@ -11,10 +11,11 @@
 // release the stage on its "empty" barrier.  Up to kStagedStages * 32 KB of
 // input is in flight per SM without holding it in registers.
 //
-// Every wait is bounded: after kSpinLimit unsuccessful polls the waiting
-// thread records VCOLL_DEVICE_ERR_TIMEOUT in g_vcoll_device_error and the CTA
-// stops issuing work; the producer then waits, again bounded, for the copies
-// it has already issued before it returns.
+// Every wait is bounded: after kWaitLimitNs of wall-clock time (the GPU's
+// global timer) the waiting thread records VCOLL_DEVICE_ERR_TIMEOUT in
+// g_vcoll_device_error and the CTA stops issuing work; the producer then
+// waits, again bounded, for the copies it has already issued before it
+// returns.
 #include "device_common.cuh"
 #include "reduce_kernels.cuh"
 #include "vcoll_internal.h"
@@ -25,7 +26,7 @@ __device__ unsigned int g_vcoll_device_error = 0;
 
 namespace {
 
-constexpr unsigned kSpinLimit = 1u << 24;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -58,12 +59,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   return done != 0;
 }
 
-// Bounded wait for the phase with the given parity; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
-  for (unsigned i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  atomicOr(&g_vcoll_device_error, (unsigned)VCOLL_DEVICE_ERR_TIMEOUT);
-  return false;
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for the phase with the given parity; false on timeout (after
+// limit_ns of wall-clock time), with VCOLL_DEVICE_ERR_TIMEOUT recorded.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > limit_ns) {
+      atomicOr(&g_vcoll_device_error, (unsigned)VCOLL_DEVICE_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
 }
 
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, unsigned bytes,
@@ -326,6 +340,19 @@ __global__ void __launch_bounds__(kGatherTmaThreads, 1) vc_gather_tma(const __gr
   for (int64_t i = consumed; i < issued; ++i) mbar_wait(&full[i % S], (unsigned)((i / S) & 1));
   bulk_wait_all();
 }
+
+// Diagnostics: one thread waits on a barrier that nothing arrives at; the
+// wait must give up after limit_ns and record the timeout.
+__global__ void vc_selftest_wait_timeout(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(&bar, 0, limit_ns);
+  }
+}
+
+const void* selftest_timeout_kernel() { return (const void*)&vc_selftest_wait_timeout; }
 
 const void* gather_tma_kernel(int elem_size) {
   return elem_size == 4 ? (const void*)&vc_gather_tma<4> : (const void*)&vc_gather_tma<2>;

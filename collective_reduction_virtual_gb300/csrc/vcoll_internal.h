@@ -153,6 +153,8 @@ inline size_t topk_workspace_bytes(int W, int64_t n) {
          (size_t)W * (size_t)(tiles > 0 ? tiles : 1) * sizeof(uint32_t) + 256;
 }
 
+const void* selftest_timeout_kernel();
+
 // Sets the thread-local message vcoll_last_error() returns; returns status.
 int report_error(int status, const char* message);
 

@@ -262,14 +262,21 @@ int vcoll_sparse_allreduce_noalloc(const void* const* in, void* const* out, void
                                    void* stream);
 
 /* Device-side error bits, OR-ed into one word per device by the kernels.
- * The staged kernels bound every wait on their shared-memory barriers; a wait
- * that gives up records VCOLL_DEVICE_ERR_TIMEOUT and the kernel returns early
- * (its outputs are then incomplete). */
+ * The staged kernels bound every wait on their shared-memory barriers (2 s of
+ * wall-clock time); a wait that gives up records VCOLL_DEVICE_ERR_TIMEOUT and
+ * the kernel returns early (its outputs are then incomplete). */
 #define VCOLL_DEVICE_ERR_TIMEOUT 0x1u
 
 /* Reads the current device's error word into *flags (and resets it when
  * clear != 0).  Synchronous: waits for all work on the device to finish. */
 int vcoll_device_errors(unsigned* flags, int clear);
+
+/* Diagnostics for the bounded waits: launches one thread that waits on a
+ * shared-memory barrier nothing ever arrives at; the wait gives up after
+ * limit_us microseconds (1 .. 10^6) and records VCOLL_DEVICE_ERR_TIMEOUT in
+ * the device error word, and the kernel returns -- the device stays usable.
+ * Read the word with vcoll_device_errors.  Asynchronous on `stream`. */
+int vcoll_selftest_wait_timeout(unsigned limit_us, void* stream);
 
 /* Segment j of an n-element buffer over W ranks (host only). */
 int vcoll_segment(int64_t n, int W, int j, int64_t* off, int64_t* len);
