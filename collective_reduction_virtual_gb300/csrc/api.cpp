@@ -215,10 +215,16 @@ int64_t tiles_per_segment(int64_t n, int W, int nseg, int V, int phase, int64_t 
   return tps;
 }
 
-int launch(const void* fn, int64_t num_tiles, int threads, size_t smem, bool small, void* params,
-           void* stream) {
+// persistent: as many CTAs as fit on the GPU at once, each looping over
+// tiles (the pipelined kernels need it to keep their stages full); otherwise
+// one CTA per tile.  Measured on the W=8 fp32 allreduce: one CTA per tile
+// reaches 7.0 TB/s where the persistent grid-stride loop reaches 6.35 TB/s --
+// the hardware scheduler keeps the CTAs in flight on a compact window of
+// addresses, while persistent CTAs drift apart over the buffers.
+int launch(const void* fn, int64_t num_tiles, int threads, size_t smem, bool persistent,
+           void* params, void* stream) {
   int64_t grid = num_tiles;
-  if (!small) {
+  if (persistent) {
     int dev = 0, sms = 0, blocks = 0;
     int rc = current_device(&dev, &sms);
     if (rc) return rc;
@@ -284,8 +290,8 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "top-K tie find launch");
   }
   const void* fn = sparse_apply_kernel(topk);
-  if ((rc = resident_blocks(dev, fn, 256, 0, &blocks))) return rc;
-  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(prm.num_tiles, (int64_t)sms * blocks));
+  (void)blocks;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(prm.num_tiles, 0x7FFFFFFF));
   void* args[] = {&prm};
   cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(256), args, 0, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse apply launch");
@@ -352,7 +358,7 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
     prm.tiles_per_seg = vec ? tiles_per_segment(n, W, prm.nseg, 4, phase, prm.tile_elems)
                             : tiles_per_segment(n, W, prm.nseg, 1, 0, prm.tile_elems);
     prm.num_tiles = prm.tiles_per_seg * prm.nseg;
-    return launch(wire_kernel(wire, W_t, ring ? 1 : 0), prm.num_tiles, threads, 0, small, &prm,
+    return launch(wire_kernel(wire, W_t, ring ? 1 : 0), prm.num_tiles, threads, 0, false, &prm,
                   stream);
   }
 
@@ -397,9 +403,9 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   prm.tiles_per_seg = tiles_per_segment(n, W, nseg, V, phase, prm.tile_elems);
   prm.num_tiles = prm.tiles_per_seg * nseg;
   if (staged)
-    return launch(fn, prm.num_tiles, kStagedThreads, (size_t)staged_smem_bytes(W_t), false, &prm,
+    return launch(fn, prm.num_tiles, kStagedThreads, (size_t)staged_smem_bytes(W_t), true, &prm,
                   stream);
-  return launch(fn, prm.num_tiles, threads, 0, small, &prm, stream);
+  return launch(fn, prm.num_tiles, threads, 0, false, &prm, stream);
 }
 
 }  // namespace
@@ -498,9 +504,9 @@ static int gather_common(const void* const* in, void* const* out, int W, const i
     prm.tiles_per_seg = tps;
     prm.num_tiles = tps * W;
     return launch(gather_tma_kernel(es), prm.num_tiles, kGatherTmaThreads,
-                  (size_t)kGatherTmaStages * kGatherTmaTileBytes + 64, false, &prm, stream);
+                  (size_t)kGatherTmaStages * kGatherTmaTileBytes + 64, true, &prm, stream);
   }
-  return launch(gather_kernel(es, vec), prm.num_tiles, threads, 0, small, &prm, stream);
+  return launch(gather_kernel(es, vec), prm.num_tiles, threads, 0, false, &prm, stream);
 }
 
 int vcoll_allgather(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,
@@ -617,7 +623,7 @@ static int fuse_common(const void* const* tensors, const int64_t* counts, int T,
       for (int t = 0; t < nt; ++t) prm.tensor[t * W + u] = (void*)tensors[(int64_t)u * T + t0 + t];
     }
     if (tiles == 0) continue;
-    rc = launch(fuse_kernel(es), tiles, threads, 0, bytes <= kSmallBytes, &prm, stream);
+    rc = launch(fuse_kernel(es), tiles, threads, 0, false, &prm, stream);
     if (rc) return rc;
   }
   return VCOLL_OK;
@@ -771,7 +777,7 @@ static int multi_run(const void* const* in, void* const* out, const int64_t* cou
       }
     prm.npieces = np;
     prm.num_tiles = tiles;
-    if (np > 0 && (rc = launch(fn, tiles, threads, 0, bytes <= kSmallBytes, &prm, stream)))
+    if (np > 0 && (rc = launch(fn, tiles, threads, 0, false, &prm, stream)))
       return rc;
     t0 += nt;
   }
