@@ -486,10 +486,9 @@ static int gather_common(const void* const* in, void* const* out, int W, const i
   }
   prm.tiles_per_seg = tps;
   prm.num_tiles = tps * W;
-  // TMA variant when asked for, and by default for W >= 8 where the write
-  // stream dominates (measured: +1 % at W = 8, +4 % at W = 16; direct is
-  // faster at W <= 4)
-  const bool tma = !(flags & VCOLL_FLAG_DIRECT) && ((flags & VCOLL_FLAG_STAGED) || W >= 8);
+  // TMA variant only when asked for: with one CTA per tile the direct kernel
+  // is ahead at every W measured (2-16)
+  const bool tma = (flags & VCOLL_FLAG_STAGED) != 0;
   if (tma && vec && !small) {
     // TMA variant: bulk loads into shared memory, W bulk stores per tile
     prm.tile_elems = kGatherTmaTileBytes / es;
