@@ -110,10 +110,6 @@ struct Buf {
   bool out;
 };
 
-bool overlaps(const Buf& x, const Buf& y) {
-  return x.nbytes && y.nbytes && x.addr < y.addr + y.nbytes && y.addr < x.addr + x.nbytes;
-}
-
 // Outputs must not overlap each other; an input may overlap an output only
 // when both map every element index to the same address (then the thread
 // that owns the index reads it before writing it).  Returns VCOLL_OK or
@@ -607,14 +603,12 @@ static int fuse_common(const void* const* tensors, const int64_t* counts, int T,
     prm.unpack = unpack;
     prm.tile_elems = tile_elems;
     int64_t tiles = 0;
-    int64_t bytes = 0;
     for (int t = 0; t < nt; ++t) {
       prm.count[t] = counts[t0 + t];
       prm.offset[t] = offset;
       prm.tile_begin[t] = tiles;
-      tiles += ceil_div(counts[t0 + t], tile_elems);
+      tiles += (int64_t)W * ceil_div(counts[t0 + t], tile_elems);  // one tile per rank and chunk
       offset += counts[t0 + t];
-      bytes += counts[t0 + t] * es;
     }
     prm.tile_begin[nt] = tiles;
     for (int u = 0; u < W; ++u) {
@@ -738,7 +732,7 @@ static int multi_run(const void* const* in, void* const* out, const int64_t* cou
     prm.do_scale = op == VCOLL_AVG ? 1 : 0;
     prm.tile_elems = tile_elems;
     int nt = 0, np = 0;
-    int64_t tiles = 0, bytes = 0;
+    int64_t tiles = 0;
     // take tensors while both the pointer table and the piece table have room
     while (t0 + nt < T && nt < max_t) {
       const int tg = t0 + nt;
@@ -763,7 +757,6 @@ static int multi_run(const void* const* in, void* const* out, const int64_t* cou
         }
         pc.phase = same ? ph / es : -1;
         tiles += std::max<int64_t>(1, ceil_div(c.len, tile_elems));
-        bytes += c.len * es;
       }
       ++nt;
     }

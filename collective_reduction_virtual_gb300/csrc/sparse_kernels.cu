@@ -73,6 +73,15 @@ __device__ __forceinline__ bool digit_of(uint32_t key, uint32_t prefix, uint32_t
   return (key >> 10) == prefix;
 }
 
+// the first-digit pass only counts bins from state.low up
+template <int MODE>
+__device__ __forceinline__ bool counted_bin(uint32_t d, uint32_t low) {
+  if constexpr (MODE == 0)
+    return d >= low;
+  else
+    return true;
+}
+
 // shared-memory histogram add, lanes that share a bin combined first
 __device__ __forceinline__ void hist_add(uint32_t* h, bool valid, uint32_t d) {
   const unsigned active = __ballot_sync(0xFFFFFFFFu, valid);
@@ -125,7 +134,8 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t d;
-          const bool m = digit_of<P>(order_key(x[q]), prefix, d) && d >= low && in_range;
+          const bool m = digit_of<P>(order_key(x[q]), prefix, d) && counted_bin<MODE>(d, low) &&
+                         in_range;
           hist_add(h, m, d);
         }
       }
@@ -135,14 +145,15 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
       if (tid >= 32 && tid - 32 < t1 - bv) i = bv + (tid - 32);
       if (i >= 0) {
         uint32_t d;
-        if (digit_of<P>(order_key(load_x(p, r, i)), prefix, d) && d >= low) atomicAdd(&h[d], 1u);
+        if (digit_of<P>(order_key(load_x(p, r, i)), prefix, d) && counted_bin<MODE>(d, low))
+          atomicAdd(&h[d], 1u);
       }
     } else {
       for (int64_t base = t0; base < t1; base += blockDim.x) {
         const int64_t i = base + tid;
         uint32_t d = 0;
         bool m = false;
-        if (i < t1) m = digit_of<P>(order_key(load_x(p, r, i)), prefix, d) && d >= low;
+        if (i < t1) m = digit_of<P>(order_key(load_x(p, r, i)), prefix, d) && counted_bin<MODE>(d, low);
         hist_add(h, m, d);
       }
     }
