@@ -607,7 +607,7 @@ static int fuse_common(const void* const* tensors, const int64_t* counts, int T,
       prm.count[t] = counts[t0 + t];
       prm.offset[t] = offset;
       prm.tile_begin[t] = tiles;
-      tiles += (int64_t)W * ceil_div(counts[t0 + t], tile_elems);  // one tile per rank and chunk
+      tiles += ceil_div(counts[t0 + t], tile_elems);
       offset += counts[t0 + t];
     }
     prm.tile_begin[nt] = tiles;

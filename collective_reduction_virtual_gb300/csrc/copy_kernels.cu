@@ -181,21 +181,18 @@ __global__ void __launch_bounds__(256) vc_fuse(const __grid_constant__ FuseParam
       else
         hi = mid - 1;
     }
-    // tensor t has W x nk tiles: rank u's chunk k is tile u * nk + k, so
-    // neighbouring CTAs copy neighbouring chunks of the same buffers
     const int t = lo;
-    const int64_t nk = (p.count[t] + p.tile_elems - 1) / p.tile_elems;
-    const int64_t local = tile - s_begin[t];
-    const int u = (int)(local / nk);
-    const int64_t k = local - (int64_t)u * nk;
+    const int64_t k = tile - s_begin[t];
     const int64_t e0 = k * p.tile_elems;
     const int64_t e1 = e0 + p.tile_elems < p.count[t] ? e0 + p.tile_elems : p.count[t];
-    char* tens = (char*)p.tensor[t * p.W + u] + e0 * ES;
-    char* fus = (char*)p.fused[u] + (p.offset[t] + e0) * ES;
-    if (p.unpack)
-      copy_range<ES>(tens, fus, (e1 - e0) * ES);
-    else
-      copy_range<ES>(fus, tens, (e1 - e0) * ES);
+    for (int u = 0; u < p.W; ++u) {
+      char* tens = (char*)p.tensor[t * p.W + u] + e0 * ES;
+      char* fus = (char*)p.fused[u] + (p.offset[t] + e0) * ES;
+      if (p.unpack)
+        copy_range<ES>(tens, fus, (e1 - e0) * ES);
+      else
+        copy_range<ES>(fus, tens, (e1 - e0) * ES);
+    }
   }
 }
 

@@ -62,8 +62,8 @@ struct GatherParams {
 // Fusion pack / unpack.  One launch copies up to kFuseMaxTensors tensors of
 // every rank.  Copy (t, u) moves count[t] elements between tensor[t * W + u]
 // (tensor-major) and fused[u] + offset[t].  Work is tiled per tensor:
-// tile_begin[t] is the first tile of tensor t (tile_begin[T] = total); a
-// tensor has W x ceil(count / tile_elems) tiles, one per rank and chunk.
+// tile_begin[t] is the first tile of tensor t (tile_begin[T] = total), each
+// tile covers tile_elems elements of that tensor on all W ranks.
 constexpr int kFuseMaxTensors = 64;
 constexpr int kFuseMaxCopies = 1024;  // W * T per launch
 struct FuseParams {
