@@ -144,26 +144,16 @@ __device__ __forceinline__ void copy_range(char* dst, const char* src, int64_t n
       }
     }
   } else {
-    // each output vector i takes bytes from aligned source vectors i and i+1;
-    // lane l loads vector i and gets i+1 from lane l+1 by a shuffle (lane 31
-    // and the last vector load theirs)
     const char* as = vs - sh;  // aligned source base
-    const int lane = tid & 31;
     for (int64_t base = 0; base < nv; base += (int64_t)U * nthr) {
       uint4 lo[U], hi[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t i = base + (int64_t)u * nthr + tid;
-        lo[u] = i < nv ? ld_stream(as + i * 16) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t i = base + (int64_t)u * nthr + tid;
-        hi[u].x = __shfl_down_sync(0xFFFFFFFFu, lo[u].x, 1);
-        hi[u].y = __shfl_down_sync(0xFFFFFFFFu, lo[u].y, 1);
-        hi[u].z = __shfl_down_sync(0xFFFFFFFFu, lo[u].z, 1);
-        hi[u].w = __shfl_down_sync(0xFFFFFFFFu, lo[u].w, 1);
-        if (i < nv && (lane == 31 || i + 1 >= nv)) hi[u] = ld_stream(as + i * 16 + 16);
+        if (i < nv) {
+          lo[u] = ld_stream(as + i * 16);
+          hi[u] = ld_stream(as + i * 16 + 16);
+        }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
