@@ -606,6 +606,47 @@ def graph_rate(launch, nbytes, reps):
             "timing": f"CUDA graph of {reps} launches"}
 
 
+# ------------------------------------------------------------------ sweep
+
+def run_sweep(args):
+    """Message-size sweep: reduce-scatter and allreduce (sum, max) and
+    allgather, fp32 uniform[-1, 1], per-rank sizes 1 KiB .. 1 GiB (powers of
+    two), W in {2, 4, 8, 16}.  Each point is timed as a CUDA graph of
+    repeated launches (many for small sizes, a few for large ones); GB/s uses
+    the algorithmic bytes of each op.  Prints one JSON line per point."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    vc.lib()
+    sizes = [1 << k for k in range(10, 31)]
+    if args.sweep_max_bytes:
+        sizes = [b for b in sizes if b <= args.sweep_max_bytes]
+    for W in (2, 4, 8, 16):
+        for nbytes in sizes:
+            n = nbytes // 4
+            ins = [I.uniform(n, I.rank_seed(I.SWEEP, u), dev) for u in range(W)]
+            outs = [torch.empty_like(t) for t in ins]
+            segs = [torch.empty(vc.segment(n, W, j)[1], device=dev) for j in range(W)]
+            reps = int(max(3, min(1000, 2e9 // (2 * W * nbytes))))
+            row = {"W": W, "bytes_per_rank": nbytes, "reps": reps}
+            for name, fn, b in (
+                    ("rs_sum", lambda s: vc.reduce_scatter(ins, segs, op="sum", stream=s),
+                     (W + 1) * nbytes),
+                    ("rs_max", lambda s: vc.reduce_scatter(ins, segs, op="max", stream=s),
+                     (W + 1) * nbytes),
+                    ("ag", lambda s: vc.allgather(segs, n, outs, stream=s), (1 + W) * nbytes),
+                    ("ar_sum", lambda s: vc.allreduce(ins, outs, op="sum", stream=s),
+                     2 * W * nbytes),
+                    ("ar_max", lambda s: vc.allreduce(ins, outs, op="max", stream=s),
+                     2 * W * nbytes)):
+                r = graph_rate(fn, b, reps)
+                row[name + "_GBps"] = r["GBps"]
+                row[name + "_us"] = round(r["ms"] * 1e3, 2)
+            row["l2"] = "fits in L2 (warm)" if 2 * W * nbytes <= L2_BYTES else "exceeds L2"
+            print(json.dumps(row), flush=True)
+            del ins, outs, segs
+            torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -659,6 +700,9 @@ def main(argv=None):
     ap.add_argument("--order", choices=["fast", "ring"], default="fast")
     ap.add_argument("--variant", choices=["auto", "direct", "staged"], default="auto",
                     help="kernel variant of the timed step (identical bits)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="run the message-size sweep (one JSON line per point) instead")
+    ap.add_argument("--sweep-max-bytes", type=int, default=0)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -671,6 +715,8 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_vcoll(args)
 
