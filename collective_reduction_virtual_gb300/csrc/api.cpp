@@ -189,6 +189,25 @@ constexpr int64_t kSmallBytes = 32 * 1024;  // latency-bound path (MLX PR #3901:
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Tile size (elements) for a one-CTA-per-tile launch over nseg segments of
+// about n / nseg elements: the kernel's full tile (threads x unroll x V) for
+// large messages, smaller tiles -- down to one vector per thread -- while
+// that gives fewer than about four CTAs per SM, so that mid-size messages
+// spread over the GPU instead of a handful of CTAs.  The kernels bound every
+// tile by its own end, so any multiple of threads x V works.
+int64_t adaptive_tile(int64_t n, int nseg, int threads, int V, int unroll) {
+  const int64_t unit = (int64_t)threads * V;
+  const int64_t full = unit * unroll;
+  int dev = 0, sms = 0;
+  if (current_device(&dev, &sms) != VCOLL_OK || sms <= 0) {
+    g_err[0] = 0;  // not fatal here: the launch reports device errors
+    return full;
+  }
+  const int64_t want = std::max<int64_t>(1, ceil_div(4LL * sms, nseg));  // tiles per segment
+  const int64_t per = ceil_div(ceil_div(n, nseg), want);
+  return std::min(full, std::max(unit, ceil_div(per, unit) * unit));
+}
+
 // Tiles per segment: enough for the longest aligned body, at least one (tile
 // 0 also does the unaligned head and tail).
 int64_t tiles_per_segment(int64_t n, int W, int nseg, int V, int phase, int64_t tile_elems) {
@@ -350,7 +369,7 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
     prm.do_scale = op == VCOLL_AVG ? 1 : 0;
     const bool small = n * es <= kSmallBytes;
     const int threads = small ? 128 : 256;
-    prm.tile_elems = (int64_t)threads * (vec ? 2 * 4 : 4);
+    prm.tile_elems = vec ? adaptive_tile(n, prm.nseg, threads, 4, 2) : (int64_t)threads * 4;
     prm.tiles_per_seg = vec ? tiles_per_segment(n, W, prm.nseg, 4, phase, prm.tile_elems)
                             : tiles_per_segment(n, W, prm.nseg, 1, 0, prm.tile_elems);
     prm.num_tiles = prm.tiles_per_seg * prm.nseg;
@@ -395,7 +414,7 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   if (staged)
     prm.tile_elems = staged_slice_bytes(W_t) / es;
   else
-    prm.tile_elems = vec ? (int64_t)threads * unroll_for(W_t) * V : (int64_t)threads * 4;
+    prm.tile_elems = vec ? adaptive_tile(n, nseg, threads, V, unroll_for(W_t)) : (int64_t)threads * 4;
   prm.tiles_per_seg = tiles_per_segment(n, W, nseg, V, phase, prm.tile_elems);
   prm.num_tiles = prm.tiles_per_seg * nseg;
   if (staged)
@@ -471,7 +490,7 @@ static int gather_common(const void* const* in, void* const* out, int W, const i
   for (int u = 0; u <= W; ++u) prm.disp[u] = disp[u];
   prm.W = W;
   prm.phase = phase;
-  prm.tile_elems = (int64_t)threads * 4 * V;
+  prm.tile_elems = adaptive_tile(n, W, threads, V, 4);
   int64_t tps = 1;
   for (int j = 0; j < W; ++j) {
     const int64_t a = disp[j], b = disp[j + 1];
