@@ -192,8 +192,10 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Tile size (elements) for a one-CTA-per-tile launch over nseg segments of
 // about n / nseg elements: the kernel's full tile (threads x unroll x V) for
 // large messages, smaller tiles -- down to one vector per thread -- while
-// that gives fewer than about four CTAs per SM, so that mid-size messages
-// spread over the GPU instead of a handful of CTAs.  The kernels bound every
+// that gives fewer than about two CTAs per SM, so that mid-size messages
+// spread over the GPU instead of a handful of CTAs (measured on GB300: a
+// target of four per SM made 2-8 MiB messages slower, one per SM left
+// 64 KiB-1 MiB messages about 1 us slower).  The kernels bound every
 // tile by its own end, so any multiple of threads x V works.
 int64_t adaptive_tile(int64_t n, int nseg, int threads, int V, int unroll) {
   const int64_t unit = (int64_t)threads * V;
@@ -203,7 +205,7 @@ int64_t adaptive_tile(int64_t n, int nseg, int threads, int V, int unroll) {
     g_err[0] = 0;  // not fatal here: the launch reports device errors
     return full;
   }
-  const int64_t want = std::max<int64_t>(1, ceil_div(4LL * sms, nseg));  // tiles per segment
+  const int64_t want = std::max<int64_t>(1, ceil_div(2LL * sms, nseg));  // tiles per segment
   const int64_t per = ceil_div(ceil_div(n, nseg), want);
   return std::min(full, std::max(unit, ceil_div(per, unit) * unit));
 }
