@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
             L.vcoll_fuse_unpack.restype = I
             L.vcoll_sparse_workspace_bytes.argtypes = [I, I64, I]
             L.vcoll_sparse_workspace_bytes.restype = ctypes.c_size_t
+            L.vcoll_sparse_workspace_min_bytes.argtypes = [I, I64, I]
+            L.vcoll_sparse_workspace_min_bytes.restype = ctypes.c_size_t
             L.vcoll_sparse_allreduce.argtypes = [PP, PP, PP, I, I64, ctypes.c_float, I, P, P,
                                                  ctypes.c_size_t, P]
             L.vcoll_sparse_allreduce.restype = I
@@ -161,6 +163,10 @@ def vcoll_allreduce_wire(in_ptrs, out_ptrs, W, n, wire, op, flags=0, stream=0) -
 
 def vcoll_sparse_workspace_bytes(W, n, topk) -> int:
     return int(lib().vcoll_sparse_workspace_bytes(W, n, 1 if topk else 0))
+
+
+def vcoll_sparse_workspace_min_bytes(W, n, topk) -> int:
+    return int(lib().vcoll_sparse_workspace_min_bytes(W, n, 1 if topk else 0))
 
 
 def vcoll_sparse_allreduce(in_ptrs, out_ptrs, acc_ptrs, W, n, threshold, topk, nnz_ptr=0,
@@ -353,7 +359,8 @@ def sparse_allreduce(ins, outs=None, accum=None, threshold=0.0, topk=False, nnz=
     top-K with K = ceil(threshold * n)).  accum: W fp32 tensors updated in
     place (error feedback) or None.  nnz: int64 CUDA tensor of W survivor
     counts (optional).  workspace: a uint8 CUDA tensor of at least
-    sparse_workspace_bytes(W, n, topk) bytes; allocated here when omitted."""
+    sparse_workspace_min_bytes(W, n, topk) bytes; sparse_workspace_bytes
+    (allocated here when omitted) adds room for the faster candidate path."""
     torch = _torch()
     W, n = len(ins), ins[0].numel()
     _check_tensors(ins, "ins")
@@ -374,6 +381,10 @@ def sparse_allreduce(ins, outs=None, accum=None, threshold=0.0, topk=False, nnz=
 
 def sparse_workspace_bytes(W, n, topk=True) -> int:
     return vcoll_sparse_workspace_bytes(W, n, topk)
+
+
+def sparse_workspace_min_bytes(W, n, topk=True) -> int:
+    return vcoll_sparse_workspace_min_bytes(W, n, topk)
 
 
 def fuse_plan(counts, dtype=F32, threshold_bytes=DEFAULT_FUSION_THRESHOLD) -> list[int]:

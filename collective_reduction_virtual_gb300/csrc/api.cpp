@@ -268,46 +268,94 @@ int copy_d2d(void* dst, const void* src, int64_t bytes, void* stream) {
 }
 
 // Launch sequence of the sparsified allreduce (shared by the entry points
-// that differ only in where the top-K workspace lives).
-int sparse_launch(SparseParams& prm, int topk, void* workspace, void* stream) {
-  int dev = 0, sms = 0, blocks = 0;
+// that differ only in where the top-K workspace lives; workspace_bytes is at
+// least topk_workspace_min_bytes).
+int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  int dev = 0, sms = 0;
   int rc = current_device(&dev, &sms);
   if (rc) return rc;
   const int W = prm.W;
   cudaStream_t st = (cudaStream_t)stream;
   if (topk) {
-    prm.hist = (uint32_t*)workspace;
-    prm.state = (TopkState*)((char*)workspace + (size_t)W * kTopkBins * sizeof(uint32_t));
-    prm.tilecnt = (uint32_t*)((char*)prm.state + (size_t)W * sizeof(TopkState));
+    const TopkLayout L = topk_layout(W, prm.n);
+    char* ws = (char*)workspace;
+    prm.hist = (uint32_t*)ws;
+    prm.state = (TopkState*)(ws + L.state);
+    prm.cand_n = (unsigned long long*)(ws + L.cand_n);
+    prm.tilecnt = (uint32_t*)(ws + L.tilecnt);
+    // candidate lists in what is left (a multiple of 4 entries per rank keeps
+    // the index list 16-byte aligned)
+    const size_t spare = workspace_bytes > L.cands ? workspace_bytes - L.cands : 0;
+    int64_t cap = (int64_t)(spare / ((size_t)W * 8));
+    cap = std::min<int64_t>(cap, topk_cand_cap_default(prm.n)) & ~(int64_t)3;
+    prm.cand_cap = cap;
+    prm.cand_key = (uint32_t*)(ws + L.cands);
+    prm.cand_idx = prm.cand_key + (size_t)W * (size_t)cap;
+    // worth it when the list can hold the 2K-4K entries a sample bound
+    // typically admits; the sample sets no bound when K >= n / 4
+    prm.use_cand = prm.K > 0 && 4 * prm.K < prm.n && cap >= 3 * prm.K;
   }
   if (topk && prm.K > 0) {
-    cudaError_t e = cudaMemsetAsync(prm.hist, 0, (size_t)W * kTopkBins * sizeof(uint32_t), st);
+    // histograms, states and candidate counts start at zero
+    cudaError_t e = cudaMemsetAsync(workspace, 0, topk_layout(W, prm.n).tilecnt, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    // data passes: one CTA per tile (per sampled tile for the sample); passes
+    // that usually find nothing to do for their rank (the whole-array ones
+    // beside the candidate path) and the candidate passes: a few CTAs per SM
     const int64_t gx = std::max<int64_t>(
         1, std::min<int64_t>(prm.tiles_per_rank, ceil_div((int64_t)sms * 4, W)));
+    const unsigned tiles = (unsigned)std::min<int64_t>(prm.tiles_per_rank, 0x7FFFFFFF);
     void* args[] = {&prm};
-    const dim3 hgrid((unsigned)gx, (unsigned)W), sgrid((unsigned)W);
-    // sample pass, lower bound, first digit (redone over all bins where the
-    // bound failed), second and third digits
-    const void* seq[][2] = {{topk_sample_kernel(), topk_select_low_kernel()},
-                            {topk_hist_kernel(0), topk_select_kernel(0)},
-                            {topk_redo_hist_kernel(), topk_redo_select_kernel()},
-                            {topk_hist_kernel(1), topk_select_kernel(1)},
-                            {topk_hist_kernel(2), topk_select_kernel(2)}};
-    for (auto& pair : seq) {
-      e = cudaLaunchKernel(pair[0], hgrid, dim3(256), args, 0, st);
-      if (e != cudaSuccess) return cuda_fail(e, "top-K histogram launch");
-      e = cudaLaunchKernel(pair[1], sgrid, dim3(1024), args, 0, st);
-      if (e != cudaSuccess) return cuda_fail(e, "top-K select launch");
+    const dim3 few((unsigned)gx, (unsigned)W), sgrid((unsigned)W);
+    // the sample: every 16th tile, up to every 64th for large arrays (at least
+    // 256 tiles, a million entries, per rank)
+    prm.sample_stride = (int)std::min<int64_t>(64, std::max<int64_t>(16, prm.tiles_per_rank / 256));
+    const dim3 every(tiles, (unsigned)W),
+        sample((unsigned)ceil_div(tiles, prm.sample_stride), (unsigned)W);
+    const dim3 full_grid = prm.use_cand ? few : every;
+    auto run = [&](const void* k, dim3 grid, unsigned threads) -> int {
+      cudaError_t e2 = cudaLaunchKernel(k, grid, dim3(threads), args, 0, st);
+      return e2 == cudaSuccess ? VCOLL_OK : cuda_fail(e2, "top-K select launch");
+    };
+    // sample pass and lower bound
+    if ((rc = run(topk_sample_kernel(), sample, 256)) || (rc = run(topk_select_low_kernel(), sgrid, 1024)))
+      return rc;
+    if (prm.use_cand) {
+      // one pass collects the candidates, the first digit from the lists
+      if ((rc = run(topk_filter_kernel(), every, 256)) ||
+          (rc = run(topk_cand_hist_kernel(0), few, 256)) ||
+          (rc = run(topk_select_kernel(0), sgrid, 1024)))
+        return rc;
+    } else {
+      // the first digit from the bound up
+      if ((rc = run(topk_hist_kernel(0), every, 256)) ||
+          (rc = run(topk_select_kernel(0), sgrid, 1024)))
+        return rc;
     }
-    e = cudaLaunchKernel(topk_tie_count_kernel(), dim3((unsigned)gx, (unsigned)W), dim3(256), args,
-                         0, st);
-    if (e != cudaSuccess) return cuda_fail(e, "top-K tie count launch");
-    e = cudaLaunchKernel(topk_tie_find_kernel(), dim3((unsigned)W), dim3(1024), args, 0, st);
-    if (e != cudaSuccess) return cuda_fail(e, "top-K tie find launch");
+    // ranks whose bound failed (or whose list did) redo it over all bins
+    if ((rc = run(topk_redo_hist_kernel(), full_grid, 256)) ||
+        (rc = run(topk_redo_select_kernel(), sgrid, 1024)))
+      return rc;
+    // second and third digits: the whole array for ranks on the full path,
+    // the lists for the others
+    for (int pass = 1; pass <= 2; ++pass) {
+      if ((rc = run(topk_hist_kernel(pass), full_grid, 256))) return rc;
+      if (prm.use_cand && (rc = run(topk_cand_hist_kernel(pass), few, 256))) return rc;
+      if ((rc = run(topk_select_kernel(pass), sgrid, 1024))) return rc;
+    }
+    // keys equal to the K-th one straddling the cut: tile counts and a scan
+    // on the full path, three index digits on the candidate path
+    if ((rc = run(topk_tie_count_kernel(), full_grid, 256)) ||
+        (rc = run(topk_tie_find_kernel(), sgrid, 1024)))
+      return rc;
+    if (prm.use_cand)
+      for (int pass = 3; pass <= 5; ++pass)
+        if ((rc = run(topk_cand_hist_kernel(pass), few, 256)) ||
+            (rc = run(topk_index_select_kernel(pass), sgrid, 1024)))
+          return rc;
   }
   const void* fn = sparse_apply_kernel(topk);
-  (void)blocks;
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(prm.num_tiles, 0x7FFFFFFF));
   void* args[] = {&prm};
   cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(256), args, 0, st);
@@ -824,6 +872,11 @@ size_t vcoll_sparse_workspace_bytes(int W, int64_t n, int topk) {
   return topk_workspace_bytes(W, n);
 }
 
+size_t vcoll_sparse_workspace_min_bytes(int W, int64_t n, int topk) {
+  if (W < 1 || W > VCOLL_MAX_RANKS || n < 0 || !topk) return 0;
+  return topk_workspace_min_bytes(W, n);
+}
+
 int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const* accum, int W,
                            int64_t n, float threshold, int topk, int64_t* nnz, void* workspace,
                            size_t workspace_bytes, void* stream) {
@@ -860,9 +913,9 @@ int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const*
     // K = ceil(threshold * num) in fp32, as SINGA computes nnzMax
     const float kf = ceilf(threshold * (float)n);
     K = kf >= (float)n ? n : (int64_t)kf;
-    if (!workspace || workspace_bytes < topk_workspace_bytes(W, n))
-      return fail(VCOLL_ERR_INVALID_ARG, "top-K needs a workspace of %zu bytes",
-                  topk_workspace_bytes(W, n));
+    if (!workspace || workspace_bytes < topk_workspace_min_bytes(W, n))
+      return fail(VCOLL_ERR_INVALID_ARG, "top-K needs a workspace of at least %zu bytes",
+                  topk_workspace_min_bytes(W, n));
     if ((uint64_t)workspace % 16) return fail(VCOLL_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
   }
   SparseParams prm;
@@ -882,7 +935,7 @@ int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const*
   prm.tile_elems = kSparseTileElems;
   prm.tiles_per_rank = ceil_div(n, prm.tile_elems);
   prm.num_tiles = prm.tiles_per_rank;
-  return sparse_launch(prm, topk, workspace, stream);
+  return sparse_launch(prm, topk, workspace, workspace_bytes, stream);
 }
 
 int vcoll_selftest_wait_timeout(unsigned limit_us, void* stream) {

@@ -65,8 +65,12 @@ extern "C" int vcoll_sparse_allreduce_noalloc(const void* const* in, void* const
                                               void* stream) {
   if (!topk)  // the threshold mode needs no working memory at all
     return vcoll_sparse_allreduce(in, out, accum, W, n, threshold, topk, nnz, nullptr, 0, stream);
-  const size_t need = vcoll_sparse_workspace_bytes(W, n, topk);
-  if (W >= 1 && W <= VCOLL_MAX_RANKS && n >= 0 && need > kNoAllocScratchBytes) {
+  // the minimum working memory; what the array holds beyond it becomes
+  // candidate-list room (a list that does not fit sends the select passes
+  // over the whole array instead)
+  const size_t need =
+      (W >= 1 && W <= VCOLL_MAX_RANKS && n >= 0) ? vcoll::topk_workspace_min_bytes(W, n) : 0;
+  if (need > kNoAllocScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof(msg),
              "top-K over W=%d ranks of n=%lld elements needs %zu bytes of working memory; the "

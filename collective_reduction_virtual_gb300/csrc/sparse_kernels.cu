@@ -20,8 +20,18 @@
 //     entry kept in index order -- then the same apply pass as the threshold
 //     mode.
 //
-// The histograms (W x 2048 counters), the per-rank selection state and the
-// per-tile tie counts live in a device workspace the caller provides.
+// Candidate path (when the workspace has room): a 1/16 - 1/64 sample of the data
+// gives a first-digit lower bound, one pass over the data appends every
+// entry at or above it to the rank's candidate list as (key, index), and the
+// select passes then read only the list -- three over the key digits and,
+// when keys equal to the K-th one straddle the cut, three over the bits of
+// the inverted index (the K largest (key, -index) pairs are the K entries
+// kept).  A rank whose list overflowed, or holds fewer than K entries, takes
+// the passes over the whole array instead; the choice is made on the device.
+//
+// The histograms (W x 2048 counters), the per-rank selection state, the
+// per-tile tie counts and the candidate lists live in a device workspace the
+// caller provides.
 #include "device_common.cuh"
 #include "vcoll_internal.h"
 
@@ -58,6 +68,49 @@ __device__ __forceinline__ void load_x4(const SparseParams& p, int r, int64_t i,
   }
 }
 
+// The pass kernels run 256 threads over tiles of kSparseTileElems entries:
+// a tile's aligned body is at most kTileVecs 16-byte vectors per thread.
+constexpr int kSparseThreads = 256;
+constexpr int kTileVecs = (int)(kSparseTileElems / 4 / kSparseThreads);
+static_assert(kTileVecs * 4 * kSparseThreads == kSparseTileElems, "tile = threads x vectors");
+
+// x for this thread's vectors v = tid + u * 256 (u < kTileVecs, v < nv) of
+// the aligned body starting at av; every load is issued before the first add
+// so that each thread keeps up to 2 x kTileVecs x 16 bytes in flight.
+// Vectors past nv read as zeros (the caller masks them).
+__device__ __forceinline__ void load_tile_x(const SparseParams& p, int r, int64_t av, int64_t nv,
+                                            float (&x)[kTileVecs][4]) {
+  uint4 a[kTileVecs], b[kTileVecs];
+#pragma unroll
+  for (int u = 0; u < kTileVecs; ++u) {
+    const int64_t v = threadIdx.x + u * kSparseThreads;
+    a[u] = make_uint4(0u, 0u, 0u, 0u);
+    b[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (v < nv) {
+      a[u] = ld_stream((const char*)p.in[r] + (av + v * 4) * 4);
+      if (p.has_acc) b[u] = ld_stream((const char*)p.acc[r] + (av + v * 4) * 4);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kTileVecs; ++u) {
+    reg_fence(a[u]);
+    reg_fence(b[u]);
+  }
+#pragma unroll
+  for (int u = 0; u < kTileVecs; ++u) {
+    x[u][0] = __uint_as_float(a[u].x);
+    x[u][1] = __uint_as_float(a[u].y);
+    x[u][2] = __uint_as_float(a[u].z);
+    x[u][3] = __uint_as_float(a[u].w);
+    if (p.has_acc) {
+      x[u][0] = __fadd_rn(x[u][0], __uint_as_float(b[u].x));
+      x[u][1] = __fadd_rn(x[u][1], __uint_as_float(b[u].y));
+      x[u][2] = __fadd_rn(x[u][2], __uint_as_float(b[u].z));
+      x[u][3] = __fadd_rn(x[u][3], __uint_as_float(b[u].w));
+    }
+  }
+}
+
 // digit of pass P and whether the key matches the prefix fixed so far
 template <int P>
 __device__ __forceinline__ bool digit_of(uint32_t key, uint32_t prefix, uint32_t& d) {
@@ -71,6 +124,21 @@ __device__ __forceinline__ bool digit_of(uint32_t key, uint32_t prefix, uint32_t
   }
   d = key & 0x3FFu;
   return (key >> 10) == prefix;
+}
+
+// digit of index pass P (3, 4, 5) of an inverted index (larger = lower index)
+template <int P>
+__device__ __forceinline__ bool index_digit_of(uint32_t inv, uint32_t prefix, uint32_t& d) {
+  if (P == 3) {
+    d = inv >> 21;
+    return true;
+  }
+  if (P == 4) {
+    d = (inv >> 10) & 0x7FFu;
+    return (inv >> 21) == prefix;
+  }
+  d = inv & 0x3FFu;
+  return (inv >> 10) == prefix;
 }
 
 // the first-digit pass only counts bins from state.low up
@@ -101,8 +169,9 @@ __device__ __forceinline__ void hist_add(uint32_t* h, bool valid, uint32_t d) {
 //         sample pass: keys below it cannot be among the K largest when the
 //         counted bins hold at least K keys -- checked by the selection);
 // MODE 1, 2: the second and third digits, keys matching the prefix so far;
-// MODE 3: the first digit over a 1/16 sample (every 16th tile);
+// MODE 3: the first digit over a sample (every sample_stride-th tile);
 // MODE 4: the first digit over all bins, only for ranks whose bound failed.
+// With candidate lists, MODES 1 and 2 run only for ranks on the full path.
 template <int MODE>
 __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ SparseParams p) {
   constexpr int P = (MODE == 1 || MODE == 2) ? MODE : 0;
@@ -111,11 +180,12 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
   const int tid = threadIdx.x;
   const TopkState& st = p.state[r];
   if (MODE == 4 && !st.redo) return;  // uniform per CTA
+  if ((MODE == 1 || MODE == 2) && p.use_cand && !st.full) return;  // read its candidates
   for (int i = tid; i < kTopkBins; i += blockDim.x) h[i] = 0;
   const uint32_t prefix = st.prefix;
   const uint32_t low = MODE == 0 ? st.low : 0u;
   __syncthreads();
-  const int64_t step = MODE == 3 ? 16 : 1;
+  const int64_t step = MODE == 3 ? p.sample_stride : 1;
   for (int64_t tile = (int64_t)blockIdx.x * step; tile < p.tiles_per_rank;
        tile += (int64_t)gridDim.x * step) {
     const int64_t t0 = tile * p.tile_elems;
@@ -123,19 +193,19 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
     if (p.phase >= 0) {
       int64_t av, bv;
       aligned_body<4>(t0, t1, p.phase, av, bv);
-      // vectors [av, bv); the loop runs the same trip count on every lane of
-      // a warp so that the warp-wide combining stays converged
+      // vectors [av, bv), all loads first; every lane of a warp makes the
+      // same hist_add calls so that the warp-wide combining stays converged
       const int64_t nv = (bv - av) / 4;
-      for (int64_t base = 0; base < nv; base += blockDim.x) {
-        const int64_t v = base + tid;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        const bool in_range = v < nv;
-        if (in_range) load_x4(p, r, av + v * 4, x);
+      float x[kTileVecs][4];
+      load_tile_x(p, r, av, nv, x);
+#pragma unroll
+      for (int u = 0; u < kTileVecs; ++u) {
+        const bool in_range = tid + u * kSparseThreads < nv;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t d;
-          const bool m = digit_of<P>(order_key(x[q]), prefix, d) && counted_bin<MODE>(d, low) &&
-                         in_range;
+          const bool m = digit_of<P>(order_key(x[u][q]), prefix, d) &&
+                         counted_bin<MODE>(d, low) && in_range;
           hist_add(h, m, d);
         }
       }
@@ -173,7 +243,10 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
 // MODE 3: after the sample pass: state.low = the highest bin whose sampled
 //   suffix holds twice the keys K calls for (scaled to the sample) plus a
 //   margin, or 0 (count everything) when K is a large fraction of n;
-// MODE 4: after the redo pass, for ranks that needed it.
+// MODE 4: after the redo pass, for ranks that needed it;
+// MODE 5, 6, 7: after index pass 3, 4, 5 over the candidates equal to T, for
+//   ranks on the candidate path whose equal keys straddle the cut; the last
+//   one sets the boundary index.
 template <int MODE>
 __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ SparseParams p) {
   const int r = blockIdx.x;
@@ -183,6 +256,8 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
   uint32_t* hist = p.hist + (int64_t)r * kTopkBins;
   TopkState* st = p.state + r;
   if (MODE == 4 && !st->redo) return;
+  // (uniform per CTA; nothing was counted for these ranks, the bins are zero)
+  if (MODE >= 5 && (p.K == 0 || st->full || st->need >= st->equal)) return;
   const int b0 = kTopkBins - 1 - 2 * t, b1 = b0 - 1;
   const unsigned long long c0 = hist[b0], c1 = hist[b1];
   unsigned long long s = c0 + c1;
@@ -210,11 +285,13 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
   if (MODE == 3) {
     // sampled keys wanted above the bound: twice K's share of the sample,
     // plus a margin; no bound when K is a quarter of n or more
-    rem = 4 * p.K >= p.n ? -1 : 2 * ((p.K + 15) / 16) + 64;
+    rem = 4 * p.K >= p.n ? -1 : 2 * ((p.K + p.sample_stride - 1) / p.sample_stride) + 64;
+  } else if (MODE == 5) {
+    rem = st->need;
   } else {
-    rem = P == 0 ? p.K : st->remaining;
+    rem = (P == 0 && MODE < 5) ? p.K : st->remaining;
   }
-  const uint32_t prefix = P == 0 ? 0u : st->prefix;
+  const uint32_t prefix = (P == 0 && MODE < 6) ? 0u : st->prefix;
   __syncthreads();  // every thread has read the state before it changes
   if (MODE == 3) {
     if (t == 0 && (rem < 0 || (long long)total < rem)) st->low = 0;
@@ -222,7 +299,10 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
       st->low = (uint32_t)((long long)(above + c0) >= rem ? b0 : b1);
     if (t == 0) st->redo = 0;
   } else if (MODE == 0 && (long long)total < rem) {
-    if (t == 0) st->redo = 1;  // the bound was too high: count every bin again
+    if (t == 0) {  // the bound was too high (or the list overflowed): count every bin again
+      st->redo = 1;
+      st->full = 1;
+    }
   } else if (rem > 0 && (long long)above < rem && rem <= (long long)incl) {
     int bin;
     unsigned long long more;  // keys strictly above the chosen bin
@@ -234,7 +314,15 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
       more = above + c0;
     }
     const long long left = rem - (long long)more;
-    if (P == 0) {
+    if (MODE == 5) {
+      st->prefix = (uint32_t)bin;
+      st->remaining = left;
+    } else if (MODE == 6) {
+      st->prefix = (prefix << 11) | (uint32_t)bin;
+      st->remaining = left;
+    } else if (MODE == 7) {  // one index per inverted index: left == 1
+      st->boundary = (int64_t)(0xFFFFFFFFu - ((prefix << 10) | (uint32_t)bin));
+    } else if (P == 0) {
       st->prefix = (uint32_t)bin;
       st->remaining = left;
       st->redo = 0;
@@ -262,6 +350,7 @@ __global__ void __launch_bounds__(256) vc_topk_tie_count(const __grid_constant__
   const int r = blockIdx.y;
   const TopkState* st = p.state + r;
   if (p.K == 0 || st->need >= st->equal) return;  // uniform per CTA
+  if (p.use_cand && !st->full) return;            // the index passes handle it
   const uint32_t T = st->T;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x) {
@@ -327,6 +416,7 @@ __global__ void __launch_bounds__(1024) vc_topk_tie_find(const __grid_constant__
   TopkState* st = p.state + r;
   const long long need = st->need, equal = st->equal;
   if (p.K == 0 || need >= equal) return;
+  if (p.use_cand && !st->full) return;
   const uint32_t T = st->T;
   const uint32_t* cnt = p.tilecnt + (int64_t)r * p.tiles_per_rank;
   __shared__ long long s_tile, s_before, s_found;
@@ -369,6 +459,176 @@ __global__ void __launch_bounds__(1024) vc_topk_tie_find(const __grid_constant__
   if (threadIdx.x == 0) st->boundary = s_found;
 }
 
+// ------------------------------------------------------------ candidates
+// One pass over the data (grid.y = rank, one tile per CTA iteration): every
+// entry whose key is at or above the sample's first-digit bound is appended
+// to the rank's candidate list as (key, index).  Each thread looks at 16
+// entries of the tile (four 16-byte vectors, all loaded before the first is
+// used) plus at most one of the tile's unaligned head or tail; a warp-wide
+// scan of the per-thread counts places every candidate, one shared atomic
+// per warp and one global atomic per tile reserve room, and the candidates
+// go from registers straight to the list (compact; the order between tiles
+// is arbitrary, the index travels with the key).  Entries past the capacity
+// are counted but not stored, which sends the rank to the full path.
+__global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ SparseParams p) {
+  constexpr int S = 4 * kTileVecs + 1;  // entries per thread and tile
+  __shared__ uint32_t s_n;
+  __shared__ unsigned long long s_base;
+  const int r = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint32_t lowkey = p.state[r].low << 21;
+  uint32_t* ckey = p.cand_key + (int64_t)r * p.cand_cap;
+  uint32_t* cidx = p.cand_idx + (int64_t)r * p.cand_cap;
+  for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x) {
+    const int64_t t0 = tile * p.tile_elems;
+    const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
+    if (tid == 0) s_n = 0;
+    uint32_t key[S];
+    uint32_t mask = 0;  // bit j: entry j is a candidate
+    int64_t av = t0, extra = -1;
+    const bool vec = p.phase >= 0;
+    if (vec) {
+      int64_t bv;
+      aligned_body<4>(t0, t1, p.phase, av, bv);
+      const int64_t nv = (bv - av) / 4;
+      float x[kTileVecs][4];
+      load_tile_x(p, r, av, nv, x);
+#pragma unroll
+      for (int u = 0; u < kTileVecs; ++u)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          key[u * 4 + q] = order_key(x[u][q]);
+          if (tid + u * kSparseThreads < nv && key[u * 4 + q] >= lowkey) mask |= 1u << (u * 4 + q);
+        }
+      // head [t0, av) and tail [bv, t1): fewer than 4 entries each
+      if (tid < av - t0) extra = t0 + tid;
+      if (tid >= 32 && tid - 32 < t1 - bv) extra = bv + (tid - 32);
+    } else {  // element-wise: entries t0 + tid + 256 j
+#pragma unroll
+      for (int j = 0; j < S - 1; ++j) {
+        const int64_t i = t0 + tid + (int64_t)j * kSparseThreads;
+        key[j] = 0;
+        if (i < t1) {
+          key[j] = order_key(load_x(p, r, i));
+          if (key[j] >= lowkey) mask |= 1u << j;
+        }
+      }
+    }
+    key[S - 1] = 0;
+    if (extra >= 0) {
+      key[S - 1] = order_key(load_x(p, r, extra));
+      if (key[S - 1] >= lowkey) mask |= 1u << (S - 1);
+    }
+    // this thread's place among the warp's candidates
+    const int c = __popc(mask);
+    int incl = c;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int wtotal = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    __syncthreads();  // s_n is zero
+    uint32_t wbase = 0;
+    if (lane == 31 && wtotal) wbase = atomicAdd(&s_n, (uint32_t)wtotal);
+    wbase = __shfl_sync(0xFFFFFFFFu, wbase, 31);
+    __syncthreads();  // every warp has reserved its share of the tile's room
+    if (tid == 0) {
+      const uint32_t tot = s_n;
+      s_base = tot ? atomicAdd(p.cand_n + r, (unsigned long long)tot) : 0ull;
+    }
+    __syncthreads();
+    if (mask) {
+      unsigned long long pos = s_base + wbase + (uint32_t)(incl - c);
+#pragma unroll
+      for (int j = 0; j < S; ++j)
+        if ((mask >> j) & 1u) {
+          int64_t i;
+          if (j == S - 1)
+            i = extra;
+          else if (vec)
+            i = av + (int64_t)(tid + (j >> 2) * kSparseThreads) * 4 + (j & 3);
+          else
+            i = t0 + tid + (int64_t)j * kSparseThreads;
+          if (pos < (unsigned long long)p.cand_cap) {
+            ckey[pos] = key[j];
+            cidx[pos] = (uint32_t)i;
+          }
+          ++pos;
+        }
+    }
+  }
+}
+
+// Histogram of digit P over a rank's candidate list: P = 0, 1, 2 the key
+// digits (as vc_topk_hist), P = 3, 4, 5 the digits of the inverted index of
+// the candidates whose key equals T.  Ranks on the full path count nothing;
+// an overflowed list counts nothing at P = 0, so the selection sends the
+// rank to the full path.
+template <int P>
+__global__ void __launch_bounds__(256) vc_topk_cand_hist(const __grid_constant__ SparseParams p) {
+  __shared__ uint32_t h[kTopkBins];
+  const int r = blockIdx.y;
+  const int tid = threadIdx.x;
+  const TopkState& st = p.state[r];
+  // uniform per CTA
+  if (st.full) return;
+  if (P >= 3 && st.need >= st.equal) return;
+  const unsigned long long cn = p.cand_n[r];
+  if (cn > (unsigned long long)p.cand_cap) return;
+  for (int i = tid; i < kTopkBins; i += blockDim.x) h[i] = 0;
+  const uint32_t prefix = st.prefix, T = st.T;
+  const uint32_t* ckey = p.cand_key + (int64_t)r * p.cand_cap;
+  const uint32_t* cidx = p.cand_idx + (int64_t)r * p.cand_cap;
+  __syncthreads();
+  auto count = [&](bool in_list, uint32_t key, int64_t i) {  // every lane calls it
+    bool valid = false;
+    uint32_t d = 0;
+    if (in_list) {
+      if (P <= 2) {
+        valid = digit_of<P>(key, prefix, d);
+      } else if (key == T) {
+        valid = index_digit_of<P>(~cidx[i], prefix, d);
+      }
+    }
+    // the first digit clusters (combine equal bins across the warp); the
+    // later digits spread over the bins, where plain atomics are cheaper
+    if (P == 0)
+      hist_add(h, valid, d);
+    else if (valid)
+      atomicAdd(&h[d], 1u);
+  };
+  // keys four at a time (the list starts 16-byte aligned), U vectors per
+  // thread loaded before any is counted; then the last m % 4 keys
+  constexpr int U = 4;
+  const int64_t m = (int64_t)cn, m4 = m / 4;
+  const uint4* k4 = reinterpret_cast<const uint4*>(ckey);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < m4; base += stride * U) {
+    uint4 kv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = base + u * stride + tid;
+      kv[u] = v < m4 ? k4[v] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = base + u * stride + tid;
+      const bool ok = v < m4;
+      count(ok, kv[u].x, v * 4);
+      count(ok, kv[u].y, v * 4 + 1);
+      count(ok, kv[u].z, v * 4 + 2);
+      count(ok, kv[u].w, v * 4 + 3);
+    }
+  }
+  if (blockIdx.x == 0 && tid < 32) {
+    const int64_t i = m4 * 4 + tid;
+    count(i < m, i < m ? ckey[i] : 0u, i);
+  }
+  __syncthreads();
+  for (int i = tid; i < kTopkBins; i += blockDim.x)
+    if (h[i]) atomicAdd(&p.hist[(int64_t)r * kTopkBins + i], h[i]);
+}
+
 // -------------------------------------------------------------------- apply
 // One pass: survivors, error feedback, rank-order sum written to every rank,
 // survivor counts per rank.
@@ -395,6 +655,9 @@ __global__ void __launch_bounds__(256) vc_sparse_apply(const __grid_constant__ S
     }
     return fabsf(x) > p.threshold && x != 0.0f;
   };
+  // the value the residual subtracts: top-K scatters the sent values into
+  // zeros first (0 + x, which turns -0 into +0), threshold mode subtracts x
+  auto sent = [&](float x) -> float { return TOPK ? __fadd_rn(0.0f, x) : x; };
   auto count = [&](int r, int c) {
     // per-warp sum of this rank's survivors, one shared atomic per warp
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
@@ -420,7 +683,7 @@ __global__ void __launch_bounds__(256) vc_sparse_apply(const __grid_constant__ S
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const bool k = keep(r, x[q], e + q);
-            s[q] = k ? x[q] : 0.0f;
+            s[q] = k ? sent(x[q]) : 0.0f;
             if (k) res[q] = __fadd_rn(x[q], res[q]);
             c += k;
           }
@@ -452,7 +715,7 @@ __global__ void __launch_bounds__(256) vc_sparse_apply(const __grid_constant__ S
         if (in_range) {
           const float x = load_x(p, r, i);
           const bool k = keep(r, x, i);
-          const float s = k ? x : 0.0f;
+          const float s = k ? sent(x) : 0.0f;
           if (k) res = __fadd_rn(x, res);
           c = k;
           if (p.has_acc) st1((char*)p.acc[r] + i * 4, __float_as_uint(__fsub_rn(x, s)));
@@ -483,6 +746,21 @@ const void* topk_hist_kernel(int pass) {
 const void* topk_select_kernel(int pass) {
   return pass == 0 ? (const void*)&vc_topk_select<0>
                    : pass == 1 ? (const void*)&vc_topk_select<1> : (const void*)&vc_topk_select<2>;
+}
+const void* topk_filter_kernel() { return (const void*)&vc_topk_filter; }
+const void* topk_cand_hist_kernel(int pass) {
+  switch (pass) {
+    case 0: return (const void*)&vc_topk_cand_hist<0>;
+    case 1: return (const void*)&vc_topk_cand_hist<1>;
+    case 2: return (const void*)&vc_topk_cand_hist<2>;
+    case 3: return (const void*)&vc_topk_cand_hist<3>;
+    case 4: return (const void*)&vc_topk_cand_hist<4>;
+    default: return (const void*)&vc_topk_cand_hist<5>;
+  }
+}
+const void* topk_index_select_kernel(int pass) {
+  return pass == 3 ? (const void*)&vc_topk_select<5>
+                   : pass == 4 ? (const void*)&vc_topk_select<6> : (const void*)&vc_topk_select<7>;
 }
 const void* topk_tie_count_kernel() { return (const void*)&vc_topk_tie_count; }
 const void* topk_tie_find_kernel() { return (const void*)&vc_topk_tie_find; }

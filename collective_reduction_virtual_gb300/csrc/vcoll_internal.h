@@ -127,6 +127,8 @@ struct TopkState {
   int64_t boundary;   // equal entries with index <= boundary are kept
   uint32_t low;       // first-digit bins below this one are not counted
   int redo;           // the first-digit pass must be repeated over all bins
+  int full;           // this rank's select passes read the whole array (its
+                      // candidate list overflowed or missed the K-th key)
 };
 struct SparseParams {
   const void* in[VCOLL_MAX_RANKS];
@@ -136,6 +138,12 @@ struct SparseParams {
   uint32_t* hist;              // workspace: W x kTopkBins
   TopkState* state;            // workspace: W entries
   uint32_t* tilecnt;           // workspace: W x tiles_per_rank (tie counts)
+  unsigned long long* cand_n;  // workspace: W candidate counts
+  uint32_t* cand_key;          // workspace: W x cand_cap candidate keys
+  uint32_t* cand_idx;          // workspace: W x cand_cap candidate indices
+  int64_t cand_cap;            // candidate list capacity per rank
+  int use_cand;                // select passes after the first read candidates
+  int sample_stride;           // the sample pass reads every sample_stride-th tile
   int64_t n;
   int64_t tiles_per_rank;      // histogram passes: grid.y = rank
   int64_t num_tiles;           // apply pass: tiles over [0, n)
@@ -147,10 +155,36 @@ struct SparseParams {
   float threshold;
 };
 constexpr int64_t kSparseTileElems = 4096;
-inline size_t topk_workspace_bytes(int W, int64_t n) {
+// Top-K working memory, regions 256-byte aligned: histograms, states,
+// candidate counts and per-tile tie counts (together the minimum a call
+// needs), then the candidate lists: cand_cap keys and cand_cap indices per
+// rank.  With room for candidates one pass over the data collects every entry
+// above the sample's lower bound, and the later select passes read only those.
+struct TopkLayout {
+  size_t state, cand_n, tilecnt, cands;  // byte offsets; cands = the minimum size
+};
+inline TopkLayout topk_layout(int W, int64_t n) {
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const int64_t tiles = (n + kSparseTileElems - 1) / kSparseTileElems;
-  return (size_t)W * kTopkBins * sizeof(uint32_t) + (size_t)W * sizeof(TopkState) +
-         (size_t)W * (size_t)(tiles > 0 ? tiles : 1) * sizeof(uint32_t) + 256;
+  TopkLayout L;
+  L.state = al((size_t)W * kTopkBins * sizeof(uint32_t));
+  L.cand_n = al(L.state + (size_t)W * sizeof(TopkState));
+  L.tilecnt = al(L.cand_n + (size_t)W * sizeof(unsigned long long));
+  L.cands = al(L.tilecnt + (size_t)W * (size_t)(tiles > 0 ? tiles : 1) * sizeof(uint32_t));
+  return L;
+}
+inline size_t topk_workspace_min_bytes(int W, int64_t n) { return topk_layout(W, n).cands; }
+// candidates per rank the recommended workspace holds: an eighth of the
+// entries (top-K fractions up to about 4 % stay on the candidate path), all
+// of them for small arrays; a multiple of 4 so that both lists stay 16-byte
+// aligned
+inline int64_t topk_cand_cap_default(int64_t n) {
+  int64_t c = n / 8 + 4096;
+  if (c > n) c = n;
+  return (c + 3) & ~(int64_t)3;
+}
+inline size_t topk_workspace_bytes(int W, int64_t n) {
+  return topk_workspace_min_bytes(W, n) + (size_t)W * (size_t)topk_cand_cap_default(n) * 8;
 }
 
 const void* selftest_timeout_kernel();
@@ -175,6 +209,9 @@ const void* topk_select_low_kernel();
 const void* topk_redo_hist_kernel();
 const void* topk_redo_select_kernel();
 const void* topk_select_kernel(int pass);
+const void* topk_filter_kernel();
+const void* topk_cand_hist_kernel(int pass);  // 0-2 key digits, 3-5 index digits
+const void* topk_index_select_kernel(int pass);  // 3-5
 const void* topk_tie_count_kernel();
 const void* topk_tie_find_kernel();
 constexpr int kGatherTmaThreads = 64;

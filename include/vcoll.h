@@ -226,12 +226,20 @@ int vcoll_fusion_allreduce(const void* const* in, void* const* out, const int64_
  * receives the sum of all ranks' survivors, added into zeros rank by rank --
  * what the allgathered sparse lists scattered with cusparseSaxpyi give.
  * nnz (device, W int64, may be NULL) receives each rank's survivor count.
- * workspace: device memory of vcoll_sparse_workspace_bytes(W, n, topk) bytes
- * (16-byte aligned; none needed in threshold mode), owned by the caller, not
- * kept after the call; calls that share a workspace must not overlap.
+ * workspace: device memory of workspace_bytes bytes, 16-byte aligned, owned
+ * by the caller, not kept after the call; calls that share a workspace must
+ * not overlap.  Threshold mode needs none.  Top-K needs at least
+ * vcoll_sparse_workspace_min_bytes(W, n, 1) (about n/1024 bytes + 8 KiB per
+ * rank; smaller gives VCOLL_ERR_INVALID_ARG); vcoll_sparse_workspace_bytes(W,
+ * n, 1) (about n bytes + 40 KiB per rank) adds room for candidate lists, which lets the
+ * select passes after the first read only the entries above a sampled bound
+ * instead of the whole array (the same results, about twice as fast at K = 1 %
+ * of n; a size in between gives smaller lists, and a rank whose list does not
+ * fit falls back to the passes over the whole array).
  * In place: out[u] == in[u].
  */
 size_t vcoll_sparse_workspace_bytes(int W, int64_t n, int topk);
+size_t vcoll_sparse_workspace_min_bytes(int W, int64_t n, int topk);
 int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const* accum, int W,
                            int64_t n, float threshold, int topk, int64_t* nnz, void* workspace,
                            size_t workspace_bytes, void* stream);
@@ -244,9 +252,11 @@ int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const*
  * is a fixed array inside the library, 1 MiB (VCOLL_SPARSE_NOALLOC_BYTES) on
  * every GPU that loads it, held until the process exits;
  * the call allocates nothing.  Arguments and results are those of
- * vcoll_sparse_allreduce; sizes whose working memory would not fit
- * (vcoll_sparse_workspace_bytes(W, n, 1) > the maximum, about n <= 120 Mi
- * elements at W = 8) return VCOLL_ERR_INVALID_ARG with an explanation.  The
+ * vcoll_sparse_allreduce; sizes whose minimum working memory would not fit
+ * (vcoll_sparse_workspace_min_bytes(W, n, 1) > the maximum, about n <= 120 Mi
+ * elements at W = 8) return VCOLL_ERR_INVALID_ARG with an explanation, and
+ * what the array holds beyond that minimum is candidate-list room (enough
+ * for the fast path up to a few million entries over all ranks at K = 1 %).  The
  * threshold mode needs no working memory and passes straight through.
  * The first top-K call on a device looks up the array's device address with
  * cudaGetSymbolAddress; make that first call before capturing a stream.

@@ -633,13 +633,16 @@ def _sparse_inputs(W, n, seed, ties=False):
     return xs
 
 
-def _check_sparse(v, ins, acc, thr, topk):
+def _check_sparse(v, ins, acc, thr, topk, workspace_bytes=None):
     W = len(ins)
     ins_np = [to_np(t) for t in ins]
     acc_np = [to_np(a).copy() for a in acc] if acc is not None else None
     want, want_nnz = oracle.sparse_allreduce(ins_np, thr, topk, acc_np)
     nnz = torch.empty(W, dtype=torch.int64, device="cuda")
-    outs = v.sparse_allreduce(ins, accum=acc, threshold=thr, topk=topk, nnz=nnz)
+    ws = None
+    if workspace_bytes is not None:
+        ws = torch.empty(workspace_bytes, dtype=torch.uint8, device="cuda")
+    outs = v.sparse_allreduce(ins, accum=acc, threshold=thr, topk=topk, nnz=nnz, workspace=ws)
     torch.cuda.synchronize()
     for u in range(W):
         assert_bit_exact(to_np(outs[u]), want[u], f"sparse topk={topk} out {u}")
@@ -666,7 +669,7 @@ def test_sparse_topk(v, W, n, frac):
     _check_sparse(v, ins, acc, frac, True)
 
 
-@pytest.mark.parametrize("frac", [0.01, 0.3, 0.77])
+@pytest.mark.parametrize("frac", [0.001, 0.01, 0.05, 0.3, 0.77])
 def test_sparse_topk_ties_straddle_the_cut(v, frac):
     W, n = 4, 50_001
     ins = _sparse_inputs(W, n, 77, ties=True)
@@ -706,3 +709,61 @@ def test_sparse_topk_sample_bound_redo(v):
         tiles[::16] = tiles[::16].abs() + 100.0
     _check_sparse(v, ins, None, 0.01, True)
     _check_sparse(v, ins, [torch.zeros(n, device="cuda") for _ in range(W)], 0.2, True)
+
+
+# The top-K select runs over candidate lists when the workspace has room for
+# them (the entries above a sampled bound), else over the whole array; a rank
+# whose list overflows or misses the K-th key falls back on the device.  Every
+# route must give the oracle's bits.
+
+@pytest.mark.parametrize("frac", [0.001, 0.01, 0.05])
+def test_sparse_topk_minimum_workspace(v, frac):
+    W, n = 4, 300_007
+    ins = _sparse_inputs(W, n, 61)
+    acc = [t * 0.3 for t in _sparse_inputs(W, n, 62)]
+    least = v.sparse_workspace_min_bytes(W, n)
+    assert least < v.sparse_workspace_bytes(W, n)
+    _check_sparse(v, ins, acc, frac, True, workspace_bytes=least)
+
+
+def test_sparse_topk_candidate_list_overflows(v):
+    # the sampled tiles (every 16th of 4096 entries) hold tiny values, so the
+    # sampled bound admits about half of every other tile: far more than the
+    # lists hold
+    W, n = 2, 64 * 4096 + 5
+    ins = _sparse_inputs(W, n, 8)
+    for t in ins:
+        tiles = t[: 64 * 4096].view(-1, 4096)
+        tiles[::16] *= 1e-6
+    _check_sparse(v, ins, None, 0.01, True)
+    _check_sparse(v, ins, [torch.zeros(n, device="cuda") for _ in range(W)], 0.03, True)
+
+
+def test_sparse_topk_mixed_routes_in_one_call(v):
+    # rank 0 overflows its list, rank 1 misses the K-th key (large values only
+    # in the sampled tiles), ranks 2 and 3 stay on their lists, ranks 3 with
+    # ties across the cut
+    W, n = 4, 128 * 4096
+    ins = _sparse_inputs(W, n, 12)
+    ins[0].view(-1, 4096)[::16] *= 1e-6
+    t1 = ins[1].view(-1, 4096)
+    t1[::16] = t1[::16].abs() + 100.0
+    ins[3] = torch.round(ins[3] * 4) / 4
+    _check_sparse(v, ins, None, 0.01, True)
+    # a workspace between the minimum and the recommended size: shorter lists
+    mid = (v.sparse_workspace_min_bytes(W, n) + v.sparse_workspace_bytes(W, n)) // 2
+    _check_sparse(v, ins, [torch.zeros(n, device="cuda") for _ in range(W)], 0.01, True,
+                  workspace_bytes=mid)
+
+
+def test_sparse_topk_all_equal_values(v):
+    # every entry ties: the K kept are the K lowest indices
+    W, n = 3, 100_000
+    ins = [torch.full((n,), 0.5, device="cuda") for _ in range(W)]
+    _check_sparse(v, ins, None, 0.01, True)
+    ins = [torch.zeros(n, device="cuda") for _ in range(W)]
+    _check_sparse(v, ins, None, 0.02, True)
+    # -0 + -0 keeps the sign: the kept -0 entries leave a residual of
+    # -0 - (0 + -0) = -0
+    ins = [torch.full((n,), -0.0, device="cuda") for _ in range(W)]
+    _check_sparse(v, ins, [torch.full((n,), -0.0, device="cuda") for _ in range(W)], 0.02, True)
