@@ -466,12 +466,15 @@ __global__ void __launch_bounds__(1024) vc_topk_tie_find(const __grid_constant__
 // entries of the tile (four 16-byte vectors, all loaded before the first is
 // used) plus at most one of the tile's unaligned head or tail; a warp-wide
 // scan of the per-thread counts places every candidate, one shared atomic
-// per warp and one global atomic per tile reserve room, and the candidates
-// go from registers straight to the list (compact; the order between tiles
-// is arbitrary, the index travels with the key).  Entries past the capacity
-// are counted but not stored, which sends the rank to the full path.
+// per warp and one global atomic per tile reserve room, and each thread then
+// visits only its own candidates (their keys parked in shared memory, so the
+// loop over set bits needs no register indexing).  The list is compact; the
+// order between tiles is arbitrary (the index travels with the key).
+// Entries past the capacity are counted but not stored, which sends the rank
+// to the full path.
 __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ SparseParams p) {
-  constexpr int S = 4 * kTileVecs + 1;  // entries per thread and tile
+  constexpr int E = 4 * kTileVecs;  // entries per thread and tile (plus one extra)
+  __shared__ __align__(16) uint32_t s_key[kSparseThreads * E];
   __shared__ uint32_t s_n;
   __shared__ unsigned long long s_base;
   const int r = blockIdx.y;
@@ -479,12 +482,14 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
   const uint32_t lowkey = p.state[r].low << 21;
   uint32_t* ckey = p.cand_key + (int64_t)r * p.cand_cap;
   uint32_t* cidx = p.cand_idx + (int64_t)r * p.cand_cap;
+  uint32_t* my = s_key + tid * E;
   for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x) {
     const int64_t t0 = tile * p.tile_elems;
     const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
     if (tid == 0) s_n = 0;
-    uint32_t key[S];
-    uint32_t mask = 0;  // bit j: entry j is a candidate
+    uint32_t mask = 0;  // bit j < E: entry j is a candidate
+    uint32_t xkey = 0;  // the extra entry (head or tail)
+    bool xhit = false;
     int64_t av = t0, extra = -1;
     const bool vec = p.phase >= 0;
     if (vec) {
@@ -494,33 +499,39 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
       float x[kTileVecs][4];
       load_tile_x(p, r, av, nv, x);
 #pragma unroll
-      for (int u = 0; u < kTileVecs; ++u)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          key[u * 4 + q] = order_key(x[u][q]);
-          if (tid + u * kSparseThreads < nv && key[u * 4 + q] >= lowkey) mask |= 1u << (u * 4 + q);
+      for (int u = 0; u < kTileVecs; ++u) {
+        uint4 k4;
+        k4.x = order_key(x[u][0]);
+        k4.y = order_key(x[u][1]);
+        k4.z = order_key(x[u][2]);
+        k4.w = order_key(x[u][3]);
+        if (tid + u * kSparseThreads < nv) {
+          mask |= (uint32_t)(k4.x >= lowkey) << (u * 4) | (uint32_t)(k4.y >= lowkey) << (u * 4 + 1) |
+                  (uint32_t)(k4.z >= lowkey) << (u * 4 + 2) | (uint32_t)(k4.w >= lowkey) << (u * 4 + 3);
         }
+        reinterpret_cast<uint4*>(my)[u] = k4;
+      }
       // head [t0, av) and tail [bv, t1): fewer than 4 entries each
       if (tid < av - t0) extra = t0 + tid;
       if (tid >= 32 && tid - 32 < t1 - bv) extra = bv + (tid - 32);
     } else {  // element-wise: entries t0 + tid + 256 j
 #pragma unroll
-      for (int j = 0; j < S - 1; ++j) {
+      for (int j = 0; j < E; ++j) {
         const int64_t i = t0 + tid + (int64_t)j * kSparseThreads;
-        key[j] = 0;
+        uint32_t k = 0;
         if (i < t1) {
-          key[j] = order_key(load_x(p, r, i));
-          if (key[j] >= lowkey) mask |= 1u << j;
+          k = order_key(load_x(p, r, i));
+          mask |= (uint32_t)(k >= lowkey) << j;
         }
+        my[j] = k;
       }
     }
-    key[S - 1] = 0;
     if (extra >= 0) {
-      key[S - 1] = order_key(load_x(p, r, extra));
-      if (key[S - 1] >= lowkey) mask |= 1u << (S - 1);
+      xkey = order_key(load_x(p, r, extra));
+      xhit = xkey >= lowkey;
     }
     // this thread's place among the warp's candidates
-    const int c = __popc(mask);
+    const int c = __popc(mask) + (xhit ? 1 : 0);
     int incl = c;
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
@@ -537,25 +548,24 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
       s_base = tot ? atomicAdd(p.cand_n + r, (unsigned long long)tot) : 0ull;
     }
     __syncthreads();
-    if (mask) {
-      unsigned long long pos = s_base + wbase + (uint32_t)(incl - c);
-#pragma unroll
-      for (int j = 0; j < S; ++j)
-        if ((mask >> j) & 1u) {
-          int64_t i;
-          if (j == S - 1)
-            i = extra;
-          else if (vec)
-            i = av + (int64_t)(tid + (j >> 2) * kSparseThreads) * 4 + (j & 3);
-          else
-            i = t0 + tid + (int64_t)j * kSparseThreads;
-          if (pos < (unsigned long long)p.cand_cap) {
-            ckey[pos] = key[j];
-            cidx[pos] = (uint32_t)i;
-          }
-          ++pos;
-        }
+    unsigned long long pos = s_base + wbase + (uint32_t)(incl - c);
+    const unsigned long long cap = (unsigned long long)p.cand_cap;
+    for (uint32_t m = mask; m; m &= m - 1u) {  // this thread's candidates only
+      const int j = __ffs(m) - 1;
+      const int64_t i = vec ? av + (int64_t)(tid + (j >> 2) * kSparseThreads) * 4 + (j & 3)
+                            : t0 + tid + (int64_t)j * kSparseThreads;
+      if (pos < cap) {
+        ckey[pos] = my[j];
+        cidx[pos] = (uint32_t)i;
+      }
+      ++pos;
     }
+    if (xhit && pos < cap) {
+      ckey[pos] = xkey;
+      cidx[pos] = (uint32_t)extra;
+    }
+    // (the next tile's writes to s_key and s_n follow the barriers above:
+    // every thread reads only its own row of s_key)
   }
 }
 
