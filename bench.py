@@ -518,7 +518,7 @@ def extras(args, stream, dev):
         lambda: vc.sparse_allreduce(ins, outs, acc, 0.01, True, nnz, ws), 4 * W * n * 4)
     out["sparse_bytes_formula"] = ("4*W*n*4: read inputs and accumulations, write outputs and "
                                    "accumulations (top-K also reads them once more to collect "
-                                   "its select candidates, plus a 1/16 sample)")
+                                   "its select candidates, plus a 1/16 to 1/64 sample)")
     del ins, outs, segs, acc
     torch.cuda.empty_cache()
 

@@ -196,13 +196,135 @@ __global__ void __launch_bounds__(256) vc_fuse(const __grid_constant__ FuseParam
   }
 }
 
+// The 16-byte body of one tile for ranks g .. g + G - 1: nv destination
+// vectors at dst_of(u) + head, the source sh bytes past a 16-byte boundary.
+// Aligned: every thread issues 8 vector loads (8 / G per rank) before its
+// first store; shifted: one vector per rank, loaded as the two aligned blocks
+// that cover it and funnel-shifted.
+template <int G, class DstOf, class SrcOf>
+__device__ __forceinline__ void fuse_group_body(DstOf dst_of, SrcOf src_of, int g, int64_t head,
+                                                int64_t nv, int sh) {
+  const int tid = threadIdx.x;
+  const int64_t nthr = blockDim.x;
+  if (sh == 0) {
+    constexpr int U = 8 / G;
+    for (int64_t base = tid; base < nv; base += U * nthr) {
+      uint4 x[U][G];
+#pragma unroll
+      for (int v = 0; v < U; ++v)
+#pragma unroll
+        for (int q = 0; q < G; ++q)
+          if (base + v * nthr < nv) x[v][q] = ld_stream(src_of(g + q) + head + (base + v * nthr) * 16);
+#pragma unroll
+      for (int v = 0; v < U; ++v)
+#pragma unroll
+        for (int q = 0; q < G; ++q) reg_fence(x[v][q]);
+#pragma unroll
+      for (int v = 0; v < U; ++v)
+#pragma unroll
+        for (int q = 0; q < G; ++q)
+          if (base + v * nthr < nv) st_stream(dst_of(g + q) + head + (base + v * nthr) * 16, x[v][q]);
+    }
+  } else {
+    for (int64_t i = tid; i < nv; i += nthr) {
+      uint4 a[G], b[G];
+#pragma unroll
+      for (int q = 0; q < G; ++q) {
+        const char* as = src_of(g + q) + head - sh + i * 16;  // aligned source blocks
+        a[q] = ld_stream(as);
+        b[q] = ld_stream(as + 16);
+      }
+#pragma unroll
+      for (int q = 0; q < G; ++q) {
+        reg_fence(a[q]);
+        reg_fence(b[q]);
+      }
+#pragma unroll
+      for (int q = 0; q < G; ++q) st_stream(dst_of(g + q) + head + i * 16, funnel16(a[q], b[q], sh));
+    }
+  }
+}
+
+// Pack / unpack with the W ranks' copies of a tile done together, G ranks at
+// a time, each thread keeping at least G 16-byte loads in flight before its
+// first store, so a tile's copies overlap instead of running rank after
+// rank (copy_range, rank by rank, keeps 4).  Needs tensors whose
+// copies share their phases on all ranks (the usual case: every buffer
+// 256-byte aligned); the others take copy_range rank by rank.
+template <int ES, int G>
+__global__ void __launch_bounds__(256, 2) vc_fuse_grouped(const __grid_constant__ FuseParams p) {
+  using B = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
+  __shared__ int64_t s_begin[kFuseMaxTensors + 1];
+  for (int i = threadIdx.x; i <= p.T; i += blockDim.x) s_begin[i] = p.tile_begin[i];
+  __syncthreads();
+  const int64_t total = s_begin[p.T];
+  const int W = p.W;
+  const int tid = threadIdx.x;
+  for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    int lo = 0, hi = p.T - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_begin[mid] <= tile)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int t = lo;
+    const int64_t k = tile - s_begin[t];
+    const int64_t e0 = k * p.tile_elems;
+    const int64_t e1 = e0 + p.tile_elems < p.count[t] ? e0 + p.tile_elems : p.count[t];
+    const int64_t nbytes = (e1 - e0) * ES;
+    const int64_t foff = (p.offset[t] + e0) * ES;
+    auto dst_of = [&](int u) -> char* {
+      return p.unpack ? (char*)p.tensor[t * W + u] + e0 * ES : (char*)p.fused[u] + foff;
+    };
+    auto src_of = [&](int u) -> const char* {
+      return p.unpack ? (const char*)p.fused[u] + foff : (const char*)p.tensor[t * W + u] + e0 * ES;
+    };
+    if (!((p.uniform >> t) & 1u)) {
+      for (int u = 0; u < W; ++u) copy_range<ES>(dst_of(u), src_of(u), nbytes);
+      continue;
+    }
+    // phases shared by every rank: split the range once
+    int64_t head = (int64_t)((16 - ((uint64_t)dst_of(0) & 15)) & 15);
+    if (head > nbytes) head = nbytes;
+    const int64_t body = (nbytes - head) & ~(int64_t)15;
+    const int64_t tail0 = head + body;
+    const int sh = (int)(((uint64_t)src_of(0) + head) & 15);
+    const int64_t nv = body >> 4;
+    {  // head and tail, one element per thread, every rank
+      int64_t off = -1;
+      if ((int64_t)tid * ES < head) off = (int64_t)tid * ES;
+      const int t2 = tid - 32;
+      if (t2 >= 0 && tail0 + (int64_t)t2 * ES < nbytes) off = tail0 + (int64_t)t2 * ES;
+      if (off >= 0)
+        for (int u = 0; u < W; ++u) st1(dst_of(u) + off, ld1<B>(src_of(u) + off));
+    }
+    for (int g = 0; g < W; g += G) fuse_group_body<G>(dst_of, src_of, g, head, nv, sh);
+  }
+}
+
 const void* gather_kernel(int elem_size, int vec) {
   if (elem_size == 4) return vec ? (const void*)&vc_gather<4, true> : (const void*)&vc_gather<4, false>;
   return vec ? (const void*)&vc_gather<2, true> : (const void*)&vc_gather<2, false>;
 }
 
-const void* fuse_kernel(int elem_size) {
-  return elem_size == 4 ? (const void*)&vc_fuse<4> : (const void*)&vc_fuse<2>;
+const void* fuse_kernel(int elem_size, int W) {
+  // G = min(W, 8) ranks per group for W in {2, 4, 8, 16}; any other W rank by rank
+  if (elem_size == 4) {
+    switch (W) {
+      case 2: return (const void*)&vc_fuse_grouped<4, 2>;
+      case 4: return (const void*)&vc_fuse_grouped<4, 4>;
+      case 8: case 16: return (const void*)&vc_fuse_grouped<4, 8>;
+      default: return (const void*)&vc_fuse<4>;
+    }
+  }
+  switch (W) {
+    case 2: return (const void*)&vc_fuse_grouped<2, 2>;
+    case 4: return (const void*)&vc_fuse_grouped<2, 4>;
+    case 8: case 16: return (const void*)&vc_fuse_grouped<2, 8>;
+    default: return (const void*)&vc_fuse<2>;
+  }
 }
 
 }  // namespace vcoll

@@ -73,6 +73,8 @@ struct FuseParams {
   int64_t offset[kFuseMaxTensors];
   int64_t tile_begin[kFuseMaxTensors + 1];
   int64_t tile_elems;
+  uint64_t uniform;  // bit t: every rank's copy of tensor t has the same source
+                     // and destination 16-byte phases (copied for all ranks at once)
   int T;
   int W;
   int unpack;  // 0: tensors -> fused, 1: fused -> tensors
@@ -219,7 +221,7 @@ constexpr int kGatherTmaStages = 4;
 constexpr int kGatherTmaTileBytes = 32768;
 // Device address of the per-device error word (VCOLL_DEVICE_ERR_* bits).
 unsigned int* device_error_symbol();
-const void* fuse_kernel(int elem_size);
+const void* fuse_kernel(int elem_size, int W);
 const void* multi_kernel_f32(int op, int W_t, int ring);
 const void* multi_kernel_bf16(int op, int W_t, int ring);
 

@@ -258,18 +258,28 @@ def test_cuda_graph_capture(v):
 
 # ---------------------------------------------------------------- fusion
 
+# W = 2, 4, 8, 16 copy all ranks of a tile together when the ranks' buffers
+# share their 16-byte phases ("same"), rank by rank otherwise ("mixed": the
+# fused buffers and the tensors of each rank at their own offsets); W = 5
+# always goes rank by rank.
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_fuse_pack_unpack(v, dtype):
-    W = 5
+@pytest.mark.parametrize("W,phases", [(5, "same"), (2, "same"), (4, "same"), (8, "same"),
+                                      (16, "same"), (4, "mixed"), (8, "mixed")])
+def test_fuse_pack_unpack(v, dtype, W, phases):
     rng = np.random.default_rng(3)
-    counts = [int(c) for c in rng.integers(0, 5000, 150)] + [1, 2, 3, 0, 7]
+    counts = [int(c) for c in rng.integers(0, 5000, 150 if W <= 8 else 60)] + [1, 2, 3, 0, 7]
     g = torch.Generator(device="cuda")
     g.manual_seed(3)
-    tens = [[torch.randn(c, generator=g, device="cuda").to(DT[dtype]) for c in counts]
-            for _ in range(W)]
+    if phases == "same":
+        tens = [[torch.randn(c, generator=g, device="cuda").to(DT[dtype]) for c in counts]
+                for _ in range(W)]
+    else:  # each rank's tensors start at their own element offset
+        tens = [[torch.randn(c + 7, generator=g, device="cuda").to(DT[dtype])[(u + t) % 7:(u + t) % 7 + c]
+                 for t, c in enumerate(counts)] for u in range(W)]
     total = sum(counts)
-    fused = [torch.empty(total + 3, dtype=DT[dtype], device="cuda")[1:1 + total]
-             for _ in range(W)]
+    shift = (lambda u: 1) if phases == "same" else (lambda u: u % 8)
+    fused = [torch.empty(total + 8, dtype=DT[dtype], device="cuda")[shift(u):shift(u) + total]
+             for u in range(W)]
     v.fuse_pack(tens, fused)
     want = oracle.fuse_pack([[to_np(t) for t in tens[u]] for u in range(W)], counts, W, ODT[dtype])
     for u in range(W):
