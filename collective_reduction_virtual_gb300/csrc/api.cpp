@@ -292,9 +292,12 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
     prm.cand_cap = cap;
     prm.cand_key = (uint32_t*)(ws + L.cands);
     prm.cand_idx = prm.cand_key + (size_t)W * (size_t)cap;
-    // worth it when the list can hold the 2K-4K entries a sample bound
-    // typically admits; the sample sets no bound when K >= n / 4
-    prm.use_cand = prm.K > 0 && 4 * prm.K < prm.n && cap >= 3 * prm.K;
+    // worth it when the list can hold what the sample typically admits:
+    // 2K-4K entries above a wide lower bound for K < n/4, else a two-sided
+    // band (the K-th key's bin and a few percent of n around it)
+    const bool wide = 4 * prm.K < prm.n && cap >= 3 * prm.K;
+    prm.band = wide ? 0 : 1;
+    prm.use_cand = prm.K > 0 && prm.K < prm.n && (wide || 10 * cap >= prm.n);
   }
   if (topk && prm.K > 0) {
     // histograms, states and candidate counts start at zero

@@ -21,13 +21,16 @@
 //     mode.
 //
 // Candidate path (when the workspace has room): a 1/16 - 1/64 sample of the data
-// gives a first-digit lower bound, one pass over the data appends every
-// entry at or above it to the rank's candidate list as (key, index), and the
+// gives a band of first digits that should hold the K-th key (for small K
+// everything from a wide lower bound up; otherwise also an upper bound, above
+// which entries are only counted), one pass over the data appends every
+// entry in the band to the rank's candidate list as (key, index), and the
 // select passes then read only the list -- three over the key digits and,
 // when keys equal to the K-th one straddle the cut, three over the bits of
 // the inverted index (the K largest (key, -index) pairs are the K entries
-// kept).  A rank whose list overflowed, or holds fewer than K entries, takes
-// the passes over the whole array instead; the choice is made on the device.
+// kept).  A rank whose list overflowed, or whose band misses the K-th key,
+// takes the passes over the whole array instead; the choice is made on the
+// device.
 //
 // The histograms (W x 2048 counters), the per-rank selection state, the
 // per-tile tie counts and the candidate lists live in a device workspace the
@@ -241,8 +244,10 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
 // MODE 0, 1, 2: after the histogram pass of that digit (MODE 0 flags a redo
 //   when the bins counted from state.low up hold fewer than K keys);
 // MODE 3: after the sample pass: state.low = the highest bin whose sampled
-//   suffix holds twice the keys K calls for (scaled to the sample) plus a
-//   margin, or 0 (count everything) when K is a large fraction of n;
+//   suffix holds comfortably more keys than K calls for (scaled to the
+//   sample), 0 (count everything) when none does; with a band also
+//   state.high = the highest bin with comfortably fewer than that strictly
+//   above it (entries above it are kept without being listed), else 2047;
 // MODE 4: after the redo pass, for ranks that needed it;
 // MODE 5, 6, 7: after index pass 3, 4, 5 over the candidates equal to T, for
 //   ranks on the candidate path whose equal keys straddle the cut; the last
@@ -282,12 +287,27 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
   const unsigned long long total = warp_sum[31];
   constexpr int P = (MODE == 1 || MODE == 2) ? MODE : 0;
   long long rem;
+  long long rhi = 0;  // MODE 3: sampled keys allowed strictly above the band
   if (MODE == 3) {
-    // sampled keys wanted above the bound: twice K's share of the sample,
-    // plus a margin; no bound when K is a quarter of n or more
-    rem = 4 * p.K >= p.n ? -1 : 2 * ((p.K + p.sample_stride - 1) / p.sample_stride) + 64;
+    // K's share of the sample; keys wanted at or above the lower bound: twice
+    // that plus 64 (wide bound), or that plus a margin -- a few standard
+    // deviations, at least 1/16 of the smaller tail -- with an upper bound
+    // the same margin below it (band); nothing when K = n
+    const long long ks = (long long)(((unsigned long long)p.K * total) / (unsigned long long)p.n);
+    if (p.K >= p.n) {
+      rem = -1;
+    } else if (!p.band) {
+      rem = 2 * ks + 64;
+    } else {
+      const long long tail = min(ks, (long long)total - ks);
+      const long long m = max((long long)(4.0f * sqrtf((float)tail)) + 64, tail / 16);
+      rem = ks + m;
+      rhi = ks - m;
+    }
   } else if (MODE == 5) {
     rem = st->need;
+  } else if (MODE == 0) {  // on the candidate path the band's share of K
+    rem = p.K - (p.use_cand ? (long long)p.cand_n[p.W + r] : 0ll);
   } else {
     rem = (P == 0 && MODE < 5) ? p.K : st->remaining;
   }
@@ -297,9 +317,12 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
     if (t == 0 && (rem < 0 || (long long)total < rem)) st->low = 0;
     if (rem >= 0 && (long long)total >= rem && (long long)above < rem && rem <= (long long)incl)
       st->low = (uint32_t)((long long)(above + c0) >= rem ? b0 : b1);
+    if (t == 0 && (rhi <= 0 || (long long)total < rhi)) st->high = kTopkBins - 1;
+    if (rhi > 0 && (long long)total >= rhi && (long long)above < rhi && rhi <= (long long)incl)
+      st->high = (uint32_t)((long long)(above + c0) >= rhi ? b0 : b1);
     if (t == 0) st->redo = 0;
-  } else if (MODE == 0 && (long long)total < rem) {
-    if (t == 0) {  // the bound was too high (or the list overflowed): count every bin again
+  } else if (MODE == 0 && (rem <= 0 || (long long)total < rem)) {
+    if (t == 0) {  // a bound missed the K-th key (or the list overflowed): count every bin again
       st->redo = 1;
       st->full = 1;
     }
@@ -461,8 +484,9 @@ __global__ void __launch_bounds__(1024) vc_topk_tie_find(const __grid_constant__
 
 // ------------------------------------------------------------ candidates
 // One pass over the data (grid.y = rank, one tile per CTA iteration): every
-// entry whose key is at or above the sample's first-digit bound is appended
-// to the rank's candidate list as (key, index).  Each thread looks at 16
+// entry whose first digit lies in the sample's band [low, high] is appended
+// to the rank's candidate list as (key, index), and the entries above the
+// band are counted (they are kept whatever the K-th key).  Each thread looks at 16
 // entries of the tile (four 16-byte vectors, all loaded before the first is
 // used) plus at most one of the tile's unaligned head or tail; a warp-wide
 // scan of the per-thread counts places every candidate, one shared atomic
@@ -475,19 +499,25 @@ __global__ void __launch_bounds__(1024) vc_topk_tie_find(const __grid_constant__
 __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ SparseParams p) {
   constexpr int E = 4 * kTileVecs;  // entries per thread and tile (plus one extra)
   __shared__ __align__(16) uint32_t s_key[kSparseThreads * E];
-  __shared__ uint32_t s_n;
+  __shared__ uint32_t s_n, s_sure;
   __shared__ unsigned long long s_base;
   const int r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31;
+  // candidates: keys in [lowkey, topkey]; keys above topkey are kept for sure
   const uint32_t lowkey = p.state[r].low << 21;
+  const uint32_t topkey = (uint32_t)((((uint64_t)p.state[r].high + 1) << 21) - 1);
   uint32_t* ckey = p.cand_key + (int64_t)r * p.cand_cap;
   uint32_t* cidx = p.cand_idx + (int64_t)r * p.cand_cap;
   uint32_t* my = s_key + tid * E;
   for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x) {
     const int64_t t0 = tile * p.tile_elems;
     const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
-    if (tid == 0) s_n = 0;
+    if (tid == 0) {
+      s_n = 0;
+      s_sure = 0;
+    }
     uint32_t mask = 0;  // bit j < E: entry j is a candidate
+    int sure = 0;       // entries above the band
     uint32_t xkey = 0;  // the extra entry (head or tail)
     bool xhit = false;
     int64_t av = t0, extra = -1;
@@ -506,8 +536,11 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
         k4.z = order_key(x[u][2]);
         k4.w = order_key(x[u][3]);
         if (tid + u * kSparseThreads < nv) {
-          mask |= (uint32_t)(k4.x >= lowkey) << (u * 4) | (uint32_t)(k4.y >= lowkey) << (u * 4 + 1) |
-                  (uint32_t)(k4.z >= lowkey) << (u * 4 + 2) | (uint32_t)(k4.w >= lowkey) << (u * 4 + 3);
+          mask |= (uint32_t)(k4.x >= lowkey && k4.x <= topkey) << (u * 4) |
+                  (uint32_t)(k4.y >= lowkey && k4.y <= topkey) << (u * 4 + 1) |
+                  (uint32_t)(k4.z >= lowkey && k4.z <= topkey) << (u * 4 + 2) |
+                  (uint32_t)(k4.w >= lowkey && k4.w <= topkey) << (u * 4 + 3);
+          sure += (k4.x > topkey) + (k4.y > topkey) + (k4.z > topkey) + (k4.w > topkey);
         }
         reinterpret_cast<uint4*>(my)[u] = k4;
       }
@@ -521,14 +554,16 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
         uint32_t k = 0;
         if (i < t1) {
           k = order_key(load_x(p, r, i));
-          mask |= (uint32_t)(k >= lowkey) << j;
+          mask |= (uint32_t)(k >= lowkey && k <= topkey) << j;
+          sure += k > topkey;
         }
         my[j] = k;
       }
     }
     if (extra >= 0) {
       xkey = order_key(load_x(p, r, extra));
-      xhit = xkey >= lowkey;
+      xhit = xkey >= lowkey && xkey <= topkey;
+      sure += xkey > topkey;
     }
     // this thread's place among the warp's candidates
     const int c = __popc(mask) + (xhit ? 1 : 0);
@@ -538,14 +573,17 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
       if (lane >= o) incl += y;
     }
     const int wtotal = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    __syncthreads();  // s_n is zero
+    const unsigned wsure = __reduce_add_sync(0xFFFFFFFFu, (unsigned)sure);
+    __syncthreads();  // s_n and s_sure are zero
     uint32_t wbase = 0;
     if (lane == 31 && wtotal) wbase = atomicAdd(&s_n, (uint32_t)wtotal);
+    if (lane == 0 && wsure) atomicAdd(&s_sure, wsure);
     wbase = __shfl_sync(0xFFFFFFFFu, wbase, 31);
     __syncthreads();  // every warp has reserved its share of the tile's room
     if (tid == 0) {
       const uint32_t tot = s_n;
       s_base = tot ? atomicAdd(p.cand_n + r, (unsigned long long)tot) : 0ull;
+      if (s_sure) atomicAdd(p.cand_n + p.W + r, (unsigned long long)s_sure);
     }
     __syncthreads();
     unsigned long long pos = s_base + wbase + (uint32_t)(incl - c);

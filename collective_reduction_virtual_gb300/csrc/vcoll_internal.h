@@ -128,6 +128,8 @@ struct TopkState {
   int64_t equal;      // entries equal to T
   int64_t boundary;   // equal entries with index <= boundary are kept
   uint32_t low;       // first-digit bins below this one are not counted
+  uint32_t high;      // candidate path: first-digit bins above this one are
+                      // kept without selection (counted, not listed)
   int redo;           // the first-digit pass must be repeated over all bins
   int full;           // this rank's select passes read the whole array (its
                       // candidate list overflowed or missed the K-th key)
@@ -140,11 +142,14 @@ struct SparseParams {
   uint32_t* hist;              // workspace: W x kTopkBins
   TopkState* state;            // workspace: W entries
   uint32_t* tilecnt;           // workspace: W x tiles_per_rank (tie counts)
-  unsigned long long* cand_n;  // workspace: W candidate counts
+  unsigned long long* cand_n;  // workspace: W candidate counts, then W counts of
+                               // entries above the candidate band
   uint32_t* cand_key;          // workspace: W x cand_cap candidate keys
   uint32_t* cand_idx;          // workspace: W x cand_cap candidate indices
   int64_t cand_cap;            // candidate list capacity per rank
   int use_cand;                // select passes after the first read candidates
+  int band;                    // the sample sets a two-sided band (else a lower
+                               // bound with a wide margin)
   int sample_stride;           // the sample pass reads every sample_stride-th tile
   int64_t n;
   int64_t tiles_per_rank;      // histogram passes: grid.y = rank
@@ -171,13 +176,14 @@ inline TopkLayout topk_layout(int W, int64_t n) {
   TopkLayout L;
   L.state = al((size_t)W * kTopkBins * sizeof(uint32_t));
   L.cand_n = al(L.state + (size_t)W * sizeof(TopkState));
-  L.tilecnt = al(L.cand_n + (size_t)W * sizeof(unsigned long long));
+  L.tilecnt = al(L.cand_n + 2 * (size_t)W * sizeof(unsigned long long));
   L.cands = al(L.tilecnt + (size_t)W * (size_t)(tiles > 0 ? tiles : 1) * sizeof(uint32_t));
   return L;
 }
 inline size_t topk_workspace_min_bytes(int W, int64_t n) { return topk_layout(W, n).cands; }
 // candidates per rank the recommended workspace holds: an eighth of the
-// entries (top-K fractions up to about 4 % stay on the candidate path), all
+// entries (room for K up to about n/24 above a lower bound, and for the
+// two-sided band of larger K), all
 // of them for small arrays; a multiple of 4 so that both lists stay 16-byte
 // aligned
 inline int64_t topk_cand_cap_default(int64_t n) {

@@ -719,6 +719,7 @@ def test_sparse_topk_sample_bound_redo(v):
         tiles[::16] = tiles[::16].abs() + 100.0
     _check_sparse(v, ins, None, 0.01, True)
     _check_sparse(v, ins, [torch.zeros(n, device="cuda") for _ in range(W)], 0.2, True)
+    _check_sparse(v, ins, None, 0.4, True)  # the band (K >= n/4) misses as well
 
 
 # The top-K select runs over candidate lists when the workspace has room for
@@ -747,6 +748,9 @@ def test_sparse_topk_candidate_list_overflows(v):
         tiles[::16] *= 1e-6
     _check_sparse(v, ins, None, 0.01, True)
     _check_sparse(v, ins, [torch.zeros(n, device="cuda") for _ in range(W)], 0.03, True)
+    # K >= n/4: the band's upper bound sits among the tiny sampled values, so
+    # far more than K entries lie above it
+    _check_sparse(v, ins, None, 0.3, True)
 
 
 def test_sparse_topk_mixed_routes_in_one_call(v):
@@ -764,6 +768,21 @@ def test_sparse_topk_mixed_routes_in_one_call(v):
     mid = (v.sparse_workspace_min_bytes(W, n) + v.sparse_workspace_bytes(W, n)) // 2
     _check_sparse(v, ins, [torch.zeros(n, device="cuda") for _ in range(W)], 0.01, True,
                   workspace_bytes=mid)
+    # K >= n/4: a band with an upper bound on the ranks whose sample holds
+    _check_sparse(v, ins, None, 0.3, True)
+    _check_sparse(v, ins, None, 0.6, True, workspace_bytes=mid)
+
+
+# K beyond what the lists hold above a wide lower bound (3K > n/8 + 4096):
+# the sample sets a two-sided band, entries above it are only counted
+@pytest.mark.parametrize("frac", [0.05, 0.1, 0.25, 0.3, 0.5, 0.9, 0.999])
+def test_sparse_topk_large_k_band(v, frac):
+    W, n = 4, 256 * 4096 + 3
+    ins = _sparse_inputs(W, n, 70)
+    acc = [t * 0.3 for t in _sparse_inputs(W, n, 71)]
+    _check_sparse(v, ins, acc, frac, True)
+    ins = [torch.round(t * 8) / 8 for t in ins]  # ties at the K-th key
+    _check_sparse(v, ins, None, frac, True)
 
 
 def test_sparse_topk_all_equal_values(v):
