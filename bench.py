@@ -328,11 +328,13 @@ def build_workload(args, dev, rank):
         if topk:
             # 13 kernels over the whole array; 22 on the candidate path, which
             # the library takes when the lists hold 3K entries (K < n/4) or a
-            # tenth of the array (a two-sided band)
+            # tenth of the array (a two-sided band), 23 when the lists also
+            # give the output
             K = math.ceil(frac * n)
             cap = ((n // 8 + 4096 if n // 8 + 4096 < n else n) + 3) & ~3
-            cand = 0 < K < n and ((4 * K < n and cap >= 3 * K) or 10 * cap >= n)
-            launches = 22 if cand else 13
+            wide = 4 * K < n and cap >= 3 * K  # lower bound only: output from the lists
+            cand = 0 < K < n and (wide or 10 * cap >= n)
+            launches = (23 if wide else 22) if cand else 13
         return dict(name=f"{what}, W={W}, f32, n={n} per rank", W=W, n=n, step=step,
                     bytes=bytes_, launches=launches, ins=ins,
                     outs=outs, es=4, reduction=red, dtype="f32")

@@ -286,11 +286,13 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
     prm.tilecnt = (uint32_t*)(ws + L.tilecnt);
     // candidate lists in what is left (a multiple of 4 entries per rank keeps
     // the index list 16-byte aligned)
-    const size_t spare = workspace_bytes > L.cands ? workspace_bytes - L.cands : 0;
+    const size_t lists = L.cands + L.chunk_bytes;
+    const size_t spare = workspace_bytes > lists ? workspace_bytes - lists : 0;
     int64_t cap = (int64_t)(spare / ((size_t)W * 8));
     cap = std::min<int64_t>(cap, topk_cand_cap_default(prm.n)) & ~(int64_t)3;
     prm.cand_cap = cap;
-    prm.cand_key = (uint32_t*)(ws + L.cands);
+    prm.chunk = (uint32_t*)(ws + L.cands);
+    prm.cand_key = (uint32_t*)(ws + lists);
     prm.cand_idx = prm.cand_key + (size_t)W * (size_t)cap;
     // worth it when the list can hold what the sample typically admits:
     // 2K-4K entries above a wide lower bound for K < n/4, else a two-sided
@@ -298,6 +300,9 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
     const bool wide = 4 * prm.K < prm.n && cap >= 3 * prm.K;
     prm.band = wide ? 0 : 1;
     prm.use_cand = prm.K > 0 && prm.K < prm.n && (wide || 10 * cap >= prm.n);
+    // with a wide lower bound the lists hold every kept entry (unless a rank
+    // falls back), so the result can be built from them
+    prm.list_out = prm.use_cand && !prm.band;
   }
   if (topk && prm.K > 0) {
     // histograms, states and candidate counts start at zero
@@ -326,8 +331,10 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
       return rc;
     if (prm.use_cand) {
       // one pass collects the candidates, the first digit from the lists
-      if ((rc = run(topk_filter_kernel(), every, 256)) ||
-          (rc = run(topk_cand_hist_kernel(0), few, 256)) ||
+      if ((rc = run(topk_filter_kernel(), every, 256))) return rc;
+      // the candidate pass stored x = in + acc in acc: later passes read acc
+      prm.x_in_acc = prm.has_acc;
+      if ((rc = run(topk_cand_hist_kernel(0), few, 256)) ||
           (rc = run(topk_select_kernel(0), sgrid, 1024)))
         return rc;
     } else {
@@ -363,6 +370,10 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
   void* args[] = {&prm};
   cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(256), args, 0, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse apply launch");
+  if (topk && prm.list_out) {  // the result from the lists (decided on the device)
+    e = cudaLaunchKernel(topk_list_out_kernel(), dim3((unsigned)grid), dim3(256), args, 0, st);
+    if (e != cudaSuccess) return cuda_fail(e, "top-K output launch");
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "sparse allreduce");
   return VCOLL_OK;

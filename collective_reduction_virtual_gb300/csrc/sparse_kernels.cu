@@ -48,8 +48,10 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// x = in (+ accumulation), one element
+// x = in (+ accumulation), one element (the accumulation alone once the
+// candidate pass has stored x there)
 __device__ __forceinline__ float load_x(const SparseParams& p, int r, int64_t i) {
+  if (p.x_in_acc) return __uint_as_float(ld1<uint32_t>((const char*)p.acc[r] + i * 4));
   float x = __uint_as_float(ld1<uint32_t>((const char*)p.in[r] + i * 4));
   if (p.has_acc) x = __fadd_rn(x, __uint_as_float(ld1<uint32_t>((const char*)p.acc[r] + i * 4)));
   return x;
@@ -57,12 +59,12 @@ __device__ __forceinline__ float load_x(const SparseParams& p, int r, int64_t i)
 
 // the same for a 16-byte vector of four elements
 __device__ __forceinline__ void load_x4(const SparseParams& p, int r, int64_t i, float (&x)[4]) {
-  const uint4 a = ld_stream((const char*)p.in[r] + i * 4);
+  const uint4 a = ld_stream((const char*)(p.x_in_acc ? p.acc[r] : p.in[r]) + i * 4);
   x[0] = __uint_as_float(a.x);
   x[1] = __uint_as_float(a.y);
   x[2] = __uint_as_float(a.z);
   x[3] = __uint_as_float(a.w);
-  if (p.has_acc) {
+  if (p.has_acc && !p.x_in_acc) {
     const uint4 b = ld_stream((const char*)p.acc[r] + i * 4);
     x[0] = __fadd_rn(x[0], __uint_as_float(b.x));
     x[1] = __fadd_rn(x[1], __uint_as_float(b.y));
@@ -90,8 +92,8 @@ __device__ __forceinline__ void load_tile_x(const SparseParams& p, int r, int64_
     a[u] = make_uint4(0u, 0u, 0u, 0u);
     b[u] = make_uint4(0u, 0u, 0u, 0u);
     if (v < nv) {
-      a[u] = ld_stream((const char*)p.in[r] + (av + v * 4) * 4);
-      if (p.has_acc) b[u] = ld_stream((const char*)p.acc[r] + (av + v * 4) * 4);
+      a[u] = ld_stream((const char*)(p.x_in_acc ? p.acc[r] : p.in[r]) + (av + v * 4) * 4);
+      if (p.has_acc && !p.x_in_acc) b[u] = ld_stream((const char*)p.acc[r] + (av + v * 4) * 4);
     }
   }
 #pragma unroll
@@ -105,7 +107,7 @@ __device__ __forceinline__ void load_tile_x(const SparseParams& p, int r, int64_
     x[u][1] = __uint_as_float(a[u].y);
     x[u][2] = __uint_as_float(a[u].z);
     x[u][3] = __uint_as_float(a[u].w);
-    if (p.has_acc) {
+    if (p.has_acc && !p.x_in_acc) {
       x[u][0] = __fadd_rn(x[u][0], __uint_as_float(b[u].x));
       x[u][1] = __fadd_rn(x[u][1], __uint_as_float(b[u].y));
       x[u][2] = __fadd_rn(x[u][2], __uint_as_float(b[u].z));
@@ -486,7 +488,9 @@ __global__ void __launch_bounds__(1024) vc_topk_tie_find(const __grid_constant__
 // One pass over the data (grid.y = rank, one tile per CTA iteration): every
 // entry whose first digit lies in the sample's band [low, high] is appended
 // to the rank's candidate list as (key, index), and the entries above the
-// band are counted (they are kept whatever the K-th key).  Each thread looks at 16
+// band are counted (they are kept whatever the K-th key).  With an
+// accumulation, x = in + acc is stored back into acc, so that every later
+// pass reads one array instead of two.  Each thread looks at 16
 // entries of the tile (four 16-byte vectors, all loaded before the first is
 // used) plus at most one of the tile's unaligned head or tail; a warp-wide
 // scan of the per-thread counts places every candidate, one shared atomic
@@ -528,6 +532,13 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
       const int64_t nv = (bv - av) / 4;
       float x[kTileVecs][4];
       load_tile_x(p, r, av, nv, x);
+      if (p.has_acc)  // later passes read x from the accumulation
+#pragma unroll
+        for (int u = 0; u < kTileVecs; ++u)
+          if (tid + u * kSparseThreads < nv)
+            st_stream((char*)p.acc[r] + (av + (int64_t)(tid + u * kSparseThreads) * 4) * 4,
+                      make_uint4(__float_as_uint(x[u][0]), __float_as_uint(x[u][1]),
+                                 __float_as_uint(x[u][2]), __float_as_uint(x[u][3])));
 #pragma unroll
       for (int u = 0; u < kTileVecs; ++u) {
         uint4 k4;
@@ -553,7 +564,9 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
         const int64_t i = t0 + tid + (int64_t)j * kSparseThreads;
         uint32_t k = 0;
         if (i < t1) {
-          k = order_key(load_x(p, r, i));
+          const float x = load_x(p, r, i);
+          if (p.has_acc) st1((char*)p.acc[r] + i * 4, __float_as_uint(x));
+          k = order_key(x);
           mask |= (uint32_t)(k >= lowkey && k <= topkey) << j;
           sure += k > topkey;
         }
@@ -561,7 +574,9 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
       }
     }
     if (extra >= 0) {
-      xkey = order_key(load_x(p, r, extra));
+      const float x = load_x(p, r, extra);
+      if (p.has_acc) st1((char*)p.acc[r] + extra * 4, __float_as_uint(x));
+      xkey = order_key(x);
       xhit = xkey >= lowkey && xkey <= topkey;
       sure += xkey > topkey;
     }
@@ -584,6 +599,10 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
       const uint32_t tot = s_n;
       s_base = tot ? atomicAdd(p.cand_n + r, (unsigned long long)tot) : 0ull;
       if (s_sure) atomicAdd(p.cand_n + p.W + r, (unsigned long long)s_sure);
+      // where this tile's entries sit in the list (read by the output pass
+      // of the list route; the start only matters below the capacity)
+      p.tilecnt[(int64_t)r * p.tiles_per_rank + tile] = tot;
+      p.chunk[(int64_t)r * p.tiles_per_rank + tile] = (uint32_t)s_base;
     }
     __syncthreads();
     unsigned long long pos = s_base + wbase + (uint32_t)(incl - c);
@@ -677,6 +696,107 @@ __global__ void __launch_bounds__(256) vc_topk_cand_hist(const __grid_constant__
     if (h[i]) atomicAdd(&p.hist[(int64_t)r * kTopkBins + i], h[i]);
 }
 
+// ------------------------------------------------------------- list route
+// The result comes from the candidate lists when every rank's K kept entries
+// are listed: the lists were usable (no rank sent to the whole-array
+// passes) and had no entries above the band.  Uniform over the grid.  The
+// output pass then reads, per tile, each rank's list entries of that tile
+// instead of the whole arrays.  (Only once every select has run.)
+__device__ __forceinline__ bool list_route(const SparseParams& p) {
+  if (!p.list_out) return false;
+  for (int r = 0; r < p.W; ++r)
+    if (p.state[r].full) return false;
+  return true;
+}
+
+// inverse of order_key
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// List route output pass (one CTA per tile; the dense apply pass returns at
+// once on this route): the lists hold every kept entry, grouped by tile, so
+// each tile's kept entries are folded into zeros in shared memory, rank after
+// rank, their accumulations (which hold x) become x - (0 + x), and the tile
+// is written to every output.  Each thread loads its entry of four ranks'
+// chunks before folding them, so a tile costs one round trip for the chunk
+// bounds and one per four ranks for the entries.
+__global__ void __launch_bounds__(256) vc_topk_list_out(const __grid_constant__ SparseParams p) {
+  if (!list_route(p)) return;
+  __shared__ uint32_t s_T[VCOLL_MAX_RANKS];
+  __shared__ long long s_bound[VCOLL_MAX_RANKS];
+  const int W = p.W;
+  const int tid = threadIdx.x;
+  for (int r = tid; r < W; r += blockDim.x) {
+    s_T[r] = p.state[r].T;
+    s_bound[r] = p.state[r].boundary;
+  }
+  __syncthreads();
+  constexpr int R = 4;  // ranks whose list entries are loaded together
+  // the tile's sums, shifted by pad (0-3) so that the aligned body starts on
+  // a 16-byte boundary of shared memory
+  __shared__ __align__(16) float s_res[kSparseTileElems + 4];
+  __shared__ uint32_t s_cnt4[VCOLL_MAX_RANKS];
+  __shared__ int64_t s_c0[VCOLL_MAX_RANKS];
+  for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    const int64_t t0 = tile * p.tile_elems;
+    const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
+    int64_t av = t0, bv = t0;
+    if (p.phase >= 0) aligned_body<4>(t0, t1, p.phase, av, bv);
+    const int64_t base = t0 - ((4 - ((av - t0) & 3)) & 3);  // s_res[i - base] holds entry i
+    for (int j = tid; j < kSparseTileElems + 4; j += blockDim.x) s_res[j] = 0.0f;
+    for (int r = tid; r < W; r += blockDim.x) {
+      s_cnt4[r] = p.tilecnt[(int64_t)r * p.tiles_per_rank + tile];
+      s_c0[r] = (int64_t)r * p.cand_cap + p.chunk[(int64_t)r * p.tiles_per_rank + tile];
+    }
+    __syncthreads();
+    auto fold = [&](int r, uint32_t key, int64_t idx) {
+      if (key > s_T[r] || (key == s_T[r] && idx <= s_bound[r])) {
+        const float x = key_value(key);
+        s_res[idx - base] = __fadd_rn(x, s_res[idx - base]);
+        if (p.has_acc)
+          st1((char*)p.acc[r] + idx * 4, __float_as_uint(__fsub_rn(x, __fadd_rn(0.0f, x))));
+      }
+    };
+    for (int g = 0; g < W; g += R) {
+      // entry tid of the chunks of ranks g .. g + R - 1, loaded together
+      uint32_t pk[R];
+      int64_t pi[R];
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        pk[q] = 0;
+        pi[q] = -1;
+        if (g + q < W && (uint32_t)tid < s_cnt4[g + q]) {
+          pk[q] = p.cand_key[s_c0[g + q] + tid];
+          pi[q] = p.cand_idx[s_c0[g + q] + tid];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        const int r = g + q;
+        if (r >= W) break;
+        if (pi[q] >= 0) fold(r, pk[q], pi[q]);
+        for (uint32_t j = tid + blockDim.x; j < s_cnt4[r]; j += blockDim.x)
+          fold(r, p.cand_key[s_c0[r] + j], p.cand_idx[s_c0[r] + j]);
+        __syncthreads();  // rank order: rank r's adds land before rank r + 1's
+      }
+    }
+    const int64_t nv = (bv - av) / 4;
+    for (int64_t v = tid; v < nv; v += blockDim.x) {
+      const uint4 o = *reinterpret_cast<const uint4*>(&s_res[av + v * 4 - base]);
+      for (int u = 0; u < W; ++u) st_stream((char*)p.out[u] + (av + v * 4) * 4, o);
+    }
+    const int64_t head = av - t0, tail = t1 - bv;
+    for (int64_t j = tid; j < head + tail; j += blockDim.x) {
+      const int64_t i = j < head ? t0 + j : bv + (j - head);
+      for (int u = 0; u < W; ++u) st1((char*)p.out[u] + i * 4, __float_as_uint(s_res[i - base]));
+    }
+    __syncthreads();  // s_res is reused by the next tile
+  }
+  if (p.nnz && blockIdx.x == 0)
+    for (int r = tid; r < W; r += blockDim.x) p.nnz[r] = p.K;  // exactly K kept per rank
+}
+
 // -------------------------------------------------------------------- apply
 // One pass: survivors, error feedback, rank-order sum written to every rank,
 // survivor counts per rank.
@@ -711,6 +831,7 @@ __global__ void __launch_bounds__(256) vc_sparse_apply(const __grid_constant__ S
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
     if ((tid & 31) == 0 && c) atomicAdd(&s_cnt[r], (unsigned long long)c);
   };
+  if (TOPK && list_route(p)) return;  // vc_topk_list_out writes the result
   for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
     const int64_t t0 = tile * p.tile_elems;
     const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
@@ -796,6 +917,7 @@ const void* topk_select_kernel(int pass) {
                    : pass == 1 ? (const void*)&vc_topk_select<1> : (const void*)&vc_topk_select<2>;
 }
 const void* topk_filter_kernel() { return (const void*)&vc_topk_filter; }
+const void* topk_list_out_kernel() { return (const void*)&vc_topk_list_out; }
 const void* topk_cand_hist_kernel(int pass) {
   switch (pass) {
     case 0: return (const void*)&vc_topk_cand_hist<0>;

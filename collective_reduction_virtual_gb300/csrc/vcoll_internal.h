@@ -141,7 +141,10 @@ struct SparseParams {
   int64_t* nnz;                // device, W counters (may be NULL)
   uint32_t* hist;              // workspace: W x kTopkBins
   TopkState* state;            // workspace: W entries
-  uint32_t* tilecnt;           // workspace: W x tiles_per_rank (tie counts)
+  uint32_t* tilecnt;           // workspace: W x tiles_per_rank (tie counts, or
+                               // on the candidate path each tile's list entries)
+  uint32_t* chunk;             // workspace: W x tiles_per_rank, where each tile's
+                               // entries start in its rank's list
   unsigned long long* cand_n;  // workspace: W candidate counts, then W counts of
                                // entries above the candidate band
   uint32_t* cand_key;          // workspace: W x cand_cap candidate keys
@@ -159,16 +162,21 @@ struct SparseParams {
   int W;
   int phase;                   // 16-byte phase shared by every buffer, or -1
   int has_acc;
+  int x_in_acc;                // acc already holds x = in + acc (written by the
+                               // top-K candidate pass): later passes read acc alone
+  int list_out;                // top-K: the result may come from the candidate lists
   float threshold;
 };
 constexpr int64_t kSparseTileElems = 4096;
 // Top-K working memory, regions 256-byte aligned: histograms, states,
 // candidate counts and per-tile tie counts (together the minimum a call
-// needs), then the candidate lists: cand_cap keys and cand_cap indices per
-// rank.  With room for candidates one pass over the data collects every entry
-// above the sample's lower bound, and the later select passes read only those.
+// needs), then per-tile list offsets and the candidate lists: cand_cap keys
+// and cand_cap indices per rank.  With room for candidates one pass over the
+// data collects every entry in the sample's band, and the later select
+// passes read only those.
 struct TopkLayout {
   size_t state, cand_n, tilecnt, cands;  // byte offsets; cands = the minimum size
+  size_t chunk_bytes;                    // per-tile list offsets (start of the lists' room)
 };
 inline TopkLayout topk_layout(int W, int64_t n) {
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
@@ -178,6 +186,7 @@ inline TopkLayout topk_layout(int W, int64_t n) {
   L.cand_n = al(L.state + (size_t)W * sizeof(TopkState));
   L.tilecnt = al(L.cand_n + 2 * (size_t)W * sizeof(unsigned long long));
   L.cands = al(L.tilecnt + (size_t)W * (size_t)(tiles > 0 ? tiles : 1) * sizeof(uint32_t));
+  L.chunk_bytes = al((size_t)W * (size_t)(tiles > 0 ? tiles : 1) * sizeof(uint32_t));
   return L;
 }
 inline size_t topk_workspace_min_bytes(int W, int64_t n) { return topk_layout(W, n).cands; }
@@ -192,7 +201,8 @@ inline int64_t topk_cand_cap_default(int64_t n) {
   return (c + 3) & ~(int64_t)3;
 }
 inline size_t topk_workspace_bytes(int W, int64_t n) {
-  return topk_workspace_min_bytes(W, n) + (size_t)W * (size_t)topk_cand_cap_default(n) * 8;
+  const TopkLayout L = topk_layout(W, n);
+  return L.cands + L.chunk_bytes + (size_t)W * (size_t)topk_cand_cap_default(n) * 8;
 }
 
 const void* selftest_timeout_kernel();
@@ -218,6 +228,7 @@ const void* topk_redo_hist_kernel();
 const void* topk_redo_select_kernel();
 const void* topk_select_kernel(int pass);
 const void* topk_filter_kernel();
+const void* topk_list_out_kernel();
 const void* topk_cand_hist_kernel(int pass);  // 0-2 key digits, 3-5 index digits
 const void* topk_index_select_kernel(int pass);  // 3-5
 const void* topk_tie_count_kernel();

@@ -240,10 +240,11 @@ def test_sparse_allreduce_errors(v):
     least = v.vcoll_sparse_workspace_min_bytes(8, 64, 1)
     assert need >= least >= 8 * 2048 * 4
     assert v.vcoll_sparse_workspace_min_bytes(8, 64, 0) == 0
-    # the recommended size adds two candidate lists of (up to) n entries per rank
+    # the recommended size adds, per rank, a list offset per tile of 4096
+    # entries and two candidate lists of (up to) n entries
     assert need - least >= 8 * 64 * 8
     big = v.vcoll_sparse_workspace_bytes(8, 1 << 26, 1) - v.vcoll_sparse_workspace_min_bytes(8, 1 << 26, 1)
-    assert big == 8 * 8 * ((1 << 26) // 8 + 4096)
+    assert big == 8 * 4 * ((1 << 26) // 4096) + 8 * 8 * ((1 << 26) // 8 + 4096)
     ins, outs = FAKE_IN[:4], FAKE_OUT[:4]
     assert f(ins, outs, None, 0, 64, 0.5, 0) == v.ERR_INVALID_ARG
     assert f(ins, outs, None, 4, -1, 0.5, 0) == v.ERR_INVALID_ARG
