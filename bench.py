@@ -521,8 +521,10 @@ def extras(args, stream, dev):
     out["sparse_topk1pct_w8_f32_2^26"] = rate(
         lambda: vc.sparse_allreduce(ins, outs, acc, 0.01, True, nnz, ws), 4 * W * n * 4)
     out["sparse_bytes_formula"] = ("4*W*n*4: read inputs and accumulations, write outputs and "
-                                   "accumulations (top-K also reads them once more to collect "
-                                   "its select candidates, plus a 1/16 to 1/64 sample)")
+                                   "accumulations (top-K: a 1/16 to 1/64 sample, a candidate "
+                                   "pass that reads both and writes x to the accumulation, and "
+                                   "for small K an output pass from the candidate lists, else "
+                                   "the dense pass reading the accumulation)")
     del ins, outs, segs, acc
     torch.cuda.empty_cache()
 
