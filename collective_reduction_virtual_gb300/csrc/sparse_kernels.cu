@@ -718,9 +718,9 @@ __device__ __forceinline__ float key_value(uint32_t key) {
 // once on this route): the lists hold every kept entry, grouped by tile, so
 // each tile's kept entries are folded into zeros in shared memory, rank after
 // rank, their accumulations (which hold x) become x - (0 + x), and the tile
-// is written to every output.  Each thread loads its entry of four ranks'
+// is written to every output.  Each thread loads its entry of eight ranks'
 // chunks before folding them, so a tile costs one round trip for the chunk
-// bounds and one per four ranks for the entries.
+// bounds and one per eight ranks for the entries.
 __global__ void __launch_bounds__(256) vc_topk_list_out(const __grid_constant__ SparseParams p) {
   if (!list_route(p)) return;
   __shared__ uint32_t s_T[VCOLL_MAX_RANKS];
@@ -732,7 +732,7 @@ __global__ void __launch_bounds__(256) vc_topk_list_out(const __grid_constant__ 
     s_bound[r] = p.state[r].boundary;
   }
   __syncthreads();
-  constexpr int R = 4;  // ranks whose list entries are loaded together
+  constexpr int R = 8;  // ranks whose list entries are loaded together
   // the tile's sums, shifted by pad (0-3) so that the aligned body starts on
   // a 16-byte boundary of shared memory
   __shared__ __align__(16) float s_res[kSparseTileElems + 4];
