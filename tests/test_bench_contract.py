@@ -1,0 +1,44 @@
+"""The benchmark's JSON line, checked on the CPU: the reference arm (the oracle
+timed on host cores) prints one line with the keys the benchmark contract
+names, and the host-side helpers that combine ranks behave as documented."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*args):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                       capture_output=True, text=True, cwd=ROOT, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    return json.loads(lines[0])
+
+
+def test_reference_arm_line_has_the_contract_keys():
+    d = _run("--impl", "reference", "--steps", "2", "--warmup", "1", "--ref-elems", "4096")
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference"
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["n_gpus"] == 1
+    assert d["higher_is_better"] is True and d["unit"] == "GB/s"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert "workload" in d["config"] and "model" not in d["config"]
+
+
+def test_reference_arm_value_counts_the_allreduce_bytes():
+    # value = 2 * W * m * 4 bytes per step / time per step (W = 8 ranks)
+    d = _run("--impl", "reference", "--steps", "1", "--warmup", "0", "--ref-elems", "8192")
+    want = 2 * 8 * 8192 * 4 / (d["ms_per_step"] * 1e-3) / 1e9
+    assert d["value"] == pytest.approx(want, rel=0.05)
