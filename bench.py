@@ -520,6 +520,11 @@ def extras(args, stream, dev):
         lambda: vc.sparse_allreduce(ins, outs, acc, 1e-3, False, nnz), 4 * W * n * 4)
     out["sparse_topk1pct_w8_f32_2^26"] = rate(
         lambda: vc.sparse_allreduce(ins, outs, acc, 0.01, True, nnz, ws), 4 * W * n * 4)
+    # the same call captured in a CUDA graph (about 24 launches per call: the
+    # host launch overhead is gone)
+    out["sparse_topk1pct_w8_f32_2^26_graph"] = graph_rate(
+        lambda s: vc.sparse_allreduce(ins, outs, acc, 0.01, True, nnz, ws, stream=s),
+        4 * W * n * 4, 10)
     out["sparse_bytes_formula"] = ("4*W*n*4: read inputs and accumulations, write outputs and "
                                    "accumulations (top-K: a 1/16 to 1/64 sample, a candidate "
                                    "pass that reads both and writes x to the accumulation, and "

@@ -796,3 +796,40 @@ def test_sparse_topk_all_equal_values(v):
     # -0 - (0 + -0) = -0
     ins = [torch.full((n,), -0.0, device="cuda") for _ in range(W)]
     _check_sparse(v, ins, [torch.full((n,), -0.0, device="cuda") for _ in range(W)], 0.02, True)
+
+
+@pytest.mark.parametrize("frac,skew", [(0.01, False), (0.3, False), (0.01, True)])
+def test_sparse_topk_in_a_cuda_graph(v, frac, skew):
+    # every route decision is taken on the device, so a captured call replays
+    # correctly on new inputs, falling back or not as the data demand; the
+    # replays must match the oracle, residuals included
+    W, n = 4, 64 * 4096 + 3
+    ins = _sparse_inputs(W, n, 90)
+    acc = [torch.zeros(n, device="cuda") for _ in range(W)]
+    outs = [torch.empty(n, device="cuda") for _ in range(W)]
+    nnz = torch.empty(W, dtype=torch.int64, device="cuda")
+    ws = torch.empty(v.sparse_workspace_bytes(W, n), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        v.sparse_allreduce(ins, outs, acc, frac, True, nnz, ws, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        v.sparse_allreduce(ins, outs, acc, frac, True, nnz, ws, stream=s)
+    for step in range(2):
+        new = _sparse_inputs(W, n, 91 + step)
+        if skew and step == 1:  # large values only in the sampled tiles: a fallback
+            for t in new:
+                tl = t[: 64 * 4096].view(-1, 4096)
+                tl[::16] = tl[::16].abs() + 100.0
+        for t, x in zip(ins, new):
+            t.copy_(x)
+        acc_np = [to_np(a).copy() for a in acc]
+        want, want_nnz = oracle.sparse_allreduce([to_np(t) for t in ins], frac, True, acc_np)
+        g.replay()
+        torch.cuda.synchronize()
+        for u in range(W):
+            assert_bit_exact(to_np(outs[u]), want[u], f"graph replay {step} out {u}")
+            assert_bit_exact(to_np(acc[u]), acc_np[u], f"graph replay {step} accum {u}")
+        assert nnz.cpu().tolist() == list(want_nnz)
