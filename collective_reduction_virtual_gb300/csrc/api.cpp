@@ -324,7 +324,7 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
     const dim3 full_grid = prm.use_cand ? few : every;
     auto run = [&](const void* k, dim3 grid, unsigned threads) -> int {
       cudaError_t e2 = cudaLaunchKernel(k, grid, dim3(threads), args, 0, st);
-      return e2 == cudaSuccess ? VCOLL_OK : cuda_fail(e2, "top-K select launch");
+      return e2 == cudaSuccess ? VCOLL_OK : cuda_fail(e2, "top-K pass launch");
     };
     // sample pass and lower bound
     if ((rc = run(topk_sample_kernel(), sample, 256)) || (rc = run(topk_select_low_kernel(), sgrid, 1024)))
