@@ -261,6 +261,14 @@ def ar_w8_f32(n_override=None):
                 es=4)
 
 
+def shifted_copy(t, k):
+    """A copy of t that starts k elements into a fresh buffer."""
+    buf = torch.empty(t.numel() + 4, dtype=t.dtype, device=t.device)
+    v = buf[k:k + t.numel()]
+    v.copy_(t)
+    return v
+
+
 def build_workload(args, dev, rank):
     """The timed step for --op (default: the W=8 fp32 2^26 allreduce).
     Returns a dict with the step function, its algorithmic bytes and the
@@ -306,6 +314,8 @@ def build_workload(args, dev, rank):
     make = {"uniform": I.uniform, "gradient": I.gradient, "outliers": I.outliers}[kind]
     wl = {"gradient": I.AR_W8_F32, "outliers": I.AR_W8_BF16, "uniform": I.SWEEP}[kind]
     ins = [make(n, I.rank_seed(wl, u) + seed_off, dev) for u in range(W)]
+    if args.misalign:  # rank u's input starts u % 4 elements past a 16-byte boundary
+        ins = [shifted_copy(t, u % 4) for u, t in enumerate(ins)]
     if args.op in ("wire", "sparse", "sparse_topk"):
         outs = [torch.empty_like(t) for t in ins]
         if args.op == "wire":
@@ -358,6 +368,8 @@ def build_workload(args, dev, rank):
         host_step = lambda hi, ho: vc.allgather(hi, n, ho)  # noqa
     dist_name = {"gradient": "normal(0,1e-3)", "uniform": "uniform[-1,1]",
                  "outliers": "normal(0,1e-2) with 1% outliers x100"}[kind]
+    if args.misalign:
+        dist_name += ", inputs at mixed 16-byte phases (element-wise path)"
     return dict(name=f"{args.op} {red}, W={W} virtual ranks, {args.dtype}, n={n} per rank, "
                      f"{dist_name}", W=W, n=n, step=step, bytes=bytes_, launches=1, ins=ins,
                 outs=outs, es=es, reduction=red, dtype=args.dtype, host_step=host_step)
@@ -717,6 +729,9 @@ def main(argv=None):
     ap.add_argument("--dtype", choices=["f32", "bf16"], default="f32")
     ap.add_argument("--reduction", choices=["sum", "max", "avg"], default=None)
     ap.add_argument("--order", choices=["fast", "ring"], default="fast")
+    ap.add_argument("--misalign", action="store_true",
+                    help="start rank u's input u %% 4 elements past a 16-byte boundary (the "
+                         "element-wise kernels)")
     ap.add_argument("--variant", choices=["auto", "direct", "staged"], default="auto",
                     help="kernel variant of the timed step (identical bits)")
     ap.add_argument("--sweep", action="store_true",

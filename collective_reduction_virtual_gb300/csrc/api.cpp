@@ -448,7 +448,18 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   const int nseg = (kind == KIND_RS || ring) ? W : 1;
   const bool small = n * es <= kSmallBytes;
   const int threads = small ? 128 : 256;
-  const int V = vec ? 16 / es : 1;
+  // inputs at other phases than outputs that share one: realigned vectors
+  bool realign = false;
+  uint64_t out_vbase = 0;
+  if (!vec) {
+    out_vbase = bufs[1].base;  // the first output's base in index space
+    realign = true;
+    for (const Buf& b : bufs)
+      if (b.out && (b.base & 15) != (out_vbase & 15)) realign = false;
+  }
+  const bool vec_like = vec || realign;
+  if (realign) phase = (int)((out_vbase & 15) / es);
+  const int V = vec_like ? 16 / es : 1;
 
   // The staged (TMA bulk copy) variant needs the 16-byte vector layout and a
   // compile-time W; everything else runs the direct kernels (same bits).
@@ -457,6 +468,9 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   if (staged)
     fn = dtype == VCOLL_F32 ? staged_kernel_f32(op, kind, W_t, ring)
                             : staged_kernel_bf16(op, kind, W_t, ring);
+  else if (realign)
+    fn = dtype == VCOLL_F32 ? reduce_kernel_f32_realign(op, kind, W_t, ring)
+                            : reduce_kernel_bf16_realign(op, kind, W_t, ring);
   else
     fn = dtype == VCOLL_F32 ? reduce_kernel_f32(op, kind, W_t, ring, vec)
                             : reduce_kernel_bf16(op, kind, W_t, ring, vec);
@@ -475,8 +489,12 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   prm.ring = ring ? 1 : 0;
   prm.scale = op == VCOLL_AVG ? 1.0f / (float)W : 1.0f;
   prm.do_scale = op == VCOLL_AVG ? 1 : 0;
+  if (realign)
+    for (int u = 0; u < W; ++u) prm.ishift[u] = (uint8_t)(((uint64_t)in[u] - out_vbase) & 15);
   if (staged)
     prm.tile_elems = staged_slice_bytes(W_t) / es;
+  else if (realign)  // the compile-time-W kernel loops over the tile, one vector a step
+    prm.tile_elems = adaptive_tile(n, nseg, threads, V, 2);
   else
     prm.tile_elems = vec ? adaptive_tile(n, nseg, threads, V, unroll_for(W_t)) : (int64_t)threads * 4;
   prm.tiles_per_seg = tiles_per_segment(n, W, nseg, V, phase, prm.tile_elems);

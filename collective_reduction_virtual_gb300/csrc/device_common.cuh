@@ -157,4 +157,30 @@ __device__ __forceinline__ void aligned_body(int64_t a, int64_t b, int phase, in
   bv = dn > av ? dn : av;
 }
 
+// out = bytes [sh, sh + 16) of the 32 bytes lo:hi (sh in 1..15).
+__device__ __forceinline__ uint4 funnel16(const uint4& lo, const uint4& hi, int sh) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  const int bs = (sh & 3) * 8;
+  uint4 o;
+  switch (sh >> 2) {
+    case 0:
+      o = make_uint4(__funnelshift_r(w[0], w[1], bs), __funnelshift_r(w[1], w[2], bs),
+                     __funnelshift_r(w[2], w[3], bs), __funnelshift_r(w[3], w[4], bs));
+      break;
+    case 1:
+      o = make_uint4(__funnelshift_r(w[1], w[2], bs), __funnelshift_r(w[2], w[3], bs),
+                     __funnelshift_r(w[3], w[4], bs), __funnelshift_r(w[4], w[5], bs));
+      break;
+    case 2:
+      o = make_uint4(__funnelshift_r(w[2], w[3], bs), __funnelshift_r(w[3], w[4], bs),
+                     __funnelshift_r(w[4], w[5], bs), __funnelshift_r(w[5], w[6], bs));
+      break;
+    default:
+      o = make_uint4(__funnelshift_r(w[3], w[4], bs), __funnelshift_r(w[4], w[5], bs),
+                     __funnelshift_r(w[5], w[6], bs), __funnelshift_r(w[6], w[7], bs));
+      break;
+  }
+  return o;
+}
+
 }  // namespace vcoll

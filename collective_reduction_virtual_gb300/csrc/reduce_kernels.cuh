@@ -279,6 +279,147 @@ __global__ void __launch_bounds__(256) vc_reduce_vec_any(const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------
+// Realigning vector kernel for inputs whose 16-byte phases differ from the
+// outputs' (shared) phase: the vector grid follows the outputs, and input u's
+// four elements at a grid position are bytes [s_u, s_u + 16) of the two
+// aligned 16-byte blocks around them (s_u = ishift[u]; one block when 0).
+// Both blocks hold bytes of the input, so no load leaves its pages.  (Taking
+// the second block from the next lane by a shuffle was slower.)  Same folds
+// as vc_reduce_vec_any and vc_reduce_elem (left fold from rank (j+1) mod W,
+// or rank 0), hence the same bits as the element-wise kernel.
+template <typename T, class Op, int KIND>
+__global__ void __launch_bounds__(256) vc_reduce_realign(const __grid_constant__ ReduceParams p) {
+  using E = Elem<T>;
+  constexpr int V = E::kVec;
+  constexpr int U = 2;
+  constexpr int G = 4;
+  const int W = p.W;
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    const TileRange tr = tile_range<V>(p, tile);
+    const int start = p.ring ? rotate(tr.j, 1, W) : 0;
+    int64_t e[U];
+    bool ok[U];
+    float acc[U][V];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      e[u] = tr.e0 + ((int64_t)u * nthr + tid) * V;
+      ok[u] = e[u] < tr.e1;
+    }
+    for (int t0 = 0; t0 < W; t0 += G) {
+      uint4 lo[U][G], hi[U][G];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int i = 0; i < G; ++i)
+          if (ok[u] && t0 + i < W) {
+            const int src = rotate(start, t0 + i, W);
+            const int sh = p.ishift[src];
+            const char* a = (const char*)p.in[src] + e[u] * E::kBytes - sh;
+            lo[u][i] = ld_stream(a);
+            hi[u][i] = sh ? ld_stream(a + 16) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          reg_fence(lo[u][i]);
+          reg_fence(hi[u][i]);
+        }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          if (ok[u] && t0 + i < W) {
+            const int sh = p.ishift[rotate(start, t0 + i, W)];
+            float x[V];
+            E::widen(sh ? funnel16(lo[u][i], hi[u][i], sh) : lo[u][i], x);
+            if (t0 + i == 0) {
+#pragma unroll
+              for (int q = 0; q < V; ++q) acc[u][q] = x[q];
+            } else {
+#pragma unroll
+              for (int q = 0; q < V; ++q) acc[u][q] = Op::apply(acc[u][q], x[q]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (ok[u]) {
+        if (p.do_scale) {
+#pragma unroll
+          for (int q = 0; q < V; ++q) acc[u][q] = __fmul_rn(acc[u][q], p.scale);
+        }
+        const uint4 o = E::narrow(acc[u]);
+        if (KIND == KIND_AR) {
+          for (int r = 0; r < W; ++r) st_stream((char*)p.out[r] + e[u] * E::kBytes, o);
+        } else {
+          st_stream((char*)p.out[tr.j] + (e[u] - tr.a) * E::kBytes, o);
+        }
+      }
+    }
+    if (tr.first) head_tail<T, Op, KIND, 0>(p, tr, W, start);
+  }
+}
+
+// The same for a compile-time rank count WT in {2, 4, 8}: every rank's blocks
+// of a vector are loaded before the fold, which takes the order of
+// vc_reduce_vec (ring, or the pairwise tree).
+template <typename T, int WT, class Op, int KIND, int RING>
+__global__ void __launch_bounds__(256) vc_reduce_realign_w(const __grid_constant__ ReduceParams p) {
+  using E = Elem<T>;
+  constexpr int V = E::kVec;
+  constexpr int TREE_W = RING ? 0 : WT;
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    const TileRange tr = tile_range<V>(p, tile);
+    const int start = RING ? rotate(tr.j, 1, WT) : 0;
+    for (int64_t e = tr.e0 + (int64_t)tid * V; e < tr.e1; e += (int64_t)nthr * V) {
+      uint4 lo[WT], hi[WT];
+#pragma unroll
+      for (int t = 0; t < WT; ++t) {
+        const int src = RING ? rotate(start, t, WT) : t;
+        const int sh = p.ishift[src];
+        const char* a = (const char*)p.in[src] + e * E::kBytes - sh;
+        lo[t] = ld_stream(a);
+        hi[t] = sh ? ld_stream(a + 16) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int t = 0; t < WT; ++t) {
+        reg_fence(lo[t]);
+        reg_fence(hi[t]);
+      }
+#pragma unroll
+      for (int t = 0; t < WT; ++t) {
+        const int sh = p.ishift[RING ? rotate(start, t, WT) : t];
+        if (sh) lo[t] = funnel16(lo[t], hi[t], sh);
+      }
+      float acc[V];
+      if (RING)
+        left_fold<T, Op, WT>(lo, acc);
+      else
+        TreeFold<T, Op, WT, 0, WT>::run(lo, acc);
+      if (p.do_scale) {
+#pragma unroll
+        for (int x = 0; x < V; ++x) acc[x] = __fmul_rn(acc[x], p.scale);
+      }
+      const uint4 o = E::narrow(acc);
+      if (KIND == KIND_AR) {
+#pragma unroll
+        for (int r = 0; r < WT; ++r) st_stream((char*)p.out[r] + e * E::kBytes, o);
+      } else {
+        st_stream((char*)p.out[tr.j] + (e - tr.a) * E::kBytes, o);
+      }
+    }
+    if (tr.first) head_tail<T, Op, KIND, TREE_W>(p, tr, WT, start);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Element-wise kernel for buffers whose 16-byte phases differ: the same
 // folds, one element per thread per step (phase is ignored; V = 1).
 template <typename T, class Op, int KIND>
@@ -339,6 +480,31 @@ __global__ void __launch_bounds__(256) vc_reduce_elem(const __grid_constant__ Re
         return (const void*)&vc_reduce_vec_any<T, Op, KIND>;                               \
     }                                                                                         \
   }                                                                                           \
+  }                                                                                           \
+  template <class Op, int KIND>                                                               \
+  const void* FNAME##_pick_realign(int W_t, int ring) {                                       \
+    switch (W_t) {                                                                            \
+      case 2: return (const void*)&vc_reduce_realign_w<T, 2, Op, KIND, 0>;                    \
+      case 4: return ring ? (const void*)&vc_reduce_realign_w<T, 4, Op, KIND, 1>              \
+                          : (const void*)&vc_reduce_realign_w<T, 4, Op, KIND, 0>;             \
+      case 8: return ring ? (const void*)&vc_reduce_realign_w<T, 8, Op, KIND, 1>              \
+                          : (const void*)&vc_reduce_realign_w<T, 8, Op, KIND, 0>;             \
+      default: return (const void*)&vc_reduce_realign<T, Op, KIND>;                           \
+    }                                                                                         \
+  }                                                                                           \
+  /* inputs at other phases than the outputs; W_t as for FNAME */                             \
+  const void* FNAME##_realign(int op, int kind, int W_t, int ring) {                          \
+    if (op == VCOLL_MAX)                                                                      \
+      return kind == KIND_AR ? FNAME##_pick_realign<OpMax, KIND_AR>(W_t, 0)                   \
+                             : FNAME##_pick_realign<OpMax, KIND_RS>(W_t, 0);                  \
+    if (op == VCOLL_MIN)                                                                      \
+      return kind == KIND_AR ? FNAME##_pick_realign<OpMin, KIND_AR>(W_t, 0)                   \
+                             : FNAME##_pick_realign<OpMin, KIND_RS>(W_t, 0);                  \
+    if (op == VCOLL_PROD)                                                                     \
+      return kind == KIND_AR ? FNAME##_pick_realign<OpProd, KIND_AR>(W_t, ring)               \
+                             : FNAME##_pick_realign<OpProd, KIND_RS>(W_t, ring);              \
+    return kind == KIND_AR ? FNAME##_pick_realign<OpSum, KIND_AR>(W_t, ring)                  \
+                           : FNAME##_pick_realign<OpSum, KIND_RS>(W_t, ring);                 \
   }                                                                                           \
   const void* FNAME(int op, int kind, int W_t, int ring, int vec) {                           \
     if (op == VCOLL_MAX)                                                                      \

@@ -43,6 +43,9 @@ struct ReduceParams {
   int ring;      // 1: ring order (start rank (j+1) mod W); 0: fastest order
   float scale;   // fl32(1/W) for avg
   int do_scale;
+  // realigning kernel: the vector grid follows the outputs' phase; input u
+  // sits ishift[u] bytes past the grid's 16-byte boundaries
+  uint8_t ishift[VCOLL_MAX_RANKS];
 };
 
 // Parameters of one allgather launch.  in[j] holds piece j, which lands at
@@ -215,6 +218,9 @@ int report_error(int status, const char* message);
 // selects the 16-byte vector path.
 const void* reduce_kernel_f32(int op, int kind, int W_t, int ring, int vec);
 const void* reduce_kernel_bf16(int op, int kind, int W_t, int ring, int vec);
+// inputs at other 16-byte phases than the (shared) phase of the outputs
+const void* reduce_kernel_f32_realign(int op, int kind, int W_t, int ring);
+const void* reduce_kernel_bf16_realign(int op, int kind, int W_t, int ring);
 const void* staged_kernel_f32(int op, int kind, int W_t, int ring);
 const void* staged_kernel_bf16(int op, int kind, int W_t, int ring);
 const void* gather_kernel(int elem_size, int vec);

@@ -833,3 +833,40 @@ def test_sparse_topk_in_a_cuda_graph(v, frac, skew):
             assert_bit_exact(to_np(outs[u]), want[u], f"graph replay {step} out {u}")
             assert_bit_exact(to_np(acc[u]), acc_np[u], f"graph replay {step} accum {u}")
         assert nnz.cpu().tolist() == list(want_nnz)
+
+
+# Inputs at mixed 16-byte phases, outputs sharing one: the realigning vector
+# kernel (each input read as the two aligned blocks around a vector and
+# funnel-shifted).  Ring order bit-exact; the fast order is the same left
+# fold as the element-wise kernel, checked to the reordering bound.
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("W", [2, 3, 5, 8, 16])
+@pytest.mark.parametrize("n", [1031, 200_003])
+def test_realigned_inputs(v, dtype, W, n):
+    V = 4 if dtype == "f32" else 8
+    shifts = [(u * 5 + 1) % 16 for u in range(W)]
+    ins = _views(W, n, dtype, shifts, 300 + W + n)
+    ins_np = [to_np(t) for t in ins]
+    s = abs_sum(ins_np)
+    outs = [torch.empty(n, dtype=DT[dtype], device="cuda") for _ in range(W)]  # one phase
+    for op in ("sum", "avg", "max", "min", "prod"):
+        want = oracle.allreduce(ins_np, op, ODT[dtype])
+        for ring in (True, False):
+            v.allreduce(ins, outs, op=op, ring_order=ring)
+            for u in range(W):
+                g = to_np(outs[u])
+                if ring or op in ("max", "min"):
+                    assert_bit_exact(g, want[u], f"AR realigned {op} ring={ring}")
+                else:
+                    assert_close_fast(g, want[u], s, W, op, f"AR realigned {op}")
+        # reduce-scatter outputs placed so that out[j] - off_j shares one phase
+        rs_want = oracle.reduce_scatter(ins_np, op, ODT[dtype])
+        rbase = [torch.empty(n + 16, dtype=DT[dtype], device="cuda") for _ in range(W)]
+        rs_out = []
+        for j in range(W):
+            off, ln = oracle.segment(n, W, j)
+            k = (off + 3) % V  # (k - off) % V == 3 for every j
+            rs_out.append(rbase[j][k:k + ln])
+        v.reduce_scatter(ins, rs_out, op=op, ring_order=True)
+        for j in range(W):
+            assert_bit_exact(to_np(rs_out[j]), rs_want[j], f"RS realigned {op}")
