@@ -1047,6 +1047,6 @@ int report_error(int status, const char* message) { return fail(status, "%s", me
 
 extern "C" {
 
-int vcoll_version(void) { return 100; }
+int vcoll_version(void) { return 200; }
 
 }  // extern "C"

@@ -56,7 +56,7 @@ def test_build_targets_sm103a_only():
 
 
 def test_version_and_status_strings(v):
-    assert v.version() == 100
+    assert v.version() == 200  # 0.2.0: vcoll_sparse_workspace_min_bytes added
     assert v.status_string(v.OK) == "success"
     assert "operation" in v.status_string(v.ERR_INVALID_OP)
     assert v.status_string(99) == "unknown status"
