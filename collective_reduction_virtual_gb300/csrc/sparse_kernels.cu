@@ -211,7 +211,10 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
           uint32_t d;
           const bool m = digit_of<P>(order_key(x[u][q]), prefix, d) &&
                          counted_bin<MODE>(d, low) && in_range;
-          hist_add(h, m, d);
+          if (P == 0)
+            hist_add(h, m, d);
+          else if (m)  // later digits: few entries match, spread over the bins
+            atomicAdd(&h[d], 1u);
         }
       }
       // head [t0, av) and tail [bv, t1): fewer than 4 elements each
@@ -229,7 +232,10 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
         uint32_t d = 0;
         bool m = false;
         if (i < t1) m = digit_of<P>(order_key(load_x(p, r, i)), prefix, d) && counted_bin<MODE>(d, low);
-        hist_add(h, m, d);
+        if (P == 0)
+          hist_add(h, m, d);
+        else if (m)
+          atomicAdd(&h[d], 1u);
       }
     }
   }
