@@ -327,13 +327,16 @@ def build_workload(args, dev, rank):
             topk = args.op == "sparse_topk"
             acc = [torch.zeros_like(t) for t in ins]
             nnz = torch.empty(W, dtype=torch.int64, device=dev)
-            ws = torch.empty(max(1, vc.sparse_workspace_bytes(W, n, topk)), dtype=torch.uint8,
-                             device=dev)
+            wsb = (vc.sparse_workspace_min_bytes(W, n, topk) if args.sparse_workspace == "min"
+                   else vc.sparse_workspace_bytes(W, n, topk))
+            ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=dev)
             frac = args.sparsity if topk else 1e-3
             step = lambda: vc.sparse_allreduce(ins, outs, acc, frac, topk, nnz, ws)  # noqa
             bytes_ = 4 * W * n * 4
             what = (f"sparsified allreduce, top-{frac:g} of each rank" if topk else
                     f"sparsified allreduce, threshold {frac:g}") + ", with error feedback"
+            if topk and args.sparse_workspace == "min":
+                what += ", minimum workspace (no candidate lists)"
         launches = 1
         if topk:
             # 13 kernels over the whole array; 22 on the candidate path, which
@@ -343,7 +346,7 @@ def build_workload(args, dev, rank):
             K = math.ceil(frac * n)
             cap = ((n // 8 + 4096 if n // 8 + 4096 < n else n) + 3) & ~3
             wide = 4 * K < n and cap >= 3 * K  # lower bound only: output from the lists
-            cand = 0 < K < n and (wide or 10 * cap >= n)
+            cand = 0 < K < n and (wide or 10 * cap >= n) and args.sparse_workspace != "min"
             launches = (23 if wide else 22) if cand else 13
         return dict(name=f"{what}, W={W}, f32, n={n} per rank", W=W, n=n, step=step,
                     bytes=bytes_, launches=launches, ins=ins,
@@ -729,6 +732,9 @@ def main(argv=None):
     ap.add_argument("--dtype", choices=["f32", "bf16"], default="f32")
     ap.add_argument("--reduction", choices=["sum", "max", "avg"], default=None)
     ap.add_argument("--order", choices=["fast", "ring"], default="fast")
+    ap.add_argument("--sparse-workspace", choices=["recommended", "min"], default="recommended",
+                    help="top-K workspace size: with candidate lists, or the minimum (the "
+                         "passes over the whole arrays)")
     ap.add_argument("--misalign", action="store_true",
                     help="start rank u's input u %% 4 elements past a 16-byte boundary (the "
                          "element-wise kernels)")
