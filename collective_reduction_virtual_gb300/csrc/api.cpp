@@ -448,17 +448,18 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   const int nseg = (kind == KIND_RS || ring) ? W : 1;
   const bool small = n * es <= kSmallBytes;
   const int threads = small ? 128 : 256;
-  // inputs at other phases than outputs that share one: realigned vectors
+  // inputs at other phases than the outputs: realigned vectors on the
+  // outputs' grid -- the allreduce's outputs must share a phase; each
+  // reduce-scatter segment follows its own output (uneven segments included)
   bool realign = false;
-  uint64_t out_vbase = 0;
   if (!vec) {
-    out_vbase = bufs[1].base;  // the first output's base in index space
     realign = true;
-    for (const Buf& b : bufs)
-      if (b.out && (b.base & 15) != (out_vbase & 15)) realign = false;
+    if (kind == KIND_AR)
+      for (int u = 1; u < W; ++u)
+        if (((uint64_t)out[u] & 15) != ((uint64_t)out[0] & 15)) realign = false;
+    if (realign && kind == KIND_AR) phase = (int)(((uint64_t)out[0] & 15) / es);
   }
   const bool vec_like = vec || realign;
-  if (realign) phase = (int)((out_vbase & 15) / es);
   const int V = vec_like ? 16 / es : 1;
 
   // The staged (TMA bulk copy) variant needs the 16-byte vector layout and a
@@ -490,7 +491,15 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   prm.scale = op == VCOLL_AVG ? 1.0f / (float)W : 1.0f;
   prm.do_scale = op == VCOLL_AVG ? 1 : 0;
   if (realign)
-    for (int u = 0; u < W; ++u) prm.ishift[u] = (uint8_t)(((uint64_t)in[u] - out_vbase) & 15);
+    for (int u = 0; u < W; ++u) {
+      prm.in_phase[u] = (uint8_t)((uint64_t)in[u] & 15);
+      const uint64_t ob = kind == KIND_AR ? (uint64_t)out[0]
+                                          : (uint64_t)out[u] - (uint64_t)seg_off[u] * es;
+      prm.out_phase[u] = (uint8_t)(ob & 15);
+    }
+  if (realign && W <= 8)
+    for (int j = 0; j < W; ++j)
+      for (int u = 0; u < W; ++u) prm.wshift[j * 8 + u] = (uint8_t)((prm.in_phase[u] - prm.out_phase[j]) & 15);
   if (staged)
     prm.tile_elems = staged_slice_bytes(W_t) / es;
   else if (realign)  // the compile-time-W kernel loops over the tile, one vector a step
@@ -498,6 +507,10 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   else
     prm.tile_elems = vec ? adaptive_tile(n, nseg, threads, V, unroll_for(W_t)) : (int64_t)threads * 4;
   prm.tiles_per_seg = tiles_per_segment(n, W, nseg, V, phase, prm.tile_elems);
+  if (realign && kind == KIND_RS)  // segments on grids of their own phases
+    for (int ph = 0; ph < V; ++ph)
+      prm.tiles_per_seg =
+          std::max(prm.tiles_per_seg, tiles_per_segment(n, W, nseg, V, ph, prm.tile_elems));
   prm.num_tiles = prm.tiles_per_seg * nseg;
   if (staged)
     return launch(fn, prm.num_tiles, kStagedThreads, (size_t)staged_smem_bytes(W_t), true, &prm,
@@ -562,12 +575,23 @@ static int gather_common(const void* const* in, void* const* out, int W, const i
 
   const bool small = n * es <= kSmallBytes;
   const int threads = small ? 128 : 256;
-  const int V = vec ? 16 / es : 1;
+  // pieces at other phases than the outputs, which share one: the vector
+  // kernel realigns them
+  bool realign = false;
+  if (!vec) {
+    realign = true;
+    for (int u = 1; u < W; ++u)
+      if (((uint64_t)out[u] & 15) != ((uint64_t)out[0] & 15)) realign = false;
+    if (realign) phase = (int)(((uint64_t)out[0] & 15) / es);
+  }
+  const int V = (vec || realign) ? 16 / es : 1;
   GatherParams prm;
   memset(&prm, 0, sizeof(prm));
   for (int u = 0; u < W; ++u) {
     prm.in[u] = in[u];
     prm.out[u] = out[u];
+    if (realign)
+      prm.ishift[u] = (uint8_t)(((uint64_t)in[u] - (uint64_t)disp[u] * es - (uint64_t)out[0]) & 15);
   }
   for (int u = 0; u <= W; ++u) prm.disp[u] = disp[u];
   prm.W = W;
@@ -602,7 +626,7 @@ static int gather_common(const void* const* in, void* const* out, int W, const i
     return launch(gather_tma_kernel(es), prm.num_tiles, kGatherTmaThreads,
                   (size_t)kGatherTmaStages * kGatherTmaTileBytes + 64, true, &prm, stream);
   }
-  return launch(gather_kernel(es, vec), prm.num_tiles, threads, 0, false, &prm, stream);
+  return launch(gather_kernel(es, vec || realign), prm.num_tiles, threads, 0, false, &prm, stream);
 }
 
 int vcoll_allgather(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,

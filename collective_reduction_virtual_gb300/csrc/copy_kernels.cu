@@ -42,11 +42,28 @@ __global__ void __launch_bounds__(256) vc_gather(const __grid_constant__ GatherP
     const int64_t e1 = e0 + p.tile_elems < bv ? e0 + p.tile_elems : bv;
     const char* src = (const char*)p.in[j] - a * ES;  // element i of segment j at src + i*ES
     if (VEC) {
-      uint4 v[U];
+      // the vectors follow the outputs' grid; a piece at another phase is
+      // read as the two aligned blocks around each vector and funnel-shifted
+      // (both blocks hold bytes of the piece)
+      const int sh = p.ishift[j];
+      uint4 v[U], hi[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t e = e0 + ((int64_t)u * nthr + tid) * V;
-        if (e < e1) v[u] = ld_stream(src + e * ES);
+        hi[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < e1) {
+          v[u] = ld_stream(src + e * ES - sh);
+          if (sh) hi[u] = ld_stream(src + e * ES - sh + 16);
+        }
+      }
+      if (sh) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          reg_fence(v[u]);
+          reg_fence(hi[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = funnel16(v[u], hi[u], sh);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {

@@ -278,11 +278,31 @@ __global__ void __launch_bounds__(256) vc_reduce_vec_any(const __grid_constant__
   }
 }
 
+// Vector grid of a realigning kernel's tile: the allreduce's outputs share
+// one grid; a reduce-scatter segment j follows its own output (element i at
+// out[j] + (i - a) * s).  p.out_phase[j] = element 0's address mod 16 on that
+// grid.
+template <int V, int KIND>
+__device__ __forceinline__ TileRange realign_range(const ReduceParams& p, int64_t tile) {
+  constexpr int S = 16 / V;  // element bytes
+  TileRange t;
+  t.j = (int)(tile / p.tiles_per_seg);
+  const int64_t k = tile - (int64_t)t.j * p.tiles_per_seg;
+  segment_bounds(p.n, p.q, p.r, p.nseg, t.j, t.a, t.b);
+  const int phase = p.out_phase[t.j] / S;
+  aligned_body<V>(t.a, t.b, phase, t.av, t.bv);
+  t.e0 = t.av + k * p.tile_elems;
+  t.e1 = t.e0 + p.tile_elems < t.bv ? t.e0 + p.tile_elems : t.bv;
+  t.first = (k == 0);
+  return t;
+}
+
 // ---------------------------------------------------------------------------
 // Realigning vector kernel for inputs whose 16-byte phases differ from the
-// outputs' (shared) phase: the vector grid follows the outputs, and input u's
-// four elements at a grid position are bytes [s_u, s_u + 16) of the two
-// aligned 16-byte blocks around them (s_u = ishift[u]; one block when 0).
+// outputs': the vector grid follows the outputs (realign_range), and input
+// u's four elements at a grid position are bytes [s_u, s_u + 16) of the two
+// aligned 16-byte blocks around them (s_u = the input's offset from the grid
+// mod 16; one block when 0).
 // Both blocks hold bytes of the input, so no load leaves its pages.  (Taking
 // the second block from the next lane by a shuffle was slower.)  Same folds
 // as vc_reduce_vec_any and vc_reduce_elem (left fold from rank (j+1) mod W,
@@ -297,8 +317,9 @@ __global__ void __launch_bounds__(256) vc_reduce_realign(const __grid_constant__
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
   for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-    const TileRange tr = tile_range<V>(p, tile);
+    const TileRange tr = realign_range<V, KIND>(p, tile);
     const int start = p.ring ? rotate(tr.j, 1, W) : 0;
+    const int oph = p.out_phase[tr.j];
     int64_t e[U];
     bool ok[U];
     float acc[U][V];
@@ -315,7 +336,7 @@ __global__ void __launch_bounds__(256) vc_reduce_realign(const __grid_constant__
         for (int i = 0; i < G; ++i)
           if (ok[u] && t0 + i < W) {
             const int src = rotate(start, t0 + i, W);
-            const int sh = p.ishift[src];
+            const int sh = (p.in_phase[src] - oph) & 15;
             const char* a = (const char*)p.in[src] + e[u] * E::kBytes - sh;
             lo[u][i] = ld_stream(a);
             hi[u][i] = sh ? ld_stream(a + 16) : make_uint4(0u, 0u, 0u, 0u);
@@ -332,7 +353,7 @@ __global__ void __launch_bounds__(256) vc_reduce_realign(const __grid_constant__
 #pragma unroll
         for (int i = 0; i < G; ++i) {
           if (ok[u] && t0 + i < W) {
-            const int sh = p.ishift[rotate(start, t0 + i, W)];
+            const int sh = (p.in_phase[rotate(start, t0 + i, W)] - oph) & 15;
             float x[V];
             E::widen(sh ? funnel16(lo[u][i], hi[u][i], sh) : lo[u][i], x);
             if (t0 + i == 0) {
@@ -365,25 +386,27 @@ __global__ void __launch_bounds__(256) vc_reduce_realign(const __grid_constant__
   }
 }
 
-// The same for a compile-time rank count WT in {2, 4, 8}: every rank's blocks
+// The same for a compile-time rank count WT in {2, 4, 8} (shifts from the
+// 8 x 8 table p.wshift): every rank's blocks
 // of a vector are loaded before the fold, which takes the order of
 // vc_reduce_vec (ring, or the pairwise tree).
 template <typename T, int WT, class Op, int KIND, int RING>
-__global__ void __launch_bounds__(256) vc_reduce_realign_w(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(256, 3) vc_reduce_realign_w(const __grid_constant__ ReduceParams p) {
   using E = Elem<T>;
   constexpr int V = E::kVec;
   constexpr int TREE_W = RING ? 0 : WT;
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
   for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-    const TileRange tr = tile_range<V>(p, tile);
+    const TileRange tr = realign_range<V, KIND>(p, tile);
     const int start = RING ? rotate(tr.j, 1, WT) : 0;
+    const uint8_t* shift = p.wshift + tr.j * 8;  // input u's bytes past the grid
     for (int64_t e = tr.e0 + (int64_t)tid * V; e < tr.e1; e += (int64_t)nthr * V) {
       uint4 lo[WT], hi[WT];
 #pragma unroll
       for (int t = 0; t < WT; ++t) {
         const int src = RING ? rotate(start, t, WT) : t;
-        const int sh = p.ishift[src];
+        const int sh = shift[src];
         const char* a = (const char*)p.in[src] + e * E::kBytes - sh;
         lo[t] = ld_stream(a);
         hi[t] = sh ? ld_stream(a + 16) : make_uint4(0u, 0u, 0u, 0u);
@@ -395,7 +418,7 @@ __global__ void __launch_bounds__(256) vc_reduce_realign_w(const __grid_constant
       }
 #pragma unroll
       for (int t = 0; t < WT; ++t) {
-        const int sh = p.ishift[RING ? rotate(start, t, WT) : t];
+        const int sh = shift[RING ? rotate(start, t, WT) : t];
         if (sh) lo[t] = funnel16(lo[t], hi[t], sh);
       }
       float acc[V];

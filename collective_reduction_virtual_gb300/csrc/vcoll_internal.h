@@ -43,9 +43,14 @@ struct ReduceParams {
   int ring;      // 1: ring order (start rank (j+1) mod W); 0: fastest order
   float scale;   // fl32(1/W) for avg
   int do_scale;
-  // realigning kernel: the vector grid follows the outputs' phase; input u
-  // sits ishift[u] bytes past the grid's 16-byte boundaries
-  uint8_t ishift[VCOLL_MAX_RANKS];
+  // realigning kernels: address mod 16 of input u's element 0, and of
+  // element 0 on the output grid of segment j (the allreduce's outputs
+  // share one grid)
+  uint8_t in_phase[VCOLL_MAX_RANKS];
+  uint8_t out_phase[VCOLL_MAX_RANKS];
+  // the same for W <= 8 as a table: wshift[j * 8 + u] = (in_phase[u] -
+  // out_phase[j]) mod 16, input u's bytes past segment j's grid
+  uint8_t wshift[64];
 };
 
 // Parameters of one allgather launch.  in[j] holds piece j, which lands at
@@ -60,6 +65,9 @@ struct GatherParams {
   int64_t tile_elems;
   int W;
   int phase;
+  // piece j's source sits ishift[j] bytes past the output grid's 16-byte
+  // boundaries (the vector grid follows the outputs)
+  uint8_t ishift[VCOLL_MAX_RANKS];
 };
 
 // Fusion pack / unpack.  One launch copies up to kFuseMaxTensors tensors of
