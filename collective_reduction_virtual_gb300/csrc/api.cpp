@@ -459,6 +459,9 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
         if (((uint64_t)out[u] & 15) != ((uint64_t)out[0] & 15)) realign = false;
     if (realign && kind == KIND_AR) phase = (int)(((uint64_t)out[0] & 15) / es);
   }
+  // aligned buffers with W in 3..7: the realigning kernel (all shifts zero)
+  // is compiled for those W, the plain vector kernels only for 2, 4, 8, 16
+  if (vec && W >= 3 && W <= 7 && W != 4 && !(flags & VCOLL_FLAG_STAGED)) realign = true;
   const bool vec_like = vec || realign;
   const int V = vec_like ? 16 / es : 1;
 
@@ -469,9 +472,9 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   if (staged)
     fn = dtype == VCOLL_F32 ? staged_kernel_f32(op, kind, W_t, ring)
                             : staged_kernel_bf16(op, kind, W_t, ring);
-  else if (realign)
-    fn = dtype == VCOLL_F32 ? reduce_kernel_f32_realign(op, kind, W_t, ring)
-                            : reduce_kernel_bf16_realign(op, kind, W_t, ring);
+  else if (realign)  // compiled in for every W up to 8
+    fn = dtype == VCOLL_F32 ? reduce_kernel_f32_realign(op, kind, W, ring)
+                            : reduce_kernel_bf16_realign(op, kind, W, ring);
   else
     fn = dtype == VCOLL_F32 ? reduce_kernel_f32(op, kind, W_t, ring, vec)
                             : reduce_kernel_bf16(op, kind, W_t, ring, vec);
@@ -502,7 +505,7 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
       for (int u = 0; u < W; ++u) prm.wshift[j * 8 + u] = (uint8_t)((prm.in_phase[u] - prm.out_phase[j]) & 15);
   if (staged)
     prm.tile_elems = staged_slice_bytes(W_t) / es;
-  else if (realign)  // the compile-time-W kernel loops over the tile, one vector a step
+  else if (realign)  // two vectors per thread (the compile-time-W kernel loops over any tile)
     prm.tile_elems = adaptive_tile(n, nseg, threads, V, 2);
   else
     prm.tile_elems = vec ? adaptive_tile(n, nseg, threads, V, unroll_for(W_t)) : (int64_t)threads * 4;

@@ -386,15 +386,18 @@ __global__ void __launch_bounds__(256) vc_reduce_realign(const __grid_constant__
   }
 }
 
-// The same for a compile-time rank count WT in {2, 4, 8} (shifts from the
-// 8 x 8 table p.wshift): every rank's blocks
-// of a vector are loaded before the fold, which takes the order of
-// vc_reduce_vec (ring, or the pairwise tree).
+// The same for a compile-time rank count WT in 2..8 (shifts from the 8 x 8
+// table p.wshift): every rank's blocks of a vector are loaded before the
+// fold.
 template <typename T, int WT, class Op, int KIND, int RING>
 __global__ void __launch_bounds__(256, 3) vc_reduce_realign_w(const __grid_constant__ ReduceParams p) {
   using E = Elem<T>;
   constexpr int V = E::kVec;
-  constexpr int TREE_W = RING ? 0 : WT;
+  // the fast order is the pairwise tree for the rank counts the plain vector
+  // kernels compile (2, 4, 8), the left fold from rank 0 otherwise -- the
+  // orders of vc_reduce_vec and vc_reduce_vec_any / the multi-tensor kernel
+  constexpr bool TREE = !RING && (WT == 2 || WT == 4 || WT == 8);
+  constexpr int TREE_W = TREE ? WT : 0;
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
   for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
@@ -422,7 +425,7 @@ __global__ void __launch_bounds__(256, 3) vc_reduce_realign_w(const __grid_const
         if (sh) lo[t] = funnel16(lo[t], hi[t], sh);
       }
       float acc[V];
-      if (RING)
+      if (RING || !TREE)
         left_fold<T, Op, WT>(lo, acc);
       else
         TreeFold<T, Op, WT, 0, WT>::run(lo, acc);
@@ -505,29 +508,37 @@ __global__ void __launch_bounds__(256) vc_reduce_elem(const __grid_constant__ Re
   }                                                                                           \
   }                                                                                           \
   template <class Op, int KIND>                                                               \
-  const void* FNAME##_pick_realign(int W_t, int ring) {                                       \
-    switch (W_t) {                                                                            \
+  const void* FNAME##_pick_realign(int W, int ring) {                                         \
+    switch (W) {                                                                              \
       case 2: return (const void*)&vc_reduce_realign_w<T, 2, Op, KIND, 0>;                    \
+      case 3: return ring ? (const void*)&vc_reduce_realign_w<T, 3, Op, KIND, 1>              \
+                          : (const void*)&vc_reduce_realign_w<T, 3, Op, KIND, 0>;             \
       case 4: return ring ? (const void*)&vc_reduce_realign_w<T, 4, Op, KIND, 1>              \
                           : (const void*)&vc_reduce_realign_w<T, 4, Op, KIND, 0>;             \
+      case 5: return ring ? (const void*)&vc_reduce_realign_w<T, 5, Op, KIND, 1>              \
+                          : (const void*)&vc_reduce_realign_w<T, 5, Op, KIND, 0>;             \
+      case 6: return ring ? (const void*)&vc_reduce_realign_w<T, 6, Op, KIND, 1>              \
+                          : (const void*)&vc_reduce_realign_w<T, 6, Op, KIND, 0>;             \
+      case 7: return ring ? (const void*)&vc_reduce_realign_w<T, 7, Op, KIND, 1>              \
+                          : (const void*)&vc_reduce_realign_w<T, 7, Op, KIND, 0>;             \
       case 8: return ring ? (const void*)&vc_reduce_realign_w<T, 8, Op, KIND, 1>              \
                           : (const void*)&vc_reduce_realign_w<T, 8, Op, KIND, 0>;             \
       default: return (const void*)&vc_reduce_realign<T, Op, KIND>;                           \
     }                                                                                         \
   }                                                                                           \
-  /* inputs at other phases than the outputs; W_t as for FNAME */                             \
-  const void* FNAME##_realign(int op, int kind, int W_t, int ring) {                          \
+  /* inputs at other phases than the outputs; W = the rank count (2..8 compiled in) */       \
+  const void* FNAME##_realign(int op, int kind, int W, int ring)   {                          \
     if (op == VCOLL_MAX)                                                                      \
-      return kind == KIND_AR ? FNAME##_pick_realign<OpMax, KIND_AR>(W_t, 0)                   \
-                             : FNAME##_pick_realign<OpMax, KIND_RS>(W_t, 0);                  \
+      return kind == KIND_AR ? FNAME##_pick_realign<OpMax, KIND_AR>(W, 0)                     \
+                             : FNAME##_pick_realign<OpMax, KIND_RS>(W, 0)  ;                  \
     if (op == VCOLL_MIN)                                                                      \
-      return kind == KIND_AR ? FNAME##_pick_realign<OpMin, KIND_AR>(W_t, 0)                   \
-                             : FNAME##_pick_realign<OpMin, KIND_RS>(W_t, 0);                  \
+      return kind == KIND_AR ? FNAME##_pick_realign<OpMin, KIND_AR>(W, 0)                     \
+                             : FNAME##_pick_realign<OpMin, KIND_RS>(W, 0)  ;                  \
     if (op == VCOLL_PROD)                                                                     \
-      return kind == KIND_AR ? FNAME##_pick_realign<OpProd, KIND_AR>(W_t, ring)               \
-                             : FNAME##_pick_realign<OpProd, KIND_RS>(W_t, ring);              \
-    return kind == KIND_AR ? FNAME##_pick_realign<OpSum, KIND_AR>(W_t, ring)                  \
-                           : FNAME##_pick_realign<OpSum, KIND_RS>(W_t, ring);                 \
+      return kind == KIND_AR ? FNAME##_pick_realign<OpProd, KIND_AR>(W, ring)                 \
+                             : FNAME##_pick_realign<OpProd, KIND_RS>(W, ring)  ;              \
+    return kind == KIND_AR ? FNAME##_pick_realign<OpSum, KIND_AR>(W, ring)                    \
+                           : FNAME##_pick_realign<OpSum, KIND_RS>(W, ring)  ;                 \
   }                                                                                           \
   const void* FNAME(int op, int kind, int W_t, int ring, int vec) {                           \
     if (op == VCOLL_MAX)                                                                      \

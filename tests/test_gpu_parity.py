@@ -870,3 +870,27 @@ def test_realigned_inputs(v, dtype, W, n):
         v.reduce_scatter(ins, rs_out, op=op, ring_order=True)
         for j in range(W):
             assert_bit_exact(to_np(rs_out[j]), rs_want[j], f"RS realigned {op}")
+
+
+# Large enough that the launch uses full-size tiles (several vectors per
+# thread per rank) for every rank count, so a kernel that covered only part
+# of a tile would show; odd n gives uneven segments (realigned vectors for
+# the reduce-scatter) and W outside {2, 4, 8, 16} the runtime-W kernels.
+@pytest.mark.parametrize("W", [3, 6, 8, 12])
+@pytest.mark.parametrize("n", [3 * (1 << 20), 3 * (1 << 20) + 5])
+def test_full_tiles_runtime_w_and_uneven(v, W, n):
+    ins = make_inputs(W, n, "f32", 500 + W + n)
+    ins_np = [to_np(t) for t in ins]
+    want = oracle.reduce_scatter(ins_np, "sum", oracle.F32)
+    outs = v.reduce_scatter(ins, op="sum", ring_order=True)
+    for j in range(W):
+        assert_bit_exact(to_np(outs[j]), want[j], f"RS full tiles W={W} n={n}")
+    want = oracle.allreduce(ins_np, "sum", oracle.F32)
+    outs = v.allreduce(ins, op="sum", ring_order=True)
+    for u in (0, W - 1):
+        assert_bit_exact(to_np(outs[u]), want[u], f"AR full tiles W={W} n={n}")
+    segs = [ins[j][:oracle.segment(n, W, j)[1]].clone() for j in range(W)]
+    ag_want = oracle.allgather([to_np(s) for s in segs], n, oracle.F32)
+    ag = v.allgather(segs, n)
+    for u in (0, W - 1):
+        assert_bit_exact(to_np(ag[u]), ag_want[u], f"AG full tiles W={W} n={n}")
