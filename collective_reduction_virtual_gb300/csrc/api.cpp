@@ -629,7 +629,8 @@ static int gather_common(const void* const* in, void* const* out, int W, const i
     return launch(gather_tma_kernel(es), prm.num_tiles, kGatherTmaThreads,
                   (size_t)kGatherTmaStages * kGatherTmaTileBytes + 64, true, &prm, stream);
   }
-  return launch(gather_kernel(es, vec || realign), prm.num_tiles, threads, 0, false, &prm, stream);
+  return launch(gather_kernel(es, vec ? 1 : realign ? 2 : 0), prm.num_tiles, threads, 0, false,
+                &prm, stream);
 }
 
 int vcoll_allgather(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,

@@ -18,8 +18,11 @@ namespace vcoll {
 
 // ------------------------------------------------------------- allgather
 
-template <int ES, bool VEC>
+// VM: 0 element-wise, 1 16-byte vectors, 2 vectors with pieces realigned to
+// the outputs' grid
+template <int ES, int VM>
 __global__ void __launch_bounds__(256) vc_gather(const __grid_constant__ GatherParams p) {
+  constexpr bool VEC = VM >= 1;
   using B = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
   constexpr int V = VEC ? 16 / ES : 1;
   constexpr int U = 4;
@@ -45,7 +48,7 @@ __global__ void __launch_bounds__(256) vc_gather(const __grid_constant__ GatherP
       // the vectors follow the outputs' grid; a piece at another phase is
       // read as the two aligned blocks around each vector and funnel-shifted
       // (both blocks hold bytes of the piece)
-      const int sh = p.ishift[j];
+      const int sh = VM == 2 ? p.ishift[j] : 0;
       uint4 v[U], hi[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -297,8 +300,11 @@ __global__ void __launch_bounds__(256, 2) vc_fuse_grouped(const __grid_constant_
 }
 
 const void* gather_kernel(int elem_size, int vec) {
-  if (elem_size == 4) return vec ? (const void*)&vc_gather<4, true> : (const void*)&vc_gather<4, false>;
-  return vec ? (const void*)&vc_gather<2, true> : (const void*)&vc_gather<2, false>;
+  if (elem_size == 4)
+    return vec == 2 ? (const void*)&vc_gather<4, 2>
+                    : vec ? (const void*)&vc_gather<4, 1> : (const void*)&vc_gather<4, 0>;
+  return vec == 2 ? (const void*)&vc_gather<2, 2>
+                  : vec ? (const void*)&vc_gather<2, 1> : (const void*)&vc_gather<2, 0>;
 }
 
 const void* fuse_kernel(int elem_size, int W) {

@@ -231,7 +231,7 @@ const void* reduce_kernel_f32_realign(int op, int kind, int W_t, int ring);
 const void* reduce_kernel_bf16_realign(int op, int kind, int W_t, int ring);
 const void* staged_kernel_f32(int op, int kind, int W_t, int ring);
 const void* staged_kernel_bf16(int op, int kind, int W_t, int ring);
-const void* gather_kernel(int elem_size, int vec);
+const void* gather_kernel(int elem_size, int vec);  // vec: 0 element-wise, 1 vectors, 2 realigned
 const void* gather_tma_kernel(int elem_size);
 const void* wire_kernel(int wire, int W_t, int ring);
 const void* sparse_apply_kernel(int topk);
