@@ -30,11 +30,15 @@
 // the inverted index (the K largest (key, -index) pairs are the K entries
 // kept).  A rank whose list overflowed, or whose band misses the K-th key,
 // takes the passes over the whole array instead; the choice is made on the
-// device.
+// device.  The candidate pass also stores x = in + acc back into acc, so the
+// later passes read one array.  With only a lower bound (small K) the lists
+// hold every kept entry, grouped by tile, and the output is built from them
+// (vc_topk_list_out) instead of by the dense apply pass -- unless a rank fell
+// back, which the kernels see on the device.
 //
 // The histograms (W x 2048 counters), the per-rank selection state, the
-// per-tile tie counts and the candidate lists live in a device workspace the
-// caller provides.
+// per-tile tie counts and list offsets and the candidate lists live in a
+// device workspace the caller provides.
 #include "device_common.cuh"
 #include "vcoll_internal.h"
 
