@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(256) vc_reduce_realign(const __grid_constant__
   using E = Elem<T>;
   constexpr int V = E::kVec;
   constexpr int U = 2;
-  constexpr int G = 4;
+  constexpr int G = 2;  // ranks per round trip: measured best (1, 2, 4, 8 tried)
   const int W = p.W;
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
