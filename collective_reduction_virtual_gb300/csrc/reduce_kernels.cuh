@@ -207,14 +207,14 @@ __global__ void __launch_bounds__(256) vc_reduce_vec(const __grid_constant__ Red
 
 // ---------------------------------------------------------------------------
 // Vector kernel for any W (runtime, <= 64): left fold from rank (j+1) mod W
-// (ring) or rank 0; the U vectors of a thread load four ranks at a time
-// (8 loads in flight) before folding them.
+// (ring) or rank 0; the U vectors of a thread load two ranks at a time
+// before folding them.
 template <typename T, class Op, int KIND>
 __global__ void __launch_bounds__(256) vc_reduce_vec_any(const __grid_constant__ ReduceParams p) {
   using E = Elem<T>;
   constexpr int V = E::kVec;
   constexpr int U = unroll_for(0);
-  constexpr int G = 4;
+  constexpr int G = 2;  // ranks per round trip: 2 beat 4 for reduce-scatter (W = 9, 12)
   const int W = p.W;
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
