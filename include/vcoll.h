@@ -13,9 +13,10 @@
  *    addressing its host pointer is a device pointer, and the kernels then
  *    read and write it directly over the CPU-GPU link, which is faster than
  *    staging copies in and out.  Each device pointer must be
- *    aligned to the element size.  Any 16-byte phase works; when all buffers
- *    of one call share the same phase the 16-byte vector path runs, otherwise
- *    an element-wise path gives the same bits more slowly.
+ *    aligned to the element size.  Any 16-byte phase works: 16-byte vectors
+ *    are used when the outputs share a phase (each reduce-scatter output on
+ *    its own grid; inputs at other phases are realigned on the fly), an
+ *    element-wise path -- same bits, slower -- when they do not.
  *  - `n` counts elements per rank (int64).  Segment j of an n-element buffer
  *    is [off_j, off_j + len_j) with q = n / W, r = n % W,
  *    off_j = j*q + min(j, r), len_j = q + (j < r): contiguous, the first r
