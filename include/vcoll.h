@@ -13,10 +13,12 @@
  *    addressing its host pointer is a device pointer, and the kernels then
  *    read and write it directly over the CPU-GPU link, which is faster than
  *    staging copies in and out.  Each device pointer must be
- *    aligned to the element size.  Any 16-byte phase works: 16-byte vectors
- *    are used when the outputs share a phase (each reduce-scatter output on
- *    its own grid; inputs at other phases are realigned on the fly), an
- *    element-wise path -- same bits, slower -- when they do not.
+ *    aligned to the element size.  Any 16-byte phase works.  Reduce-scatter,
+ *    allreduce and allgather use 16-byte vectors whenever their outputs share
+ *    a phase (each reduce-scatter output on a grid of its own), realigning
+ *    inputs at other phases on the fly; the other entry points when all their
+ *    buffers share one.  Otherwise an element-wise path gives the same bits,
+ *    more slowly.
  *  - `n` counts elements per rank (int64).  Segment j of an n-element buffer
  *    is [off_j, off_j + len_j) with q = n / W, r = n % W,
  *    off_j = j*q + min(j, r), len_j = q + (j < r): contiguous, the first r
