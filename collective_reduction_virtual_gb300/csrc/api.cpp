@@ -238,6 +238,25 @@ int64_t tiles_per_segment(int64_t n, int W, int nseg, int V, int phase, int64_t 
 // reaches 7.0 TB/s where the persistent grid-stride loop reaches 6.35 TB/s --
 // the hardware scheduler keeps the CTAs in flight on a compact window of
 // addresses, while persistent CTAs drift apart over the buffers.
+// cudaLaunchKernel with programmatic stream serialization: the kernel's
+// blocks may be scheduled while the previous kernel in the stream finishes;
+// each waits (griddepcontrol, pdl_enter) for it to complete before touching
+// memory, so only launch latency is hidden, never an ordering
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, size_t smem,
+                       cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 int launch(const void* fn, int64_t num_tiles, int threads, size_t smem, bool persistent,
            void* params, void* stream) {
   int64_t grid = num_tiles;
@@ -251,8 +270,8 @@ int launch(const void* fn, int64_t num_tiles, int threads, size_t smem, bool per
   }
   grid = std::max<int64_t>(1, std::min<int64_t>(grid, 0x7FFFFFFF));
   void* args[] = {params};
-  cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(threads), args, smem,
-                                   (cudaStream_t)stream);
+  cudaError_t e = launch_pdl(fn, dim3((unsigned)grid), dim3(threads), args, smem,
+                             (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -323,7 +342,7 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
         sample((unsigned)ceil_div(tiles, prm.sample_stride), (unsigned)W);
     const dim3 full_grid = prm.use_cand ? few : every;
     auto run = [&](const void* k, dim3 grid, unsigned threads) -> int {
-      cudaError_t e2 = cudaLaunchKernel(k, grid, dim3(threads), args, 0, st);
+      cudaError_t e2 = launch_pdl(k, grid, dim3(threads), args, 0, st);
       return e2 == cudaSuccess ? VCOLL_OK : cuda_fail(e2, "top-K pass launch");
     };
     // sample pass and lower bound
@@ -368,10 +387,10 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
   const void* fn = sparse_apply_kernel(topk);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(prm.num_tiles, 0x7FFFFFFF));
   void* args[] = {&prm};
-  cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)grid), dim3(256), args, 0, st);
+  cudaError_t e = launch_pdl(fn, dim3((unsigned)grid), dim3(256), args, 0, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse apply launch");
   if (topk && prm.list_out) {  // the result from the lists (decided on the device)
-    e = cudaLaunchKernel(topk_list_out_kernel(), dim3((unsigned)grid), dim3(256), args, 0, st);
+    e = launch_pdl(topk_list_out_kernel(), dim3((unsigned)grid), dim3(256), args, 0, st);
     if (e != cudaSuccess) return cuda_fail(e, "top-K output launch");
   }
   e = cudaGetLastError();

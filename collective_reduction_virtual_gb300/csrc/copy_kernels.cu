@@ -22,6 +22,7 @@ namespace vcoll {
 // the outputs' grid
 template <int ES, int VM>
 __global__ void __launch_bounds__(256) vc_gather(const __grid_constant__ GatherParams p) {
+  pdl_enter();
   constexpr bool VEC = VM >= 1;
   using B = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
   constexpr int V = VEC ? 16 / ES : 1;
@@ -161,6 +162,7 @@ __device__ __forceinline__ void copy_range(char* dst, const char* src, int64_t n
 
 template <int ES>
 __global__ void __launch_bounds__(256) vc_fuse(const __grid_constant__ FuseParams p) {
+  pdl_enter();
   // tile table in shared memory: the per-tile search stays on chip
   __shared__ int64_t s_begin[kFuseMaxTensors + 1];
   for (int i = threadIdx.x; i <= p.T; i += blockDim.x) s_begin[i] = p.tile_begin[i];
@@ -248,6 +250,7 @@ __device__ __forceinline__ void fuse_group_body(DstOf dst_of, SrcOf src_of, int 
 // 256-byte aligned); the others take copy_range rank by rank.
 template <int ES, int G>
 __global__ void __launch_bounds__(256, 2) vc_fuse_grouped(const __grid_constant__ FuseParams p) {
+  pdl_enter();
   using B = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
   __shared__ int64_t s_begin[kFuseMaxTensors + 1];
   for (int i = threadIdx.x; i <= p.T; i += blockDim.x) s_begin[i] = p.tile_begin[i];

@@ -116,6 +116,17 @@ __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
   __stcs(reinterpret_cast<uint4*>(p), v);
 }
 
+// Programmatic dependent launch (sm_90+): the host launches these kernels
+// with programmatic stream serialization, so a kernel may start while the
+// previous one in the stream is still finishing.  Before touching memory it
+// waits until that kernel has completed and its writes are visible (a no-op
+// when launched without the attribute); then it lets the next kernel begin
+// launching, whose blocks in turn wait for this one to finish.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Empty volatile statement that claims to rewrite v: placed after a group of
 // ld_stream calls it keeps every consumer of v behind the whole group, so the
 // compiler cannot interleave adds between the loads.

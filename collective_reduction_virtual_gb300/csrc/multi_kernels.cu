@@ -65,6 +65,7 @@ __device__ __forceinline__ void multi_one(const MultiParams& p, int W, int t, in
 
 template <typename T, int WT, class Op, int RING>
 __global__ void __launch_bounds__(256, 2) vc_allreduce_multi(const __grid_constant__ MultiParams p) {
+  pdl_enter();
   using E = Elem<T>;
   constexpr int V = E::kVec;
   constexpr int U = unroll_for(WT);

@@ -154,6 +154,7 @@ __device__ __forceinline__ void head_tail(const ReduceParams& p, const TileRange
 // folded left; RING = 0: natural rank order, pairwise tree.
 template <typename T, int WT, class Op, int KIND, int RING>
 __global__ void __launch_bounds__(256) vc_reduce_vec(const __grid_constant__ ReduceParams p) {
+  pdl_enter();
   using E = Elem<T>;
   constexpr int V = E::kVec;
   constexpr int U = unroll_for(WT);
@@ -211,6 +212,7 @@ __global__ void __launch_bounds__(256) vc_reduce_vec(const __grid_constant__ Red
 // before folding them.
 template <typename T, class Op, int KIND>
 __global__ void __launch_bounds__(256) vc_reduce_vec_any(const __grid_constant__ ReduceParams p) {
+  pdl_enter();
   using E = Elem<T>;
   constexpr int V = E::kVec;
   constexpr int U = unroll_for(0);
@@ -309,6 +311,7 @@ __device__ __forceinline__ TileRange realign_range(const ReduceParams& p, int64_
 // or rank 0), hence the same bits as the element-wise kernel.
 template <typename T, class Op, int KIND>
 __global__ void __launch_bounds__(256) vc_reduce_realign(const __grid_constant__ ReduceParams p) {
+  pdl_enter();
   using E = Elem<T>;
   constexpr int V = E::kVec;
   constexpr int U = 2;
@@ -391,6 +394,7 @@ __global__ void __launch_bounds__(256) vc_reduce_realign(const __grid_constant__
 // fold.
 template <typename T, int WT, class Op, int KIND, int RING>
 __global__ void __launch_bounds__(256, 3) vc_reduce_realign_w(const __grid_constant__ ReduceParams p) {
+  pdl_enter();
   using E = Elem<T>;
   constexpr int V = E::kVec;
   // the fast order is the pairwise tree for the rank counts the plain vector
@@ -450,6 +454,7 @@ __global__ void __launch_bounds__(256, 3) vc_reduce_realign_w(const __grid_const
 // folds, one element per thread per step (phase is ignored; V = 1).
 template <typename T, class Op, int KIND>
 __global__ void __launch_bounds__(256) vc_reduce_elem(const __grid_constant__ ReduceParams p) {
+  pdl_enter();
   const int W = p.W;
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;

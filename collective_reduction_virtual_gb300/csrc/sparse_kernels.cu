@@ -183,6 +183,7 @@ __device__ __forceinline__ void hist_add(uint32_t* h, bool valid, uint32_t d) {
 // With candidate lists, MODES 1 and 2 run only for ranks on the full path.
 template <int MODE>
 __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ SparseParams p) {
+  pdl_enter();
   constexpr int P = (MODE == 1 || MODE == 2) ? MODE : 0;
   __shared__ uint32_t h[kTopkBins];
   const int r = blockIdx.y;
@@ -266,6 +267,7 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
 //   one sets the boundary index.
 template <int MODE>
 __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ SparseParams p) {
+  pdl_enter();
   const int r = blockIdx.x;
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
@@ -381,6 +383,7 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
 // per rank scans the tile counts to the tile holding the need-th equal entry
 // and then that tile in index order; the entry's index is the boundary.
 __global__ void __launch_bounds__(256) vc_topk_tie_count(const __grid_constant__ SparseParams p) {
+  pdl_enter();
   __shared__ int wc[8];
   const int r = blockIdx.y;
   const TopkState* st = p.state + r;
@@ -447,6 +450,7 @@ __device__ __forceinline__ long long block_excl_scan(long long v, long long* tot
 }
 
 __global__ void __launch_bounds__(1024) vc_topk_tie_find(const __grid_constant__ SparseParams p) {
+  pdl_enter();
   const int r = blockIdx.x;
   TopkState* st = p.state + r;
   const long long need = st->need, equal = st->equal;
@@ -511,6 +515,7 @@ __global__ void __launch_bounds__(1024) vc_topk_tie_find(const __grid_constant__
 // Entries past the capacity are counted but not stored, which sends the rank
 // to the full path.
 __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ SparseParams p) {
+  pdl_enter();
   constexpr int E = 4 * kTileVecs;  // entries per thread and tile (plus one extra)
   __shared__ __align__(16) uint32_t s_key[kSparseThreads * E];
   __shared__ uint32_t s_n, s_sure;
@@ -643,6 +648,7 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
 // rank to the full path.
 template <int P>
 __global__ void __launch_bounds__(256) vc_topk_cand_hist(const __grid_constant__ SparseParams p) {
+  pdl_enter();
   __shared__ uint32_t h[kTopkBins];
   const int r = blockIdx.y;
   const int tid = threadIdx.x;
@@ -732,6 +738,7 @@ __device__ __forceinline__ float key_value(uint32_t key) {
 // chunks before folding them, so a tile costs one round trip for the chunk
 // bounds and one per eight ranks for the entries.
 __global__ void __launch_bounds__(256) vc_topk_list_out(const __grid_constant__ SparseParams p) {
+  pdl_enter();
   if (!list_route(p)) return;
   __shared__ uint32_t s_T[VCOLL_MAX_RANKS];
   __shared__ long long s_bound[VCOLL_MAX_RANKS];
@@ -812,6 +819,7 @@ __global__ void __launch_bounds__(256) vc_topk_list_out(const __grid_constant__ 
 // survivor counts per rank.
 template <int TOPK>
 __global__ void __launch_bounds__(256) vc_sparse_apply(const __grid_constant__ SparseParams p) {
+  pdl_enter();
   __shared__ uint32_t s_T[VCOLL_MAX_RANKS];
   __shared__ long long s_bound[VCOLL_MAX_RANKS];
   __shared__ unsigned long long s_cnt[VCOLL_MAX_RANKS];

@@ -112,6 +112,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 template <typename T, int WT, class Op, int KIND, int RING>
 __global__ void __launch_bounds__(kStagedThreads, 1)
     vc_reduce_staged(const __grid_constant__ ReduceParams p) {
+  pdl_enter();
   using E = Elem<T>;
   constexpr int V = E::kVec;
   constexpr int SLICE = staged_slice_bytes(WT);
@@ -258,6 +259,7 @@ constexpr int kGatherTileBytes = kGatherTmaTileBytes;
 
 template <int ES>
 __global__ void __launch_bounds__(kGatherTmaThreads, 1) vc_gather_tma(const __grid_constant__ GatherParams p) {
+  pdl_enter();
   using B = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
   constexpr int V = 16 / ES;
   constexpr int S = kGatherStages;

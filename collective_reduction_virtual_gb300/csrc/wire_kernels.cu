@@ -90,6 +90,7 @@ __device__ __forceinline__ void wire_one(const ReduceParams& p, int W, int start
 
 template <int WIRE, int WT, class Op, int RING>
 __global__ void __launch_bounds__(256) vc_allreduce_wire(const __grid_constant__ ReduceParams p) {
+  pdl_enter();
   constexpr int V = 4;  // fp32 lanes per 16-byte vector
   constexpr int WR = WT > 0 ? WT : 1;
   const int W = WT > 0 ? WT : p.W;
