@@ -519,9 +519,10 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
                                           : (uint64_t)out[u] - (uint64_t)seg_off[u] * es;
       prm.out_phase[u] = (uint8_t)(ob & 15);
     }
-  if (realign && W <= 8)
+  if (realign && W <= 8)  // the compiled-W kernels read the shifts from a table
     for (int j = 0; j < W; ++j)
-      for (int u = 0; u < W; ++u) prm.wshift[j * 8 + u] = (uint8_t)((prm.in_phase[u] - prm.out_phase[j]) & 15);
+      for (int u = 0; u < W; ++u)
+        prm.wshift[j * 8 + u] = (uint8_t)((prm.in_phase[u] - prm.out_phase[j]) & 15);
   if (staged)
     prm.tile_elems = staged_slice_bytes(W_t) / es;
   else if (realign)  // two vectors per thread (the compile-time-W kernel loops over any tile)
