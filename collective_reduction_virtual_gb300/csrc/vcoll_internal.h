@@ -247,6 +247,9 @@ const void* topk_cand_hist_kernel(int pass);  // 0-2 key digits, 3-5 index digit
 const void* topk_index_select_kernel(int pass);  // 3-5
 const void* topk_tie_count_kernel();
 const void* topk_tie_find_kernel();
+// dynamic shared memory the realigned allgather requests without using it,
+// to run two CTAs per SM
+constexpr size_t kGatherRealignSmem = 100 * 1024;
 constexpr int kGatherTmaThreads = 64;
 constexpr int kGatherTmaStages = 4;
 constexpr int kGatherTmaTileBytes = 32768;
