@@ -364,14 +364,24 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
     // sample pass and lower bound
     if ((rc = run(topk_sample_kernel(), sample, 256)) || (rc = run(topk_select_low_kernel(), sgrid, 1024)))
       return rc;
+    // on the list route: the second digit over the same sample narrows the
+    // settled bound (whose residuals the candidate pass writes, with
+    // accumulations) and the lower bound to a 22-bit prefix
+    if (prm.list_out &&
+        ((rc = run(topk_sample2_kernel(), sample, 256)) ||
+         (rc = run(topk_select_refine_kernel(), sgrid, 1024))))
+      return rc;
     if (prm.use_cand) {
       // one pass collects the candidates, the first digit from the lists
-      if ((rc = run(topk_filter_kernel(), every, 256))) return rc;
+      if ((rc = run(topk_filter_kernel(prm.has_acc), every, 256))) return rc;
       // the candidate pass stored x = in + acc in acc: later passes read acc
       prm.x_in_acc = prm.has_acc;
       if ((rc = run(topk_cand_hist_kernel(0), few, 256)) ||
           (rc = run(topk_select_kernel(0), sgrid, 1024)))
         return rc;
+      // off the list route (decided by that selection), x comes back where
+      // the candidate pass stored settled residuals
+      if (prm.list_out && prm.has_acc && (rc = run(topk_restore_kernel(), few, 256))) return rc;
     } else {
       // the first digit from the bound up
       if ((rc = run(topk_hist_kernel(0), every, 256)) ||

@@ -52,6 +52,18 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// inverse of order_key
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// the accumulation's new word for a kept entry: its residual x - (0 + x)
+// (the sent values are scattered into zeros first, which turns -0 into +0)
+__device__ __forceinline__ uint32_t kept_residual_bits(uint32_t key) {
+  const float x = key_value(key);
+  return __float_as_uint(__fsub_rn(x, __fadd_rn(0.0f, x)));
+}
+
 // x = in (+ accumulation), one element (the accumulation alone once the
 // candidate pass has stored x there)
 __device__ __forceinline__ float load_x(const SparseParams& p, int r, int64_t i) {
@@ -159,6 +171,14 @@ __device__ __forceinline__ bool counted_bin(uint32_t d, uint32_t low) {
     return true;
 }
 
+// The first-digit bin the second-digit sample pass refines: the settled
+// bound's, else the lower bound's when it still wants keys inside its bin;
+// -1: neither (nothing settled, no lower bound)
+__device__ __forceinline__ int refined_bin(const TopkState& st) {
+  if (st.setkey != 0xFFFFFFFFu) return (int)(st.setkey >> 21);
+  return st.low_rem > 0 ? (int)(st.lowkey >> 21) : -1;
+}
+
 // shared-memory histogram add, lanes that share a bin combined first
 __device__ __forceinline__ void hist_add(uint32_t* h, bool valid, uint32_t d) {
   const unsigned active = __ballot_sync(0xFFFFFFFFu, valid);
@@ -171,31 +191,38 @@ __device__ __forceinline__ void hist_add(uint32_t* h, bool valid, uint32_t d) {
 
 // ---------------------------------------------------------------- histogram
 // grid.y = rank; each CTA counts the digits of its tiles of that rank into a
-// shared histogram (lanes sharing a bin combined into one atomic), then adds
-// it to the rank's global histogram.
+// shared histogram, then adds it to the rank's global histogram.  The first
+// digit above a lower bound clusters in a few bins, so lanes sharing a bin
+// combine into one atomic there; the sample's first digit spreads over the
+// whole distribution and the later digits over many bins, where plain
+// shared atomics are cheaper.
 //
 // MODE 0: the first digit, bins >= state.low only (a lower bound from the
 //         sample pass: keys below it cannot be among the K largest when the
 //         counted bins hold at least K keys -- checked by the selection);
 // MODE 1, 2: the second and third digits, keys matching the prefix so far;
 // MODE 3: the first digit over a sample (every sample_stride-th tile);
-// MODE 4: the first digit over all bins, only for ranks whose bound failed.
+// MODE 4: the first digit over all bins, only for ranks whose bound failed;
+// MODE 5: the second digit over the same sample, keys in the first-digit bin
+//         of the settled bound (which refines it, and the lower bound when
+//         that lies in the same bin), else in the lower bound's bin.
 // With candidate lists, MODES 1 and 2 run only for ranks on the full path.
 template <int MODE>
 __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ SparseParams p) {
   pdl_enter();
-  constexpr int P = (MODE == 1 || MODE == 2) ? MODE : 0;
+  constexpr int P = (MODE == 1 || MODE == 2) ? MODE : MODE == 5 ? 1 : 0;
   __shared__ uint32_t h[kTopkBins];
   const int r = blockIdx.y;
   const int tid = threadIdx.x;
   const TopkState& st = p.state[r];
   if (MODE == 4 && !st.redo) return;  // uniform per CTA
   if ((MODE == 1 || MODE == 2) && p.use_cand && !st.full) return;  // read its candidates
+  if (MODE == 5 && refined_bin(st) < 0) return;                      // nothing to refine
   for (int i = tid; i < kTopkBins; i += blockDim.x) h[i] = 0;
-  const uint32_t prefix = st.prefix;
+  const uint32_t prefix = MODE == 5 ? (uint32_t)refined_bin(st) : st.prefix;
   const uint32_t low = MODE == 0 ? st.low : 0u;
   __syncthreads();
-  const int64_t step = MODE == 3 ? p.sample_stride : 1;
+  const int64_t step = (MODE == 3 || MODE == 5) ? p.sample_stride : 1;
   for (int64_t tile = (int64_t)blockIdx.x * step; tile < p.tiles_per_rank;
        tile += (int64_t)gridDim.x * step) {
     const int64_t t0 = tile * p.tile_elems;
@@ -216,10 +243,10 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
           uint32_t d;
           const bool m = digit_of<P>(order_key(x[u][q]), prefix, d) &&
                          counted_bin<MODE>(d, low) && in_range;
-          if (P == 0)
+          if (P == 0 && MODE != 3)
             hist_add(h, m, d);
-          else if (m)  // later digits: few entries match, spread over the bins
-            atomicAdd(&h[d], 1u);
+          else if (m)  // later digits (and the sample's first digit, which
+            atomicAdd(&h[d], 1u);  // spans the whole distribution): plain atomics
         }
       }
       // head [t0, av) and tail [bv, t1): fewer than 4 elements each
@@ -237,7 +264,7 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
         uint32_t d = 0;
         bool m = false;
         if (i < t1) m = digit_of<P>(order_key(load_x(p, r, i)), prefix, d) && counted_bin<MODE>(d, low);
-        if (P == 0)
+        if (P == 0 && MODE != 3)
           hist_add(h, m, d);
         else if (m)
           atomicAdd(&h[d], 1u);
@@ -261,10 +288,19 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
 //   sample), 0 (count everything) when none does; with a band also
 //   state.high = the highest bin with comfortably fewer than that strictly
 //   above it (entries above it are kept without being listed), else 2047;
+//   state.lowkey = the first key of state.low; on the list route (with
+//   accumulations) state.setkey = the last key of the bin that state.high
+//   would be without a band (entries above it are listed, and kept for
+//   certain unless the sample misled), else 0xFFFFFFFF; low_rem and set_rem
+//   keep what each bound still needs inside its bin;
 // MODE 4: after the redo pass, for ranks that needed it;
 // MODE 5, 6, 7: after index pass 3, 4, 5 over the candidates equal to T, for
 //   ranks on the candidate path whose equal keys straddle the cut; the last
-//   one sets the boundary index.
+//   one sets the boundary index;
+// MODE 8: after the second-digit sample pass: setkey moves down to the last
+//   key of the second-digit bin holding its set_rem-th sampled key, and
+//   lowkey, when it starts the refined first-digit bin, up to the first key
+//   of the second-digit bin holding its low_rem-th one.
 template <int MODE>
 __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ SparseParams p) {
   pdl_enter();
@@ -276,7 +312,8 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
   TopkState* st = p.state + r;
   if (MODE == 4 && !st->redo) return;
   // (uniform per CTA; nothing was counted for these ranks, the bins are zero)
-  if (MODE >= 5 && (p.K == 0 || st->full || st->need >= st->equal)) return;
+  if (MODE >= 5 && MODE <= 7 && (p.K == 0 || st->full || st->need >= st->equal)) return;
+  if (MODE == 8 && refined_bin(*st) < 0) return;
   const int b0 = kTopkBins - 1 - 2 * t, b1 = b0 - 1;
   const unsigned long long c0 = hist[b0], c1 = hist[b1];
   unsigned long long s = c0 + c1;
@@ -302,16 +339,20 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
   constexpr int P = (MODE == 1 || MODE == 2) ? MODE : 0;
   long long rem;
   long long rhi = 0;  // MODE 3: sampled keys allowed strictly above the band
+  long long rset = 0; // MODE 3: sampled keys allowed strictly above the settled bin
   if (MODE == 3) {
     // K's share of the sample; keys wanted at or above the lower bound: twice
     // that plus 64 (wide bound), or that plus a margin -- a few standard
     // deviations, at least 1/16 of the smaller tail -- with an upper bound
-    // the same margin below it (band); nothing when K = n
+    // the same margin below it (band); nothing when K = n.  The settled bin
+    // of the wide bound leaves the same margin below K.
     const long long ks = (long long)(((unsigned long long)p.K * total) / (unsigned long long)p.n);
     if (p.K >= p.n) {
       rem = -1;
     } else if (!p.band) {
       rem = 2 * ks + 64;
+      if (p.list_out && p.has_acc)
+        rset = ks - max((long long)(4.0f * sqrtf((float)ks)) + 64, ks / 16);
     } else {
       const long long tail = min(ks, (long long)total - ks);
       const long long m = max((long long)(4.0f * sqrtf((float)tail)) + 64, tail / 16);
@@ -320,21 +361,64 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
     }
   } else if (MODE == 5) {
     rem = st->need;
+  } else if (MODE == 8) {
+    rem = 0;  // two targets, below
   } else if (MODE == 0) {  // on the candidate path the band's share of K
     rem = p.K - (p.use_cand ? (long long)p.cand_n[p.W + r] : 0ll);
   } else {
     rem = (P == 0 && MODE < 5) ? p.K : st->remaining;
   }
   const uint32_t prefix = (P == 0 && MODE < 6) ? 0u : st->prefix;
+  // MODE 8: the refined first-digit bin, what both bounds still need inside
+  // it, and whether each bound lies in it
+  const uint32_t sbin = MODE == 8 ? (uint32_t)refined_bin(*st) : 0u;
+  const bool set_here = MODE == 8 && st->setkey != 0xFFFFFFFFu;
+  const long long set_rem = MODE == 8 ? st->set_rem : 0, low_rem = MODE == 8 ? st->low_rem : 0;
+  const bool low_here = MODE == 8 && low_rem > 0 && st->lowkey == sbin << 21;
   __syncthreads();  // every thread has read the state before it changes
+  // the bin (b0 or b1) holding the target-th key, and the keys above it
+  auto pick = [&](long long target, unsigned long long& more) -> uint32_t {
+    if ((long long)(above + c0) >= target) {
+      more = above;
+      return (uint32_t)b0;
+    }
+    more = above + c0;
+    return (uint32_t)b1;
+  };
   if (MODE == 3) {
-    if (t == 0 && (rem < 0 || (long long)total < rem)) st->low = 0;
-    if (rem >= 0 && (long long)total >= rem && (long long)above < rem && rem <= (long long)incl)
-      st->low = (uint32_t)((long long)(above + c0) >= rem ? b0 : b1);
+    unsigned long long more;
+    if (t == 0 && (rem < 0 || (long long)total < rem)) {
+      st->low = 0;
+      st->lowkey = 0;
+      st->low_rem = 0;
+    }
+    if (rem >= 0 && (long long)total >= rem && (long long)above < rem && rem <= (long long)incl) {
+      const uint32_t bin = pick(rem, more);
+      st->low = bin;
+      st->lowkey = bin << 21;
+      st->low_rem = rem - (long long)more;
+    }
     if (t == 0 && (rhi <= 0 || (long long)total < rhi)) st->high = kTopkBins - 1;
     if (rhi > 0 && (long long)total >= rhi && (long long)above < rhi && rhi <= (long long)incl)
-      st->high = (uint32_t)((long long)(above + c0) >= rhi ? b0 : b1);
+      st->high = pick(rhi, more);
+    if (t == 0 && (rset <= 0 || (long long)total < rset)) {
+      st->setkey = 0xFFFFFFFFu;
+      st->set_rem = 0;
+    }
+    if (rset > 0 && (long long)total >= rset && (long long)above < rset && rset <= (long long)incl) {
+      const uint32_t bin = pick(rset, more);
+      st->setkey = (uint32_t)((((uint64_t)bin + 1) << 21) - 1);
+      st->set_rem = rset - (long long)more;
+    }
     if (t == 0) st->redo = 0;
+  } else if (MODE == 8) {
+    unsigned long long more;
+    if (set_here && set_rem > 0 && (long long)above < set_rem && set_rem <= (long long)incl) {
+      const uint64_t p22 = ((uint64_t)sbin << 11) | pick(set_rem, more);
+      st->setkey = (uint32_t)(((p22 + 1) << 10) - 1);
+    }
+    if (low_here && (long long)above < low_rem && low_rem <= (long long)incl)
+      st->lowkey = (sbin << 21) | (pick(low_rem, more) << 10);
   } else if (MODE == 0 && (rem <= 0 || (long long)total < rem)) {
     if (t == 0) {  // a bound missed the K-th key (or the list overflowed): count every bin again
       st->redo = 1;
@@ -499,32 +583,46 @@ __global__ void __launch_bounds__(1024) vc_topk_tie_find(const __grid_constant__
 }
 
 // ------------------------------------------------------------ candidates
+// Keys above this one are settled (0xFFFFFFFF: none are).
+__device__ __forceinline__ uint32_t settled_key(const SparseParams& p, int r) {
+  if (!p.list_out || !p.has_acc) return 0xFFFFFFFFu;
+  return p.state[r].setkey;
+}
+
 // One pass over the data (grid.y = rank, one tile per CTA iteration): every
 // entry whose first digit lies in the sample's band [low, high] is appended
 // to the rank's candidate list as (key, index), and the entries above the
 // band are counted (they are kept whatever the K-th key).  With an
 // accumulation, x = in + acc is stored back into acc, so that every later
-// pass reads one array instead of two.  Each thread looks at 16
-// entries of the tile (four 16-byte vectors, all loaded before the first is
-// used) plus at most one of the tile's unaligned head or tail; a warp-wide
-// scan of the per-thread counts places every candidate, one shared atomic
-// per warp and one global atomic per tile reserve room, and each thread then
-// visits only its own candidates (their keys parked in shared memory, so the
-// loop over set bits needs no register indexing).  The list is compact; the
-// order between tiles is arbitrary (the index travels with the key).
-// Entries past the capacity are counted but not stored, which sends the rank
-// to the full path.
+// pass reads one array instead of two -- except that a candidate above the
+// settled bin gets its residual x - (0 + x) at once, when its whole tile is
+// listed (the output pass undoes it in the rare case the entry is not kept
+// after all, and so does vc_topk_restore when the result does not come from
+// the lists).  Each thread looks at 16 entries of the tile (four 16-byte
+// vectors, all loaded before the first is used) plus at most one of the
+// tile's unaligned head or tail; a warp-wide scan of the per-thread counts
+// places every candidate, one shared atomic per warp and one global atomic
+// per tile reserve room, and each thread then visits only its own candidates
+// (their keys parked in shared memory, so the loop over set bits needs no
+// register indexing).  The list is compact; the order between tiles is
+// arbitrary (the index travels with the key).  Entries past the capacity are
+// counted but not stored, which sends the rank to the full path.  ACC: with
+// accumulations (compiled apart: the deferred stores cost the pass without
+// accumulations a sixth of its time even when they never run).
+template <bool ACC>
 __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ SparseParams p) {
   pdl_enter();
   constexpr int E = 4 * kTileVecs;  // entries per thread and tile (plus one extra)
   __shared__ __align__(16) uint32_t s_key[kSparseThreads * E];
   __shared__ uint32_t s_n, s_sure;
   __shared__ unsigned long long s_base;
+  __shared__ int s_listed;  // the whole tile fits in the list
   const int r = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31;
   // candidates: keys in [lowkey, topkey]; keys above topkey are kept for sure
-  const uint32_t lowkey = p.state[r].low << 21;
+  const uint32_t lowkey = p.state[r].lowkey;
   const uint32_t topkey = (uint32_t)((((uint64_t)p.state[r].high + 1) << 21) - 1);
+  const uint32_t setkey = ACC ? settled_key(p, r) : 0xFFFFFFFFu;
   uint32_t* ckey = p.cand_key + (int64_t)r * p.cand_cap;
   uint32_t* cidx = p.cand_idx + (int64_t)r * p.cand_cap;
   uint32_t* my = s_key + tid * E;
@@ -535,25 +633,20 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
       s_n = 0;
       s_sure = 0;
     }
-    uint32_t mask = 0;  // bit j < E: entry j is a candidate
-    int sure = 0;       // entries above the band
-    uint32_t xkey = 0;  // the extra entry (head or tail)
+    uint32_t mask = 0;     // bit j < E: entry j is a candidate
+    uint32_t settle = 0;   // bit j: a candidate above the settled bin
+    int sure = 0;          // entries above the band
+    uint32_t xkey = 0;     // the extra entry (head or tail)
     bool xhit = false;
     int64_t av = t0, extra = -1;
     const bool vec = p.phase >= 0;
+    int64_t nv = 0;
     if (vec) {
       int64_t bv;
       aligned_body<4>(t0, t1, p.phase, av, bv);
-      const int64_t nv = (bv - av) / 4;
+      nv = (bv - av) / 4;
       float x[kTileVecs][4];
       load_tile_x(p, r, av, nv, x);
-      if (p.has_acc)  // later passes read x from the accumulation
-#pragma unroll
-        for (int u = 0; u < kTileVecs; ++u)
-          if (tid + u * kSparseThreads < nv)
-            st_stream((char*)p.acc[r] + (av + (int64_t)(tid + u * kSparseThreads) * 4) * 4,
-                      make_uint4(__float_as_uint(x[u][0]), __float_as_uint(x[u][1]),
-                                 __float_as_uint(x[u][2]), __float_as_uint(x[u][3])));
 #pragma unroll
       for (int u = 0; u < kTileVecs; ++u) {
         uint4 k4;
@@ -561,37 +654,46 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
         k4.y = order_key(x[u][1]);
         k4.z = order_key(x[u][2]);
         k4.w = order_key(x[u][3]);
+        uint32_t m4 = 0, s4 = 0;
         if (tid + u * kSparseThreads < nv) {
-          mask |= (uint32_t)(k4.x >= lowkey && k4.x <= topkey) << (u * 4) |
-                  (uint32_t)(k4.y >= lowkey && k4.y <= topkey) << (u * 4 + 1) |
-                  (uint32_t)(k4.z >= lowkey && k4.z <= topkey) << (u * 4 + 2) |
-                  (uint32_t)(k4.w >= lowkey && k4.w <= topkey) << (u * 4 + 3);
+          m4 = (uint32_t)(k4.x >= lowkey && k4.x <= topkey) |
+               (uint32_t)(k4.y >= lowkey && k4.y <= topkey) << 1 |
+               (uint32_t)(k4.z >= lowkey && k4.z <= topkey) << 2 |
+               (uint32_t)(k4.w >= lowkey && k4.w <= topkey) << 3;
+          s4 = m4 & ((uint32_t)(k4.x > setkey) | (uint32_t)(k4.y > setkey) << 1 |
+                     (uint32_t)(k4.z > setkey) << 2 | (uint32_t)(k4.w > setkey) << 3);
           sure += (k4.x > topkey) + (k4.y > topkey) + (k4.z > topkey) + (k4.w > topkey);
+          // later passes read x from the accumulation; a vector holding a
+          // settled candidate is stored once its tile's room is known
+          if (ACC && !s4)
+            st_stream((char*)p.acc[r] + (av + (int64_t)(tid + u * kSparseThreads) * 4) * 4,
+                      make_uint4(__float_as_uint(x[u][0]), __float_as_uint(x[u][1]),
+                                 __float_as_uint(x[u][2]), __float_as_uint(x[u][3])));
         }
+        mask |= m4 << (u * 4);
+        settle |= s4 << (u * 4);
         reinterpret_cast<uint4*>(my)[u] = k4;
       }
       // head [t0, av) and tail [bv, t1): fewer than 4 entries each
       if (tid < av - t0) extra = t0 + tid;
       if (tid >= 32 && tid - 32 < t1 - bv) extra = bv + (tid - 32);
-    } else {  // element-wise: entries t0 + tid + 256 j
+    } else {  // element-wise: entries t0 + tid + 256 j, stored below
 #pragma unroll
       for (int j = 0; j < E; ++j) {
         const int64_t i = t0 + tid + (int64_t)j * kSparseThreads;
         uint32_t k = 0;
         if (i < t1) {
-          const float x = load_x(p, r, i);
-          if (p.has_acc) st1((char*)p.acc[r] + i * 4, __float_as_uint(x));
-          k = order_key(x);
-          mask |= (uint32_t)(k >= lowkey && k <= topkey) << j;
+          k = order_key(load_x(p, r, i));
+          const bool hit = k >= lowkey && k <= topkey;
+          mask |= (uint32_t)hit << j;
+          settle |= (uint32_t)(hit && k > setkey) << j;
           sure += k > topkey;
         }
         my[j] = k;
       }
     }
-    if (extra >= 0) {
-      const float x = load_x(p, r, extra);
-      if (p.has_acc) st1((char*)p.acc[r] + extra * 4, __float_as_uint(x));
-      xkey = order_key(x);
+    if (extra >= 0) {  // stored below
+      xkey = order_key(load_x(p, r, extra));
       xhit = xkey >= lowkey && xkey <= topkey;
       sure += xkey > topkey;
     }
@@ -613,6 +715,7 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
     if (tid == 0) {
       const uint32_t tot = s_n;
       s_base = tot ? atomicAdd(p.cand_n + r, (unsigned long long)tot) : 0ull;
+      s_listed = s_base + tot <= (unsigned long long)p.cand_cap;
       if (s_sure) atomicAdd(p.cand_n + p.W + r, (unsigned long long)s_sure);
       // where this tile's entries sit in the list (read by the output pass
       // of the list route; the start only matters below the capacity)
@@ -636,8 +739,38 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
       ckey[pos] = xkey;
       cidx[pos] = (uint32_t)extra;
     }
-    // (the next tile's writes to s_key and s_n follow the barriers above:
-    // every thread reads only its own row of s_key)
+    if (ACC) {
+      // settled candidates take their residual only when the whole tile is
+      // listed (else the rank goes to the full path, which reads x)
+      const bool listed = s_listed;
+      const uint32_t res = listed ? settle : 0u;
+      auto word = [&](uint32_t key, bool settled) -> uint32_t {
+        return settled ? kept_residual_bits(key) : __float_as_uint(key_value(key));
+      };
+      if (vec) {
+#pragma unroll
+        for (int u = 0; u < kTileVecs; ++u)
+          if (tid + u * kSparseThreads < nv && ((settle >> (u * 4)) & 15u)) {
+            const uint4 k4 = reinterpret_cast<const uint4*>(my)[u];
+            st_stream((char*)p.acc[r] + (av + (int64_t)(tid + u * kSparseThreads) * 4) * 4,
+                      make_uint4(word(k4.x, (res >> (u * 4)) & 1u),
+                                 word(k4.y, (res >> (u * 4 + 1)) & 1u),
+                                 word(k4.z, (res >> (u * 4 + 2)) & 1u),
+                                 word(k4.w, (res >> (u * 4 + 3)) & 1u)));
+          }
+      } else {
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          const int64_t i = t0 + tid + (int64_t)j * kSparseThreads;
+          if (i < t1) st1((char*)p.acc[r] + i * 4, word(my[j], (res >> j) & 1u));
+        }
+      }
+      if (extra >= 0) st1((char*)p.acc[r] + extra * 4, word(xkey, listed && xhit && xkey > setkey));
+    }
+    // (after the second barrier only thread 0 reads s_n and s_sure, so it
+    // may reset them for the next tile; s_base and s_listed change only
+    // after the next tile's second barrier, which every thread passes after
+    // these reads; each thread reads only its own row of s_key)
   }
 }
 
@@ -717,7 +850,8 @@ __global__ void __launch_bounds__(256) vc_topk_cand_hist(const __grid_constant__
 // are listed: the lists were usable (no rank sent to the whole-array
 // passes) and had no entries above the band.  Uniform over the grid.  The
 // output pass then reads, per tile, each rank's list entries of that tile
-// instead of the whole arrays.  (Only once every select has run.)
+// instead of the whole arrays.  (Final once the first-digit selection has
+// run: no later pass sends a rank to the full path.)
 __device__ __forceinline__ bool list_route(const SparseParams& p) {
   if (!p.list_out) return false;
   for (int r = 0; r < p.W; ++r)
@@ -725,28 +859,48 @@ __device__ __forceinline__ bool list_route(const SparseParams& p) {
   return true;
 }
 
-// inverse of order_key
-__device__ __forceinline__ float key_value(uint32_t key) {
-  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+// After the first selection, when the result will not come from the lists
+// (a rank's list overflowed or missed its K-th key): the passes that follow
+// read x from the accumulations, so the residuals the candidate pass wrote
+// for settled entries are undone from the lists (x is the key's value; an
+// entry of a tile that was not wholly listed holds x already, and writing it
+// again changes nothing).  grid.y = rank.
+__global__ void __launch_bounds__(256) vc_topk_restore(const __grid_constant__ SparseParams p) {
+  pdl_enter();
+  if (!p.list_out || !p.has_acc || list_route(p)) return;  // uniform over the grid
+  const int r = blockIdx.y;
+  const uint32_t setkey = settled_key(p, r);
+  if (setkey == 0xFFFFFFFFu) return;
+  const unsigned long long cn = p.cand_n[r], cap = (unsigned long long)p.cand_cap;
+  const int64_t m = (int64_t)(cn < cap ? cn : cap);
+  const uint32_t* ckey = p.cand_key + (int64_t)r * p.cand_cap;
+  const uint32_t* cidx = p.cand_idx + (int64_t)r * p.cand_cap;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < m;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t k = ckey[i];
+    if (k > setkey) st1((char*)p.acc[r] + (int64_t)cidx[i] * 4, __float_as_uint(key_value(k)));
+  }
 }
 
 // List route output pass (one CTA per tile; the dense apply pass returns at
 // once on this route): the lists hold every kept entry, grouped by tile, so
 // each tile's kept entries are folded into zeros in shared memory, rank after
-// rank, their accumulations (which hold x) become x - (0 + x), and the tile
-// is written to every output.  Each thread loads its entry of eight ranks'
-// chunks before folding them, so a tile costs one round trip for the chunk
-// bounds and one per eight ranks for the entries.
+// rank, their accumulations (which hold x, or already the residual above the
+// settled key) become x - (0 + x), and the tile is written to every output.
+// Each thread loads its entry of eight ranks' chunks before folding them, so
+// a tile costs one round trip for the chunk bounds and one per eight ranks
+// for the entries.
 __global__ void __launch_bounds__(256) vc_topk_list_out(const __grid_constant__ SparseParams p) {
   pdl_enter();
   if (!list_route(p)) return;
-  __shared__ uint32_t s_T[VCOLL_MAX_RANKS];
+  __shared__ uint32_t s_T[VCOLL_MAX_RANKS], s_set[VCOLL_MAX_RANKS];
   __shared__ long long s_bound[VCOLL_MAX_RANKS];
   const int W = p.W;
   const int tid = threadIdx.x;
   for (int r = tid; r < W; r += blockDim.x) {
     s_T[r] = p.state[r].T;
     s_bound[r] = p.state[r].boundary;
+    s_set[r] = settled_key(p, r);
   }
   __syncthreads();
   constexpr int R = 8;  // ranks whose list entries are loaded together
@@ -767,12 +921,15 @@ __global__ void __launch_bounds__(256) vc_topk_list_out(const __grid_constant__ 
       s_c0[r] = (int64_t)r * p.cand_cap + p.chunk[(int64_t)r * p.tiles_per_rank + tile];
     }
     __syncthreads();
+    // (an entry above the settled key already holds its residual: only a
+    // settled entry that is not kept after all gets x back)
     auto fold = [&](int r, uint32_t key, int64_t idx) {
       if (key > s_T[r] || (key == s_T[r] && idx <= s_bound[r])) {
         const float x = key_value(key);
         s_res[idx - base] = __fadd_rn(x, s_res[idx - base]);
-        if (p.has_acc)
-          st1((char*)p.acc[r] + idx * 4, __float_as_uint(__fsub_rn(x, __fadd_rn(0.0f, x))));
+        if (p.has_acc && key <= s_set[r]) st1((char*)p.acc[r] + idx * 4, kept_residual_bits(key));
+      } else if (p.has_acc && key > s_set[r]) {
+        st1((char*)p.acc[r] + idx * 4, __float_as_uint(key_value(key)));
       }
     };
     for (int g = 0; g < W; g += R) {
@@ -924,6 +1081,8 @@ const void* sparse_apply_kernel(int topk) {
 }
 const void* topk_sample_kernel() { return (const void*)&vc_topk_hist<3>; }
 const void* topk_select_low_kernel() { return (const void*)&vc_topk_select<3>; }
+const void* topk_sample2_kernel() { return (const void*)&vc_topk_hist<5>; }
+const void* topk_select_refine_kernel() { return (const void*)&vc_topk_select<8>; }
 const void* topk_redo_hist_kernel() { return (const void*)&vc_topk_hist<4>; }
 const void* topk_redo_select_kernel() { return (const void*)&vc_topk_select<4>; }
 const void* topk_hist_kernel(int pass) {
@@ -934,8 +1093,11 @@ const void* topk_select_kernel(int pass) {
   return pass == 0 ? (const void*)&vc_topk_select<0>
                    : pass == 1 ? (const void*)&vc_topk_select<1> : (const void*)&vc_topk_select<2>;
 }
-const void* topk_filter_kernel() { return (const void*)&vc_topk_filter; }
+const void* topk_filter_kernel(int has_acc) {
+  return has_acc ? (const void*)&vc_topk_filter<true> : (const void*)&vc_topk_filter<false>;
+}
 const void* topk_list_out_kernel() { return (const void*)&vc_topk_list_out; }
+const void* topk_restore_kernel() { return (const void*)&vc_topk_restore; }
 const void* topk_cand_hist_kernel(int pass) {
   switch (pass) {
     case 0: return (const void*)&vc_topk_cand_hist<0>;

@@ -144,6 +144,13 @@ struct TopkState {
   int redo;           // the first-digit pass must be repeated over all bins
   int full;           // this rank's select passes read the whole array (its
                       // candidate list overflowed or missed the K-th key)
+  uint32_t lowkey;    // candidate path: keys below this one are not listed
+  uint32_t setkey;    // list route: keys above this one are kept for certain
+                      // (unless the sample misled), so the candidate pass
+                      // writes their residuals itself (0xFFFFFFFF: none)
+  int64_t low_rem;    // sample keys still wanted at or above lowkey inside its
+  int64_t set_rem;    // bin, and allowed above setkey inside its bin (the
+                      // second-digit refinement of both bounds)
 };
 struct SparseParams {
   const void* in[VCOLL_MAX_RANKS];
@@ -238,11 +245,14 @@ const void* sparse_apply_kernel(int topk);
 const void* topk_hist_kernel(int pass);
 const void* topk_sample_kernel();
 const void* topk_select_low_kernel();
+const void* topk_sample2_kernel();         // second digit over the sample
+const void* topk_select_refine_kernel();   // refines the settled and lower bounds
 const void* topk_redo_hist_kernel();
 const void* topk_redo_select_kernel();
 const void* topk_select_kernel(int pass);
-const void* topk_filter_kernel();
+const void* topk_filter_kernel(int has_acc);
 const void* topk_list_out_kernel();
+const void* topk_restore_kernel();
 const void* topk_cand_hist_kernel(int pass);  // 0-2 key digits, 3-5 index digits
 const void* topk_index_select_kernel(int pass);  // 3-5
 const void* topk_tie_count_kernel();

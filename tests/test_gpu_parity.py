@@ -643,7 +643,7 @@ def _sparse_inputs(W, n, seed, ties=False):
     return xs
 
 
-def _check_sparse(v, ins, acc, thr, topk, workspace_bytes=None):
+def _check_sparse(v, ins, acc, thr, topk, workspace_bytes=None, outs=None):
     W = len(ins)
     ins_np = [to_np(t) for t in ins]
     acc_np = [to_np(a).copy() for a in acc] if acc is not None else None
@@ -652,7 +652,8 @@ def _check_sparse(v, ins, acc, thr, topk, workspace_bytes=None):
     ws = None
     if workspace_bytes is not None:
         ws = torch.empty(workspace_bytes, dtype=torch.uint8, device="cuda")
-    outs = v.sparse_allreduce(ins, accum=acc, threshold=thr, topk=topk, nnz=nnz, workspace=ws)
+    outs = v.sparse_allreduce(ins, outs, accum=acc, threshold=thr, topk=topk, nnz=nnz,
+                              workspace=ws)
     torch.cuda.synchronize()
     for u in range(W):
         assert_bit_exact(to_np(outs[u]), want[u], f"sparse topk={topk} out {u}")
@@ -698,6 +699,47 @@ def test_sparse_misaligned_and_in_place(v):
     v.sparse_allreduce(bufs, bufs, threshold=0.05, topk=True)
     for u in range(W):
         assert_bit_exact(to_np(bufs[u]), want[u], "sparse in place")
+
+
+# With accumulations and output from the lists, the candidate pass writes the
+# residual of entries above the sample's settled bin itself; the output pass
+# undoes it for any that are not kept, and so does a restore pass when the
+# result does not come from the lists.  These cover the candidate pass's
+# three layouts (shared 16-byte phase, a head and tail per tile, mixed phases)
+# and a settled bin that the data contradict.
+
+@pytest.mark.parametrize("shift", [0, 1, "mixed"])
+@pytest.mark.parametrize("frac", [0.01, 0.02])
+def test_sparse_topk_settled_residuals_layouts(v, shift, frac):
+    W, n = 3, 128 * 4096 + 11
+    base = _sparse_inputs(W, n + 4, 300 + W)
+    abase = [t * 0.3 for t in _sparse_inputs(W, n + 4, 301 + W)]
+    obase = [torch.empty(n + 4, device="cuda") for _ in range(W)]
+    # shift 0 / 1: every buffer at that element offset (16-byte phase 0, or a
+    # head and tail per tile); mixed: inputs, accumulations and outputs at
+    # different phases (the element-wise candidate pass)
+    ph = {"in": lambda u: u % 4, "acc": lambda u: (u + 1) % 4, "out": lambda u: 0} \
+        if shift == "mixed" else {k: (lambda u: shift) for k in ("in", "acc", "out")}
+    ins = [b[ph["in"](u): ph["in"](u) + n] for u, b in enumerate(base)]
+    acc = [a[ph["acc"](u): ph["acc"](u) + n] for u, a in enumerate(abase)]
+    outs = [o[ph["out"](u): ph["out"](u) + n] for u, o in enumerate(obase)]
+    _check_sparse(v, ins, acc, frac, True, outs=outs)
+    _check_sparse(v, ins, acc, frac, True, outs=outs)  # a second step on the new residuals
+
+
+def test_sparse_topk_settled_bin_contradicted(v):
+    # the sampled tiles (every 16th of 4096 entries) hold smaller values than
+    # the rest, so the sample places the settled bin too low (about twice K
+    # entries lie above it) while the lower bound still holds the K-th key:
+    # the settled entries that are not kept must get their x back
+    W, n = 2, 64 * 4096
+    ins = _sparse_inputs(W, n, 17)
+    for t in ins:
+        tiles = t.view(-1, 4096)
+        tiles[::16] *= 0.75
+    acc = [torch.zeros(n, device="cuda") for _ in range(W)]
+    _check_sparse(v, ins, acc, 0.01, True)
+    _check_sparse(v, ins, acc, 0.02, True)
 
 
 def test_sparse_topk_larger(v):
