@@ -34,7 +34,11 @@
 // later passes read one array.  With only a lower bound (small K) the lists
 // hold every kept entry, grouped by tile, and the output is built from them
 // (vc_topk_list_out) instead of by the dense apply pass -- unless a rank fell
-// back, which the kernels see on the device.
+// back, which the kernels see on the device.  On that route a second pass
+// over the sample (its second key digit) narrows the lower bound and sets a
+// settled key, 22 bits fine: with accumulations the candidate pass writes
+// the residual of every candidate above it at once, so the output pass
+// revisits the accumulation only for the kept entries at or below it.
 //
 // The histograms (W x 2048 counters), the per-rank selection state, the
 // per-tile tie counts and list offsets and the candidate lists live in a
@@ -595,10 +599,10 @@ __device__ __forceinline__ uint32_t settled_key(const SparseParams& p, int r) {
 // band are counted (they are kept whatever the K-th key).  With an
 // accumulation, x = in + acc is stored back into acc, so that every later
 // pass reads one array instead of two -- except that a candidate above the
-// settled bin gets its residual x - (0 + x) at once, when its whole tile is
-// listed (the output pass undoes it in the rare case the entry is not kept
-// after all, and so does vc_topk_restore when the result does not come from
-// the lists).  Each thread looks at 16 entries of the tile (four 16-byte
+// settled key gets its residual x - (0 + x) instead, kept when its whole
+// tile is listed (the output pass undoes it in the rare case the entry is
+// not kept after all, and so does vc_topk_restore when the result does not
+// come from the lists).  Each thread looks at 16 entries of the tile (four 16-byte
 // vectors, all loaded before the first is used) plus at most one of the
 // tile's unaligned head or tail; a warp-wide scan of the per-thread counts
 // places every candidate, one shared atomic per warp and one global atomic
@@ -607,8 +611,8 @@ __device__ __forceinline__ uint32_t settled_key(const SparseParams& p, int r) {
 // register indexing).  The list is compact; the order between tiles is
 // arbitrary (the index travels with the key).  Entries past the capacity are
 // counted but not stored, which sends the rank to the full path.  ACC: with
-// accumulations (compiled apart: the deferred stores cost the pass without
-// accumulations a sixth of its time even when they never run).
+// accumulations (compiled apart: their code slowed the pass without them by
+// a tenth even where it never ran).
 template <bool ACC>
 __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ SparseParams p) {
   pdl_enter();
@@ -663,12 +667,18 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
           s4 = m4 & ((uint32_t)(k4.x > setkey) | (uint32_t)(k4.y > setkey) << 1 |
                      (uint32_t)(k4.z > setkey) << 2 | (uint32_t)(k4.w > setkey) << 3);
           sure += (k4.x > topkey) + (k4.y > topkey) + (k4.z > topkey) + (k4.w > topkey);
-          // later passes read x from the accumulation; a vector holding a
-          // settled candidate is stored once its tile's room is known
-          if (ACC && !s4)
-            st_stream((char*)p.acc[r] + (av + (int64_t)(tid + u * kSparseThreads) * 4) * 4,
-                      make_uint4(__float_as_uint(x[u][0]), __float_as_uint(x[u][1]),
-                                 __float_as_uint(x[u][2]), __float_as_uint(x[u][3])));
+          // later passes read x from the accumulation; a settled candidate
+          // gets its residual at once (undone below in the rare tile that
+          // does not fit in the list)
+          if (ACC) {
+            uint4 o = make_uint4(__float_as_uint(x[u][0]), __float_as_uint(x[u][1]),
+                                 __float_as_uint(x[u][2]), __float_as_uint(x[u][3]));
+            if (s4 & 1u) o.x = kept_residual_bits(k4.x);
+            if (s4 & 2u) o.y = kept_residual_bits(k4.y);
+            if (s4 & 4u) o.z = kept_residual_bits(k4.z);
+            if (s4 & 8u) o.w = kept_residual_bits(k4.w);
+            st_stream((char*)p.acc[r] + (av + (int64_t)(tid + u * kSparseThreads) * 4) * 4, o);
+          }
         }
         mask |= m4 << (u * 4);
         settle |= s4 << (u * 4);
@@ -740,7 +750,7 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
       cidx[pos] = (uint32_t)extra;
     }
     if (ACC) {
-      // settled candidates take their residual only when the whole tile is
+      // settled candidates keep their residual only when the whole tile is
       // listed (else the rank goes to the full path, which reads x)
       const bool listed = s_listed;
       const uint32_t res = listed ? settle : 0u;
@@ -748,16 +758,15 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
         return settled ? kept_residual_bits(key) : __float_as_uint(key_value(key));
       };
       if (vec) {
+        if (!listed)  // x again where a residual went
 #pragma unroll
-        for (int u = 0; u < kTileVecs; ++u)
-          if (tid + u * kSparseThreads < nv && ((settle >> (u * 4)) & 15u)) {
-            const uint4 k4 = reinterpret_cast<const uint4*>(my)[u];
-            st_stream((char*)p.acc[r] + (av + (int64_t)(tid + u * kSparseThreads) * 4) * 4,
-                      make_uint4(word(k4.x, (res >> (u * 4)) & 1u),
-                                 word(k4.y, (res >> (u * 4 + 1)) & 1u),
-                                 word(k4.z, (res >> (u * 4 + 2)) & 1u),
-                                 word(k4.w, (res >> (u * 4 + 3)) & 1u)));
-          }
+          for (int u = 0; u < kTileVecs; ++u)
+            if (tid + u * kSparseThreads < nv && ((settle >> (u * 4)) & 15u)) {
+              const uint4 k4 = reinterpret_cast<const uint4*>(my)[u];
+              st_stream((char*)p.acc[r] + (av + (int64_t)(tid + u * kSparseThreads) * 4) * 4,
+                        make_uint4(word(k4.x, false), word(k4.y, false), word(k4.z, false),
+                                   word(k4.w, false)));
+            }
       } else {
 #pragma unroll
         for (int j = 0; j < E; ++j) {
