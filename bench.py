@@ -544,9 +544,10 @@ def extras(args, stream, dev):
         4 * W * n * 4, 10)
     out["sparse_bytes_formula"] = ("4*W*n*4: read inputs and accumulations, write outputs and "
                                    "accumulations (top-K: a 1/16 to 1/64 sample, a candidate "
-                                   "pass that reads both and writes x to the accumulation, and "
-                                   "for small K an output pass from the candidate lists, else "
-                                   "the dense pass reading the accumulation)")
+                                   "pass that reads both and writes x -- or, above a settled "
+                                   "key, the residual -- to the accumulation, and for small K "
+                                   "an output pass from the candidate lists, else the dense "
+                                   "pass reading the accumulation)")
     del ins, outs, segs, acc
     torch.cuda.empty_cache()
 
