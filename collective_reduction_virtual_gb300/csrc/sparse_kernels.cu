@@ -38,7 +38,9 @@
 // over the sample (its second key digit) narrows the lower bound and sets a
 // settled key, 22 bits fine: with accumulations the candidate pass writes
 // the residual of every candidate above it at once, so the output pass
-// revisits the accumulation only for the kept entries at or below it.
+// revisits the accumulation only for the kept entries at or below it (and
+// when a rank falls back, a restore pass puts x back from the lists before
+// the passes over the whole array read it).
 //
 // The histograms (W x 2048 counters), the per-rank selection state, the
 // per-tile tie counts and list offsets and the candidate lists live in a
@@ -602,9 +604,9 @@ __device__ __forceinline__ uint32_t settled_key(const SparseParams& p, int r) {
 // settled key gets its residual x - (0 + x) instead, kept when its whole
 // tile is listed (the output pass undoes it in the rare case the entry is
 // not kept after all, and so does vc_topk_restore when the result does not
-// come from the lists).  Each thread looks at 16 entries of the tile (four 16-byte
-// vectors, all loaded before the first is used) plus at most one of the
-// tile's unaligned head or tail; a warp-wide scan of the per-thread counts
+// come from the lists).  Each thread looks at 16 entries of the tile (four
+// 16-byte vectors, all loaded before the first is used) plus at most one of
+// the tile's unaligned head or tail; a warp-wide scan of the per-thread counts
 // places every candidate, one shared atomic per warp and one global atomic
 // per tile reserve room, and each thread then visits only its own candidates
 // (their keys parked in shared memory, so the loop over set bits needs no
@@ -638,7 +640,7 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
       s_sure = 0;
     }
     uint32_t mask = 0;     // bit j < E: entry j is a candidate
-    uint32_t settle = 0;   // bit j: a candidate above the settled bin
+    uint32_t settle = 0;   // bit j: a candidate above the settled key
     int sure = 0;          // entries above the band
     uint32_t xkey = 0;     // the extra entry (head or tail)
     bool xhit = false;
