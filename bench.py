@@ -537,9 +537,8 @@ def extras(args, stream, dev):
         lambda: vc.sparse_allreduce(ins, outs, acc, 1e-3, False, nnz), 4 * W * n * 4)
     out["sparse_topk1pct_w8_f32_2^26"] = rate(
         lambda: vc.sparse_allreduce(ins, outs, acc, 0.01, True, nnz, ws), 4 * W * n * 4)
-    # the same call captured in a CUDA graph (27 launches per call with the nnz
-    # memset: the
-    # host launch overhead is gone)
+    # the same call captured in a CUDA graph (26 kernels and two memsets per
+    # call: the host launch overhead is gone)
     out["sparse_topk1pct_w8_f32_2^26_graph"] = graph_rate(
         lambda s: vc.sparse_allreduce(ins, outs, acc, 0.01, True, nnz, ws, stream=s),
         4 * W * n * 4, 10)
