@@ -412,8 +412,12 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
   }
   const void* fn = sparse_apply_kernel(topk);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(prm.num_tiles, 0x7FFFFFFF));
+  // on the list route the dense pass works only for a call where a rank fell
+  // back (it returns at once otherwise): a few CTAs per SM, looping over the
+  // tiles, keep its launch cheap (one CTA per tile cost 19 us to return)
+  const int64_t agrid = prm.list_out ? std::min<int64_t>(grid, (int64_t)sms * 8) : grid;
   void* args[] = {&prm};
-  cudaError_t e = launch_pdl(fn, dim3((unsigned)grid), dim3(256), args, 0, st);
+  cudaError_t e = launch_pdl(fn, dim3((unsigned)agrid), dim3(256), args, 0, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse apply launch");
   if (topk && prm.list_out) {  // the result from the lists (decided on the device)
     e = launch_pdl(topk_list_out_kernel(), dim3((unsigned)grid), dim3(256), args, 0, st);
