@@ -225,7 +225,10 @@ int vcoll_fusion_allreduce(const void* const* in, void* const* out, const int64_
  * x != 0); top-K mode: the K = ceil(threshold * n) entries (threshold in
  * [0, 1], computed in fp32 as SINGA does) with the largest values survive,
  * ties broken toward the lower index.  With accum, accum[u] becomes x minus
- * the survivors (zero where an entry survived, x elsewhere).  Every out[u]
+ * the sent values: x elsewhere; where an entry survived, x - x in threshold
+ * mode and x - (0 + x) in top-K mode (the sent values are scattered into
+ * zeros first): zero for a finite x (-0 for a kept -0 in top-K mode), NaN for
+ * an infinite one.  Every out[u]
  * receives the sum of all ranks' survivors, added into zeros rank by rank --
  * what the allgathered sparse lists scattered with cusparseSaxpyi give.
  * nnz (device, W int64, may be NULL) receives each rank's survivor count.
