@@ -60,6 +60,11 @@ MUTANTS = {
                           "    for (int u = W - 1; u >= 0; --u)\n      for (int64_t k = 0; k < len[u]; ++k)"),
     "sparse_index_base": ("result[lists[u][k].idx - 1] = 1.0f * lists[u][k].val + result[lists[u][k].idx - 1];",
                           "result[lists[u][k].idx % n] = 1.0f * lists[u][k].val + result[lists[u][k].idx % n];"),
+    "sparse_tie_higher_index_first": ("return x->idx < y->idx ? -1 : (x->idx > y->idx ? 1 : 0);",
+                                      "return x->idx > y->idx ? -1 : (x->idx < y->idx ? 1 : 0);"),
+    "sparse_topk_residual_without_zero_scatter": (
+        "for (int64_t k = 0; k < K; ++k) acc[lists[u][k].idx - 1] += 1.0f * lists[u][k].val;",
+        "for (int64_t k = 0; k < K; ++k) acc[lists[u][k].idx - 1] = lists[u][k].val;"),
     "allgatherv_block": ("int b = ufr[(W + p - s) % W]; /* block held at step s */",
                          "int b = ufr[(W + p + s) % W]; /* block held at step s */"),
     "allgatherv_displacement": ("char* dst = (char*)out[me] + disp[b] * es;",
@@ -102,6 +107,7 @@ pins = [
     (P.test_sparse_threshold_matches_dense_definition, (3, True)),
     (P.test_sparse_topk_matches_sorted_selection, (2, 0.05)),
     (P.test_sparse_topk_count_rounding, ()),
+    (P.test_sparse_topk_ties_and_signed_zero_hand_derived, ()),
 ]
 failed = []
 with oracle.using({so!r}):

@@ -534,6 +534,40 @@ def test_sparse_allreduce_hand_derived():
     assert float(oracle.sparse_allreduce(x, 0.5)[0][0][0]) == 0.0
 
 
+def _golden_cases(name):
+    """Blocks of a "case <name>" golden file as dicts of lists of fp32 arrays."""
+    def val(tok):
+        if tok.startswith("0x"):
+            return np.array([int(tok, 16)], np.uint32).view(np.float32)[0]
+        return np.float32(float(tok))
+    cases, cur = [], None
+    for line in _golden_lines(name):
+        key, *toks = line.split()
+        if key == "case":
+            cur = {"name": toks[0]}
+            cases.append(cur)
+        elif key in ("threshold",):
+            cur[key] = float(toks[0])
+        elif key == "nnz":
+            cur[key] = [int(t) for t in toks]
+        else:
+            cur.setdefault(key, []).append(np.array([val(t) for t in toks], np.float32))
+    return cases
+
+
+def test_sparse_topk_ties_and_signed_zero_hand_derived():
+    # ties across the cut keep the lower indices; a kept -0 leaves a -0
+    # residual (the sent values are added into zeros first) and adds +0
+    for c in _golden_cases("singa_topk_ties_signed_zero.txt"):
+        acc = [a.copy() for a in c["acc"]]
+        outs, nnz = oracle.sparse_allreduce(c["in"], c["threshold"], True, acc)
+        for o in outs:
+            assert o.tobytes() == c["result"][0].tobytes(), c["name"]
+        for a, want in zip(acc, c["residual"]):
+            assert a.tobytes() == want.tobytes(), c["name"]
+        assert list(nnz) == c["nnz"], c["name"]
+
+
 def _keys(a):
     u = a.view(np.uint32).astype(np.uint64)
     return np.where(u & 0x80000000, (~u) & 0xFFFFFFFF, u | 0x80000000)
