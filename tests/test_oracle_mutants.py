@@ -65,6 +65,8 @@ MUTANTS = {
     "sparse_topk_residual_without_zero_scatter": (
         "for (int64_t k = 0; k < K; ++k) acc[lists[u][k].idx - 1] += 1.0f * lists[u][k].val;",
         "for (int64_t k = 0; k < K; ++k) acc[lists[u][k].idx - 1] = lists[u][k].val;"),
+    "sparse_k_in_double": ("int64_t K = (int64_t)ceilf(threshold * (float)n);",
+                           "int64_t K = (int64_t)ceil((double)threshold * (double)n);"),
     "allgatherv_block": ("int b = ufr[(W + p - s) % W]; /* block held at step s */",
                          "int b = ufr[(W + p + s) % W]; /* block held at step s */"),
     "allgatherv_displacement": ("char* dst = (char*)out[me] + disp[b] * es;",

@@ -629,8 +629,11 @@ def test_sparse_topk_matches_sorted_selection(W, frac):
 
 
 def test_sparse_topk_count_rounding():
-    # K = ceil(threshold * n) in fp32, as the page computes it
-    for n, thr, K in ((10, 0.25, 3), (1000, 0.01, 10), (7, 1.0, 7), (100, 0.0, 0), (3, 0.34, 2)):
+    # K = ceil(threshold * n) in fp32, as the page computes it: 0.1f * 10
+    # rounds to exactly 1 in fp32 (K = 1), where double gives 1.0000000149
+    # (K = 2)
+    for n, thr, K in ((10, 0.25, 3), (1000, 0.01, 10), (7, 1.0, 7), (100, 0.0, 0), (3, 0.34, 2),
+                      (10, 0.1, 1)):
         xs = [np.arange(n, dtype=np.float32)]
         _, nnz = oracle.sparse_allreduce(xs, thr, True)
         assert nnz[0] == K, (n, thr)
