@@ -67,6 +67,11 @@ MUTANTS = {
         "for (int64_t k = 0; k < K; ++k) acc[lists[u][k].idx - 1] = lists[u][k].val;"),
     "sparse_k_in_double": ("int64_t K = (int64_t)ceilf(threshold * (float)n);",
                            "int64_t K = (int64_t)ceil((double)threshold * (double)n);"),
+    "bf16_nan_rounded_like_a_number": (
+        "if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)\n",
+        "if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0 && 0)\n"),
+    "f16_nan_not_quieted": ("return (uint16_t)(sign | (man ? 0x7E00u | (man >> 13) : 0x7C00u));",
+                            "return (uint16_t)(sign | (man ? 0x7C00u | (man >> 13) : 0x7C00u));"),
     "allgatherv_block": ("int b = ufr[(W + p - s) % W]; /* block held at step s */",
                          "int b = ufr[(W + p + s) % W]; /* block held at step s */"),
     "allgatherv_displacement": ("char* dst = (char*)out[me] + disp[b] * es;",
@@ -90,6 +95,7 @@ pins = [
     (P.test_max_matches_numpy, (4,)),
     (P.test_max_signed_zero_and_nan, ()),
     (P.test_bf16_rne_golden, ()),
+    (P.test_bf16_nan_stays_nan, ()),
     (P.test_bf16_allreduce_accumulates_in_fp32, ()),
     (P.test_allgather_of_reduce_scatter_is_allreduce, (3, 10, oracle.F32, "sum")),
     (P.test_allgather_is_concatenation, (5,)),
@@ -102,6 +108,7 @@ pins = [
     (P.test_prod_of_small_integers_exact, (3,)),
     (P.test_allgatherv_is_concatenation, (3,)),
     (P.test_f16_rne_golden, ()),
+    (P.test_f16_nan_stays_nan, ()),
     (P.test_f16_widening_matches_numpy_for_all_patterns, ()),
     (P.test_wire_hop_rounding_hand_derived, ()),
     (P.test_wire_integer_sums_exact, ("f16", 3)),

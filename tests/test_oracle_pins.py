@@ -462,6 +462,20 @@ def test_f16_matches_numpy_conversion():
     assert np.array_equal(oracle.f16_from_f32(f), want)
 
 
+def test_f16_nan_stays_nan():
+    # IEEE narrowing keeps a NaN a NaN (quiet), whatever its payload -- also
+    # a signaling one whose payload lies only in the 13 bits binary16 drops.
+    # (Passed one by one the values become Python floats, which quiets them;
+    # the wire allreduce narrows the buffer's own bit patterns.)
+    f = np.array([0x7FC00000, 0xFFC00001, 0x7F800001, 0x7FBFFFFF, 0xFF801FFF],
+                 np.uint32).view(np.float32)
+    h = oracle.f16_from_f32(f).astype(np.uint32)
+    assert all(((v & 0x7C00) == 0x7C00) and (v & 0x3FF) != 0 and (v & 0x200) for v in h)
+    for wire in ("f16", "bf16"):
+        out = oracle.allreduce_wire([f.copy()], wire, "sum")[0]  # one rank: a round trip
+        assert np.all(np.isnan(out)), wire
+
+
 def test_f16_widening_matches_numpy_for_all_patterns():
     h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
     got = oracle.f32_from_f16(h)
