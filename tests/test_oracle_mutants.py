@@ -72,6 +72,8 @@ MUTANTS = {
         "if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0 && 0)\n"),
     "f16_nan_not_quieted": ("return (uint16_t)(sign | (man ? 0x7E00u | (man >> 13) : 0x7C00u));",
                             "return (uint16_t)(sign | (man ? 0x7C00u | (man >> 13) : 0x7C00u));"),
+    "sampled_wrong_segment": ("if (idx[i] >= off && idx[i] < off + len) j = u;",
+                              "if (idx[i] >= off && idx[i] < off + len) j = (u + 1) % W;"),
     "allgatherv_block": ("int b = ufr[(W + p - s) % W]; /* block held at step s */",
                          "int b = ufr[(W + p + s) % W]; /* block held at step s */"),
     "allgatherv_displacement": ("char* dst = (char*)out[me] + disp[b] * es;",
@@ -112,6 +114,7 @@ pins = [
     (P.test_f16_widening_matches_numpy_for_all_patterns, ()),
     (P.test_wire_hop_rounding_hand_derived, ()),
     (P.test_wire_integer_sums_exact, ("f16", 3)),
+    (P.test_sampled_equals_full, (8, 1000, "sum", oracle.F32)),
     (P.test_sparse_allreduce_hand_derived, ()),
     (P.test_sparse_threshold_matches_dense_definition, (3, True)),
     (P.test_sparse_topk_matches_sorted_selection, (2, 0.05)),
