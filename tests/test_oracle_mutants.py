@@ -74,6 +74,8 @@ MUTANTS = {
                             "return (uint16_t)(sign | (man ? 0x7C00u | (man >> 13) : 0x7C00u));"),
     "sampled_wrong_segment": ("if (idx[i] >= off && idx[i] < off + len) j = u;",
                               "if (idx[i] >= off && idx[i] < off + len) j = (u + 1) % W;"),
+    "wire_avg_scales_unrounded_sum": ("if (hop) v = round_to(v, dtype);\n          if (op == ORACLE_AVG)",
+                                      "if (0) v = round_to(v, dtype);\n          if (op == ORACLE_AVG)"),
     "allgatherv_block": ("int b = ufr[(W + p - s) % W]; /* block held at step s */",
                          "int b = ufr[(W + p + s) % W]; /* block held at step s */"),
     "allgatherv_displacement": ("char* dst = (char*)out[me] + disp[b] * es;",

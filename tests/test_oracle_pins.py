@@ -487,12 +487,13 @@ def test_f16_widening_matches_numpy_for_all_patterns():
 
 def test_wire_hop_rounding_hand_derived():
     for line in _golden_lines("wire_hop_rounding.txt"):
-        wire, xs, res = (p.strip() for p in line.split(";"))
+        wire, xs, res, *rest = (p.strip() for p in line.split(";"))
+        op = rest[0] if rest else "sum"
         x = [np.full(3, float(v), np.float32) for v in xs.split()]
         want = [float(v) for v in res.split()]
-        got = oracle.allreduce_wire(x, wire, "sum")
+        got = oracle.allreduce_wire(x, wire, op)
         for u in range(3):
-            assert list(got[u]) == want, wire
+            assert list(got[u]) == want, (wire, op)
 
 
 @pytest.mark.parametrize("wire", ["f16", "bf16"])
