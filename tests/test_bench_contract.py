@@ -42,3 +42,24 @@ def test_reference_arm_value_counts_the_allreduce_bytes():
     d = _run("--impl", "reference", "--steps", "1", "--warmup", "0", "--ref-elems", "8192")
     want = 2 * 8 * 8192 * 4 / (d["ms_per_step"] * 1e-3) / 1e9
     assert d["value"] == pytest.approx(want, rel=0.05)
+
+
+def test_reference_arm_under_torchrun_prints_once_from_rank_0():
+    # N > 1: rank 0 alone runs the oracle and prints; the other rank exits 0
+    # without work (no process group is needed for that)
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                        "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0",
+                        "--ref-elems", "4096"],
+                       capture_output=True, text=True, cwd=ROOT, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
