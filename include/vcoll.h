@@ -239,9 +239,10 @@ int vcoll_fusion_allreduce(const void* const* in, void* const* out, const int64_
  * rank; smaller gives VCOLL_ERR_INVALID_ARG); vcoll_sparse_workspace_bytes(W,
  * n, 1) (about n bytes + 40 KiB per rank) adds room for candidate lists, which lets the
  * select passes after the first read only the entries above a sampled bound
- * instead of the whole array (the same results, about twice as fast at K = 1 %
- * of n; a size in between gives smaller lists, and a rank whose list does not
- * fit falls back to the passes over the whole array).
+ * instead of the whole array, and for small K lets the output come from the
+ * lists (the same results, about three times as fast at K = 1 % of n; a size
+ * in between gives smaller lists, and a rank whose list does not fit falls
+ * back to the passes over the whole array).
  * In place: out[u] == in[u].
  */
 size_t vcoll_sparse_workspace_bytes(int W, int64_t n, int topk);
