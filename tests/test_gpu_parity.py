@@ -469,6 +469,28 @@ def test_prod_ring_order_hand_derived_on_gpu(v):
     assert [float(o[0]) for o in outs] == [1.0, 0.0, 1.0, float("inf")]
 
 
+@pytest.mark.parametrize("n", [7, 4099, 65541])
+def test_avg_scale_rounding_hand_derived_on_gpu(v, n):
+    # the hand-derived avg bits for W = 3 and 5 (fl32(1/W) times the sum,
+    # then the cast): integer inputs sum exactly in any order, so both
+    # orders and both reduce-scatter and allreduce must give these bits
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "avg_scale_rounding.txt")
+    rows = [ln.strip() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    for line in rows:
+        dt, xs, bits = (p.strip() for p in line.split(";"))
+        x = [torch.full((n,), float(val), device="cuda", dtype=DT[dt]) for val in xs.split()]
+        want = int(bits, 16)
+        view = torch.int32 if dt == "f32" else torch.int16
+        mask = 0xFFFFFFFF if dt == "f32" else 0xFFFF
+        for ring in (True, False):
+            outs = v.allreduce(x, op="avg", ring_order=ring)
+            outs += [torch.cat(v.reduce_scatter(x, op="avg", ring_order=ring))]
+            for o in outs:
+                got = (o.view(view).to(torch.int64) & mask).unique().tolist()
+                assert got == [want], (line, ring, [hex(g) for g in got])
+
+
 # ------------------------------------------------------------ allgatherv
 
 @pytest.mark.parametrize("W", [1, 2, 3, 8, 16])
@@ -600,10 +622,15 @@ def test_allreduce_wire(v, wire, W, n):
         fast = v.allreduce_wire(ins, wire=wire, op=op)
         for r in range(W):
             assert_bit_exact(to_np(ring[r]), want[r], f"wire {wire} {op} ring")
-            # fastest order: both orders are W-1 roundings away from the same
-            # rounded inputs; each rounding errs by at most u_w |partial| or,
-            # below the wire type's normal range, by half its subnormal
-            # spacing (2^-25 for fp16); the final scale of avg rounds once more
+            # fastest order: both orders start from the same rounded inputs
+            # and each is W-1 hop roundings from their exact sum; a rounding
+            # errs by at most u_w |partial| + eta, where eta is half the wire
+            # type's subnormal spacing (2^-25 for fp16; bf16 has fp32's
+            # range, where 2^-25 is ample) and |partial| <= s = sum |x_r|
+            # (divided by W for avg, whose hop errors the scale divides too);
+            # avg's scale multiply and its second rounding to the wire type
+            # add two more terms.  So each order is within (W+1)(u_w s + eta)
+            # of the exact sum and the two within twice that.
             s = abs_sum([(to_np(t)) for t in ins]) / (W if op == "avg" else 1)
             bound = 2 * (W + 1) * (u * s + 2.0 ** -25)
             d = np.abs(to_np(fast[r]).astype(np.float64) - want[r].astype(np.float64))

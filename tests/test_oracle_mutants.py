@@ -29,6 +29,10 @@ MUTANTS = {
     "bf16_round_half_up": ("u += 0x7FFFu + lsb;", "u += 0x8000u;"),
     "bf16_widen_shift": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;"),
     "avg_scale_dropped": ("if (op == ORACLE_AVG) v = v * scale;", ";"),
+    "avg_divides_by_w": ("if (op == ORACLE_AVG) v = v * scale;",
+                         "if (op == ORACLE_AVG) v = v / (float)W;"),
+    "avg_casts_before_scale": ("if (op == ORACLE_AVG) v = v * scale;",
+                               "if (op == ORACLE_AVG) v = round_to(v, dtype) * scale;"),
     "fusion_threshold_strict": ("size + counts[t] * es <= threshold_bytes",
                                 "size + counts[t] * es < threshold_bytes"),
     "allgather_block": ("int b = ufr[(p - s + W) % W];", "int b = ufr[(p + s) % W];"),
@@ -96,6 +100,7 @@ pins = [
     (P.test_brute_force_tiny, (4, 16)),
     (P.test_integer_valued_sums_exact, (7,)),
     (P.test_avg_power_of_two_exact, (3,)),
+    (P.test_avg_scale_rounding_hand_derived, ()),
     (P.test_max_matches_numpy, (4,)),
     (P.test_max_signed_zero_and_nan, ()),
     (P.test_bf16_rne_golden, ()),

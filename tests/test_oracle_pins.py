@@ -184,6 +184,31 @@ def test_avg_close_to_exact_mean(W):
         assert abs(Fraction(float(got[i])) - exact) <= gamma * mag
 
 
+def test_avg_scale_rounding_hand_derived():
+    # avg multiplies the ring sum by fl32(1/W) once and casts after that:
+    # for W = 3 and 5 this differs in the last bit from dividing by W, and
+    # for bf16 output from casting the sum before the scale
+    for line in _golden_lines("avg_scale_rounding.txt"):
+        dt, xs, bits = (p.strip() for p in line.split(";"))
+        xs = [float(v) for v in xs.split()]
+        W, n = len(xs), 7
+        if dt == "f32":
+            dtype = oracle.F32
+            ins = [np.full(n, v, np.float32) for v in xs]
+        else:
+            # the inputs are exact in bf16: the high half of their fp32 bits
+            dtype = oracle.BF16
+            ins = [np.full(n, np.float32(v).view(np.uint32) >> 16, np.uint16) for v in xs]
+        want = int(bits, 16)
+        ring = list(range(W))[::-1]
+        for ufr in (None, ring):
+            outs = oracle.allreduce(ins, "avg", dtype, ufr)
+            outs += [np.concatenate(oracle.reduce_scatter(ins, "avg", dtype, ufr))]
+            for o in outs:
+                got = o.view(np.uint32 if dtype == oracle.F32 else np.uint16)
+                assert [int(g) for g in got] == [want] * n, (line, ufr)
+
+
 # ------------------------------------------------------------------- max
 
 @pytest.mark.parametrize("W", [2, 3, 4, 8, 16])
