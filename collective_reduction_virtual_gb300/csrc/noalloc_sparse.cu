@@ -13,6 +13,7 @@
 // the library (kNoAllocScratchBytes, 1 MiB), so the call itself allocates
 // nothing.  Every GPU that loads the library holds the array until the
 // process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -29,12 +30,54 @@ constexpr size_t kNoAllocScratchBytes = VCOLL_SPARSE_NOALLOC_BYTES;
 // never taken from the name itself.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The address is looked up once per device and context.  A device's context
+// can be replaced within one process (cudaDeviceReset, or a caller that makes
+// its own context current), and the new context loads the library's module
+// afresh, so the array may then sit at another address: the cache keeps the
+// id of the context it was resolved in and resolves again when the current
+// one differs.  The context functions come from the driver through the
+// runtime's entry-point query, so the library does not link libcuda.
 constexpr int kMaxDevices = 64;
+struct ScratchSlot {
+  unsigned long long ctx_id;  // 0: not resolved
+  void* addr;
+};
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices];  // device address per device, set up once
+ScratchSlot g_slot[kMaxDevices];
 
-// Looks up the array's device address on the current device (once per
-// device, with that device current).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+std::once_flag g_driver_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// The id of the context current on this thread, or 0 when none is current or
+// the driver does not provide the query.
+unsigned long long current_context_id() {
+  std::call_once(g_driver_once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = (CtxGetCurrentFn)f;
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = (CtxGetIdFn)f;
+  });
+  if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Looks up the array's device address on the current device, with that
+// device current: once per device and context (every call, if the context
+// cannot be identified).
 int scratch_address(void** addr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -42,18 +85,24 @@ int scratch_address(void** addr) {
   if (dev < 0 || dev >= kMaxDevices)
     return vcoll::report_error(VCOLL_ERR_UNSUPPORTED, "device index out of range");
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p) {
-      char msg[256];
-      snprintf(msg, sizeof(msg), "cudaGetSymbolAddress of the fixed scratch failed: %s",
-               cudaGetErrorString(e));
-      return vcoll::report_error(VCOLL_ERR_CUDA, msg);
-    }
-    g_scratch_addr[dev] = p;
+  unsigned long long id = current_context_id();
+  if (id && g_slot[dev].ctx_id == id) {
+    *addr = g_slot[dev].addr;
+    return VCOLL_OK;
   }
-  *addr = g_scratch_addr[dev];
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p) {
+    char msg[256];
+    snprintf(msg, sizeof(msg), "cudaGetSymbolAddress of the fixed scratch failed: %s",
+             cudaGetErrorString(e));
+    return vcoll::report_error(VCOLL_ERR_CUDA, msg);
+  }
+  // the lookup makes the runtime's context current if none was
+  if (!id) id = current_context_id();
+  g_slot[dev].ctx_id = id;
+  g_slot[dev].addr = p;
+  *addr = p;
   return VCOLL_OK;
 }
 

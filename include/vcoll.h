@@ -266,7 +266,8 @@ int vcoll_sparse_allreduce(const void* const* in, void* const* out, void* const*
  * for the fast path up to a few million entries over all ranks at K = 1 %).  The
  * threshold mode needs no working memory and passes straight through.
  * The first top-K call on a device looks up the array's device address with
- * cudaGetSymbolAddress; make that first call before capturing a stream.
+ * cudaGetSymbolAddress (again after the device's context changes, as after
+ * cudaDeviceReset); make that first call before capturing a stream.
  * All calls share the one array and it keeps the last call's contents (the
  * call clears what must start at zero), so calls that may run at the same
  * time on the GPU -- on different streams, or from different threads --

@@ -26,9 +26,20 @@ def _ptrs(ts):
     return [t.data_ptr() for t in ts]
 
 
-@pytest.mark.parametrize("topk,frac", [(True, 0.01), (True, 0.3), (False, 0.9)])
-def test_noalloc_matches_workspace_entry_two_calls_in_a_row(v, topk, frac):
-    W, n = 8, (1 << 20) + 3
+# What the fixed 1 MiB leaves beyond the minimum is candidate-list room:
+# - n = 2^20 + 3: about 15K entries per rank, too few for K = 1 % (3K = 31K),
+#   so the select passes read the whole array;
+# - n = 2^18 + 5, K = 1 %: 3K = 7.9K entries fit, so the candidate lists and
+#   the output from the lists are used;
+# - n = 62.6 M: the minimum nearly fills the array and leaves 56 entries per
+#   rank; K = 16 (3K = 48) still asks for the lists, which the sampled bound
+#   can overflow, sending a rank back to the whole-array passes.
+@pytest.mark.parametrize("topk,frac,n", [(True, 0.01, (1 << 20) + 3), (True, 0.3, (1 << 20) + 3),
+                                         (False, 0.9, (1 << 20) + 3),
+                                         (True, 0.01, (1 << 18) + 5),
+                                         (True, 2.5e-7, 62_600_000)])
+def test_noalloc_matches_workspace_entry_two_calls_in_a_row(v, topk, frac, n):
+    W = 8
     g = torch.Generator(device="cuda")
     g.manual_seed(2026)
     ins = [torch.randn(n, generator=g, device="cuda") for _ in range(W)]
