@@ -227,7 +227,7 @@ class ClockSampler:
 def timed_steps(step, steps, warmup, stream, per_launch=True):
     """Run warmup untimed steps, then time `steps` steps with CUDA events on
     `stream` (barrier + synchronize on both sides).  Returns (total seconds,
-    mean seconds per launch)."""
+    median seconds per launch)."""
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
@@ -248,7 +248,8 @@ def timed_steps(step, steps, warmup, stream, per_launch=True):
     torch.cuda.synchronize()
     barrier()
     total = t0.elapsed_time(t1) / 1e3
-    per = (sum(a.elapsed_time(b) for a, b in ev) / 1e3 / steps) if per_launch else total / steps
+    per = (statistics.median(a.elapsed_time(b) for a, b in ev) / 1e3) if per_launch \
+        else total / steps
     return total, per
 
 
@@ -267,6 +268,20 @@ def shifted_copy(t, k):
     v = buf[k:k + t.numel()]
     v.copy_(t)
     return v
+
+
+def fusion_pipeline_bytes(counts, es, W):
+    """Algorithmic bytes and launches of the fusion-buffer pipeline: per
+    batch of two or more tensors pack, allreduce and unpack (6*W*B_batch,
+    3 launches), per batch of one tensor one allreduce (2*W*B, 1 launch)."""
+    begin = vc.fuse_plan(counts, 0 if es == 4 else 1)
+    nbytes = launches = 0
+    for b in range(len(begin) - 1):
+        bb = sum(counts[begin[b]:begin[b + 1]]) * es
+        multi = begin[b + 1] - begin[b] > 1
+        nbytes += (6 if multi else 2) * W * bb
+        launches += 3 if multi else 1
+    return nbytes, launches
 
 
 def build_workload(args, dev, rank):
@@ -292,9 +307,9 @@ def build_workload(args, dev, rank):
         if args.op == "fusion":
             fused = [torch.empty((64 << 20) // es, dtype=dt, device=dev) for _ in range(W)]
             step = lambda: vc.fusion_allreduce(tens, outs, fused, op=red, ring_order=ring)  # noqa
-            nb = len(vc.fuse_plan(counts, 0 if es == 4 else 1)) - 1
-            bytes_, launches = 6 * W * B, 3 * nb
-            desc = "pack + in-place allreduce + unpack per 64 MiB batch (6*W*B)"
+            bytes_, launches = fusion_pipeline_bytes(counts, es, W)
+            desc = ("one C call: pack + in-place allreduce + unpack per 64 MiB batch (6*W*B; a "
+                    "batch of one tensor is allreduced straight, 2*W*B)")
         else:
             plan = vc.FusionPlan(tens, outs, op=red, ring_order=ring)
             step = lambda: plan()  # noqa
@@ -325,16 +340,17 @@ def build_workload(args, dev, rank):
             what = "fp16-wire allreduce"
         else:
             topk = args.op == "sparse_topk"
-            acc = [torch.zeros_like(t) for t in ins]
+            acc = None if args.no_accumulation else [torch.zeros_like(t) for t in ins]
             nnz = torch.empty(W, dtype=torch.int64, device=dev)
             wsb = (vc.sparse_workspace_min_bytes(W, n, topk) if args.sparse_workspace == "min"
                    else vc.sparse_workspace_bytes(W, n, topk))
             ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=dev)
             frac = args.sparsity if topk else 1e-3
             step = lambda: vc.sparse_allreduce(ins, outs, acc, frac, topk, nnz, ws)  # noqa
-            bytes_ = 4 * W * n * 4
+            bytes_ = (2 if acc is None else 4) * W * n * 4
             what = (f"sparsified allreduce, top-{frac:g} of each rank" if topk else
-                    f"sparsified allreduce, threshold {frac:g}") + ", with error feedback"
+                    f"sparsified allreduce, threshold {frac:g}") + \
+                (", without accumulations" if acc is None else ", with error feedback")
             if topk and args.sparse_workspace == "min":
                 what += ", minimum workspace (no candidate lists)"
         launches = 1
@@ -349,7 +365,7 @@ def build_workload(args, dev, rank):
             cap = ((n // 8 + 4096 if n // 8 + 4096 < n else n) + 3) & ~3
             wide = 4 * K < n and cap >= 3 * K  # lower bound only: output from the lists
             cand = 0 < K < n and (wide or 10 * cap >= n) and args.sparse_workspace != "min"
-            launches = (26 if wide else 22) if cand else 13
+            launches = ((26 if acc is not None else 25) if wide else 22) if cand else 13
         return dict(name=f"{what}, W={W}, f32, n={n} per rank", W=W, n=n, step=step,
                     bytes=bytes_, launches=launches, ins=ins,
                     outs=outs, es=4, reduction=red, dtype="f32")
@@ -505,7 +521,7 @@ def cpu_baseline(cfg, seconds):
 def extras(args, stream, dev):
     out = {}
 
-    def rate(fn, nbytes, steps=10, warmup=3):
+    def rate(fn, nbytes, steps=20, warmup=3):
         total, per = timed_steps(fn, steps, warmup, stream)
         return {"GBps": round(nbytes / per / 1e9, 1), "ms": round(per * 1e3, 4)}
 
@@ -537,6 +553,10 @@ def extras(args, stream, dev):
         lambda: vc.sparse_allreduce(ins, outs, acc, 1e-3, False, nnz), 4 * W * n * 4)
     out["sparse_topk1pct_w8_f32_2^26"] = rate(
         lambda: vc.sparse_allreduce(ins, outs, acc, 0.01, True, nnz, ws), 4 * W * n * 4)
+    # without accumulations (no error feedback): reads the inputs, writes the
+    # outputs
+    out["sparse_topk1pct_w8_f32_2^26_noacc"] = rate(
+        lambda: vc.sparse_allreduce(ins, outs, None, 0.01, True, nnz, ws), 2 * W * n * 4)
     # the same call captured in a CUDA graph (26 kernels and two memsets per
     # call: the host launch overhead is gone)
     out["sparse_topk1pct_w8_f32_2^26_graph"] = graph_rate(
@@ -563,16 +583,24 @@ def extras(args, stream, dev):
     del ins, outs
     torch.cuda.empty_cache()
 
-    # W=4 fp32 n=2^20 reduce-scatter: hot (L2-resident) and cold (L2 flushed)
+    # W=4 fp32 n=2^20 reduce-scatter: hot (L2-resident) and cold.  Cold is
+    # taken two ways: (a) one launch timed with events right after a kernel
+    # that READS a buffer of twice L2's size (a write flush would leave L2
+    # full of dirty lines that the timed kernel then pays to write back),
+    # median of 20; (b) a CUDA graph cycling through 16 input sets (320 MiB,
+    # more than L2), so every launch finds its inputs evicted, with no flush
+    # or event between launches
     W, n = 4, 1 << 20
     ins = I.rank_buffers("uniform", W, n, I.RS_W4, dev)
     segs = [torch.empty(vc.segment(n, W, j)[1], device=dev) for j in range(W)]
+    nb = (W + 1) * n * 4
     out["rs_sum_w4_f32_2^20_hot"] = graph_rate(
-        lambda s: vc.reduce_scatter(ins, segs, op="sum", stream=s), (W + 1) * n * 4, 200)
-    flush = torch.empty(2 * L2_BYTES // 4, device=dev)
+        lambda s: vc.reduce_scatter(ins, segs, op="sum", stream=s), nb, 200)
+    flush = torch.ones(2 * L2_BYTES // 4, device=dev)
+    sink = torch.empty((), device=dev)
     times = []
-    for i in range(13):
-        flush.fill_(float(i))
+    for i in range(23):
+        torch.sum(flush, dim=0, out=sink)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         vc.reduce_scatter(ins, segs, op="sum")
@@ -581,9 +609,21 @@ def extras(args, stream, dev):
         if i >= 3:
             times.append(a.elapsed_time(b) / 1e3)
     per = statistics.median(times)
-    out["rs_sum_w4_f32_2^20_cold"] = {"GBps": round((W + 1) * n * 4 / per / 1e9, 1),
-                                      "ms": round(per * 1e3, 4), "l2": "flushed before each"}
-    del ins, segs, flush
+    out["rs_sum_w4_f32_2^20_cold"] = {
+        "GBps": round(nb / per / 1e9, 1), "ms": round(per * 1e3, 4),
+        "l2": "a 258 MiB read before each launch; median of 20 event-timed launches"}
+    sets = [ins] + [[t.clone() for t in ins] for _ in range(15)]
+    osets = [[torch.empty_like(t) for t in segs] for _ in range(16)]
+    it = iter(range(1 << 30))
+
+    def cycle(s):
+        k = next(it) % 16
+        vc.reduce_scatter(sets[k], osets[k], op="sum", stream=s)
+
+    r = graph_rate(cycle, nb, 160)
+    r["l2"] = "16 input sets (320 MiB) cycled in a CUDA graph: every launch reads evicted inputs"
+    out["rs_sum_w4_f32_2^20_cold_cycled"] = r
+    del ins, segs, flush, sets, osets
     torch.cuda.empty_cache()
 
     # fusion: 200 fp32 tensors per rank, W=8, 64 MiB buffer, pack + AR avg + unpack
@@ -593,11 +633,13 @@ def extras(args, stream, dev):
     fouts = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
     fused = [torch.empty((64 << 20) // 4, device=dev) for _ in range(W)]
     tot = sum(counts) * 4
+    fb, _ = fusion_pipeline_bytes(counts, 4, W)
     out["fusion_w8_200tensors"] = rate(
-        lambda: vc.fusion_allreduce(tens, fouts, fused, op="avg"), 6 * W * tot, steps=5, warmup=2)
-    out["fusion_w8_200tensors"]["bytes_formula"] = "6*W*B_total (pack + AR + unpack)"
+        lambda: vc.fusion_allreduce(tens, fouts, fused, op="avg"), fb)
+    out["fusion_w8_200tensors"]["bytes_formula"] = \
+        "6*W*B per batch (pack + AR + unpack in one C call; 2*W*B for a one-tensor batch)"
     plan = vc.FusionPlan(tens, fouts, op="avg")
-    out["fusion_w8_200tensors_direct"] = rate(lambda: plan(), 2 * W * tot, steps=10, warmup=3)
+    out["fusion_w8_200tensors_direct"] = rate(lambda: plan(), 2 * W * tot)
     out["fusion_w8_200tensors_direct"]["bytes_formula"] = \
         "2*W*B_total (one pass, no fusion buffer); same bits as the pipeline"
     del tens, fouts, fused
@@ -735,6 +777,8 @@ def main(argv=None):
     ap.add_argument("--dtype", choices=["f32", "bf16"], default="f32")
     ap.add_argument("--reduction", choices=["sum", "max", "avg"], default=None)
     ap.add_argument("--order", choices=["fast", "ring"], default="fast")
+    ap.add_argument("--no-accumulation", action="store_true",
+                    help="sparsified allreduce without accumulations (no error feedback)")
     ap.add_argument("--sparse-workspace", choices=["recommended", "min"], default="recommended",
                     help="top-K workspace size: with candidate lists, or the minimum (the "
                          "passes over the whole arrays)")

@@ -76,6 +76,9 @@ def lib() -> ctypes.CDLL:
             L.vcoll_sparse_allreduce_noalloc.argtypes = [PP, PP, PP, I, I64, ctypes.c_float, I, P,
                                                          P]
             L.vcoll_sparse_allreduce_noalloc.restype = I
+            for name in ("vcoll_reduce_scatter_ring", "vcoll_allreduce_ring"):
+                getattr(L, name).argtypes = [PP, PP, I, I64, I, I, IP, P]
+                getattr(L, name).restype = I
             L.vcoll_allreduce_wire.argtypes = [PP, PP, I, I64, I, I, U, P]
             L.vcoll_allreduce_wire.restype = I
             L.vcoll_allgatherv.argtypes = [PP, I64P, PP, I, I, P]
@@ -84,6 +87,9 @@ def lib() -> ctypes.CDLL:
             L.vcoll_allreduce_multi.restype = I
             L.vcoll_fusion_allreduce.argtypes = [PP, PP, I64P, I, I, I, I, U, I64, IP, P]
             L.vcoll_fusion_allreduce.restype = I
+            L.vcoll_fusion_allreduce_buffered.argtypes = [PP, PP, I64P, I, PP, I64, I, I, I, U,
+                                                          I64, IP, P]
+            L.vcoll_fusion_allreduce_buffered.restype = I
             L.vcoll_segment.argtypes = [I64, I, I, I64P, I64P]
             L.vcoll_segment.restype = I
             L.vcoll_status_string.argtypes = [I]
@@ -149,6 +155,24 @@ def device_errors(clear: bool = False) -> int:
 def vcoll_reduce_scatter(in_ptrs, out_ptrs, W, n, dtype, op, flags=0, stream=0) -> int:
     return lib().vcoll_reduce_scatter(_ptr_array(in_ptrs), _ptr_array(out_ptrs), W, n, dtype, op,
                                       flags, stream or None)
+
+
+def _ring_array(user_from_ring):
+    if user_from_ring is None:
+        return None
+    return (ctypes.c_int * max(1, len(user_from_ring)))(*[int(v) for v in user_from_ring])
+
+
+def vcoll_reduce_scatter_ring(in_ptrs, out_ptrs, W, n, dtype, op, user_from_ring=None,
+                              stream=0) -> int:
+    return lib().vcoll_reduce_scatter_ring(_ptr_array(in_ptrs), _ptr_array(out_ptrs), W, n, dtype,
+                                           op, _ring_array(user_from_ring), stream or None)
+
+
+def vcoll_allreduce_ring(in_ptrs, out_ptrs, W, n, dtype, op, user_from_ring=None,
+                         stream=0) -> int:
+    return lib().vcoll_allreduce_ring(_ptr_array(in_ptrs), _ptr_array(out_ptrs), W, n, dtype, op,
+                                      _ring_array(user_from_ring), stream or None)
 
 
 def vcoll_allgather(in_ptrs, out_ptrs, W, n, dtype, op=SUM, flags=0, stream=0) -> int:
@@ -274,8 +298,11 @@ def segment(n: int, W: int, j: int) -> tuple[int, int]:
     return off, ln
 
 
-def reduce_scatter(ins, outs=None, op="sum", ring_order=False, stream=None, flags=0):
-    """ins: W CUDA tensors of n elements.  Returns W segment tensors."""
+def reduce_scatter(ins, outs=None, op="sum", ring_order=False, stream=None, flags=0,
+                   user_from_ring=None):
+    """ins: W CUDA tensors of n elements.  Returns W segment tensors.
+    user_from_ring (W ints, the rank at each ring position): ring order on
+    that ring (implies ring_order)."""
     torch = _torch()
     W, n = len(ins), ins[0].numel()
     _check_tensors(ins, "ins")
@@ -283,10 +310,15 @@ def reduce_scatter(ins, outs=None, op="sum", ring_order=False, stream=None, flag
         outs = [torch.empty(segment(n, W, j)[1], dtype=ins[0].dtype, device=ins[0].device)
                 for j in range(W)]
     _check_tensors(outs, "outs")
+    opc = OPS[op] if isinstance(op, str) else op
+    if user_from_ring is not None:
+        _check(vcoll_reduce_scatter_ring([t.data_ptr() for t in ins], [t.data_ptr() for t in outs],
+                                         W, n, _dtype_code(ins[0]), opc, list(user_from_ring),
+                                         _stream_handle(stream)))
+        return outs
     fl = flags | (FLAG_RING_ORDER if ring_order else 0)
     _check(vcoll_reduce_scatter([t.data_ptr() for t in ins], [t.data_ptr() for t in outs], W, n,
-                                _dtype_code(ins[0]), OPS[op] if isinstance(op, str) else op, fl,
-                                _stream_handle(stream)))
+                                _dtype_code(ins[0]), opc, fl, _stream_handle(stream)))
     return outs
 
 
@@ -319,15 +351,22 @@ def allgatherv(pieces, outs=None, stream=None):
     return outs
 
 
-def allreduce(ins, outs=None, op="sum", ring_order=False, stream=None, flags=0):
+def allreduce(ins, outs=None, op="sum", ring_order=False, stream=None, flags=0,
+              user_from_ring=None):
     """ins: W CUDA tensors of n elements; outs defaults to new tensors
-    (pass ``outs=ins`` for in place).  Returns outs."""
+    (pass ``outs=ins`` for in place).  Returns outs.  user_from_ring: ring
+    order on that ring (implies ring_order)."""
     torch = _torch()
     W, n = len(ins), ins[0].numel()
     _check_tensors(ins, "ins")
     if outs is None:
         outs = [torch.empty_like(t) for t in ins]
     _check_tensors(outs, "outs")
+    if user_from_ring is not None:
+        _check(vcoll_allreduce_ring([t.data_ptr() for t in ins], [t.data_ptr() for t in outs], W,
+                                    n, _dtype_code(ins[0]), OPS[op] if isinstance(op, str) else op,
+                                    list(user_from_ring), _stream_handle(stream)))
+        return outs
     fl = flags | (FLAG_RING_ORDER if ring_order else 0)
     _check(vcoll_allreduce([t.data_ptr() for t in ins], [t.data_ptr() for t in outs], W, n,
                            _dtype_code(ins[0]), OPS[op] if isinstance(op, str) else op, fl,
@@ -448,6 +487,18 @@ def vcoll_fusion_allreduce(in_ptrs, out_ptrs, counts, T, W, dtype, op, flags=0,
     return rc, nb.value
 
 
+def vcoll_fusion_allreduce_buffered(in_ptrs, out_ptrs, counts, T, fused_ptrs, fused_bytes, W,
+                                    dtype, op, flags=0, threshold_bytes=DEFAULT_FUSION_THRESHOLD,
+                                    stream=0):
+    """Returns (status, number of batches)."""
+    nb = ctypes.c_int()
+    rc = lib().vcoll_fusion_allreduce_buffered(
+        _ptr_array(in_ptrs), _ptr_array(out_ptrs), _i64_array(counts), T, _ptr_array(fused_ptrs),
+        int(fused_bytes), W, dtype, op, flags, int(threshold_bytes), ctypes.byref(nb),
+        stream or None)
+    return rc, nb.value
+
+
 class FusionPlan:
     """Device pointers of a fixed set of tensors marshalled once, so that
     repeated fusion allreduces (one per training step) cost one C call."""
@@ -489,19 +540,24 @@ def fusion_allreduce_direct(tensors, outs, op="avg", ring_order=False,
 
 def fusion_allreduce(tensors, outs, fused, op="avg", ring_order=False,
                      threshold_bytes=DEFAULT_FUSION_THRESHOLD, stream=None):
-    """Horovod-style tensor fusion: plan greedy batches, then per batch pack
-    the tensors of every rank into its fusion buffer ``fused[u]`` (at least
-    the largest batch), allreduce the buffers in place, and unpack into
-    ``outs[u][t]``.  Three library launches per batch."""
+    """Horovod-style tensor fusion through fusion buffers, one C call: plan
+    greedy batches, then per batch of two or more tensors pack every rank's
+    tensors into its fusion buffer ``fused[u]`` (at least the largest batch),
+    allreduce the buffers in place and unpack into ``outs[u][t]``; a batch of
+    one tensor is allreduced straight into its output."""
     W, T = len(tensors), len(tensors[0])
+    flat_in = [tensors[u][t] for u in range(W) for t in range(T)]
+    flat_out = [outs[u][t] for u in range(W) for t in range(T)]
+    _check_tensors(flat_in, "tensors")
+    _check_tensors(flat_out, "outs")
+    _check_tensors(fused, "fused")
     counts = [tensors[0][t].numel() for t in range(T)]
-    dt = _dtype_code(fused[0])
-    begin = fuse_plan(counts, dt, threshold_bytes)
-    for b in range(len(begin) - 1):
-        t0, t1 = begin[b], begin[b + 1]
-        nb = sum(counts[t0:t1])
-        bufs = [f[:nb] for f in fused]
-        fuse_pack([tensors[u][t0:t1] for u in range(W)], bufs, stream)
-        allreduce(bufs, bufs, op, ring_order, stream)
-        fuse_unpack(bufs, [outs[u][t0:t1] for u in range(W)], stream)
+    fbytes = min(f.numel() * f.element_size() for f in fused)
+    flags = FLAG_RING_ORDER if ring_order else 0
+    nb = ctypes.c_int()
+    _check(lib().vcoll_fusion_allreduce_buffered(
+        _ptr_array([t.data_ptr() for t in flat_in]), _ptr_array([t.data_ptr() for t in flat_out]),
+        _i64_array(counts), T, _ptr_array([f.data_ptr() for f in fused]), fbytes, W,
+        _dtype_code(fused[0]), OPS[op] if isinstance(op, str) else op, flags,
+        int(threshold_bytes), ctypes.byref(nb), _stream_handle(stream) or None))
     return outs

@@ -431,7 +431,8 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
 // wire >= 0: the reduced-precision allreduce (fp32 buffers, arithmetic rounded
 // to the 16-bit wire type every hop); -1: the plain collectives.
 int reduce_common(int kind, const void* const* in, void* const* out, int W, int64_t n, int dtype,
-                  int op, unsigned flags, void* stream, int wire = -1) {
+                  int op, unsigned flags, void* stream, int wire = -1,
+                  const int* user_from_ring = nullptr) {
   g_err[0] = 0;
   int rc = check_common(W, n, dtype, op);
   if (rc) return rc;
@@ -460,6 +461,31 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   int vec, phase;
   if ((rc = analyse(bufs, es, &vec, &phase))) return rc;
 
+  // ring order: the kernels fold segment j from input ring_start[j] on.  The
+  // identity ring starts at rank j + 1; a user ring (NCCL's userFromRing:
+  // user_from_ring[p] is the rank at ring position p) reorders the inputs by
+  // ring position and starts segment j at the position after rank j's, so
+  // the fold runs around the ring and ends at rank j
+  const void* ring_in[VCOLL_MAX_RANKS];
+  uint8_t ring_start[VCOLL_MAX_RANKS];
+  for (int j = 0; j < W; ++j) {
+    ring_in[j] = in[j];
+    ring_start[j] = (uint8_t)((j + 1) % W);
+  }
+  if (user_from_ring) {
+    int pos[VCOLL_MAX_RANKS];
+    for (int u = 0; u < W; ++u) pos[u] = -1;
+    for (int q = 0; q < W; ++q) {
+      const int u = user_from_ring[q];
+      if (u < 0 || u >= W || pos[u] >= 0)
+        return fail(VCOLL_ERR_INVALID_ARG, "user_from_ring is not a permutation of 0..%d", W - 1);
+      pos[u] = q;
+    }
+    for (int q = 0; q < W; ++q) ring_in[q] = in[user_from_ring[q]];
+    for (int j = 0; j < W; ++j) ring_start[j] = (uint8_t)((pos[j] + 1) % W);
+    in = ring_in;
+  }
+
   if (wire >= 0) {
     // every rank count, W = 1 included, goes through the kernel: even a single
     // rank's values are rounded to the wire type and back
@@ -478,6 +504,7 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
     prm.nseg = ring ? W : 1;
     prm.phase = vec ? phase : -1;
     prm.ring = ring ? 1 : 0;
+    memcpy(prm.ring_start, ring_start, sizeof(prm.ring_start));
     prm.scale = op == VCOLL_AVG ? 1.0f / (float)W : 1.0f;
     prm.do_scale = op == VCOLL_AVG ? 1 : 0;
     const bool small = n * es <= kSmallBytes;
@@ -540,6 +567,7 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   prm.nseg = nseg;
   prm.phase = phase;
   prm.ring = ring ? 1 : 0;
+  memcpy(prm.ring_start, ring_start, sizeof(prm.ring_start));
   prm.scale = op == VCOLL_AVG ? 1.0f / (float)W : 1.0f;
   prm.do_scale = op == VCOLL_AVG ? 1 : 0;
   if (realign)
@@ -584,6 +612,18 @@ int vcoll_reduce_scatter(const void* const* in, void* const* out, int W, int64_t
 int vcoll_allreduce(const void* const* in, void* const* out, int W, int64_t n, int dtype, int op,
                     unsigned flags, void* stream) {
   return reduce_common(KIND_AR, in, out, W, n, dtype, op, flags, stream);
+}
+
+int vcoll_reduce_scatter_ring(const void* const* in, void* const* out, int W, int64_t n,
+                              int dtype, int op, const int* user_from_ring, void* stream) {
+  return reduce_common(KIND_RS, in, out, W, n, dtype, op, VCOLL_FLAG_RING_ORDER, stream, -1,
+                       user_from_ring);
+}
+
+int vcoll_allreduce_ring(const void* const* in, void* const* out, int W, int64_t n, int dtype,
+                         int op, const int* user_from_ring, void* stream) {
+  return reduce_common(KIND_AR, in, out, W, n, dtype, op, VCOLL_FLAG_RING_ORDER, stream, -1,
+                       user_from_ring);
 }
 
 int vcoll_allreduce_wire(const void* const* in, void* const* out, int W, int64_t n, int wire, int op,
@@ -995,6 +1035,70 @@ int vcoll_fusion_allreduce(const void* const* in, void* const* out, const int64_
   begin.resize(nb + 1);
   if (nbatches) *nbatches = nb;
   return multi_run(in, out, counts, T, W, dtype, op, flags, begin, stream);
+}
+
+int vcoll_fusion_allreduce_buffered(const void* const* in, void* const* out,
+                                    const int64_t* counts, int T, void* const* fused,
+                                    int64_t fused_bytes, int W, int dtype, int op, unsigned flags,
+                                    int64_t threshold_bytes, int* nbatches, void* stream) {
+  g_err[0] = 0;
+  int rc = check_common(W, 0, dtype, op);
+  if (rc) return rc;
+  if (flags & ~(VCOLL_FLAG_RING_ORDER | VCOLL_FLAG_STAGED | VCOLL_FLAG_DIRECT))
+    return fail(VCOLL_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+  if (T < 0) return fail(VCOLL_ERR_INVALID_ARG, "T = %d < 0", T);
+  if (T > 0 && (!counts || !in || !out))
+    return fail(VCOLL_ERR_INVALID_ARG, "invalid fusion arguments");
+  if (!fused || fused_bytes < 0) return fail(VCOLL_ERR_INVALID_ARG, "invalid fusion buffers");
+  const int es = elem_size(dtype);
+  std::vector<int> begin(T + 1);
+  int nb = 0;
+  if ((rc = vcoll_fuse_plan(counts, T, dtype, threshold_bytes, begin.data(), &nb))) return rc;
+  // every check before the first launch: a call that fails enqueues nothing
+  for (int u = 0; u < W; ++u) {
+    if (!fused[u]) return fail(VCOLL_ERR_INVALID_ARG, "fused[%d] is NULL", u);
+    for (int t = 0; t < T; ++t) {
+      const int64_t e = (int64_t)u * T + t;
+      if (counts[t] && (!in[e] || !out[e]))
+        return fail(VCOLL_ERR_INVALID_ARG, "tensor %d of rank %d is NULL", t, u);
+    }
+  }
+  for (int b = 0; b < nb; ++b) {
+    if (begin[b + 1] - begin[b] < 2) continue;
+    int64_t bytes = 0;
+    for (int t = begin[b]; t < begin[b + 1]; ++t) bytes += counts[t] * es;
+    if (bytes > fused_bytes)
+      return fail(VCOLL_ERR_INVALID_ARG,
+                  "batch %d of the plan needs %lld bytes of fusion buffer, fused_bytes = %lld", b,
+                  (long long)bytes, (long long)fused_bytes);
+  }
+  if (nbatches) *nbatches = nb;
+  std::vector<const void*> bin((size_t)W * (T > 0 ? T : 1)), bout((size_t)W * (T > 0 ? T : 1));
+  for (int b = 0; b < nb; ++b) {
+    const int t0 = begin[b], nt = begin[b + 1] - begin[b];
+    // the batch's tensors, rank-major
+    for (int u = 0; u < W; ++u)
+      for (int t = 0; t < nt; ++t) {
+        bin[(size_t)u * nt + t] = in[(int64_t)u * T + t0 + t];
+        bout[(size_t)u * nt + t] = out[(int64_t)u * T + t0 + t];
+      }
+    if (nt == 1) {  // one tensor: allreduced straight from its input to its output
+      if ((rc = reduce_common(KIND_AR, bin.data(), (void* const*)bout.data(), W, counts[t0], dtype,
+                              op, flags, stream)))
+        return rc;
+      continue;
+    }
+    int64_t n = 0;
+    for (int t = t0; t < t0 + nt; ++t) n += counts[t];
+    if ((rc = fuse_common(bin.data(), counts + t0, nt, (const void* const*)fused, W, dtype, 0,
+                          stream)) ||
+        (rc = reduce_common(KIND_AR, (const void* const*)fused, fused, W, n, dtype, op, flags,
+                            stream)) ||
+        (rc = fuse_common(bout.data(), counts + t0, nt, (const void* const*)fused, W, dtype, 1,
+                          stream)))
+      return rc;
+  }
+  return VCOLL_OK;
 }
 
 size_t vcoll_sparse_workspace_bytes(int W, int64_t n, int topk) {

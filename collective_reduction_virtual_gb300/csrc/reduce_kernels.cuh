@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(256) vc_reduce_vec(const __grid_constant__ Red
   const int nthr = blockDim.x;
   for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
     const TileRange tr = tile_range<V>(p, tile);
-    const int start = RING ? rotate(tr.j, 1, WT) : 0;
+    const int start = RING ? p.ring_start[tr.j] : 0;
     uint4 v[U][WT];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(256) vc_reduce_vec_any(const __grid_constant__
   const int nthr = blockDim.x;
   for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
     const TileRange tr = tile_range<V>(p, tile);
-    const int start = p.ring ? rotate(tr.j, 1, W) : 0;
+    const int start = p.ring ? p.ring_start[tr.j] : 0;
     int64_t e[U];
     bool ok[U];
     float acc[U][V];
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(256) vc_reduce_realign(const __grid_constant__
   const int nthr = blockDim.x;
   for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
     const TileRange tr = realign_range<V, KIND>(p, tile);
-    const int start = p.ring ? rotate(tr.j, 1, W) : 0;
+    const int start = p.ring ? p.ring_start[tr.j] : 0;
     const int oph = p.out_phase[tr.j];
     int64_t e[U];
     bool ok[U];
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(256, 3) vc_reduce_realign_w(const __grid_const
   const int nthr = blockDim.x;
   for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
     const TileRange tr = realign_range<V, KIND>(p, tile);
-    const int start = RING ? rotate(tr.j, 1, WT) : 0;
+    const int start = RING ? p.ring_start[tr.j] : 0;
     const uint8_t* shift = p.wshift + tr.j * 8;  // input u's bytes past the grid
     for (int64_t e = tr.e0 + (int64_t)tid * V; e < tr.e1; e += (int64_t)nthr * V) {
       uint4 lo[WT], hi[WT];
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(256) vc_reduce_elem(const __grid_constant__ Re
   const int nthr = blockDim.x;
   for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
     const TileRange tr = tile_range<1>(p, tile);
-    const int start = p.ring ? rotate(tr.j, 1, W) : 0;
+    const int start = p.ring ? p.ring_start[tr.j] : 0;
 #pragma unroll 4
     for (int64_t e = tr.e0 + tid; e < tr.e1; e += nthr)
       reduce_one<T, Op, KIND, 0>(p, W, start, tr.j, tr.a, e);

@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
         const unsigned bytes = (unsigned)(n_el * E::kBytes);
         mbar_arrive_expect_tx(&full[s], bytes * WT);
         if (bytes) {
-          const int start = RING ? rotate(tr.j, 1, WT) : 0;
+          const int start = RING ? p.ring_start[tr.j] : 0;
           unsigned char* st = smem + s * STAGE;
 #pragma unroll
           for (int t = 0; t < WT; ++t) {
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
       break;
     }
     const TileRange tr = tile_range<V>(p, tile);
-    const int start = RING ? rotate(tr.j, 1, WT) : 0;
+    const int start = RING ? p.ring_start[tr.j] : 0;
     const int64_t nvec = tr.e1 > tr.e0 ? (tr.e1 - tr.e0) / V : 0;
     const unsigned char* st = smem + s * STAGE;
     for (int64_t vi = tid; vi < nvec; vi += kStagedConsumerWarps * 32) {

@@ -40,7 +40,7 @@ struct ReduceParams {
   int W;
   int nseg;
   int phase;
-  int ring;      // 1: ring order (start rank (j+1) mod W); 0: fastest order
+  int ring;      // 1: ring order (segment j's fold starts at ring_start[j]); 0: fastest order
   float scale;   // fl32(1/W) for avg
   int do_scale;
   // realigning kernels: address mod 16 of input u's element 0, and of
@@ -51,6 +51,12 @@ struct ReduceParams {
   // the same for W <= 8 as a table: wshift[j * 8 + u] = (in_phase[u] -
   // out_phase[j]) mod 16, input u's bytes past segment j's grid
   uint8_t wshift[64];
+  // ring order: the input (in[] index) whose value starts segment j's fold;
+  // the fold then takes in[ring_start[j] + 1], ... (mod W), so it ends at
+  // ring_start[j] - 1.  With the identity ring ring_start[j] = (j + 1) mod W;
+  // for NCCL's userFromRing permutation the host orders in[] by ring
+  // position and sets ring_start[j] to the position after rank j's
+  uint8_t ring_start[VCOLL_MAX_RANKS];
 };
 
 // Parameters of one allgather launch.  in[j] holds piece j, which lands at

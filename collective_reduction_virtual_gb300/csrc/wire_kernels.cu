@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(256) vc_allreduce_wire(const __grid_constant__
   const int nthr = blockDim.x;
   for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
     const TileRange tr = tile_range<V>(p, tile);
-    const int start = RING ? rotate(tr.j, 1, W) : 0;
+    const int start = RING ? p.ring_start[tr.j] : 0;
     if (p.phase < 0) {  // buffers at different 16-byte phases: element-wise
       for (int64_t e = tr.a + (tile - (int64_t)tr.j * p.tiles_per_seg) * p.tile_elems + tid;
            e < tr.b && e < tr.a + (tile - (int64_t)tr.j * p.tiles_per_seg + 1) * p.tile_elems;

@@ -147,6 +147,27 @@ int vcoll_allreduce(const void* const* in, void* const* out, int W, int64_t n, i
                     unsigned flags, void* stream);
 
 /*
+ * Ring order on a user ring (early NCCL src/reduce_scatter.cu: GetBlock maps
+ * a ring position and step to a block through comm->userFromRing, and the
+ * schedule comment of ncclReduceScatterWithTypeAndFunc works a 4-GPU ring
+ * userFromRing = {1, 2, 0, 3}).  user_from_ring[p] is the rank at ring
+ * position p, a permutation of 0 .. W-1 (host array of W ints; NULL: the
+ * identity ring, the same as VCOLL_FLAG_RING_ORDER).  Segment j is folded
+ * the way the ring reduce-scatter folds block j: it starts with the rank at
+ * the ring position after rank j's, takes the following positions' ranks in
+ * ring order (accumulator first), and ends at rank j.  The result is written
+ * as by vcoll_reduce_scatter / vcoll_allreduce (an allreduce holds the
+ * reduce-scatter's segments in every output: its allgather is a bit copy).
+ * Arguments, aliasing and errors as vcoll_reduce_scatter / vcoll_allreduce;
+ * a user_from_ring that is not a permutation gives VCOLL_ERR_INVALID_ARG.
+ * max and min give the same bits in every order.
+ */
+int vcoll_reduce_scatter_ring(const void* const* in, void* const* out, int W, int64_t n,
+                              int dtype, int op, const int* user_from_ring, void* stream);
+int vcoll_allreduce_ring(const void* const* in, void* const* out, int W, int64_t n, int dtype,
+                         int op, const int* user_from_ring, void* stream);
+
+/*
  * Reduced-precision ("wire") allreduce, Apache SINGA Communicator::synchHalf /
  * fusedSynchHalf: fp32 inputs are converted to the 16-bit wire type (wire =
  * VCOLL_F16 as SINGA's float2half, or VCOLL_BF16), allreduced in that type by
@@ -216,6 +237,31 @@ int vcoll_allreduce_multi(const void* const* in, void* const* out, const int64_t
 int vcoll_fusion_allreduce(const void* const* in, void* const* out, const int64_t* counts, int T,
                            int W, int dtype, int op, unsigned flags, int64_t threshold_bytes,
                            int* nbatches, void* stream);
+
+/*
+ * Tensor fusion through fusion buffers, Horovod operations.cc PerformOperation
+ * (the NCCL allreduce path): the tensors are planned into the batches of
+ * vcoll_fuse_plan(counts, T, dtype, threshold_bytes); for each batch of two or
+ * more tensors every rank's tensors are copied back to back into that rank's
+ * fusion buffer fused[u] (MEMCPY_IN_FUSION_BUFFER), the W buffers are
+ * allreduced in place (NCCL_ALLREDUCE), and the results are copied out to
+ * the output tensors (MEMCPY_OUT_FUSION_BUFFER); a batch of one tensor is
+ * allreduced straight from its input to its output, as Horovod does with a
+ * single entry.  The same fusion buffers serve every batch, in order, on
+ * `stream`: the whole pipeline (3 launches per fused batch) runs from one
+ * call.  The bits equal vcoll_fusion_allreduce's.
+ * in, out: host arrays of W*T device pointers, rank-major; out[e] may equal
+ * in[e] (in place), no other tensor may overlap another.  counts: host, T
+ * element counts.  fused: host array of W device pointers, each to
+ * fused_bytes bytes that overlap no tensor; every batch of two or more
+ * tensors must fit (VCOLL_ERR_INVALID_ARG otherwise, before anything is
+ * enqueued).  *nbatches (may be NULL) receives the batch count.  Other
+ * arguments and errors as vcoll_allreduce.
+ */
+int vcoll_fusion_allreduce_buffered(const void* const* in, void* const* out,
+                                    const int64_t* counts, int T, void* const* fused,
+                                    int64_t fused_bytes, int W, int dtype, int op, unsigned flags,
+                                    int64_t threshold_bytes, int* nbatches, void* stream);
 
 /*
  * Sparsified allreduce with error feedback (Apache SINGA

@@ -220,6 +220,39 @@ def test_fusion_allreduce_errors(v):
     assert rc == v.OK and nb == 1
 
 
+def test_ring_permutation_errors(v):
+    W = 4
+    for f in (v.vcoll_reduce_scatter_ring, v.vcoll_allreduce_ring):
+        assert f(FAKE_IN[:W], FAKE_OUT[:W], W, 64, v.F32, v.SUM, [0, 1, 1, 3]) == \
+            v.ERR_INVALID_ARG
+        assert "permutation" in v.last_error()
+        assert f(FAKE_IN[:W], FAKE_OUT[:W], W, 64, v.F32, v.SUM, [0, 1, 2, 4]) == \
+            v.ERR_INVALID_ARG
+        assert f(FAKE_IN[:W], FAKE_OUT[:W], W, 64, 7, v.SUM, [0, 1, 2, 3]) == v.ERR_INVALID_TYPE
+        assert f(FAKE_IN[:W], FAKE_OUT[:W], W, 64, v.F32, 9, [0, 1, 2, 3]) == v.ERR_INVALID_OP
+        # n == 0 enqueues nothing
+        assert f(FAKE_IN[:W], FAKE_OUT[:W], W, 0, v.F32, v.SUM, [3, 2, 1, 0]) == v.OK
+
+
+def test_fusion_allreduce_buffered_errors(v):
+    ins = [0x100000 * (i + 1) for i in range(4)]
+    outs = [0x10000000 + 0x100000 * i for i in range(4)]
+    fused = [0x20000000, 0x21000000]
+    f = v.vcoll_fusion_allreduce_buffered
+    assert f(ins, outs, [10, 20], 2, fused, 120, 2, v.F32, 9)[0] == v.ERR_INVALID_OP
+    assert f(ins, outs, [10, 20], 2, fused, 120, 2, 5, v.SUM)[0] == v.ERR_INVALID_TYPE
+    assert f(ins, outs, [10, -1], 2, fused, 120, 2, v.F32, v.SUM)[0] == v.ERR_INVALID_ARG
+    assert f(ins, outs, [10, 20], 2, [0, 0], 120, 2, v.F32, v.SUM)[0] == v.ERR_INVALID_ARG
+    assert f(ins, outs, [10, 20], 2, fused, -1, 2, v.F32, v.SUM)[0] == v.ERR_INVALID_ARG
+    # the plan's one batch of two tensors needs 120 bytes per rank: refused
+    # before anything is enqueued
+    rc, _ = f(ins, outs, [10, 20], 2, fused, 119, 2, v.F32, v.SUM)
+    assert rc == v.ERR_INVALID_ARG and "fusion buffer" in v.last_error()
+    # zero-length tensors: nothing to do
+    rc, nb = f([0] * 4, [0] * 4, [0, 0], 2, fused, 0, 2, v.F32, v.SUM, 0, 64)
+    assert rc == v.OK and nb == 1
+
+
 def test_allreduce_wire_errors(v):
     f = v.vcoll_allreduce_wire
     assert f(FAKE_IN[:4], FAKE_OUT[:4], 4, 64, v.F32, v.SUM) == v.ERR_INVALID_TYPE

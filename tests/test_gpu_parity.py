@@ -403,6 +403,26 @@ def test_allreduce_multi_in_place_and_many_tensors(v):
             assert_bit_exact(to_np(tens[u][t]), want[u][t], "multi in place")
 
 
+def test_fusion_buffered_in_place_and_one_tensor_batches(v):
+    # the C pipeline in place (outputs are the inputs), with batches of one
+    # tensor (above the threshold: allreduced straight, no buffer) between
+    # fused ones, and a fusion buffer exactly as large as the largest batch
+    W = 4
+    counts = [1000, 3, 9000, 250, 1, 60, 20000, 7, 7]
+    thr = 4 * 5000
+    tens = _tensor_list(W, counts, "f32", 41)
+    want = oracle.fusion_allreduce([[to_np(t) for t in tens[u]] for u in range(W)], counts, "sum",
+                                   oracle.F32, thr)
+    begin = v.fuse_plan(counts, v.F32, thr)
+    largest = max(sum(counts[begin[b]:begin[b + 1]]) for b in range(len(begin) - 1)
+                  if begin[b + 1] - begin[b] > 1)
+    fused = [torch.empty(largest, device="cuda") for _ in range(W)]
+    v.fusion_allreduce(tens, tens, fused, op="sum", ring_order=True, threshold_bytes=thr)
+    for u in range(W):
+        for t in range(len(counts)):
+            assert_bit_exact(to_np(tens[u][t]), want[u][t], f"buffered in place {u} {t}")
+
+
 def test_fusion_direct_equals_pipeline_full_workload(v):
     # 200 fp32 tensors per rank, W = 8, 64 MiB batches: the one-pass path and
     # the pack -> allreduce -> unpack path give the same bits everywhere
@@ -489,6 +509,58 @@ def test_avg_scale_rounding_hand_derived_on_gpu(v, n):
             for o in outs:
                 got = (o.view(view).to(torch.int64) & mask).unique().tolist()
                 assert got == [want], (line, ring, [hex(g) for g in got])
+
+
+# Ring order on a user ring (NCCL's userFromRing): the page's 4-GPU example
+# by hand, then random rings against the oracle's ring simulation.
+
+@pytest.mark.parametrize("n", [4, 4 * 50_000])
+def test_ring_permutation_hand_derived_on_gpu(v, n):
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "ring_order_cancellation.txt")
+    rows = [ln.strip() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    x = [torch.full((n,), val, device="cuda") for val in (1e8, 1.0, -1e8, 1.0)]
+    for line in rows:
+        ring_s, res_s = line.split(":")
+        ring = [0, 1, 2, 3] if ring_s.strip() == "identity" else [int(q) for q in ring_s.split()]
+        want = [float(q) for q in res_s.split()]
+        segs = v.reduce_scatter(x, op="sum", user_from_ring=ring)
+        assert [s.unique().tolist() for s in segs] == [[w] for w in want], ring_s
+        ar = v.allreduce(x, op="sum", user_from_ring=ring)
+        for u in range(4):
+            assert [ar[u][j * n // 4: (j + 1) * n // 4].unique().tolist() for j in range(4)] == \
+                [[w] for w in want], ring_s
+
+
+@pytest.mark.parametrize("W", [3, 4, 5, 8, 16, 64])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shift", [0, "mixed"])
+def test_ring_permutation_matches_oracle(v, W, dtype, shift):
+    n = 40_000 + W + 3  # several tiles per segment, uneven segments
+    rng = np.random.default_rng(1000 + W)
+    ring = [int(q) for q in rng.permutation(W)]
+    base = make_inputs(W, n + 4, dtype, 77 + W)
+    ins = [b[(u % 4 if shift == "mixed" else 0):][:n] for u, b in enumerate(base)]
+    ins_np = [to_np(t) for t in ins]
+    for op in ("sum", "avg", "prod"):
+        want = oracle.reduce_scatter(ins_np, op, ODT[dtype], ring)
+        segs = v.reduce_scatter(ins, op=op, user_from_ring=ring)
+        for j in range(W):
+            assert_bit_exact(to_np(segs[j]), want[j], f"ring RS {op} W={W} seg {j}")
+        want_ar = oracle.allreduce(ins_np, op, ODT[dtype], ring)
+        outs = v.allreduce(ins, op=op, user_from_ring=ring)
+        for u in range(W):
+            assert_bit_exact(to_np(outs[u]), want_ar[u], f"ring AR {op} W={W} rank {u}")
+
+
+def test_ring_permutation_in_place(v):
+    W, n = 8, 100_003
+    ring = [3, 7, 0, 5, 1, 6, 2, 4]
+    bufs = make_inputs(W, n, "f32", 5)
+    want = oracle.allreduce([to_np(t) for t in bufs], "sum", oracle.F32, ring)
+    v.allreduce(bufs, bufs, op="sum", user_from_ring=ring)
+    for u in range(W):
+        assert_bit_exact(to_np(bufs[u]), want[u], f"ring AR in place {u}")
 
 
 # ------------------------------------------------------------ allgatherv
@@ -752,6 +824,23 @@ def test_sparse_topk_settled_residuals_layouts(v, shift, frac):
     outs = [o[ph["out"](u): ph["out"](u) + n] for u, o in enumerate(obase)]
     _check_sparse(v, ins, acc, frac, True, outs=outs)
     _check_sparse(v, ins, acc, frac, True, outs=outs)  # a second step on the new residuals
+
+
+# Without accumulations the candidate pass takes two tiles per CTA (one list
+# reservation for both): odd and even tile counts, a head and tail in every
+# tile, and mixed phases (the element-wise form) must all give the oracle's
+# bits, on the list route (small K) and with the two-sided band.
+@pytest.mark.parametrize("shift", [0, 1, 3, "mixed"])
+@pytest.mark.parametrize("n", [129 * 4096 + 11, 128 * 4096 - 1, 4096 + 5])
+@pytest.mark.parametrize("frac", [0.01, 0.3])
+def test_sparse_topk_no_accumulation_layouts(v, shift, n, frac):
+    W = 8
+    base = _sparse_inputs(W, n + 4, 310 + n % 97)
+    obase = [torch.empty(n + 4, device="cuda") for _ in range(W)]
+    pin = (lambda u: u % 4) if shift == "mixed" else (lambda u: shift)
+    ins = [b[pin(u): pin(u) + n] for u, b in enumerate(base)]
+    outs = [o[pin(u): pin(u) + n] for u, o in enumerate(obase)]
+    _check_sparse(v, ins, None, frac, True, outs=outs)
 
 
 def test_sparse_topk_settled_bin_contradicted(v):
