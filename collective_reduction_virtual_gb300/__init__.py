@@ -538,26 +538,51 @@ def fusion_allreduce_direct(tensors, outs, op="avg", ring_order=False,
     return outs
 
 
+class FusionBufferPlan:
+    """Horovod-style tensor fusion through fusion buffers with the device
+    pointers marshalled once: each call plans the greedy batches and runs,
+    per batch of two or more tensors, pack into ``fused[u]`` -> in-place
+    allreduce -> unpack (a batch of one tensor is allreduced straight), all
+    in one C call."""
+
+    def __init__(self, tensors, outs, fused, op="avg", ring_order=False,
+                 threshold_bytes=DEFAULT_FUSION_THRESHOLD):
+        W, T = len(tensors), len(tensors[0])
+        flat_in = [tensors[u][t] for u in range(W) for t in range(T)]
+        flat_out = [outs[u][t] for u in range(W) for t in range(T)]
+        _check_tensors(flat_in, "tensors")
+        _check_tensors(flat_out, "outs")
+        _check_tensors(fused, "fused")
+        self.W, self.T = W, T
+        self.counts = [tensors[0][t].numel() for t in range(T)]
+        self._in = _ptr_array([t.data_ptr() for t in flat_in])
+        self._out = _ptr_array([t.data_ptr() for t in flat_out])
+        self._fused = _ptr_array([f.data_ptr() for f in fused])
+        self._counts = _i64_array(self.counts)
+        self.fused_bytes = min(f.numel() * f.element_size() for f in fused)
+        self.dtype = _dtype_code(fused[0])
+        self.op = OPS[op] if isinstance(op, str) else op
+        self.flags = FLAG_RING_ORDER if ring_order else 0
+        self.threshold = int(threshold_bytes)
+        self._keep = (flat_in, flat_out, list(fused))
+        self.nbatches = 0
+
+    def __call__(self, stream=None):
+        nb = ctypes.c_int()
+        _check(lib().vcoll_fusion_allreduce_buffered(
+            self._in, self._out, self._counts, self.T, self._fused, self.fused_bytes, self.W,
+            self.dtype, self.op, self.flags, self.threshold, ctypes.byref(nb),
+            _stream_handle(stream) or None))
+        self.nbatches = nb.value
+
+
 def fusion_allreduce(tensors, outs, fused, op="avg", ring_order=False,
                      threshold_bytes=DEFAULT_FUSION_THRESHOLD, stream=None):
     """Horovod-style tensor fusion through fusion buffers, one C call: plan
     greedy batches, then per batch of two or more tensors pack every rank's
     tensors into its fusion buffer ``fused[u]`` (at least the largest batch),
     allreduce the buffers in place and unpack into ``outs[u][t]``; a batch of
-    one tensor is allreduced straight into its output."""
-    W, T = len(tensors), len(tensors[0])
-    flat_in = [tensors[u][t] for u in range(W) for t in range(T)]
-    flat_out = [outs[u][t] for u in range(W) for t in range(T)]
-    _check_tensors(flat_in, "tensors")
-    _check_tensors(flat_out, "outs")
-    _check_tensors(fused, "fused")
-    counts = [tensors[0][t].numel() for t in range(T)]
-    fbytes = min(f.numel() * f.element_size() for f in fused)
-    flags = FLAG_RING_ORDER if ring_order else 0
-    nb = ctypes.c_int()
-    _check(lib().vcoll_fusion_allreduce_buffered(
-        _ptr_array([t.data_ptr() for t in flat_in]), _ptr_array([t.data_ptr() for t in flat_out]),
-        _i64_array(counts), T, _ptr_array([f.data_ptr() for f in fused]), fbytes, W,
-        _dtype_code(fused[0]), OPS[op] if isinstance(op, str) else op, flags,
-        int(threshold_bytes), ctypes.byref(nb), _stream_handle(stream) or None))
+    one tensor is allreduced straight into its output.  (Repeated calls on
+    the same tensors: FusionBufferPlan marshals the pointers once.)"""
+    FusionBufferPlan(tensors, outs, fused, op, ring_order, threshold_bytes)(stream)
     return outs

@@ -612,9 +612,9 @@ __device__ __forceinline__ uint32_t settled_key(const SparseParams& p, int r) {
 // (their keys parked in shared memory, so the loop over set bits needs no
 // register indexing).  The list is compact; the order between tiles is
 // arbitrary (the index travels with the key).  Entries past the capacity are
-// counted but not stored, which sends the rank to the full path.  ACC: with
-// accumulations (compiled apart: their code slowed the pass without them by
-// a tenth even where it never ran).
+// counted but not stored, which sends the rank to the full path.  Only the
+// form with accumulations (ACC) runs; the pass without them is
+// vc_topk_filter_raw below.
 template <bool ACC>
 __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ SparseParams p) {
   pdl_enter();
@@ -782,6 +782,193 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
     // may reset them for the next tile; s_base and s_listed change only
     // after the next tile's second barrier, which every thread passes after
     // these reads; each thread reads only its own row of s_key)
+  }
+}
+
+// "key >= bound" on the raw fp32 bits u, without forming the key: for a
+// bound at or above the key of +0 (sign bit set) it is a signed compare of u
+// against the bound's low 31 bits (negative u, -0 included, lies below);
+// below it an unsigned compare against ~bound (every non-negative u passes,
+// a negative u when ~u >= bound).  NaNs order as their keys do.
+struct RawBound {
+  uint32_t t;
+  bool sgn;
+};
+__device__ __forceinline__ RawBound raw_bound(uint32_t key) {
+  return (key & 0x80000000u) ? RawBound{key & 0x7FFFFFFFu, true} : RawBound{~key, false};
+}
+template <bool SGN>
+__device__ __forceinline__ bool raw_at_least(uint32_t u, uint32_t t) {
+  return SGN ? (int32_t)u >= (int32_t)t : u <= t;
+}
+
+// One tile of the candidate pass without accumulations: each thread loads
+// four 16-byte vectors (vector v = tid + 256 u of the tile's aligned body)
+// and at most one of the tile's unaligned head or tail entries; bit 4 u + q
+// of the thread's mask is entry q of its vector u.  LOW_SGN: the lower
+// bound's compare form (uniform per rank); BAND: an upper bound is set
+// (entries above it are counted, not listed).  The keys of the listed
+// entries are formed only for those entries.
+template <bool LOW_SGN, bool BAND>
+__device__ __forceinline__ void filter_tile_raw(const SparseParams& p, int r, int64_t tile,
+                                                uint32_t* s_raw, uint32_t& s_n, uint32_t& s_sure,
+                                                unsigned long long& s_base) {
+  constexpr int E = 4 * kTileVecs;  // entries per thread (plus one extra)
+  const int tid = threadIdx.x, lane = tid & 31;
+  const RawBound lo = raw_bound(p.state[r].lowkey);
+  const uint32_t topkey = (uint32_t)((((uint64_t)p.state[r].high + 1) << 21) - 1);
+  // above the band: key >= topkey + 1 (BAND only, so topkey < 0xFFFFFFFF)
+  const RawBound hi = raw_bound(BAND ? topkey + 1 : 0xFFFFFFFFu);
+  auto above = [&](uint32_t u) -> bool {
+    return BAND && (hi.sgn ? raw_at_least<true>(u, hi.t) : raw_at_least<false>(u, hi.t));
+  };
+  auto cand = [&](uint32_t u) -> bool { return raw_at_least<LOW_SGN>(u, lo.t) && !above(u); };
+  const char* src = (const char*)p.in[r];
+  const bool vec = p.phase >= 0;
+  const int64_t t0 = tile * p.tile_elems;
+  const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
+  int64_t av = t0, bv = t0;
+  if (vec) aligned_body<4>(t0, t1, p.phase, av, bv);
+  const int nv = (int)((bv - av) / 4);
+  if (tid == 0) {
+    s_n = 0;
+    s_sure = 0;
+  }
+  uint32_t mask = 0;
+  int sure = 0;  // entries above the band
+  // the one extra entry: threads 0-31 take the tile's head, 32-63 its tail
+  int64_t extra = -1;
+  uint32_t xraw = 0;
+  bool xhit = false;
+  if (vec) {
+    uint4 a[kTileVecs];
+    const char* tp = src + av * 4 + tid * 16;
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) {
+      a[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (tid + u * kSparseThreads < nv) a[u] = ld_stream(tp + u * kSparseThreads * 16);
+    }
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) reg_fence(a[u]);
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) {
+      const uint4 x = a[u];
+      if (tid + u * kSparseThreads < nv) {
+        mask |= ((uint32_t)cand(x.x) | (uint32_t)cand(x.y) << 1 | (uint32_t)cand(x.z) << 2 |
+                 (uint32_t)cand(x.w) << 3)
+                << (u * 4);
+        if (BAND) sure += above(x.x) + above(x.y) + above(x.z) + above(x.w);
+      }
+      // vector u of every thread side by side: a warp's stores are contiguous
+      reinterpret_cast<uint4*>(s_raw)[u * kSparseThreads + tid] = x;
+    }
+    if (tid < av - t0) extra = t0 + tid;
+    if (tid >= 32 && tid - 32 < t1 - bv) extra = bv + (tid - 32);
+  } else {  // element-wise: entries t0 + tid + 256 j
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const int64_t i = t0 + tid + (int64_t)j * kSparseThreads;
+      uint32_t x = 0;
+      if (i < t1) {
+        x = ld1<uint32_t>(src + i * 4);
+        mask |= (uint32_t)cand(x) << j;
+        if (BAND) sure += above(x);
+      }
+      s_raw[j * kSparseThreads + tid] = x;
+    }
+  }
+  if (extra >= 0) {
+    xraw = ld1<uint32_t>(src + extra * 4);
+    xhit = cand(xraw);
+    if (BAND) sure += above(xraw);
+  }
+  // this thread's place among the warp's candidates
+  const uint32_t c = __popc(mask) + (xhit ? 1u : 0u);
+  uint32_t incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t wtotal = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  unsigned wsure = 0;
+  if (BAND) wsure = __reduce_add_sync(0xFFFFFFFFu, (unsigned)sure);
+  __syncthreads();  // s_n and s_sure are zero
+  uint32_t wbase = 0;
+  if (lane == 31 && wtotal) wbase = atomicAdd(&s_n, wtotal);
+  if (BAND && lane == 0 && wsure) atomicAdd(&s_sure, wsure);
+  wbase = __shfl_sync(0xFFFFFFFFu, wbase, 31);
+  __syncthreads();  // every warp has reserved its share of the tile's room
+  if (tid == 0) {
+    const uint32_t tot = s_n;
+    const unsigned long long base = tot ? atomicAdd(p.cand_n + r, (unsigned long long)tot) : 0ull;
+    s_base = base;
+    if (BAND && s_sure) atomicAdd(p.cand_n + p.W + r, (unsigned long long)s_sure);
+    p.tilecnt[(int64_t)r * p.tiles_per_rank + tile] = tot;
+    p.chunk[(int64_t)r * p.tiles_per_rank + tile] = (uint32_t)base;
+  }
+  __syncthreads();
+  const unsigned long long cap = (unsigned long long)p.cand_cap;
+  uint32_t* ckey = p.cand_key + (int64_t)r * p.cand_cap;
+  uint32_t* cidx = p.cand_idx + (int64_t)r * p.cand_cap;
+  unsigned long long pos = s_base + wbase + (incl - c);
+  for (uint32_t m = mask; m; m &= m - 1u) {  // this thread's candidates only
+    const int j = __ffs(m) - 1;
+    int64_t i;
+    int sj;
+    if (vec) {
+      i = av + (int64_t)(tid + (j >> 2) * kSparseThreads) * 4 + (j & 3);
+      sj = ((j >> 2) * kSparseThreads + tid) * 4 + (j & 3);
+    } else {
+      i = t0 + tid + (int64_t)j * kSparseThreads;
+      sj = j * kSparseThreads + tid;
+    }
+    if (pos < cap) {
+      ckey[pos] = order_key(__uint_as_float(s_raw[sj]));
+      cidx[pos] = (uint32_t)i;
+    }
+    ++pos;
+  }
+  if (xhit && pos < cap) {
+    ckey[pos] = order_key(__uint_as_float(xraw));
+    cidx[pos] = (uint32_t)extra;
+  }
+  // (on to the next tile without a barrier: only thread 0 read s_n, s_base
+  // changes only after the next tile's second barrier, which every thread
+  // passes after its reads above, and each thread reads only its own slots
+  // of s_raw)
+}
+
+// The candidate pass without accumulations reads one array per rank, and its
+// cost per tile is latency -- the tile's loads, then the list reservation (a
+// global atomic round trip behind two barriers) -- more than bytes.  So this
+// form keeps as many tiles in flight as it can: 32 registers and 16 KiB of
+// shared memory per 256-thread CTA give 8 CTAs per SM (the form with
+// accumulations needs 40 registers and gets 6).  It spends few instructions
+// per entry: the band test is one integer compare on the raw fp32 bits per
+// bound, the count above the band runs only when there is one, and keys are
+// formed only for the listed entries.  Every warp's shared-memory stores are
+// contiguous (vector u of all threads side by side).
+__global__ void __launch_bounds__(256, 8) vc_topk_filter_raw(const __grid_constant__ SparseParams p) {
+  pdl_enter();
+  __shared__ __align__(16) uint32_t s_raw[kSparseThreads * 4 * kTileVecs];
+  __shared__ uint32_t s_n, s_sure;
+  __shared__ unsigned long long s_base;
+  const int r = blockIdx.y;
+  const bool band = p.state[r].high < kTopkBins - 1;  // uniform per CTA
+  const bool sgn = (p.state[r].lowkey & 0x80000000u) != 0;
+  for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x) {
+    if (band) {
+      if (sgn)
+        filter_tile_raw<true, true>(p, r, tile, s_raw, s_n, s_sure, s_base);
+      else
+        filter_tile_raw<false, true>(p, r, tile, s_raw, s_n, s_sure, s_base);
+    } else {
+      if (sgn)
+        filter_tile_raw<true, false>(p, r, tile, s_raw, s_n, s_sure, s_base);
+      else
+        filter_tile_raw<false, false>(p, r, tile, s_raw, s_n, s_sure, s_base);
+    }
   }
 }
 
@@ -1105,7 +1292,7 @@ const void* topk_select_kernel(int pass) {
                    : pass == 1 ? (const void*)&vc_topk_select<1> : (const void*)&vc_topk_select<2>;
 }
 const void* topk_filter_kernel(int has_acc) {
-  return has_acc ? (const void*)&vc_topk_filter<true> : (const void*)&vc_topk_filter<false>;
+  return has_acc ? (const void*)&vc_topk_filter<true> : (const void*)&vc_topk_filter_raw;
 }
 const void* topk_list_out_kernel() { return (const void*)&vc_topk_list_out; }
 const void* topk_restore_kernel() { return (const void*)&vc_topk_restore; }

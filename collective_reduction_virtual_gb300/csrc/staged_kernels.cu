@@ -27,6 +27,10 @@ __device__ unsigned int g_vcoll_device_error = 0;
 namespace {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// The drain before a producer returns: copies already issued cannot be
+// cancelled, and the CTA (its shared memory and mbarriers) must stay resident
+// until they land, so this wait is allowed much longer before it gives up.
+constexpr uint64_t kDrainLimitNs = 20000000000ull;  // 20 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -162,9 +166,11 @@ __global__ void __launch_bounds__(kStagedThreads, 1)
           }
         }
       }
-      // wait (bounded) until every copy this CTA issued has landed
+      // wait (bounded, with the longer drain limit) until every copy this
+      // CTA issued has landed; the other threads may have returned, but the
+      // CTA stays resident while this lane waits
       for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i)
-        mbar_wait(&full[i % S], (i / S) & 1);
+        mbar_wait(&full[i % S], (i / S) & 1, kDrainLimitNs);
     }
     return;
   }
@@ -338,8 +344,10 @@ __global__ void __launch_bounds__(kGatherTmaThreads, 1) vc_gather_tma(const __gr
       ++issued;
     }
   }
-  // after a timeout: wait (bounded) for the loads issued but not consumed
-  for (int64_t i = consumed; i < issued; ++i) mbar_wait(&full[i % S], (unsigned)((i / S) & 1));
+  // after a timeout: wait (bounded, with the longer drain limit) for the
+  // loads issued but not consumed
+  for (int64_t i = consumed; i < issued; ++i)
+    mbar_wait(&full[i % S], (unsigned)((i / S) & 1), kDrainLimitNs);
   bulk_wait_all();
 }
 
