@@ -333,13 +333,13 @@ def build_workload(args, dev, rank):
         ins = [shifted_copy(t, u % 4) for u, t in enumerate(ins)]
     if args.op in ("wire", "sparse", "sparse_topk"):
         outs = [torch.empty_like(t) for t in ins]
+        topk = args.op == "sparse_topk"
         if args.op == "wire":
             step = lambda: vc.allreduce_wire(ins, outs, wire="f16", op=red,  # noqa
                                              ring_order=ring)
             bytes_ = 2 * W * n * 4
             what = "fp16-wire allreduce"
         else:
-            topk = args.op == "sparse_topk"
             acc = None if args.no_accumulation else [torch.zeros_like(t) for t in ins]
             nnz = torch.empty(W, dtype=torch.int64, device=dev)
             wsb = (vc.sparse_workspace_min_bytes(W, n, topk) if args.sparse_workspace == "min"
@@ -657,6 +657,29 @@ def extras(args, stream, dev):
             lat[f"ar_sum_W{W}_{nbytes}B"] = {"us": round(r["ms"] * 1e3, 2), "GBps": r["GBps"]}
             del ins, outs
     out["small_message_graph_1000"] = lat
+
+    # a slice of the message-size sweep (--sweep runs all 420 points): W = 8,
+    # fp32 sum, per-rank sizes from the latency path to past L2, each point
+    # a CUDA graph of repeated launches (bytes per op as above)
+    W = 8
+    sweep = {}
+    for nbytes in (1 << 12, 1 << 16, 1 << 20, 1 << 23, 1 << 26):
+        n = nbytes // 4
+        ins = [I.uniform(n, I.rank_seed(I.SWEEP, u), dev) for u in range(W)]
+        outs = [torch.empty_like(t) for t in ins]
+        segs = [torch.empty(vc.segment(n, W, j)[1], device=dev) for j in range(W)]
+        reps = int(max(3, min(1000, 2e9 // (2 * W * nbytes))))
+        row = {}
+        for name, fn, b in (
+                ("rs", lambda s: vc.reduce_scatter(ins, segs, op="sum", stream=s), (W + 1) * nbytes),
+                ("ag", lambda s: vc.allgather(segs, n, outs, stream=s), (1 + W) * nbytes),
+                ("ar", lambda s: vc.allreduce(ins, outs, op="sum", stream=s), 2 * W * nbytes)):
+            r = graph_rate(fn, b, reps)
+            row[name] = {"GBps": r["GBps"], "us": round(r["ms"] * 1e3, 2)}
+        sweep[f"W8_{nbytes}B_per_rank"] = row
+        del ins, outs, segs
+    torch.cuda.empty_cache()
+    out["sweep_w8_f32_sum_graph"] = sweep
     return out
 
 

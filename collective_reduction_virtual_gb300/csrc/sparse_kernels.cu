@@ -1087,8 +1087,10 @@ __global__ void __launch_bounds__(256) vc_topk_restore(const __grid_constant__ S
 // settled key) become x - (0 + x), and the tile is written to every output.
 // Each thread loads its entry of eight ranks' chunks before folding them, so
 // a tile costs one round trip for the chunk bounds and one per eight ranks
-// for the entries.
-__global__ void __launch_bounds__(256) vc_topk_list_out(const __grid_constant__ SparseParams p) {
+// for the entries.  Those round trips are latency the tile's writes cannot
+// hide, so the kernel is held to 32 registers (32-bit list indices) for 8
+// CTAs per SM.
+__global__ void __launch_bounds__(256, 8) vc_topk_list_out(const __grid_constant__ SparseParams p) {
   pdl_enter();
   if (!list_route(p)) return;
   __shared__ uint32_t s_T[VCOLL_MAX_RANKS], s_set[VCOLL_MAX_RANKS];
@@ -1133,11 +1135,11 @@ __global__ void __launch_bounds__(256) vc_topk_list_out(const __grid_constant__ 
     for (int g = 0; g < W; g += R) {
       // entry tid of the chunks of ranks g .. g + R - 1, loaded together
       uint32_t pk[R];
-      int64_t pi[R];
+      uint32_t pi[R];  // list indices are 32-bit; 0xFFFFFFFF: none
 #pragma unroll
       for (int q = 0; q < R; ++q) {
         pk[q] = 0;
-        pi[q] = -1;
+        pi[q] = 0xFFFFFFFFu;
         if (g + q < W && (uint32_t)tid < s_cnt4[g + q]) {
           pk[q] = p.cand_key[s_c0[g + q] + tid];
           pi[q] = p.cand_idx[s_c0[g + q] + tid];
@@ -1147,7 +1149,7 @@ __global__ void __launch_bounds__(256) vc_topk_list_out(const __grid_constant__ 
       for (int q = 0; q < R; ++q) {
         const int r = g + q;
         if (r >= W) break;
-        if (pi[q] >= 0) fold(r, pk[q], pi[q]);
+        if (pi[q] != 0xFFFFFFFFu) fold(r, pk[q], (int64_t)pi[q]);
         for (uint32_t j = tid + blockDim.x; j < s_cnt4[r]; j += blockDim.x)
           fold(r, p.cand_key[s_c0[r] + j], p.cand_idx[s_c0[r] + j]);
         __syncthreads();  // rank order: rank r's adds land before rank r + 1's

@@ -2,8 +2,9 @@
  * A plain C client of the vcoll C ABI (include/vcoll.h), built by
  * tests/test_c_client.py.  Mode "host": argument checks and the host-only
  * helpers, no GPU needed.  Mode "gpu": integer-valued fp32 buffers on the
- * device, reduce-scatter / allgather / allreduce through the ABI, results
- * printed for the test to check against exact sums.
+ * device through reduce-scatter / allgather / allreduce, the user-ring
+ * reduce-scatter and the fusion-buffer pipeline; every output element is
+ * printed as its bits for the test to check against the oracle.
  */
 #include <stdio.h>
 #include <stdlib.h>
@@ -38,6 +39,20 @@ static int host_mode(void) {
   return 0;
 }
 
+static void print_bits(const char* tag, int u, const float* d, int n) {
+  float* h = (float*)malloc(sizeof(float) * (n > 0 ? n : 1));
+  cudaMemcpy(h, d, sizeof(float) * n, cudaMemcpyDeviceToHost);
+  for (int i = 0; i < n; ++i) {
+    unsigned bits;
+    memcpy(&bits, &h[i], 4);
+    printf("%s %d %d %08x\n", tag, u, i, bits);
+  }
+  free(h);
+}
+
+/* Integer-valued inputs through reduce-scatter + allgather, allreduce, the
+ * user-ring reduce-scatter and the fusion-buffer pipeline; every output
+ * element is printed as its bits for the test to compare with the oracle. */
 static int gpu_mode(void) {
   float* h = (float*)malloc(sizeof(float) * N);
   float* d_in[W];
@@ -58,19 +73,43 @@ static int gpu_mode(void) {
                        0, NULL);
   if (rc) { printf("ag %d %s\n", rc, vcoll_last_error()); return 1; }
   cudaDeviceSynchronize();
-  for (int u = 0; u < W; ++u) {
-    cudaMemcpy(h, d_out[u], sizeof(float) * N, cudaMemcpyDeviceToHost);
-    double s = 0;
-    for (int i = 0; i < N; ++i) s += h[i] * (double)(i % 5 + 1);
-    printf("ag_checksum %d %.1f\n", u, s);
-  }
+  for (int u = 0; u < W; ++u) print_bits("ag", u, d_out[u], N);
   rc = vcoll_allreduce(in, (void* const*)d_out, W, N, VCOLL_F32, VCOLL_SUM, 0, NULL);
   if (rc) { printf("ar %d %s\n", rc, vcoll_last_error()); return 1; }
   cudaDeviceSynchronize();
-  cudaMemcpy(h, d_out[W - 1], sizeof(float) * N, cudaMemcpyDeviceToHost);
-  double s = 0;
-  for (int i = 0; i < N; ++i) s += h[i] * (double)(i % 5 + 1);
-  printf("ar_checksum %.1f\n", s);
+  for (int u = 0; u < W; ++u) print_bits("ar", u, d_out[u], N);
+  /* avg over the ring {1, 2, 0, 3}: segment j ends at rank j */
+  const int ring[W] = {1, 2, 0, 3};
+  rc = vcoll_reduce_scatter_ring(in, (void* const*)d_seg, W, N, VCOLL_F32, VCOLL_AVG, ring, NULL);
+  if (rc) { printf("rsr %d %s\n", rc, vcoll_last_error()); return 1; }
+  cudaDeviceSynchronize();
+  for (int j = 0; j < W; ++j) {
+    int64_t off, len;
+    vcoll_segment(N, W, j, &off, &len);
+    print_bits("rsr", j, d_seg[j], (int)len);
+  }
+  /* fusion buffers: three tensors per rank (the first N - 353, then 3, then
+   * 350 elements of d_in[u]) through d_seg[u], in place into d_out[u] */
+  const int64_t counts[3] = {N - 353, 3, 350};
+  const void* tin[W * 3];
+  void* tout[W * 3];
+  for (int u = 0; u < W; ++u) {
+    cudaMemcpy(d_out[u], d_in[u], sizeof(float) * N, cudaMemcpyDeviceToDevice);
+    int64_t o = 0;
+    for (int t = 0; t < 3; ++t) {
+      tin[u * 3 + t] = d_out[u] + o;
+      tout[u * 3 + t] = d_out[u] + o;
+      o += counts[t];
+    }
+  }
+  int nb = 0;
+  rc = vcoll_fusion_allreduce_buffered(tin, tout, counts, 3, (void* const*)d_seg,
+                                       (int64_t)sizeof(float) * N, W, VCOLL_F32, VCOLL_SUM, 0,
+                                       (int64_t)1 << 20, &nb, NULL);
+  if (rc) { printf("fb %d %s\n", rc, vcoll_last_error()); return 1; }
+  cudaDeviceSynchronize();
+  printf("fb_batches %d\n", nb);
+  for (int u = 0; u < W; ++u) print_bits("fb", u, d_out[u], N);
   for (int u = 0; u < W; ++u) {
     cudaFree(d_in[u]);
     cudaFree(d_out[u]);

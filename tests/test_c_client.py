@@ -48,18 +48,33 @@ def test_c_client_host_mode(client):
     assert " ".join(d["status"]) == "invalid reduction operation"
 
 
-def _expected_checksum():
+def _inputs():
     n, W = 1003, 4
-    ins = [np.array([(i * 7 + u * 13) % 41 - 20 for i in range(n)], np.float32) for u in range(W)]
-    total = oracle.allreduce(ins, "sum", oracle.F32)[0].astype(np.float64)
-    return float(np.sum(total * (np.arange(n) % 5 + 1)))
+    return [np.array([(i * 7 + u * 13) % 41 - 20 for i in range(n)], np.float32) for u in range(W)]
+
+
+def _bits(lines, tag):
+    out = {}
+    for ln in lines:
+        if ln[0] == tag:
+            out.setdefault(int(ln[1]), []).append((int(ln[2]), int(ln[3], 16)))
+    return {u: [b for _, b in sorted(v)] for u, v in out.items()}
 
 
 @pytest.mark.gpu
 def test_c_client_gpu_mode(client):
     lines = _run(client, "gpu")
-    want = _expected_checksum()
-    ag = [float(ln[2]) for ln in lines if ln[0] == "ag_checksum"]
-    ar = [float(ln[1]) for ln in lines if ln[0] == "ar_checksum"]
-    assert ag == [want] * 4
-    assert ar == [want]
+    ins = _inputs()
+    W = len(ins)
+    ar = [a.view(np.uint32).tolist() for a in oracle.allreduce(ins, "sum", oracle.F32)]
+    assert _bits(lines, "ag") == {u: ar[u] for u in range(W)}
+    assert _bits(lines, "ar") == {u: ar[u] for u in range(W)}
+    rsr = oracle.reduce_scatter(ins, "avg", oracle.F32, [1, 2, 0, 3])
+    assert _bits(lines, "rsr") == {j: rsr[j].view(np.uint32).tolist() for j in range(W)}
+    counts = [1003 - 353, 3, 350]
+    offs = np.cumsum([0] + counts)
+    tens = [[ins[u][offs[t]:offs[t + 1]] for t in range(3)] for u in range(W)]
+    fb = oracle.fusion_allreduce(tens, counts, "sum", oracle.F32, 1 << 20)
+    assert _bits(lines, "fb") == {u: np.concatenate(fb[u]).view(np.uint32).tolist()
+                                  for u in range(W)}
+    assert [ln for ln in lines if ln[0] == "fb_batches"] == [["fb_batches", "1"]]
