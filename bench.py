@@ -355,9 +355,9 @@ def build_workload(args, dev, rank):
                 what += ", minimum workspace (no candidate lists)"
         launches = 1
         if topk:
-            # 13 kernels over the whole array; 22 on the candidate path, which
+            # 13 kernels over the whole array; 23 on the candidate path, which
             # the library takes when the lists hold 3K entries (K < n/4) or a
-            # tenth of the array (a two-sided band), 26 when the lists also
+            # tenth of the array (a two-sided band), 27 when the lists also
             # give the output (a second-digit sample pass and its selection,
             # an output pass, and, with accumulations, a pass that restores x
             # in them should a rank's list fail)
@@ -365,7 +365,7 @@ def build_workload(args, dev, rank):
             cap = ((n // 8 + 4096 if n // 8 + 4096 < n else n) + 3) & ~3
             wide = 4 * K < n and cap >= 3 * K  # lower bound only: output from the lists
             cand = 0 < K < n and (wide or 10 * cap >= n) and args.sparse_workspace != "min"
-            launches = ((26 if acc is not None else 25) if wide else 22) if cand else 13
+            launches = ((27 if acc is not None else 26) if wide else 23) if cand else 13
         return dict(name=f"{what}, W={W}, f32, n={n} per rank", W=W, n=n, step=step,
                     bytes=bytes_, launches=launches, ins=ins,
                     outs=outs, es=4, reduction=red, dtype="f32")
@@ -557,7 +557,7 @@ def extras(args, stream, dev):
     # outputs
     out["sparse_topk1pct_w8_f32_2^26_noacc"] = rate(
         lambda: vc.sparse_allreduce(ins, outs, None, 0.01, True, nnz, ws), 2 * W * n * 4)
-    # the same call captured in a CUDA graph (26 kernels and two memsets per
+    # the same call captured in a CUDA graph (27 kernels and two memsets per
     # call: the host launch overhead is gone)
     out["sparse_topk1pct_w8_f32_2^26_graph"] = graph_rate(
         lambda s: vc.sparse_allreduce(ins, outs, acc, 0.01, True, nnz, ws, stream=s),

@@ -404,11 +404,16 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
     if ((rc = run(topk_tie_count_kernel(), full_grid, 256)) ||
         (rc = run(topk_tie_find_kernel(), sgrid, 1024)))
       return rc;
-    if (prm.use_cand)
+    // on the candidate path one pass collects the equal keys' indices and
+    // picks the boundary (the last CTA of each rank); ranks with more equal
+    // keys than it holds take three index-digit passes
+    if (prm.use_cand) {
+      if ((rc = run(topk_ties_kernel(), few, 256))) return rc;
       for (int pass = 3; pass <= 5; ++pass)
         if ((rc = run(topk_cand_hist_kernel(pass), few, 256)) ||
             (rc = run(topk_index_select_kernel(pass), sgrid, 1024)))
           return rc;
+    }
   }
   const void* fn = sparse_apply_kernel(topk);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(prm.num_tiles, 0x7FFFFFFF));

@@ -318,7 +318,9 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
   TopkState* st = p.state + r;
   if (MODE == 4 && !st->redo) return;
   // (uniform per CTA; nothing was counted for these ranks, the bins are zero)
-  if (MODE >= 5 && MODE <= 7 && (p.K == 0 || st->full || st->need >= st->equal)) return;
+  if (MODE >= 5 && MODE <= 7 &&
+      (p.K == 0 || st->full || st->need >= st->equal || st->tie_resolved))
+    return;
   if (MODE == 8 && refined_bin(*st) < 0) return;
   const int b0 = kTopkBins - 1 - 2 * t, b1 = b0 - 1;
   const unsigned long long c0 = hist[b0], c1 = hist[b1];
@@ -986,7 +988,7 @@ __global__ void __launch_bounds__(256) vc_topk_cand_hist(const __grid_constant__
   const TopkState& st = p.state[r];
   // uniform per CTA
   if (st.full) return;
-  if (P >= 3 && st.need >= st.equal) return;
+  if (P >= 3 && (st.need >= st.equal || st.tie_resolved)) return;
   const unsigned long long cn = p.cand_n[r];
   if (cn > (unsigned long long)p.cand_cap) return;
   for (int i = tid; i < kTopkBins; i += blockDim.x) h[i] = 0;
@@ -1041,6 +1043,89 @@ __global__ void __launch_bounds__(256) vc_topk_cand_hist(const __grid_constant__
   __syncthreads();
   for (int i = tid; i < kTopkBins; i += blockDim.x)
     if (h[i]) atomicAdd(&p.hist[(int64_t)r * kTopkBins + i], h[i]);
+}
+
+// ------------------------------------------------------------- list ties
+// Keys equal to the K-th one (T) straddling the cut on the candidate path:
+// the kept ones are the `need` lowest indices among the candidates whose key
+// is T, so the boundary is the need-th smallest such index.  When there are
+// at most kTieCap equal keys (at W = 8, 2^26 per rank and K = 1 % a handful
+// of fp32 keys repeat on most calls), one pass finds it: every CTA scans its
+// share of the rank's list and appends the indices of the equal keys to a
+// small buffer (the first kTieCap slots of the rank's histogram, zero at
+// this point); the last CTA of the rank to finish (a counter, no waiting)
+// ranks them by counting the smaller ones, sets the boundary, marks the rank
+// resolved and clears the slots.  More equal keys (massive ties, such as
+// quantised values) are left to the three index-digit passes that follow,
+// which skip resolved ranks.
+constexpr uint32_t kTieCap = 256;
+
+__global__ void __launch_bounds__(256) vc_topk_ties(const __grid_constant__ SparseParams p) {
+  pdl_enter();
+  const int r = blockIdx.y;
+  const int tid = threadIdx.x;
+  TopkState* st = p.state + r;
+  // uniform per rank: nothing to resolve, the rank is on the full path, or
+  // too many equal keys for the buffer
+  if (p.K == 0 || st->full || st->need >= st->equal) return;
+  if ((unsigned long long)st->equal > kTieCap) return;
+  const unsigned long long cn = p.cand_n[r];
+  if (cn > (unsigned long long)p.cand_cap) return;
+  const int64_t m = (int64_t)cn;
+  const uint32_t T = st->T;
+  const uint32_t* ckey = p.cand_key + (int64_t)r * p.cand_cap;
+  const uint32_t* cidx = p.cand_idx + (int64_t)r * p.cand_cap;
+  uint32_t* slots = p.hist + (int64_t)r * kTopkBins;  // zero here
+  auto take = [&](uint32_t key, int64_t i) {
+    if (key == T) {
+      const uint32_t pos = atomicAdd(&st->tie_n, 1u);
+      if (pos < kTieCap) slots[pos] = cidx[i];
+    }
+  };
+  // keys four at a time (the list starts 16-byte aligned), U vectors per
+  // thread loaded before any is tested; then the last m % 4 keys
+  constexpr int U = 4;
+  const int64_t m4 = m / 4;
+  const uint4* k4 = reinterpret_cast<const uint4*>(ckey);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < m4; base += stride * U) {
+    uint4 kv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = base + u * stride + tid;
+      kv[u] = v < m4 ? k4[v] : make_uint4(~T, ~T, ~T, ~T);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = base + u * stride + tid;
+      take(kv[u].x, v * 4);
+      take(kv[u].y, v * 4 + 1);
+      take(kv[u].z, v * 4 + 2);
+      take(kv[u].w, v * 4 + 3);
+    }
+  }
+  if (blockIdx.x == 0 && tid < 4 && m4 * 4 + tid < m) take(ckey[m4 * 4 + tid], m4 * 4 + tid);
+  // the last CTA of this rank to get here resolves it
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&st->tie_done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int64_t need = st->need;
+  const uint32_t cnt = *(volatile uint32_t*)&st->tie_n;  // == equal <= kTieCap
+  __shared__ uint32_t s_idx[kTieCap];
+  for (uint32_t i = tid; i < cnt && i < kTieCap; i += blockDim.x)
+    s_idx[i] = *(volatile uint32_t*)&slots[i];
+  __syncthreads();
+  for (uint32_t i = tid; i < cnt && i < kTieCap; i += blockDim.x) {
+    uint32_t below = 0;
+    for (uint32_t j = 0; j < cnt && j < kTieCap; ++j) below += s_idx[j] < s_idx[i];
+    if ((int64_t)below == need - 1) st->boundary = (int64_t)s_idx[i];
+    slots[i] = 0;
+  }
+  if (tid == 0) st->tie_resolved = 1;
 }
 
 // ------------------------------------------------------------- list route
@@ -1314,5 +1399,6 @@ const void* topk_index_select_kernel(int pass) {
 }
 const void* topk_tie_count_kernel() { return (const void*)&vc_topk_tie_count; }
 const void* topk_tie_find_kernel() { return (const void*)&vc_topk_tie_find; }
+const void* topk_ties_kernel() { return (const void*)&vc_topk_ties; }
 
 }  // namespace vcoll

@@ -157,6 +157,10 @@ struct TopkState {
   int64_t low_rem;    // sample keys still wanted at or above lowkey inside its
   int64_t set_rem;    // bin, and allowed above setkey inside its bin (the
                       // second-digit refinement of both bounds)
+  uint32_t tie_n;     // candidate path: candidates equal to T collected so far
+  uint32_t tie_done;  // candidate path: CTAs of the tie pass that finished
+  int tie_resolved;   // candidate path: the tie pass set the boundary (the
+                      // index-digit passes have nothing left to do)
 };
 struct SparseParams {
   const void* in[VCOLL_MAX_RANKS];
@@ -263,6 +267,7 @@ const void* topk_cand_hist_kernel(int pass);  // 0-2 key digits, 3-5 index digit
 const void* topk_index_select_kernel(int pass);  // 3-5
 const void* topk_tie_count_kernel();
 const void* topk_tie_find_kernel();
+const void* topk_ties_kernel();
 // dynamic shared memory the realigned allgather requests without using it,
 // to run two CTAs per SM
 constexpr size_t kGatherRealignSmem = 100 * 1024;

@@ -943,6 +943,26 @@ def test_sparse_topk_large_k_band(v, frac):
     _check_sparse(v, ins, None, frac, True)
 
 
+@pytest.mark.parametrize("extra", [1, 6, 255, 300])
+@pytest.mark.parametrize("with_acc", [False, True])
+def test_sparse_topk_few_ties_at_the_cut(v, extra, with_acc):
+    # `extra` entries below the K-th largest value are raised to it, so that
+    # keys equal to the K-th one straddle the cut: up to 256 of them are
+    # collected and ranked by index, more take the digit passes
+    W, n, frac = 2, 64 * 4096 + 7, 0.01
+    K = int(np.ceil(np.float32(frac) * np.float32(n)))
+    ins = _sparse_inputs(W, n, 900 + extra)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(extra)
+    for t in ins:
+        kth = torch.topk(t, K).values[-1]
+        below = torch.nonzero(t < kth).flatten()
+        pick = below[torch.randperm(below.numel(), generator=g, device="cuda")[:extra]]
+        t[pick] = kth
+    acc = [torch.zeros(n, device="cuda") for _ in range(W)] if with_acc else None
+    _check_sparse(v, ins, acc, frac, True)
+
+
 def test_sparse_topk_all_equal_values(v):
     # every entry ties: the K kept are the K lowest indices
     W, n = 3, 100_000
