@@ -695,13 +695,25 @@ static int gather_common(const void* const* in, void* const* out, int W, const i
   prm.W = W;
   prm.phase = phase;
   prm.tile_elems = adaptive_tile(n, W, threads, V, 4);
-  int64_t tps = 1;
-  for (int j = 0; j < W; ++j) {
-    const int64_t a = disp[j], b = disp[j + 1];
-    const int64_t up = a + ((V - ((a + phase) % V)) % V);
-    const int64_t av = std::min(up, b);
-    const int64_t bv = std::max(b - ((b + phase) % V), av);
-    tps = std::max(tps, ceil_div(bv - av, prm.tile_elems));
+  auto gather_tiles = [&](int64_t tile) {  // tiles per segment
+    int64_t t = 1;
+    for (int j = 0; j < W; ++j) {
+      const int64_t a = disp[j], b = disp[j + 1];
+      const int64_t up = a + ((V - ((a + phase) % V)) % V);
+      const int64_t av = std::min(up, b);
+      const int64_t bv = std::max(b - ((b + phase) % V), av);
+      t = std::max(t, ceil_div(bv - av, tile));
+    }
+    return t;
+  };
+  int64_t tps = gather_tiles(prm.tile_elems);
+  // Launches of about 512 CTAs ran 25-30 % slower than half or twice as
+  // many at every W measured on GB300 (2-16; 2-8 MiB per rank, L2-resident
+  // or not): such a launch takes tiles half the size instead
+  const int64_t unit = (int64_t)threads * V;
+  if (tps * W >= 400 && tps * W <= 640 && prm.tile_elems >= 2 * unit) {
+    prm.tile_elems = ceil_div(prm.tile_elems / 2, unit) * unit;
+    tps = gather_tiles(prm.tile_elems);
   }
   prm.tiles_per_seg = tps;
   prm.num_tiles = tps * W;
