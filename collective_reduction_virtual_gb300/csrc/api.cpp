@@ -861,19 +861,12 @@ static int fuse_common(const void* const* tensors, const int64_t* counts, int T,
       prm.fused[u] = (void*)fused[u];
       for (int t = 0; t < nt; ++t) prm.tensor[t * W + u] = (void*)tensors[(int64_t)u * T + t0 + t];
     }
-    // tensors whose W copies share source and destination 16-byte phases
-    prm.uniform = 0;
-    for (int t = 0; t < nt; ++t) {
-      const uint64_t fo = (uint64_t)(prm.offset[t] * es);
-      const uint64_t tp = (uint64_t)prm.tensor[t * W] & 15, fp = ((uint64_t)fused[0] + fo) & 15;
-      bool same = true;
-      for (int u = 1; u < W && same; ++u)
-        same = ((uint64_t)prm.tensor[t * W + u] & 15) == tp && (((uint64_t)fused[u] + fo) & 15) == fp;
-      if (same) prm.uniform |= 1ull << t;
-    }
     if (tiles == 0) continue;
-    rc = launch(fuse_kernel(es, W), tiles, threads, 0, false, &prm, stream);
-    if (rc) return rc;
+    // one CTA per (tile, rank)
+    void* args[] = {&prm};
+    cudaError_t e = launch_pdl(fuse_flat_kernel(es), dim3((unsigned)tiles, (unsigned)W),
+                               dim3(threads), args, 0, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fusion copy launch");
   }
   return VCOLL_OK;
 }

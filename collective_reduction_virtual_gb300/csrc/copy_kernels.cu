@@ -16,6 +16,8 @@
 
 namespace vcoll {
 
+constexpr int kFuseThreads = 256;  // the pack / unpack launch's CTA size
+
 // ------------------------------------------------------------- allgather
 
 // VM: 0 element-wise, 1 16-byte vectors, 2 vectors with pieces realigned to
@@ -96,209 +98,101 @@ __global__ void __launch_bounds__(256) vc_gather(const __grid_constant__ GatherP
 
 // ------------------------------------------------------------------ fusion
 
+// Bytes [sh, sh + 16) of the 32 bytes lo:hi, sh in 1..15: the word shift
+// ws = sh / 4 picks five words with selects (ws is uniform, so the
+// predicates are computed once) and a funnel shift moves the remaining
+// (sh % 4) bytes -- no branch per shift, so that four vectors in flight stay
+// in registers.
+__device__ __forceinline__ uint4 shift_window(const uint4& lo, const uint4& hi, int sh) {
+  const int ws = sh >> 2, bs = (sh & 3) * 8;
+  const bool s0 = ws == 0, s1 = ws == 1, s2 = ws == 2;
+  const uint32_t w0 = s0 ? lo.x : s1 ? lo.y : s2 ? lo.z : lo.w;
+  const uint32_t w1 = s0 ? lo.y : s1 ? lo.z : s2 ? lo.w : hi.x;
+  const uint32_t w2 = s0 ? lo.z : s1 ? lo.w : s2 ? hi.x : hi.y;
+  const uint32_t w3 = s0 ? lo.w : s1 ? hi.x : s2 ? hi.y : hi.z;
+  const uint32_t w4 = s0 ? hi.x : s1 ? hi.y : s2 ? hi.z : hi.w;
+  return make_uint4(__funnelshift_r(w0, w1, bs), __funnelshift_r(w1, w2, bs),
+                    __funnelshift_r(w2, w3, bs), __funnelshift_r(w3, w4, bs));
+}
 
-// Block-cooperative copy of nbytes (a multiple of ES) from src to dst, both
-// ES-aligned.  Destination-aligned 16-byte stores; the body loads either one
-// aligned source vector (same phase) or the two aligned vectors covering the
-// shifted source bytes.  Both of those lie in 16-byte blocks that hold at
-// least one byte of the source range, so no access leaves the source's pages.
+// Pack / unpack with one CTA per (tile, rank): grid.y = rank.  Each CTA
+// copies one tile of one tensor for one rank -- at most 1024 destination-
+// aligned 16-byte vectors, four per thread, all loads in flight before the
+// first store; a source at another 16-byte phase is read as the two aligned
+// blocks around each vector and funnel-shifted.  Addresses are one base per
+// thread plus constant offsets, so the kernel fits 64 registers (4 CTAs per
+// SM) where the grouped kernel below keeps 2 CTAs per SM (128 registers).
 template <int ES>
-__device__ __forceinline__ void copy_range(char* dst, const char* src, int64_t nbytes) {
+__global__ void __launch_bounds__(256, 4) vc_fuse_flat(const __grid_constant__ FuseParams p) {
+  pdl_enter();
   using B = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
   constexpr int U = 4;
+  __shared__ int64_t s_begin[kFuseMaxTensors + 1];
+  for (int i = threadIdx.x; i <= p.T; i += blockDim.x) s_begin[i] = p.tile_begin[i];
+  __syncthreads();
+  const int64_t total = s_begin[p.T];
+  const int u = blockIdx.y;
   const int tid = threadIdx.x;
-  const int nthr = blockDim.x;
-  const uint64_t d0 = (uint64_t)dst;
-  int64_t head = (int64_t)((16 - (d0 & 15)) & 15);
-  if (head > nbytes) head = nbytes;
-  const int64_t body = (nbytes - head) & ~(int64_t)15;
-  const int64_t tail0 = head + body;
-  // head and tail, one element per thread
-  {
-    int64_t off = -1;
-    if ((int64_t)tid * ES < head) off = (int64_t)tid * ES;
-    const int t2 = tid - 32;
-    if (t2 >= 0 && tail0 + (int64_t)t2 * ES < nbytes) off = tail0 + (int64_t)t2 * ES;
-    if (off >= 0) st1(dst + off, ld1<B>(src + off));
-  }
-  const int64_t nv = body >> 4;
-  char* vd = dst + head;
-  const char* vs = src + head;
-  const int sh = (int)((uint64_t)vs & 15);
-  if (sh == 0) {
-    for (int64_t base = 0; base < nv; base += (int64_t)U * nthr) {
+  for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    int lo = 0, hi = p.T - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_begin[mid] <= tile)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int t = lo;
+    const int64_t e0 = (tile - s_begin[t]) * p.tile_elems;
+    const int64_t e1 = e0 + p.tile_elems < p.count[t] ? e0 + p.tile_elems : p.count[t];
+    char* tens = (char*)p.tensor[t * p.W + u] + e0 * ES;
+    char* fus = (char*)p.fused[u] + (p.offset[t] + e0) * ES;
+    char* dst = p.unpack ? tens : fus;
+    const char* src = p.unpack ? fus : tens;
+    const int nbytes = (int)((e1 - e0) * ES);
+    int head = (int)((16 - ((uint64_t)dst & 15)) & 15);
+    if (head > nbytes) head = nbytes;
+    const int body = (nbytes - head) & ~15;
+    const int tail0 = head + body;
+    {  // head and tail, one element per thread
+      int off = -1;
+      if (tid * ES < head) off = tid * ES;
+      if (tid >= 32 && tail0 + (tid - 32) * ES < nbytes) off = tail0 + (tid - 32) * ES;
+      if (off >= 0) st1(dst + off, ld1<B>(src + off));
+    }
+    const int nv = body >> 4;
+    char* vd = dst + head + tid * 16;
+    const int sh = (int)((uint64_t)(src + head) & 15);
+    if (sh == 0) {
+      const char* vs = src + head + tid * 16;
       uint4 x[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t i = base + (int64_t)u * nthr + tid;
-        if (i < nv) x[u] = ld_stream(vs + i * 16);
-      }
+      for (int q = 0; q < U; ++q)
+        if (tid + q * kFuseThreads < nv) x[q] = ld_stream(vs + q * kFuseThreads * 16);
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t i = base + (int64_t)u * nthr + tid;
-        if (i < nv) st_stream(vd + i * 16, x[u]);
-      }
-    }
-  } else {
-    const char* as = vs - sh;  // aligned source base
-    for (int64_t base = 0; base < nv; base += (int64_t)U * nthr) {
-      uint4 lo[U], hi[U];
+      for (int q = 0; q < U; ++q) reg_fence(x[q]);
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t i = base + (int64_t)u * nthr + tid;
-        if (i < nv) {
-          lo[u] = ld_stream(as + i * 16);
-          hi[u] = ld_stream(as + i * 16 + 16);
+      for (int q = 0; q < U; ++q)
+        if (tid + q * kFuseThreads < nv) st_stream(vd + q * kFuseThreads * 16, x[q]);
+    } else {
+      const char* as = src + head - sh + tid * 16;  // the aligned block below each vector
+      uint4 a4[U], b4[U];
+#pragma unroll
+      for (int q = 0; q < U; ++q)
+        if (tid + q * kFuseThreads < nv) {
+          a4[q] = ld_stream(as + q * kFuseThreads * 16);
+          b4[q] = ld_stream(as + q * kFuseThreads * 16 + 16);
         }
+#pragma unroll
+      for (int q = 0; q < U; ++q) {
+        reg_fence(a4[q]);
+        reg_fence(b4[q]);
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t i = base + (int64_t)u * nthr + tid;
-        if (i < nv) st_stream(vd + i * 16, funnel16(lo[u], hi[u], sh));
-      }
+      for (int q = 0; q < U; ++q)
+        if (tid + q * kFuseThreads < nv)
+          st_stream(vd + q * kFuseThreads * 16, shift_window(a4[q], b4[q], sh));
     }
-  }
-}
-
-template <int ES>
-__global__ void __launch_bounds__(256) vc_fuse(const __grid_constant__ FuseParams p) {
-  pdl_enter();
-  // tile table in shared memory: the per-tile search stays on chip
-  __shared__ int64_t s_begin[kFuseMaxTensors + 1];
-  for (int i = threadIdx.x; i <= p.T; i += blockDim.x) s_begin[i] = p.tile_begin[i];
-  __syncthreads();
-  const int64_t total = s_begin[p.T];
-  for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
-    // tensor t with tile_begin[t] <= tile < tile_begin[t + 1]
-    int lo = 0, hi = p.T - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_begin[mid] <= tile)
-        lo = mid;
-      else
-        hi = mid - 1;
-    }
-    const int t = lo;
-    const int64_t k = tile - s_begin[t];
-    const int64_t e0 = k * p.tile_elems;
-    const int64_t e1 = e0 + p.tile_elems < p.count[t] ? e0 + p.tile_elems : p.count[t];
-    for (int u = 0; u < p.W; ++u) {
-      char* tens = (char*)p.tensor[t * p.W + u] + e0 * ES;
-      char* fus = (char*)p.fused[u] + (p.offset[t] + e0) * ES;
-      if (p.unpack)
-        copy_range<ES>(tens, fus, (e1 - e0) * ES);
-      else
-        copy_range<ES>(fus, tens, (e1 - e0) * ES);
-    }
-  }
-}
-
-// The 16-byte body of one tile for ranks g .. g + G - 1: nv destination
-// vectors at dst_of(u) + head, the source sh bytes past a 16-byte boundary.
-// Aligned: every thread issues 8 vector loads (8 / G per rank) before its
-// first store; shifted: one vector per rank, loaded as the two aligned blocks
-// that cover it and funnel-shifted.
-template <int G, class DstOf, class SrcOf>
-__device__ __forceinline__ void fuse_group_body(DstOf dst_of, SrcOf src_of, int g, int64_t head,
-                                                int64_t nv, int sh) {
-  const int tid = threadIdx.x;
-  const int64_t nthr = blockDim.x;
-  if (sh == 0) {
-    constexpr int U = 8 / G;
-    for (int64_t base = tid; base < nv; base += U * nthr) {
-      uint4 x[U][G];
-#pragma unroll
-      for (int v = 0; v < U; ++v)
-#pragma unroll
-        for (int q = 0; q < G; ++q)
-          if (base + v * nthr < nv) x[v][q] = ld_stream(src_of(g + q) + head + (base + v * nthr) * 16);
-#pragma unroll
-      for (int v = 0; v < U; ++v)
-#pragma unroll
-        for (int q = 0; q < G; ++q) reg_fence(x[v][q]);
-#pragma unroll
-      for (int v = 0; v < U; ++v)
-#pragma unroll
-        for (int q = 0; q < G; ++q)
-          if (base + v * nthr < nv) st_stream(dst_of(g + q) + head + (base + v * nthr) * 16, x[v][q]);
-    }
-  } else {
-    for (int64_t i = tid; i < nv; i += nthr) {
-      uint4 a[G], b[G];
-#pragma unroll
-      for (int q = 0; q < G; ++q) {
-        const char* as = src_of(g + q) + head - sh + i * 16;  // aligned source blocks
-        a[q] = ld_stream(as);
-        b[q] = ld_stream(as + 16);
-      }
-#pragma unroll
-      for (int q = 0; q < G; ++q) {
-        reg_fence(a[q]);
-        reg_fence(b[q]);
-      }
-#pragma unroll
-      for (int q = 0; q < G; ++q) st_stream(dst_of(g + q) + head + i * 16, funnel16(a[q], b[q], sh));
-    }
-  }
-}
-
-// Pack / unpack with the W ranks' copies of a tile done together, G ranks at
-// a time, each thread keeping at least G 16-byte loads in flight before its
-// first store, so a tile's copies overlap instead of running rank after
-// rank (copy_range, rank by rank, keeps 4).  Needs tensors whose
-// copies share their phases on all ranks (the usual case: every buffer
-// 256-byte aligned); the others take copy_range rank by rank.
-template <int ES, int G>
-__global__ void __launch_bounds__(256, 2) vc_fuse_grouped(const __grid_constant__ FuseParams p) {
-  pdl_enter();
-  using B = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;
-  __shared__ int64_t s_begin[kFuseMaxTensors + 1];
-  for (int i = threadIdx.x; i <= p.T; i += blockDim.x) s_begin[i] = p.tile_begin[i];
-  __syncthreads();
-  const int64_t total = s_begin[p.T];
-  const int W = p.W;
-  const int tid = threadIdx.x;
-  for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
-    int lo = 0, hi = p.T - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_begin[mid] <= tile)
-        lo = mid;
-      else
-        hi = mid - 1;
-    }
-    const int t = lo;
-    const int64_t k = tile - s_begin[t];
-    const int64_t e0 = k * p.tile_elems;
-    const int64_t e1 = e0 + p.tile_elems < p.count[t] ? e0 + p.tile_elems : p.count[t];
-    const int64_t nbytes = (e1 - e0) * ES;
-    const int64_t foff = (p.offset[t] + e0) * ES;
-    auto dst_of = [&](int u) -> char* {
-      return p.unpack ? (char*)p.tensor[t * W + u] + e0 * ES : (char*)p.fused[u] + foff;
-    };
-    auto src_of = [&](int u) -> const char* {
-      return p.unpack ? (const char*)p.fused[u] + foff : (const char*)p.tensor[t * W + u] + e0 * ES;
-    };
-    if (!((p.uniform >> t) & 1u)) {
-      for (int u = 0; u < W; ++u) copy_range<ES>(dst_of(u), src_of(u), nbytes);
-      continue;
-    }
-    // phases shared by every rank: split the range once
-    int64_t head = (int64_t)((16 - ((uint64_t)dst_of(0) & 15)) & 15);
-    if (head > nbytes) head = nbytes;
-    const int64_t body = (nbytes - head) & ~(int64_t)15;
-    const int64_t tail0 = head + body;
-    const int sh = (int)(((uint64_t)src_of(0) + head) & 15);
-    const int64_t nv = body >> 4;
-    {  // head and tail, one element per thread, every rank
-      int64_t off = -1;
-      if ((int64_t)tid * ES < head) off = (int64_t)tid * ES;
-      const int t2 = tid - 32;
-      if (t2 >= 0 && tail0 + (int64_t)t2 * ES < nbytes) off = tail0 + (int64_t)t2 * ES;
-      if (off >= 0)
-        for (int u = 0; u < W; ++u) st1(dst_of(u) + off, ld1<B>(src_of(u) + off));
-    }
-    for (int g = 0; g < W; g += G) fuse_group_body<G>(dst_of, src_of, g, head, nv, sh);
   }
 }
 
@@ -310,22 +204,8 @@ const void* gather_kernel(int elem_size, int vec) {
                   : vec ? (const void*)&vc_gather<2, 1> : (const void*)&vc_gather<2, 0>;
 }
 
-const void* fuse_kernel(int elem_size, int W) {
-  // G = min(W, 8) ranks per group for W in {2, 4, 8, 16}; any other W rank by rank
-  if (elem_size == 4) {
-    switch (W) {
-      case 2: return (const void*)&vc_fuse_grouped<4, 2>;
-      case 4: return (const void*)&vc_fuse_grouped<4, 4>;
-      case 8: case 16: return (const void*)&vc_fuse_grouped<4, 8>;
-      default: return (const void*)&vc_fuse<4>;
-    }
-  }
-  switch (W) {
-    case 2: return (const void*)&vc_fuse_grouped<2, 2>;
-    case 4: return (const void*)&vc_fuse_grouped<2, 4>;
-    case 8: case 16: return (const void*)&vc_fuse_grouped<2, 8>;
-    default: return (const void*)&vc_fuse<2>;
-  }
+const void* fuse_flat_kernel(int elem_size) {
+  return elem_size == 4 ? (const void*)&vc_fuse_flat<4> : (const void*)&vc_fuse_flat<2>;
 }
 
 }  // namespace vcoll

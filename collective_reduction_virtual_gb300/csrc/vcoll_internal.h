@@ -80,7 +80,8 @@ struct GatherParams {
 // every rank.  Copy (t, u) moves count[t] elements between tensor[t * W + u]
 // (tensor-major) and fused[u] + offset[t].  Work is tiled per tensor:
 // tile_begin[t] is the first tile of tensor t (tile_begin[T] = total), each
-// tile covers tile_elems elements of that tensor on all W ranks.
+// tile covers tile_elems elements of that tensor; one CTA per (tile, rank),
+// the rank in grid.y.
 constexpr int kFuseMaxTensors = 64;
 constexpr int kFuseMaxCopies = 1024;  // W * T per launch
 struct FuseParams {
@@ -90,8 +91,6 @@ struct FuseParams {
   int64_t offset[kFuseMaxTensors];
   int64_t tile_begin[kFuseMaxTensors + 1];
   int64_t tile_elems;
-  uint64_t uniform;  // bit t: every rank's copy of tensor t has the same source
-                     // and destination 16-byte phases (copied for all ranks at once)
   int T;
   int W;
   int unpack;  // 0: tensors -> fused, 1: fused -> tensors
@@ -276,7 +275,7 @@ constexpr int kGatherTmaStages = 4;
 constexpr int kGatherTmaTileBytes = 32768;
 // Device address of the per-device error word (VCOLL_DEVICE_ERR_* bits).
 unsigned int* device_error_symbol();
-const void* fuse_kernel(int elem_size, int W);
+const void* fuse_flat_kernel(int elem_size);
 const void* multi_kernel_f32(int op, int W_t, int ring);
 const void* multi_kernel_bf16(int op, int W_t, int ring);
 
