@@ -26,12 +26,15 @@
 // which entries are only counted), one pass over the data appends every
 // entry in the band to the rank's candidate list as (key, index), and the
 // select passes then read only the list -- three over the key digits and,
-// when keys equal to the K-th one straddle the cut, three over the bits of
-// the inverted index (the K largest (key, -index) pairs are the K entries
-// kept).  A rank whose list overflowed, or whose band misses the K-th key,
+// when keys equal to the K-th one straddle the cut (the K largest
+// (key, -index) pairs are the K entries kept), one pass that collects up to
+// 256 equal keys' indices and ranks them, or for more three passes over the
+// bits of the inverted index.  A rank whose list overflowed, or whose band
+// misses the K-th key,
 // takes the passes over the whole array instead; the choice is made on the
 // device.  The candidate pass also stores x = in + acc back into acc, so the
-// later passes read one array.  With only a lower bound (small K) the lists
+// later passes read one array (without accumulations a separate form of the
+// pass, vc_topk_filter_raw, tests the raw input bits).  With only a lower bound (small K) the lists
 // hold every kept entry, grouped by tile, and the output is built from them
 // (vc_topk_list_out) instead of by the dense apply pass -- unless a rank fell
 // back, which the kernels see on the device.  On that route a second pass
