@@ -943,17 +943,18 @@ def test_sparse_topk_large_k_band(v, frac):
     _check_sparse(v, ins, None, frac, True)
 
 
-@pytest.mark.parametrize("extra", [1, 6, 255, 300])
+@pytest.mark.parametrize("extra,W", [(1, 2), (6, 2), (255, 2), (300, 2), (6, 8), (300, 8)])
 @pytest.mark.parametrize("with_acc", [False, True])
-def test_sparse_topk_few_ties_at_the_cut(v, extra, with_acc):
+def test_sparse_topk_few_ties_at_the_cut(v, extra, W, with_acc):
     # `extra` entries below the K-th largest value are raised to it, so that
     # keys equal to the K-th one straddle the cut: up to 256 of them are
-    # collected and ranked by index, more take the digit passes
-    W, n, frac = 2, 64 * 4096 + 7, 0.01
+    # collected and ranked by index, more take the digit passes (every rank
+    # at once with W = 8)
+    n, frac = 64 * 4096 + 7, 0.01
     K = int(np.ceil(np.float32(frac) * np.float32(n)))
-    ins = _sparse_inputs(W, n, 900 + extra)
+    ins = _sparse_inputs(W, n, 900 + extra + W)
     g = torch.Generator(device="cuda")
-    g.manual_seed(extra)
+    g.manual_seed(extra + W)
     for t in ins:
         kth = torch.topk(t, K).values[-1]
         below = torch.nonzero(t < kth).flatten()
