@@ -373,7 +373,11 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
       return rc;
     if (prm.use_cand) {
       // one pass collects the candidates, the first digit from the lists
-      if ((rc = run(topk_filter_kernel(prm.has_acc), every, 256))) return rc;
+      // (without accumulations a CTA takes every fourth tile of a quarter of
+      // the grid: its setup is paid once for four tiles)
+      const dim3 fgrid = prm.has_acc ? every
+                                     : dim3((unsigned)ceil_div((int64_t)tiles, 4), (unsigned)W);
+      if ((rc = run(topk_filter_kernel(prm.has_acc), fgrid, 256))) return rc;
       // the candidate pass stored x = in + acc in acc: later passes read acc
       prm.x_in_acc = prm.has_acc;
       if ((rc = run(topk_cand_hist_kernel(0), few, 256)) ||

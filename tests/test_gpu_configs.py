@@ -229,3 +229,32 @@ def test_sweep_largest_point(v):
     del ar
     rs = v.reduce_scatter(ins, op="max")
     sampled_allreduce_check(ins, [torch.cat(rs)], n, W, "max", False, 10, m=20_000)
+
+
+def test_largest_indices_beyond_32_bits(v):
+    # W = 2, n = 2^31 + 3 fp32 per rank (8 GiB each): element indices past
+    # 2^31 and byte offsets past 2^32, with a ragged tail and uneven segments
+    W, n = 2, (1 << 31) + 3
+    ins = [torch.rand(n, device="cuda", generator=torch.Generator(device="cuda").manual_seed(31 + u))
+           for u in range(W)]
+    idx = np.unique(np.concatenate([sample_indices(n, W, 4000, 11),
+                                    np.arange((1 << 31) - 8, (1 << 31) + 3),
+                                    np.arange((1 << 30) - 4, (1 << 30) + 4)])).astype(np.int64)
+    vals = gather(ins, idx)
+    it = torch.from_numpy(idx).cuda()
+    for ring in (True, False):
+        ar = v.allreduce(ins, op="sum", ring_order=ring)
+        want = oracle.allreduce_sampled(vals, idx, n, "sum", oracle.F32)
+        got = to_np(ar[1][it])
+        if ring:
+            assert_bit_exact(got, want, "AR 2^31 + 3 ring")
+        else:
+            assert_close_fast(got, want, np.abs(widen(vals)).sum(axis=1), W, "sum", "AR 2^31 + 3")
+        assert torch.equal(ar[0][it], ar[1][it])
+        del ar
+    segs = v.reduce_scatter(ins, op="sum", ring_order=True)
+    ag = v.allgather(segs, n)
+    del segs
+    assert_bit_exact(to_np(ag[0][it]), oracle.allreduce_sampled(vals, idx, n, "sum", oracle.F32),
+                     "RS + AG 2^31 + 3 ring")
+
