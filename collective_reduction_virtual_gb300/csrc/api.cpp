@@ -373,10 +373,9 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
       return rc;
     if (prm.use_cand) {
       // one pass collects the candidates, the first digit from the lists
-      // (without accumulations a CTA takes every fourth tile of a quarter of
-      // the grid: its setup is paid once for four tiles)
-      const dim3 fgrid = prm.has_acc ? every
-                                     : dim3((unsigned)ceil_div((int64_t)tiles, 4), (unsigned)W);
+      // (a CTA loops over two tiles with accumulations, four without: its
+      // setup is paid once for them; measured at W = 8, 2^26 per rank)
+      const dim3 fgrid((unsigned)ceil_div((int64_t)tiles, prm.has_acc ? 2 : 4), (unsigned)W);
       if ((rc = run(topk_filter_kernel(prm.has_acc), fgrid, 256))) return rc;
       // the candidate pass stored x = in + acc in acc: later passes read acc
       prm.x_in_acc = prm.has_acc;
