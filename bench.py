@@ -563,7 +563,7 @@ def extras(args, stream, dev):
         lambda s: vc.sparse_allreduce(ins, outs, acc, 0.01, True, nnz, ws, stream=s),
         4 * W * n * 4, 10)
     out["sparse_bytes_formula"] = ("4*W*n*4: read inputs and accumulations, write outputs and "
-                                   "accumulations (top-K: a 1/16 to 1/64 sample, a candidate "
+                                   "accumulations (top-K: a 1/16 to 1/128 sample, a candidate "
                                    "pass that reads both and writes x -- or, above a settled "
                                    "key, the residual -- to the accumulation, and for small K "
                                    "an output pass from the candidate lists, else the dense "

@@ -20,7 +20,7 @@
 //     entry kept in index order -- then the same apply pass as the threshold
 //     mode.
 //
-// Candidate path (when the workspace has room): a 1/16 - 1/64 sample of the data
+// Candidate path (when the workspace has room): a 1/16 - 1/128 sample of the data
 // gives a band of first digits that should hold the K-th key (for small K
 // everything from a wide lower bound up; otherwise also an upper bound, above
 // which entries are only counted), one pass over the data appends every
@@ -104,12 +104,25 @@ constexpr int kSparseThreads = 256;
 constexpr int kTileVecs = (int)(kSparseTileElems / 4 / kSparseThreads);
 static_assert(kTileVecs * 4 * kSparseThreads == kSparseTileElems, "tile = threads x vectors");
 
+// A 16-byte load with the default L2 policy: for data read again shortly
+// (the sample, whose second-digit pass follows its first-digit pass).
+__device__ __forceinline__ uint4 ld_keep(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // x for this thread's vectors v = tid + u * 256 (u < kTileVecs, v < nv) of
 // the aligned body starting at av; every load is issued before the first add
 // so that each thread keeps up to 2 x kTileVecs x 16 bytes in flight.
-// Vectors past nv read as zeros (the caller masks them).
+// Vectors past nv read as zeros (the caller masks them).  KEEP: loads that
+// leave the tile in L2 for a pass that reads it again.
+template <bool KEEP = false>
 __device__ __forceinline__ void load_tile_x(const SparseParams& p, int r, int64_t av, int64_t nv,
                                             float (&x)[kTileVecs][4]) {
+  auto ld = [](const void* q) { return KEEP ? ld_keep(q) : ld_stream(q); };
   uint4 a[kTileVecs], b[kTileVecs];
 #pragma unroll
   for (int u = 0; u < kTileVecs; ++u) {
@@ -117,8 +130,8 @@ __device__ __forceinline__ void load_tile_x(const SparseParams& p, int r, int64_
     a[u] = make_uint4(0u, 0u, 0u, 0u);
     b[u] = make_uint4(0u, 0u, 0u, 0u);
     if (v < nv) {
-      a[u] = ld_stream((const char*)(p.x_in_acc ? p.acc[r] : p.in[r]) + (av + v * 4) * 4);
-      if (p.has_acc && !p.x_in_acc) b[u] = ld_stream((const char*)p.acc[r] + (av + v * 4) * 4);
+      a[u] = ld((const char*)(p.x_in_acc ? p.acc[r] : p.in[r]) + (av + v * 4) * 4);
+      if (p.has_acc && !p.x_in_acc) b[u] = ld((const char*)p.acc[r] + (av + v * 4) * 4);
     }
   }
 #pragma unroll
@@ -243,7 +256,7 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
       // same hist_add calls so that the warp-wide combining stays converged
       const int64_t nv = (bv - av) / 4;
       float x[kTileVecs][4];
-      load_tile_x(p, r, av, nv, x);
+      load_tile_x<MODE == 3>(p, r, av, nv, x);  // the sample stays in L2 for MODE 5
 #pragma unroll
       for (int u = 0; u < kTileVecs; ++u) {
         const bool in_range = tid + u * kSparseThreads < nv;
@@ -816,14 +829,11 @@ __device__ __forceinline__ bool raw_at_least(uint32_t u, uint32_t t) {
 // entries are formed only for those entries.
 template <bool LOW_SGN, bool BAND>
 __device__ __forceinline__ void filter_tile_raw(const SparseParams& p, int r, int64_t tile,
-                                                uint32_t* s_raw, uint32_t& s_n, uint32_t& s_sure,
-                                                unsigned long long& s_base) {
+                                                const RawBound lo, const RawBound hi,
+                                                uint32_t* s_raw, uint32_t* s_n, uint32_t* s_sure,
+                                                int par, unsigned long long& s_base) {
   constexpr int E = 4 * kTileVecs;  // entries per thread (plus one extra)
   const int tid = threadIdx.x, lane = tid & 31;
-  const RawBound lo = raw_bound(p.state[r].lowkey);
-  const uint32_t topkey = (uint32_t)((((uint64_t)p.state[r].high + 1) << 21) - 1);
-  // above the band: key >= topkey + 1 (BAND only, so topkey < 0xFFFFFFFF)
-  const RawBound hi = raw_bound(BAND ? topkey + 1 : 0xFFFFFFFFu);
   auto above = [&](uint32_t u) -> bool {
     return BAND && (hi.sgn ? raw_at_least<true>(u, hi.t) : raw_at_least<false>(u, hi.t));
   };
@@ -835,10 +845,6 @@ __device__ __forceinline__ void filter_tile_raw(const SparseParams& p, int r, in
   int64_t av = t0, bv = t0;
   if (vec) aligned_body<4>(t0, t1, p.phase, av, bv);
   const int nv = (int)((bv - av) / 4);
-  if (tid == 0) {
-    s_n = 0;
-    s_sure = 0;
-  }
   uint32_t mask = 0;
   int sure = 0;  // entries above the band
   // the one extra entry: threads 0-31 take the tile's head, 32-63 its tail
@@ -898,50 +904,63 @@ __device__ __forceinline__ void filter_tile_raw(const SparseParams& p, int r, in
   const uint32_t wtotal = __shfl_sync(0xFFFFFFFFu, incl, 31);
   unsigned wsure = 0;
   if (BAND) wsure = __reduce_add_sync(0xFFFFFFFFu, (unsigned)sure);
-  __syncthreads();  // s_n and s_sure are zero
+  // the tile's counters s_n[par], s_sure[par] are zero (cleared by thread 0
+  // before the previous tile's last barrier, or before the first tile)
   uint32_t wbase = 0;
-  if (lane == 31 && wtotal) wbase = atomicAdd(&s_n, wtotal);
-  if (BAND && lane == 0 && wsure) atomicAdd(&s_sure, wsure);
+  if (lane == 31 && wtotal) wbase = atomicAdd(&s_n[par], wtotal);
+  if (BAND && lane == 0 && wsure) atomicAdd(&s_sure[par], wsure);
   wbase = __shfl_sync(0xFFFFFFFFu, wbase, 31);
   __syncthreads();  // every warp has reserved its share of the tile's room
   if (tid == 0) {
-    const uint32_t tot = s_n;
+    const uint32_t tot = s_n[par];
     const unsigned long long base = tot ? atomicAdd(p.cand_n + r, (unsigned long long)tot) : 0ull;
     s_base = base;
-    if (BAND && s_sure) atomicAdd(p.cand_n + p.W + r, (unsigned long long)s_sure);
+    if (BAND && s_sure[par]) atomicAdd(p.cand_n + p.W + r, (unsigned long long)s_sure[par]);
     p.tilecnt[(int64_t)r * p.tiles_per_rank + tile] = tot;
     p.chunk[(int64_t)r * p.tiles_per_rank + tile] = (uint32_t)base;
+    s_n[par ^ 1] = 0;  // for the next tile (last read by this thread, a tile ago)
+    s_sure[par ^ 1] = 0;
   }
   __syncthreads();
   const unsigned long long cap = (unsigned long long)p.cand_cap;
-  uint32_t* ckey = p.cand_key + (int64_t)r * p.cand_cap;
-  uint32_t* cidx = p.cand_idx + (int64_t)r * p.cand_cap;
-  unsigned long long pos = s_base + wbase + (incl - c);
-  for (uint32_t m = mask; m; m &= m - 1u) {  // this thread's candidates only
-    const int j = __ffs(m) - 1;
-    int64_t i;
-    int sj;
-    if (vec) {
-      i = av + (int64_t)(tid + (j >> 2) * kSparseThreads) * 4 + (j & 3);
-      sj = ((j >> 2) * kSparseThreads + tid) * 4 + (j & 3);
-    } else {
-      i = t0 + tid + (int64_t)j * kSparseThreads;
-      sj = j * kSparseThreads + tid;
+  const unsigned long long pos0 = s_base + wbase + (incl - c);
+  uint32_t* ckey = p.cand_key + (int64_t)r * p.cand_cap + pos0;
+  uint32_t* cidx = p.cand_idx + (int64_t)r * p.cand_cap + pos0;
+  // entry j of this thread sits at offset off of the tile's body both in
+  // s_raw and in the array (list indices are 32-bit)
+  const uint32_t ibase = (uint32_t)(vec ? av : t0);
+  auto offset = [&](int j) -> uint32_t {
+    return vec ? (uint32_t)(((j >> 2) * kSparseThreads + tid) * 4 + (j & 3))
+               : (uint32_t)(j * kSparseThreads + tid);
+  };
+  if (pos0 + c <= cap) {  // the usual case: all of this thread's entries fit
+    uint32_t k = 0;
+    for (uint32_t m = mask; m; m &= m - 1u, ++k) {
+      const uint32_t off = offset(__ffs(m) - 1);
+      ckey[k] = order_key(__uint_as_float(s_raw[off]));
+      cidx[k] = ibase + off;
     }
-    if (pos < cap) {
-      ckey[pos] = order_key(__uint_as_float(s_raw[sj]));
-      cidx[pos] = (uint32_t)i;
+    if (xhit) {
+      ckey[k] = order_key(__uint_as_float(xraw));
+      cidx[k] = (uint32_t)extra;
     }
-    ++pos;
+  } else {
+    uint32_t k = 0;
+    for (uint32_t m = mask; m; m &= m - 1u, ++k) {
+      if (pos0 + k >= cap) break;
+      const uint32_t off = offset(__ffs(m) - 1);
+      ckey[k] = order_key(__uint_as_float(s_raw[off]));
+      cidx[k] = ibase + off;
+    }
+    if (xhit && pos0 + k < cap) {
+      ckey[k] = order_key(__uint_as_float(xraw));
+      cidx[k] = (uint32_t)extra;
+    }
   }
-  if (xhit && pos < cap) {
-    ckey[pos] = order_key(__uint_as_float(xraw));
-    cidx[pos] = (uint32_t)extra;
-  }
-  // (on to the next tile without a barrier: only thread 0 read s_n, s_base
-  // changes only after the next tile's second barrier, which every thread
-  // passes after its reads above, and each thread reads only its own slots
-  // of s_raw)
+  // (on to the next tile without a barrier: only thread 0 reads s_n and
+  // s_sure, the next tile's warps add to the other pair, s_base changes only
+  // after the next tile's first barrier, which every thread passes after its
+  // reads above, and each thread reads only its own slots of s_raw)
 }
 
 // The candidate pass without accumulations reads one array per rank, and its
@@ -960,22 +979,31 @@ __device__ __forceinline__ void filter_tile_raw(const SparseParams& p, int r, in
 __global__ void __launch_bounds__(256, 8) vc_topk_filter_raw(const __grid_constant__ SparseParams p) {
   pdl_enter();
   __shared__ __align__(16) uint32_t s_raw[kSparseThreads * 4 * kTileVecs];
-  __shared__ uint32_t s_n, s_sure;
+  __shared__ uint32_t s_n[2], s_sure[2];  // per tile, alternating
   __shared__ unsigned long long s_base;
   const int r = blockIdx.y;
-  const bool band = p.state[r].high < kTopkBins - 1;  // uniform per CTA
-  const bool sgn = (p.state[r].lowkey & 0x80000000u) != 0;
-  for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x) {
+  if (threadIdx.x < 2) {
+    s_n[threadIdx.x] = 0;
+    s_sure[threadIdx.x] = 0;
+  }
+  __syncthreads();
+  const uint32_t high = p.state[r].high;
+  const bool band = high < kTopkBins - 1;  // uniform per CTA
+  const RawBound lo = raw_bound(p.state[r].lowkey);
+  // above the band: key >= the last key of bin high, plus one (so only with a band)
+  const RawBound hi = raw_bound(band ? (uint32_t)(((uint64_t)high + 1) << 21) : 0xFFFFFFFFu);
+  int par = 0;
+  for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x, par ^= 1) {
     if (band) {
-      if (sgn)
-        filter_tile_raw<true, true>(p, r, tile, s_raw, s_n, s_sure, s_base);
+      if (lo.sgn)
+        filter_tile_raw<true, true>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
       else
-        filter_tile_raw<false, true>(p, r, tile, s_raw, s_n, s_sure, s_base);
+        filter_tile_raw<false, true>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
     } else {
-      if (sgn)
-        filter_tile_raw<true, false>(p, r, tile, s_raw, s_n, s_sure, s_base);
+      if (lo.sgn)
+        filter_tile_raw<true, false>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
       else
-        filter_tile_raw<false, false>(p, r, tile, s_raw, s_n, s_sure, s_base);
+        filter_tile_raw<false, false>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
     }
   }
 }
@@ -1178,28 +1206,38 @@ __global__ void __launch_bounds__(256) vc_topk_restore(const __grid_constant__ S
 // settled key) become x - (0 + x), and the tile is written to every output.
 // Each thread loads its entry of eight ranks' chunks before folding them, so
 // a tile costs one round trip for the chunk bounds and one per eight ranks
-// for the entries.  Those round trips are latency the tile's writes cannot
-// hide, so the kernel is held to 32 registers (32-bit list indices) for 8
-// CTAs per SM.
+// for the entries; the first tile's chunk bounds come in the same round trip
+// as the ranks' states (the route, the cut), loaded before the route is
+// known (the workspace holds them either way).  Those round trips are
+// latency the tile's writes cannot hide, so the kernel is held to 32
+// registers (32-bit list indices) for 8 CTAs per SM.
 __global__ void __launch_bounds__(256, 8) vc_topk_list_out(const __grid_constant__ SparseParams p) {
   pdl_enter();
-  if (!list_route(p)) return;
+  if (!p.list_out) return;
   __shared__ uint32_t s_T[VCOLL_MAX_RANKS], s_set[VCOLL_MAX_RANKS];
   __shared__ long long s_bound[VCOLL_MAX_RANKS];
+  __shared__ uint32_t s_cnt4[VCOLL_MAX_RANKS];
+  __shared__ int64_t s_c0[VCOLL_MAX_RANKS];
   const int W = p.W;
   const int tid = threadIdx.x;
+  auto chunk_bounds = [&](int r, int64_t tile) {
+    s_cnt4[r] = p.tilecnt[(int64_t)r * p.tiles_per_rank + tile];
+    s_c0[r] = (int64_t)r * p.cand_cap + p.chunk[(int64_t)r * p.tiles_per_rank + tile];
+  };
+  bool full = false;  // a rank on the full path: the lists do not hold the result
   for (int r = tid; r < W; r += blockDim.x) {
-    s_T[r] = p.state[r].T;
-    s_bound[r] = p.state[r].boundary;
+    const TopkState& st = p.state[r];
+    full |= st.full != 0;
+    s_T[r] = st.T;
+    s_bound[r] = st.boundary;
     s_set[r] = settled_key(p, r);
+    chunk_bounds(r, blockIdx.x);  // (grid <= tiles)
   }
-  __syncthreads();
+  if (__syncthreads_or(full)) return;  // the route, uniform over the grid
   constexpr int R = 8;  // ranks whose list entries are loaded together
   // the tile's sums, shifted by pad (0-3) so that the aligned body starts on
   // a 16-byte boundary of shared memory
   __shared__ __align__(16) float s_res[kSparseTileElems + 4];
-  __shared__ uint32_t s_cnt4[VCOLL_MAX_RANKS];
-  __shared__ int64_t s_c0[VCOLL_MAX_RANKS];
   for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
     const int64_t t0 = tile * p.tile_elems;
     const int64_t t1 = t0 + p.tile_elems < p.n ? t0 + p.tile_elems : p.n;
@@ -1207,10 +1245,8 @@ __global__ void __launch_bounds__(256, 8) vc_topk_list_out(const __grid_constant
     if (p.phase >= 0) aligned_body<4>(t0, t1, p.phase, av, bv);
     const int64_t base = t0 - ((4 - ((av - t0) & 3)) & 3);  // s_res[i - base] holds entry i
     for (int j = tid; j < kSparseTileElems + 4; j += blockDim.x) s_res[j] = 0.0f;
-    for (int r = tid; r < W; r += blockDim.x) {
-      s_cnt4[r] = p.tilecnt[(int64_t)r * p.tiles_per_rank + tile];
-      s_c0[r] = (int64_t)r * p.cand_cap + p.chunk[(int64_t)r * p.tiles_per_rank + tile];
-    }
+    if (tile != blockIdx.x)
+      for (int r = tid; r < W; r += blockDim.x) chunk_bounds(r, tile);
     __syncthreads();
     // (an entry above the settled key already holds its residual: only a
     // settled entry that is not kept after all gets x back)
