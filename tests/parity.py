@@ -105,3 +105,38 @@ def abs_sum(ins_np) -> np.ndarray:
     for a in ins_np:
         acc += np.abs(widen(a))
     return acc
+
+
+def topk_sparse_definition(xs, K: int, residuals: bool):
+    """SINGA's top-K sparsified allreduce (Apache SINGA, Communicator::
+    topKSparsAllReduce) from its definition, for arrays of any size: each rank
+    sends the K entries of x (its input plus its accumulation) with the largest
+    values -- values ordered by their order-preserving 32-bit keys, equal keys by
+    lower index first; every result starts at zero and receives rank 0's sent
+    values, then rank 1's, and so on, one fp32 add each; a rank's new
+    accumulation is x - x where it sent and x elsewhere.  The oracle reaches the
+    same by sorting every rank's (index, value) pairs; this form picks the K-th
+    key with a partition and so runs at full size.
+
+    xs: W fp32 arrays x.  Returns (result, [accumulations] or None)."""
+    n = xs[0].size
+    result = np.zeros(n, np.float32)
+    accs = [] if residuals else None
+    for x in xs:
+        b = x.view(np.uint32)
+        key = b ^ ((b >> np.uint32(31)) * np.uint32(0x7FFFFFFF) | np.uint32(0x80000000))
+        if K <= 0:
+            sent = np.zeros(n, bool)
+        elif K >= n:
+            sent = np.ones(n, bool)
+        else:
+            T = np.partition(key, n - K)[n - K]  # the K-th largest key
+            sent = key > T
+            need = K - int(np.count_nonzero(sent))
+            sent[np.flatnonzero(key == T)[:need]] = True
+        result[sent] = x[sent] + result[sent]
+        if residuals:
+            r = x.copy()
+            r[sent] = x[sent] - x[sent]
+            accs.append(r)
+    return result, accs

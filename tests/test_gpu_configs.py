@@ -1,5 +1,6 @@
-"""GPU parity at the full sizes of the five benchmark workloads, in the launch
-configurations the benchmark times.
+"""GPU parity at the full sizes of the five benchmark workloads and of the
+benchmark's top-1 % sparsified allreduce, in the launch configurations the
+benchmark times.
 
 Full-size outputs are checked two ways: at sampled indices against the
 oracle, which computes each sampled output one by one through its ring
@@ -7,7 +8,8 @@ simulation (bit-exact in ring order and for max, tolerance otherwise), and on
 every element through properties that hold at any size (all allreduce
 outputs identical; ring-order allreduce equals the concatenated ring-order
 reduce-scatter; the fastest order within the reordering bound of the ring
-order).
+order).  The sparsified allreduce is checked on every element against its
+definition (one partition per rank finds the K-th key).
 """
 import numpy as np
 import pytest
@@ -15,7 +17,8 @@ import torch
 
 import oracle
 from collective_reduction_virtual_gb300 import inputs as I
-from parity import assert_bit_exact, assert_close_fast, fp32_bound, to_np, widen
+from parity import (assert_bit_exact, assert_close_fast, fp32_bound, to_np,
+                    topk_sparse_definition, widen)
 
 pytestmark = pytest.mark.gpu
 
@@ -258,3 +261,34 @@ def test_largest_indices_beyond_32_bits(v):
     assert_bit_exact(to_np(ag[0][it]), oracle.allreduce_sampled(vals, idx, n, "sum", oracle.F32),
                      "RS + AG 2^31 + 3 ring")
 
+
+
+@pytest.mark.parametrize("with_acc", [True, False])
+def test_sparse_topk_full_size(v, with_acc):
+    # The benchmark's top-1 % sparsified allreduce (W = 8, 2^26 fp32 per rank,
+    # gradient-like inputs, the recommended workspace), every element checked
+    # bit for bit against SINGA's definition (tests/parity.py, tied to the
+    # oracle in test_topk_definition.py).  With accumulations two calls in a
+    # row, so the second selects from inputs plus the first call's residuals.
+    W, n, frac = 8, 1 << 26, 0.01
+    K = int(np.ceil(np.float32(frac) * np.float32(n)))
+    ins = [I.gradient(n, I.rank_seed(I.AR_W8_F32, u), "cuda") for u in range(W)]
+    outs = [torch.empty_like(t) for t in ins]
+    acc = [torch.zeros_like(t) for t in ins] if with_acc else None
+    nnz = torch.zeros(W, dtype=torch.int64, device="cuda")
+    ws = torch.empty(v.sparse_workspace_bytes(W, n, True), dtype=torch.uint8, device="cuda")
+    acc_np = [np.zeros(n, np.float32) for _ in range(W)] if with_acc else None
+    for call in range(2 if with_acc else 1):
+        xs = [to_np(ins[u]) + acc_np[u] for u in range(W)] if with_acc else [to_np(t) for t in ins]
+        v.sparse_allreduce(ins, outs, acc, frac, True, nnz, ws)
+        torch.cuda.synchronize()
+        want, want_acc = topk_sparse_definition(xs, K, with_acc)
+        del xs
+        assert nnz.tolist() == [K] * W
+        assert_bit_exact(to_np(outs[0]), want, f"top-K output, call {call}")
+        for u in range(1, W):
+            assert torch.equal(outs[u].view(torch.int32), outs[0].view(torch.int32))
+        if with_acc:
+            for u in range(W):
+                assert_bit_exact(to_np(acc[u]), want_acc[u], f"top-K residual of rank {u}, call {call}")
+            acc_np = want_acc
