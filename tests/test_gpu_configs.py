@@ -292,3 +292,32 @@ def test_sparse_topk_full_size(v, with_acc):
             for u in range(W):
                 assert_bit_exact(to_np(acc[u]), want_acc[u], f"top-K residual of rank {u}, call {call}")
             acc_np = want_acc
+
+
+def test_sparse_threshold_full_size(v):
+    # The benchmark's threshold sparsified allreduce (W = 8, 2^26 fp32 per
+    # rank, threshold 1e-3, accumulations over two calls in a row).  Each index
+    # is independent in this mode, so the oracle computes the sampled outputs
+    # and residuals exactly from the sampled inputs and accumulations; the
+    # per-rank counts are checked on the whole array (entries with |x| above
+    # the threshold).
+    W, n, thr = 8, 1 << 26, 1e-3
+    ins = [I.gradient(n, I.rank_seed(I.AR_W8_F32, u), "cuda") for u in range(W)]
+    outs = [torch.empty_like(t) for t in ins]
+    acc = [torch.zeros_like(t) for t in ins]
+    nnz = torch.zeros(W, dtype=torch.int64, device="cuda")
+    idx = sample_indices(n, W, 200_000, 12)
+    it = torch.from_numpy(idx).cuda()
+    vals = gather(ins, idx)
+    for call in range(2):
+        acc_before = gather(acc, idx)
+        counts = [int(torch.count_nonzero((ins[u] + acc[u]).abs() > np.float32(thr))) for u in range(W)]
+        v.sparse_allreduce(ins, outs, acc, thr, False, nnz)
+        torch.cuda.synchronize()
+        acc_want = [np.ascontiguousarray(acc_before[:, u]) for u in range(W)]
+        want, _ = oracle.sparse_allreduce([np.ascontiguousarray(vals[:, u]) for u in range(W)], thr,
+                                          False, acc_want)
+        assert nnz.tolist() == counts
+        for u in range(W):
+            assert_bit_exact(to_np(outs[u][it]), want[u], f"threshold output {u}, call {call}")
+            assert_bit_exact(to_np(acc[u][it]), acc_want[u], f"threshold residual {u}, call {call}")
