@@ -190,6 +190,14 @@ def test_fusion_w8_full(v):
         for t in range(0, len(counts), 17):
             for u in range(1, W):
                 assert torch.equal(outs[u][t], outs[0][t])
+        # the one-pass fusion (no buffer) gives the pipeline's bits in either order
+        one = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+        v.FusionPlan(tens, one, op="avg", ring_order=ring, threshold_bytes=thr)()
+        for u in range(W):
+            for t in range(len(counts)):
+                assert torch.equal(one[u][t].view(torch.int32), outs[u][t].view(torch.int32)), \
+                    f"one-pass fusion vs pipeline, ring={ring}, rank {u}, tensor {t}"
+        del one
 
 
 # ----------------------------------------------------------- size sweep
@@ -321,3 +329,83 @@ def test_sparse_threshold_full_size(v):
         for u in range(W):
             assert_bit_exact(to_np(outs[u][it]), want[u], f"threshold output {u}, call {call}")
             assert_bit_exact(to_np(acc[u][it]), acc_want[u], f"threshold residual {u}, call {call}")
+
+
+# ------------------------ the other launch forms the benchmark times at 2^26
+
+def bits_equal(a, b):
+    return torch.equal(a.view(torch.int32 if a.element_size() == 4 else torch.int16),
+                       b.view(torch.int32 if b.element_size() == 4 else torch.int16))
+
+
+def test_staged_and_tma_variants_full_size(v):
+    # At W = 8, 2^26 fp32 per rank the TMA-staged allreduce and reduce-scatter
+    # run persistent grids with their own tiles and the TMA allgather its own
+    # stages; each gives the direct kernel's bits (which the tests above pin to
+    # the oracle), in either order.
+    W, n = 8, 1 << 26
+    ins = I.rank_buffers("gradient", W, n, I.AR_W8_F32, "cuda")
+    assert v.device_errors(clear=True) == 0
+    for ring in (False, True):
+        d = v.allreduce(ins, op="sum", ring_order=ring, flags=v.FLAG_DIRECT)
+        st = v.allreduce(ins, op="sum", ring_order=ring, flags=v.FLAG_STAGED)
+        for u in range(W):
+            assert bits_equal(st[u], d[u]), f"AR staged, ring={ring}, rank {u}"
+        del st, d
+        rs = v.reduce_scatter(ins, op="sum", ring_order=ring, flags=v.FLAG_DIRECT)
+        rs_st = v.reduce_scatter(ins, op="sum", ring_order=ring, flags=v.FLAG_STAGED)
+        for j in range(W):
+            assert bits_equal(rs_st[j], rs[j]), f"RS staged, ring={ring}, segment {j}"
+        del rs_st
+        ag = v.allgather(rs, n, flags=v.FLAG_DIRECT)
+        ag_t = v.allgather(rs, n, flags=v.FLAG_STAGED)
+        cat = torch.cat(rs)
+        for u in range(W):
+            assert bits_equal(ag[u], cat) and bits_equal(ag_t[u], cat), f"AG, rank {u}"
+        del ag, ag_t, cat, rs
+    assert v.device_errors(clear=True) == 0
+
+
+def test_staged_bf16_avg_full_size(v):
+    W, n = 8, 1 << 28
+    ins = I.rank_buffers("outliers", W, n, I.AR_W8_BF16, "cuda")
+    assert v.device_errors(clear=True) == 0
+    d = v.allreduce(ins, op="avg", flags=v.FLAG_DIRECT)
+    st = v.allreduce(ins, op="avg", flags=v.FLAG_STAGED)
+    for u in range(W):
+        assert bits_equal(st[u], d[u]), f"bf16 avg staged, rank {u}"
+    assert v.device_errors(clear=True) == 0
+
+
+def test_wire_allreduce_full_size(v):
+    # SINGA's fp16-wire allreduce at W = 8, 2^26 fp32 per rank.  The oracle
+    # computes the sampled indices in one call of W * m elements: sample i
+    # sits in its own segment (the one holding its index under the full n),
+    # at slot segment * m + i, so its fold starts at the same ring position
+    # as in the full problem; the other slots hold zeros and never mix with it.
+    W, n = 8, 1 << 26
+    ins = I.rank_buffers("gradient", W, n, I.AR_W8_F32, "cuda")
+    idx = sample_indices(n, W, 20_000, 13)
+    m = idx.size
+    offs = np.array([oracle.segment(n, W, j)[0] for j in range(W)])
+    seg = np.searchsorted(offs, idx, side="right") - 1
+    for j in range(W):
+        assert oracle.segment(W * m, W, j) == (j * m, m)
+    vals = gather(ins, idx)
+    pos = seg * m + np.arange(m)
+    emb = [np.zeros(W * m, np.float32) for _ in range(W)]
+    for u in range(W):
+        emb[u][pos] = vals[:, u]
+    want = oracle.allreduce_wire(emb, "f16", "sum")[0][pos]
+    it = torch.from_numpy(idx).cuda()
+    ring = v.allreduce_wire(ins, wire="f16", op="sum", ring_order=True)
+    all_ranks_equal(ring)
+    assert_bit_exact(to_np(ring[0][it]), want, "wire f16 ring")
+    del ring
+    fast = v.allreduce_wire(ins, wire="f16", op="sum")  # the benchmark's call
+    all_ranks_equal(fast)
+    # the fast order's bound against the ring order (as in test_allreduce_wire)
+    s_abs = np.abs(vals.astype(np.float64)).sum(axis=1)
+    bound = 2 * (W + 1) * (2.0 ** -11 * s_abs + 2.0 ** -25)
+    diff = np.abs(to_np(fast[0][it]).astype(np.float64) - want.astype(np.float64))
+    assert bool((diff <= bound).all()), float((diff - bound).max())
