@@ -355,17 +355,17 @@ def build_workload(args, dev, rank):
                 what += ", minimum workspace (no candidate lists)"
         launches = 1
         if topk:
-            # 13 kernels over the whole array; 23 on the candidate path, which
+            # 13 kernels over the whole array; 25 on the candidate path, which
             # the library takes when the lists hold 3K entries (K < n/4) or a
-            # tenth of the array (a two-sided band), 27 when the lists also
-            # give the output (a second-digit sample pass and its selection,
-            # an output pass, and, with accumulations, a pass that restores x
-            # in them should a rank's list fail)
+            # tenth of the array (a two-sided band; a second-digit sample pass
+            # and its selection included), 27 when the lists also give the
+            # output (an output pass, and, with accumulations, a pass that
+            # restores x in them should a rank's list fail)
             K = math.ceil(frac * n)
             cap = ((n // 8 + 4096 if n // 8 + 4096 < n else n) + 3) & ~3
             wide = 4 * K < n and cap >= 3 * K  # lower bound only: output from the lists
             cand = 0 < K < n and (wide or 10 * cap >= n) and args.sparse_workspace != "min"
-            launches = ((27 if acc is not None else 26) if wide else 23) if cand else 13
+            launches = ((27 if acc is not None else 26) if wide else 25) if cand else 13
         return dict(name=f"{what}, W={W}, f32, n={n} per rank", W=W, n=n, step=step,
                     bytes=bytes_, launches=launches, ins=ins,
                     outs=outs, es=4, reduction=red, dtype="f32")

@@ -365,10 +365,11 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
     // sample pass and lower bound
     if ((rc = run(topk_sample_kernel(), sample, 256)) || (rc = run(topk_select_low_kernel(), sgrid, 1024)))
       return rc;
-    // on the list route: the second digit over the same sample narrows the
-    // settled bound (whose residuals the candidate pass writes, with
-    // accumulations) and the lower bound to a 22-bit prefix
-    if (prm.list_out &&
+    // on the candidate path: the second digit over the same sample narrows
+    // the settled bound (list route with accumulations: the candidate pass
+    // writes those residuals), the lower bound and the band's upper bound to
+    // 22-bit prefixes
+    if (prm.use_cand &&
         ((rc = run(topk_sample2_kernel(), sample, 256)) ||
          (rc = run(topk_select_refine_kernel(), sgrid, 1024))))
       return rc;
@@ -377,7 +378,7 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
       // (a CTA loops over two tiles with accumulations, four without: its
       // setup is paid once for them; measured at W = 8, 2^26 per rank)
       const dim3 fgrid((unsigned)ceil_div((int64_t)tiles, prm.has_acc ? 2 : 4), (unsigned)W);
-      if ((rc = run(topk_filter_kernel(prm.has_acc), fgrid, 256))) return rc;
+      if ((rc = run(topk_filter_kernel(prm.has_acc, prm.band), fgrid, 256))) return rc;
       // the candidate pass stored x = in + acc in acc: later passes read acc
       prm.x_in_acc = prm.has_acc;
       if ((rc = run(topk_cand_hist_kernel(0), few, 256)) ||

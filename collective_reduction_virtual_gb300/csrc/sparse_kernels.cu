@@ -198,7 +198,8 @@ __device__ __forceinline__ bool counted_bin(uint32_t d, uint32_t low) {
 // -1: neither (nothing settled, no lower bound)
 __device__ __forceinline__ int refined_bin(const TopkState& st) {
   if (st.setkey != 0xFFFFFFFFu) return (int)(st.setkey >> 21);
-  return st.low_rem > 0 ? (int)(st.lowkey >> 21) : -1;
+  if (st.low_rem > 0) return (int)(st.lowkey >> 21);
+  return st.hi_rem > 0 ? (int)(st.topkey >> 21) : -1;
 }
 
 // shared-memory histogram add, lanes that share a bin combined first
@@ -227,7 +228,9 @@ __device__ __forceinline__ void hist_add(uint32_t* h, bool valid, uint32_t d) {
 // MODE 4: the first digit over all bins, only for ranks whose bound failed;
 // MODE 5: the second digit over the same sample, keys in the first-digit bin
 //         of the settled bound (which refines it, and the lower bound when
-//         that lies in the same bin), else in the lower bound's bin.
+//         that lies in the same bin), else in the lower bound's bin (which
+//         refines it, and a band's upper bound when that lies in the same
+//         bin), else in the upper bound's bin.
 // With candidate lists, MODES 1 and 2 run only for ranks on the full path.
 template <int MODE>
 __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ SparseParams p) {
@@ -309,20 +312,23 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
 //   suffix holds comfortably more keys than K calls for (scaled to the
 //   sample), 0 (count everything) when none does; with a band also
 //   state.high = the highest bin with comfortably fewer than that strictly
-//   above it (entries above it are kept without being listed), else 2047;
+//   above it (entries above it are kept without being listed), else 2047,
+//   and state.topkey = the last key of that bin (0xFFFFFFFF without a band);
 //   state.lowkey = the first key of state.low; on the list route (with
 //   accumulations) state.setkey = the last key of the bin that state.high
 //   would be without a band (entries above it are listed, and kept for
-//   certain unless the sample misled), else 0xFFFFFFFF; low_rem and set_rem
-//   keep what each bound still needs inside its bin;
+//   certain unless the sample misled), else 0xFFFFFFFF; low_rem, set_rem and
+//   hi_rem keep what each bound still needs inside its bin;
 // MODE 4: after the redo pass, for ranks that needed it;
 // MODE 5, 6, 7: after index pass 3, 4, 5 over the candidates equal to T, for
 //   ranks on the candidate path whose equal keys straddle the cut; the last
 //   one sets the boundary index;
 // MODE 8: after the second-digit sample pass: setkey moves down to the last
-//   key of the second-digit bin holding its set_rem-th sampled key, and
-//   lowkey, when it starts the refined first-digit bin, up to the first key
-//   of the second-digit bin holding its low_rem-th one.
+//   key of the second-digit bin holding its set_rem-th sampled key, lowkey,
+//   when it starts the refined first-digit bin, up to the first key of the
+//   second-digit bin holding its low_rem-th one, and a band's topkey, when it
+//   ends the refined bin, down to the last key of the second-digit bin
+//   holding its hi_rem-th one.
 template <int MODE>
 __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ SparseParams p) {
   pdl_enter();
@@ -399,6 +405,9 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
   const bool set_here = MODE == 8 && st->setkey != 0xFFFFFFFFu;
   const long long set_rem = MODE == 8 ? st->set_rem : 0, low_rem = MODE == 8 ? st->low_rem : 0;
   const bool low_here = MODE == 8 && low_rem > 0 && st->lowkey == sbin << 21;
+  const long long hi_rem = MODE == 8 ? st->hi_rem : 0;
+  const bool hi_here = MODE == 8 && hi_rem > 0 && st->topkey != 0xFFFFFFFFu &&
+                       (st->topkey >> 21) == sbin;
   __syncthreads();  // every thread has read the state before it changes
   // the bin (b0 or b1) holding the target-th key, and the keys above it
   auto pick = [&](long long target, unsigned long long& more) -> uint32_t {
@@ -422,9 +431,17 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
       st->lowkey = bin << 21;
       st->low_rem = rem - (long long)more;
     }
-    if (t == 0 && (rhi <= 0 || (long long)total < rhi)) st->high = kTopkBins - 1;
-    if (rhi > 0 && (long long)total >= rhi && (long long)above < rhi && rhi <= (long long)incl)
-      st->high = pick(rhi, more);
+    if (t == 0 && (rhi <= 0 || (long long)total < rhi)) {
+      st->high = kTopkBins - 1;
+      st->topkey = 0xFFFFFFFFu;
+      st->hi_rem = 0;
+    }
+    if (rhi > 0 && (long long)total >= rhi && (long long)above < rhi && rhi <= (long long)incl) {
+      const uint32_t bin = pick(rhi, more);
+      st->high = bin;
+      st->topkey = (uint32_t)((((uint64_t)bin + 1) << 21) - 1);
+      st->hi_rem = rhi - (long long)more;
+    }
     if (t == 0 && (rset <= 0 || (long long)total < rset)) {
       st->setkey = 0xFFFFFFFFu;
       st->set_rem = 0;
@@ -443,6 +460,10 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
     }
     if (low_here && (long long)above < low_rem && low_rem <= (long long)incl)
       st->lowkey = (sbin << 21) | (pick(low_rem, more) << 10);
+    if (hi_here && (long long)above < hi_rem && hi_rem <= (long long)incl) {
+      const uint64_t p22 = ((uint64_t)sbin << 11) | pick(hi_rem, more);
+      st->topkey = (uint32_t)(((p22 + 1) << 10) - 1);
+    }
   } else if (MODE == 0 && (rem <= 0 || (long long)total < rem)) {
     if (t == 0) {  // a bound missed the K-th key (or the list overflowed): count every bin again
       st->redo = 1;
@@ -645,7 +666,7 @@ __global__ void __launch_bounds__(256) vc_topk_filter(const __grid_constant__ Sp
   const int tid = threadIdx.x, lane = tid & 31;
   // candidates: keys in [lowkey, topkey]; keys above topkey are kept for sure
   const uint32_t lowkey = p.state[r].lowkey;
-  const uint32_t topkey = (uint32_t)((((uint64_t)p.state[r].high + 1) << 21) - 1);
+  const uint32_t topkey = p.state[r].topkey;
   const uint32_t setkey = ACC ? settled_key(p, r) : 0xFFFFFFFFu;
   uint32_t* ckey = p.cand_key + (int64_t)r * p.cand_cap;
   uint32_t* cidx = p.cand_idx + (int64_t)r * p.cand_cap;
@@ -824,19 +845,20 @@ __device__ __forceinline__ bool raw_at_least(uint32_t u, uint32_t t) {
 // four 16-byte vectors (vector v = tid + 256 u of the tile's aligned body)
 // and at most one of the tile's unaligned head or tail entries; bit 4 u + q
 // of the thread's mask is entry q of its vector u.  LOW_SGN: the lower
-// bound's compare form (uniform per rank); BAND: an upper bound is set
-// (entries above it are counted, not listed).  The keys of the listed
-// entries are formed only for those entries.
-template <bool LOW_SGN, bool BAND>
+// bound's compare form (uniform per rank); HI: no upper bound (0), or a
+// band's upper bound in the unsigned (1) or signed (2) compare form --
+// entries at or above it are counted, not listed: one mask of them per
+// thread, counted once.  The keys of the listed entries are formed only for
+// those entries.
+template <bool LOW_SGN, int HI>
 __device__ __forceinline__ void filter_tile_raw(const SparseParams& p, int r, int64_t tile,
                                                 const RawBound lo, const RawBound hi,
                                                 uint32_t* s_raw, uint32_t* s_n, uint32_t* s_sure,
                                                 int par, unsigned long long& s_base) {
   constexpr int E = 4 * kTileVecs;  // entries per thread (plus one extra)
   const int tid = threadIdx.x, lane = tid & 31;
-  auto above = [&](uint32_t u) -> bool {
-    return BAND && (hi.sgn ? raw_at_least<true>(u, hi.t) : raw_at_least<false>(u, hi.t));
-  };
+  constexpr bool BAND = HI != 0;
+  auto above = [&](uint32_t u) -> bool { return BAND && raw_at_least<HI == 2>(u, hi.t); };
   auto cand = [&](uint32_t u) -> bool { return raw_at_least<LOW_SGN>(u, lo.t) && !above(u); };
   const char* src = (const char*)p.in[r];
   const bool vec = p.phase >= 0;
@@ -846,7 +868,8 @@ __device__ __forceinline__ void filter_tile_raw(const SparseParams& p, int r, in
   if (vec) aligned_body<4>(t0, t1, p.phase, av, bv);
   const int nv = (int)((bv - av) / 4);
   uint32_t mask = 0;
-  int sure = 0;  // entries above the band
+  uint32_t hmask = 0;  // entries above the band (as mask)
+  int sure = 0;        // entries above the band
   // the one extra entry: threads 0-31 take the tile's head, 32-63 its tail
   int64_t extra = -1;
   uint32_t xraw = 0;
@@ -865,10 +888,18 @@ __device__ __forceinline__ void filter_tile_raw(const SparseParams& p, int r, in
     for (int u = 0; u < kTileVecs; ++u) {
       const uint4 x = a[u];
       if (tid + u * kSparseThreads < nv) {
-        mask |= ((uint32_t)cand(x.x) | (uint32_t)cand(x.y) << 1 | (uint32_t)cand(x.z) << 2 |
-                 (uint32_t)cand(x.w) << 3)
-                << (u * 4);
-        if (BAND) sure += above(x.x) + above(x.y) + above(x.z) + above(x.w);
+        const uint32_t ge = (uint32_t)raw_at_least<LOW_SGN>(x.x, lo.t) |
+                            (uint32_t)raw_at_least<LOW_SGN>(x.y, lo.t) << 1 |
+                            (uint32_t)raw_at_least<LOW_SGN>(x.z, lo.t) << 2 |
+                            (uint32_t)raw_at_least<LOW_SGN>(x.w, lo.t) << 3;
+        if (BAND) {
+          const uint32_t up = (uint32_t)above(x.x) | (uint32_t)above(x.y) << 1 |
+                              (uint32_t)above(x.z) << 2 | (uint32_t)above(x.w) << 3;
+          mask |= (ge & ~up) << (u * 4);
+          hmask |= up << (u * 4);
+        } else {
+          mask |= ge << (u * 4);
+        }
       }
       // vector u of every thread side by side: a warp's stores are contiguous
       reinterpret_cast<uint4*>(s_raw)[u * kSparseThreads + tid] = x;
@@ -903,7 +934,7 @@ __device__ __forceinline__ void filter_tile_raw(const SparseParams& p, int r, in
   }
   const uint32_t wtotal = __shfl_sync(0xFFFFFFFFu, incl, 31);
   unsigned wsure = 0;
-  if (BAND) wsure = __reduce_add_sync(0xFFFFFFFFu, (unsigned)sure);
+  if (BAND) wsure = __reduce_add_sync(0xFFFFFFFFu, (unsigned)(sure + __popc(hmask)));
   // the tile's counters s_n[par], s_sure[par] are zero (cleared by thread 0
   // before the previous tile's last barrier, or before the first tile)
   uint32_t wbase = 0;
@@ -976,6 +1007,10 @@ __device__ __forceinline__ void filter_tile_raw(const SparseParams& p, int r, in
 // quarter of the tiles and each CTA loops over four, so its setup (state,
 // bounds, pointers) is paid once for four tiles (per call at W = 8, 2^26 per
 // rank: one tile per CTA 0.813 ms, two 0.803, four 0.800).
+// BANDED: launched on the band route, where a rank may have an upper bound;
+// the list route's form holds only the bodies without one (a smaller kernel
+// measured 3-4 us faster per call at W = 8, 2^26).
+template <bool BANDED>
 __global__ void __launch_bounds__(256, 8) vc_topk_filter_raw(const __grid_constant__ SparseParams p) {
   pdl_enter();
   __shared__ __align__(16) uint32_t s_raw[kSparseThreads * 4 * kTileVecs];
@@ -987,23 +1022,33 @@ __global__ void __launch_bounds__(256, 8) vc_topk_filter_raw(const __grid_consta
     s_sure[threadIdx.x] = 0;
   }
   __syncthreads();
-  const uint32_t high = p.state[r].high;
-  const bool band = high < kTopkBins - 1;  // uniform per CTA
+  const uint32_t topkey = p.state[r].topkey;
+  const bool band = topkey != 0xFFFFFFFFu;  // uniform per CTA
   const RawBound lo = raw_bound(p.state[r].lowkey);
-  // above the band: key >= the last key of bin high, plus one (so only with a band)
-  const RawBound hi = raw_bound(band ? (uint32_t)(((uint64_t)high + 1) << 21) : 0xFFFFFFFFu);
+  // above the band: key >= topkey + 1 (so only with a band)
+  const RawBound hi = raw_bound(band ? topkey + 1 : 0xFFFFFFFFu);
   int par = 0;
+  const int hmode = band ? (hi.sgn ? 2 : 1) : 0;  // the upper bound's compare form
   for (int64_t tile = blockIdx.x; tile < p.tiles_per_rank; tile += gridDim.x, par ^= 1) {
-    if (band) {
+    if (!BANDED) {  // no upper bound on the list route
       if (lo.sgn)
-        filter_tile_raw<true, true>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
+        filter_tile_raw<true, 0>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
       else
-        filter_tile_raw<false, true>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
+        filter_tile_raw<false, 0>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
+    } else if (lo.sgn) {
+      if (hmode == 2)
+        filter_tile_raw<true, 2>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
+      else if (hmode == 1)  // (not reached: a bound above a signed-form one is signed-form)
+        filter_tile_raw<true, 1>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
+      else
+        filter_tile_raw<true, 0>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
     } else {
-      if (lo.sgn)
-        filter_tile_raw<true, false>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
+      if (hmode == 2)
+        filter_tile_raw<false, 2>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
+      else if (hmode == 1)
+        filter_tile_raw<false, 1>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
       else
-        filter_tile_raw<false, false>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
+        filter_tile_raw<false, 0>(p, r, tile, lo, hi, s_raw, s_n, s_sure, par, s_base);
     }
   }
 }
@@ -1420,8 +1465,9 @@ const void* topk_select_kernel(int pass) {
   return pass == 0 ? (const void*)&vc_topk_select<0>
                    : pass == 1 ? (const void*)&vc_topk_select<1> : (const void*)&vc_topk_select<2>;
 }
-const void* topk_filter_kernel(int has_acc) {
-  return has_acc ? (const void*)&vc_topk_filter<true> : (const void*)&vc_topk_filter_raw;
+const void* topk_filter_kernel(int has_acc, int band) {
+  if (has_acc) return (const void*)&vc_topk_filter<true>;
+  return band ? (const void*)&vc_topk_filter_raw<true> : (const void*)&vc_topk_filter_raw<false>;
 }
 const void* topk_list_out_kernel() { return (const void*)&vc_topk_list_out; }
 const void* topk_restore_kernel() { return (const void*)&vc_topk_restore; }

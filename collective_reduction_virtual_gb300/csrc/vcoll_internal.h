@@ -146,6 +146,9 @@ struct TopkState {
   uint32_t low;       // first-digit bins below this one are not counted
   uint32_t high;      // candidate path: first-digit bins above this one are
                       // kept without selection (counted, not listed)
+  uint32_t topkey;    // candidate path: the last key listed; keys above it
+                      // are kept without selection (the end of bin high, or
+                      // of a 22-bit prefix inside it; 0xFFFFFFFF: no band)
   int redo;           // the first-digit pass must be repeated over all bins
   int full;           // this rank's select passes read the whole array (its
                       // candidate list overflowed or missed the K-th key)
@@ -154,8 +157,9 @@ struct TopkState {
                       // (unless the sample misled), so the candidate pass
                       // writes their residuals itself (0xFFFFFFFF: none)
   int64_t low_rem;    // sample keys still wanted at or above lowkey inside its
-  int64_t set_rem;    // bin, and allowed above setkey inside its bin (the
-                      // second-digit refinement of both bounds)
+  int64_t set_rem;    // bin, allowed above setkey inside its bin, and allowed
+  int64_t hi_rem;     // above topkey inside its bin (the second-digit
+                      // refinement of the bounds)
   uint32_t tie_n;     // candidate path: candidates equal to T collected so far
   uint32_t tie_done;  // candidate path: CTAs of the tie pass that finished
   int tie_resolved;   // candidate path: the tie pass set the boundary (the
@@ -259,7 +263,7 @@ const void* topk_select_refine_kernel();   // refines the settled and lower boun
 const void* topk_redo_hist_kernel();
 const void* topk_redo_select_kernel();
 const void* topk_select_kernel(int pass);
-const void* topk_filter_kernel(int has_acc);
+const void* topk_filter_kernel(int has_acc, int band);
 const void* topk_list_out_kernel();
 const void* topk_restore_kernel();
 const void* topk_cand_hist_kernel(int pass);  // 0-2 key digits, 3-5 index digits
