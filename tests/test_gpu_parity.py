@@ -880,6 +880,25 @@ def test_sparse_topk_sample_bound_redo(v):
     _check_sparse(v, ins, None, 0.4, True)  # the band (K >= n/4) misses as well
 
 
+@pytest.mark.parametrize("scale", [0.85, 0.97, 0.997, 1.003, 1.03, 1.15])
+@pytest.mark.parametrize("frac", [0.05, 0.1, 0.3])
+def test_sparse_topk_band_refined_bounds_contradicted(v, scale, frac):
+    # the two-sided band (lists too small for 3K entries), refined to 22-bit
+    # bounds by the second sample pass: the sampled tiles (every 16th of 4096
+    # entries, four tiles here, so the band's margin is about 14 % of K's
+    # share) are scaled so that the band sits below or above the K-th key of
+    # the whole array (0.85, 1.15: too many entries above the band, or the
+    # K-th key below it, and the rank falls back) or near its edges (the
+    # bounds still hold)
+    W, n = 2, 64 * 4096
+    ins = _sparse_inputs(W, n, 23)
+    for t in ins:
+        tiles = t.view(-1, 4096)
+        tiles[::16] *= scale
+    _check_sparse(v, ins, None, frac, True)
+    _check_sparse(v, ins, [t * 0.1 for t in _sparse_inputs(W, n, 24)], frac, True)
+
+
 # The top-K select runs over candidate lists when the workspace has room for
 # them (the entries above a sampled bound), else over the whole array; a rank
 # whose list overflows or misses the K-th key falls back on the device.  Every
