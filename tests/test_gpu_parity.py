@@ -880,6 +880,29 @@ def test_sparse_topk_sample_bound_redo(v):
     _check_sparse(v, ins, None, 0.4, True)  # the band (K >= n/4) misses as well
 
 
+@pytest.mark.parametrize("frac", [0.001, 0.01, 0.1])
+def test_sparse_topk_layered_buffer(v, frac):
+    # a fused gradient buffer: tensors of log-uniform sizes, each at its own
+    # scale (10^U(-4, -2)), so the sampled tiles see a mixture of layers
+    from collective_reduction_virtual_gb300 import inputs as I
+    W, n = 4, (1 << 22) + 5
+    counts = I.fusion_counts(T=200, lo=256, hi=262144)
+    rng = np.random.default_rng(9)
+    scales = 10.0 ** rng.uniform(-4, -2, counts.size)
+    ins = _sparse_inputs(W, n, 91)
+    for t in ins:
+        off = 0
+        for c, sc in zip(counts, scales):
+            if off >= n:
+                break
+            t[off:off + int(c)] *= float(sc)
+            off += int(c)
+    acc = [torch.zeros(n, device="cuda") for _ in range(W)]
+    _check_sparse(v, ins, acc, frac, True)
+    _check_sparse(v, ins, acc, frac, True)  # the error feedback is nonzero now
+    _check_sparse(v, ins, None, frac, True)
+
+
 @pytest.mark.parametrize("scale", [0.85, 0.97, 0.997, 1.003, 1.03, 1.15])
 @pytest.mark.parametrize("frac", [0.05, 0.1, 0.3])
 def test_sparse_topk_band_refined_bounds_contradicted(v, scale, frac):
