@@ -311,14 +311,14 @@ __global__ void __launch_bounds__(256) vc_topk_hist(const __grid_constant__ Spar
 // MODE 3: after the sample pass: state.low = the highest bin whose sampled
 //   suffix holds comfortably more keys than K calls for (scaled to the
 //   sample), 0 (count everything) when none does; with a band also
-//   state.high = the highest bin with comfortably fewer than that strictly
-//   above it (entries above it are kept without being listed), else 2047,
-//   and state.topkey = the last key of that bin (0xFFFFFFFF without a band);
-//   state.lowkey = the first key of state.low; on the list route (with
-//   accumulations) state.setkey = the last key of the bin that state.high
-//   would be without a band (entries above it are listed, and kept for
-//   certain unless the sample misled), else 0xFFFFFFFF; low_rem, set_rem and
-//   hi_rem keep what each bound still needs inside its bin;
+//   state.topkey = the last key of the highest bin with comfortably fewer
+//   than that strictly above it (entries above it are kept without being
+//   listed), else 0xFFFFFFFF; state.lowkey = the first key of state.low; on
+//   the list route (with accumulations) state.setkey = the last key of the
+//   bin that bound would end without a band (entries above it are listed,
+//   and kept for certain unless the sample misled), else 0xFFFFFFFF;
+//   low_rem, set_rem and hi_rem keep what each bound still needs inside its
+//   bin;
 // MODE 4: after the redo pass, for ranks that needed it;
 // MODE 5, 6, 7: after index pass 3, 4, 5 over the candidates equal to T, for
 //   ranks on the candidate path whose equal keys straddle the cut; the last
@@ -432,13 +432,11 @@ __global__ void __launch_bounds__(1024) vc_topk_select(const __grid_constant__ S
       st->low_rem = rem - (long long)more;
     }
     if (t == 0 && (rhi <= 0 || (long long)total < rhi)) {
-      st->high = kTopkBins - 1;
       st->topkey = 0xFFFFFFFFu;
       st->hi_rem = 0;
     }
     if (rhi > 0 && (long long)total >= rhi && (long long)above < rhi && rhi <= (long long)incl) {
       const uint32_t bin = pick(rhi, more);
-      st->high = bin;
       st->topkey = (uint32_t)((((uint64_t)bin + 1) << 21) - 1);
       st->hi_rem = rhi - (long long)more;
     }
@@ -635,9 +633,9 @@ __device__ __forceinline__ uint32_t settled_key(const SparseParams& p, int r) {
 }
 
 // One pass over the data (grid.y = rank, one tile per CTA iteration): every
-// entry whose first digit lies in the sample's band [low, high] is appended
-// to the rank's candidate list as (key, index), and the entries above the
-// band are counted (they are kept whatever the K-th key).  With an
+// entry whose key lies in the sample's band [lowkey, topkey] is appended to
+// the rank's candidate list as (key, index), and the entries above the band
+// are counted (they are kept whatever the K-th key).  With an
 // accumulation, x = in + acc is stored back into acc, so that every later
 // pass reads one array instead of two -- except that a candidate above the
 // settled key gets its residual x - (0 + x) instead, kept when its whole

@@ -144,11 +144,10 @@ struct TopkState {
   int64_t equal;      // entries equal to T
   int64_t boundary;   // equal entries with index <= boundary are kept
   uint32_t low;       // first-digit bins below this one are not counted
-  uint32_t high;      // candidate path: first-digit bins above this one are
-                      // kept without selection (counted, not listed)
   uint32_t topkey;    // candidate path: the last key listed; keys above it
-                      // are kept without selection (the end of bin high, or
-                      // of a 22-bit prefix inside it; 0xFFFFFFFF: no band)
+                      // are kept without selection, counted, not listed (the
+                      // end of a first-digit bin, or of a 22-bit prefix
+                      // inside it; 0xFFFFFFFF: no band)
   int redo;           // the first-digit pass must be repeated over all bins
   int full;           // this rank's select passes read the whole array (its
                       // candidate list overflowed or missed the K-th key)
