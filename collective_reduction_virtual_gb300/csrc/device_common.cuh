@@ -67,7 +67,10 @@ struct Elem<float> {
 };
 
 // bf16 is the upper half of an fp32 value: widening shifts it up (exact);
-// narrowing rounds to nearest even with the CUDA conversion intrinsic.
+// narrowing rounds to nearest even with the CUDA conversion intrinsic, and a
+// NaN keeps its sign and top payload bits and is made quiet (the intrinsic
+// gives 0x7FFF for every NaN; the canonical fp32 NaN of max and min must
+// become 0x7FC0).
 template <>
 struct Elem<__nv_bfloat16> {
   static constexpr int kBytes = 2;
@@ -77,9 +80,15 @@ struct Elem<__nv_bfloat16> {
     lo = __uint_as_float(w << 16);
     hi = __uint_as_float(w & 0xFFFF0000u);
   }
+  static __device__ __forceinline__ uint32_t quiet_nan(float f) {
+    return (__float_as_uint(f) >> 16) | 0x0040u;
+  }
   static __device__ __forceinline__ uint32_t narrow2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
+    uint32_t w = *reinterpret_cast<uint32_t*>(&h);
+    if (lo != lo) w = (w & 0xFFFF0000u) | quiet_nan(lo);
+    if (hi != hi) w = (w & 0x0000FFFFu) | (quiet_nan(hi) << 16);
+    return w;
   }
   static __device__ __forceinline__ void widen(const uint4& v, float (&f)[kVec]) {
     widen2(v.x, f[0], f[1]);
@@ -96,7 +105,7 @@ struct Elem<__nv_bfloat16> {
   }
   static __device__ __forceinline__ Bits narrow1(float f) {
     __nv_bfloat16 h = __float2bfloat16_rn(f);
-    return *reinterpret_cast<uint16_t*>(&h);
+    return f != f ? (Bits)quiet_nan(f) : *reinterpret_cast<uint16_t*>(&h);
   }
 };
 

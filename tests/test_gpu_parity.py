@@ -482,6 +482,49 @@ def test_min_prod_small(v, W, n, dtype):
             assert_bit_exact(to_np(multi[u][0]), want[u], f"multi {op}")
 
 
+# special values for max and min: signed zeros, quiet and signalling NaNs of
+# either sign, infinities, subnormals, the largest finite values
+_SPECIAL_F32 = np.array([0x00000000, 0x80000000, 0x3F800000, 0xBF800000, 0x7F800000, 0xFF800000,
+                         0x7FC00000, 0xFFC00000, 0x7F800001, 0x7FA00001, 0x00000001, 0x80000001,
+                         0x007FFFFF, 0x7F7FFFFF, 0xFF7FFFFF, 0x40000000, 0xC0000000], dtype=np.uint32)
+_SPECIAL_BF16 = np.array([0x0000, 0x8000, 0x3F80, 0xBF80, 0x7F80, 0xFF80, 0x7FC0, 0xFFC0, 0x7F81,
+                          0x7FA1, 0x0001, 0x8001, 0x007F, 0x7F7F, 0xFF7F, 0x4000, 0xC000],
+                         dtype=np.uint16)
+
+
+def _special_inputs(W, n, dtype, seed, shift):
+    rng = np.random.default_rng(seed)
+    outs = []
+    for _ in range(W):
+        pool = _SPECIAL_F32 if dtype == "f32" else _SPECIAL_BF16
+        bits = pool[rng.integers(0, pool.size, n + shift)]
+        t = torch.from_numpy(bits.view(np.int32 if dtype == "f32" else np.int16).copy()).cuda()
+        t = t.view(torch.float32 if dtype == "f32" else torch.bfloat16)
+        outs.append(t[shift:])  # shift 1: a 16-byte phase other than the outputs'
+    return outs
+
+
+@pytest.mark.parametrize("W", [2, 3, 4, 8])
+@pytest.mark.parametrize("n", [4099, 65541])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shift", [0, 1])
+def test_max_min_special_values(v, W, n, dtype, shift):
+    # every element drawn from the special values above: max and min must give
+    # the oracle's bits exactly -- the canonical quiet NaN, +0 from max(+0, -0)
+    # and -0 from min -- in every order, every kernel form
+    ins = _special_inputs(W, n, dtype, 300 * W + n + shift, shift)
+    ins_np = [to_np(t) for t in ins]
+    for op in ("max", "min"):
+        want = oracle.allreduce(ins_np, op, ODT[dtype])
+        rs_want = oracle.reduce_scatter(ins_np, op, ODT[dtype])
+        for ring in (True, False):
+            got = v.allreduce(ins, op=op, ring_order=ring)
+            rs = v.reduce_scatter(ins, op=op, ring_order=ring)
+            for u in range(W):
+                assert to_np(got[u]).tobytes() == want[u].tobytes(), f"AR {op} ring={ring} rank {u}"
+                assert to_np(rs[u]).tobytes() == rs_want[u].tobytes(), f"RS {op} ring={ring} {u}"
+
+
 def test_prod_ring_order_hand_derived_on_gpu(v):
     x = [torch.full((4,), val, device="cuda") for val in (2.0 ** 100, 2.0 ** 100, 2.0 ** -100,
                                                           2.0 ** -100)]
