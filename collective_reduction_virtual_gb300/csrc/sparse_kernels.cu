@@ -55,11 +55,15 @@ namespace vcoll {
 
 namespace {
 
-// larger value -> larger key; -0 just below +0; NaNs beyond the infinities
-__device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f);
+// larger value -> larger key; -0 just below +0; NaNs beyond the infinities.
+// The bits go through an opaque move: without it the sign test was compiled,
+// in the dense apply pass, into something that put a positive NaN below the
+// cut (the pass then dropped kept NaNs that the selection had counted).
+__device__ __forceinline__ uint32_t key_of_bits(uint32_t u) {
+  asm("mov.b32 %0, %0;" : "+r"(u));
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+__device__ __forceinline__ uint32_t order_key(float f) { return key_of_bits(__float_as_uint(f)); }
 
 // inverse of order_key
 __device__ __forceinline__ float key_value(uint32_t key) {
@@ -1360,12 +1364,15 @@ __global__ void __launch_bounds__(256) vc_sparse_apply(const __grid_constant__ S
     s_cnt[r] = 0;
   }
   __syncthreads();
-  auto keep = [&](int r, float x, int64_t i) -> bool {
+  // xb: the bits of x (the top-K key is taken from the bits themselves, so a
+  // NaN keeps its place in the key order)
+  auto keep = [&](int r, uint32_t xb, int64_t i) -> bool {
     if (TOPK) {
       if (p.K == 0) return false;
-      const uint32_t k = order_key(x);
+      const uint32_t k = key_of_bits(xb);
       return k > s_T[r] || (k == s_T[r] && i <= s_bound[r]);
     }
+    const float x = __uint_as_float(xb);
     return fabsf(x) > p.threshold && x != 0.0f;
   };
   // the value the residual subtracts: top-K scatters the sent values into
@@ -1396,7 +1403,7 @@ __global__ void __launch_bounds__(256) vc_sparse_apply(const __grid_constant__ S
           float s[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const bool k = keep(r, x[q], e + q);
+            const bool k = keep(r, __float_as_uint(x[q]), e + q);
             s[q] = k ? sent(x[q]) : 0.0f;
             if (k) res[q] = __fadd_rn(x[q], res[q]);
             c += k;
@@ -1428,7 +1435,7 @@ __global__ void __launch_bounds__(256) vc_sparse_apply(const __grid_constant__ S
         int c = 0;
         if (in_range) {
           const float x = load_x(p, r, i);
-          const bool k = keep(r, x, i);
+          const bool k = keep(r, __float_as_uint(x), i);
           const float s = k ? sent(x) : 0.0f;
           if (k) res = __fadd_rn(x, res);
           c = k;

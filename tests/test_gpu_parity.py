@@ -525,6 +525,26 @@ def test_max_min_special_values(v, W, n, dtype, shift):
                 assert to_np(rs[u]).tobytes() == rs_want[u].tobytes(), f"RS {op} ring={ring} {u}"
 
 
+@pytest.mark.parametrize("W", [2, 4])
+@pytest.mark.parametrize("frac", [0.01, 0.3])
+@pytest.mark.parametrize("topk", [True, False])
+def test_sparse_special_values(v, W, frac, topk):
+    # SINGA's sparsified allreduce over special values: without accumulations
+    # x is the input itself, so NaNs of either sign take their keys' places in
+    # the top-K order; with accumulations the inputs hold no NaN and the
+    # accumulations are finite, so no sum makes one (the sign and payload of
+    # a NaN sum are not fixed by IEEE 754, and the GPU and the host differ)
+    n = 100_003
+    ins = _special_inputs(W, n, "f32", 900 + W, 0)
+    thr = frac if topk else 1.0
+    _check_sparse(v, ins, None, thr, topk)
+    no_nan = [torch.where(torch.isnan(t), torch.full_like(t, 3.0), t) for t in ins]
+    acc = [t * 0.5 for t in _sparse_inputs(W, n, 901)]
+    acc[0][::7] = -0.0
+    acc[-1][::11] = 1e-40  # subnormal
+    _check_sparse(v, no_nan, acc, thr, topk)
+
+
 def test_prod_ring_order_hand_derived_on_gpu(v):
     x = [torch.full((4,), val, device="cuda") for val in (2.0 ** 100, 2.0 ** 100, 2.0 ** -100,
                                                           2.0 ** -100)]
