@@ -525,6 +525,45 @@ def test_max_min_special_values(v, W, n, dtype, shift):
                 assert to_np(rs[u]).tobytes() == rs_want[u].tobytes(), f"RS {op} ring={ring} {u}"
 
 
+@pytest.mark.parametrize("W", [2, 3, 8])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shift", [0, 1])
+def test_sum_avg_prod_special_values(v, W, dtype, shift):
+    # the special values under sum, avg and prod in ring order: signed zeros
+    # (-0 + -0 = -0, -0 + +0 = +0), infinities and their NaNs, subnormals kept
+    # (no flush to zero), overflow to infinity; NaN payloads of these ops are
+    # not fixed (NaN matches NaN).  Also the one-pass multi-tensor form.
+    n = 4099
+    ins = _special_inputs(W, n, dtype, 500 * W + shift, shift)
+    ins_np = [to_np(t) for t in ins]
+    for op in ("sum", "avg", "prod"):
+        want = oracle.allreduce(ins_np, op, ODT[dtype])
+        rs_want = oracle.reduce_scatter(ins_np, op, ODT[dtype])
+        got = v.allreduce(ins, op=op, ring_order=True)
+        rs = v.reduce_scatter(ins, op=op, ring_order=True)
+        multi = v.allreduce_multi([[t] for t in ins], op=op, ring_order=True)
+        for u in range(W):
+            assert_bit_exact(to_np(got[u]), want[u], f"AR {op} rank {u}")
+            assert_bit_exact(to_np(rs[u]), rs_want[u], f"RS {op} segment {u}")
+            assert_bit_exact(to_np(multi[u][0]), want[u], f"multi {op} rank {u}")
+
+
+@pytest.mark.parametrize("wire", ["f16", "bf16"])
+@pytest.mark.parametrize("W", [2, 3, 8])
+def test_wire_special_values(v, wire, W):
+    # SINGA's reduced-precision allreduce over special values, ring order:
+    # every hop rounds to the wire type (fp16 overflows above 65504 and has
+    # subnormals of its own; bf16 keeps fp32's range)
+    n = 4099
+    ins = _special_inputs(W, n, "f32", 600 * W, 0)
+    ins_np = [to_np(t) for t in ins]
+    for op in ("sum", "avg"):
+        want = oracle.allreduce_wire(ins_np, wire, op)
+        got = v.allreduce_wire(ins, wire=wire, op=op, ring_order=True)
+        for u in range(W):
+            assert_bit_exact(to_np(got[u]), want[u], f"wire {wire} {op} rank {u}")
+
+
 @pytest.mark.parametrize("W", [2, 4])
 @pytest.mark.parametrize("frac", [0.01, 0.3])
 @pytest.mark.parametrize("topk", [True, False])
