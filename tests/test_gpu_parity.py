@@ -523,6 +523,12 @@ def test_max_min_special_values(v, W, n, dtype, shift):
             for u in range(W):
                 assert to_np(got[u]).tobytes() == want[u].tobytes(), f"AR {op} ring={ring} rank {u}"
                 assert to_np(rs[u]).tobytes() == rs_want[u].tobytes(), f"RS {op} ring={ring} {u}"
+            if W in (2, 4, 8):  # the TMA-staged forms
+                st = v.allreduce(ins, op=op, ring_order=ring, flags=v.FLAG_STAGED)
+                rs_st = v.reduce_scatter(ins, op=op, ring_order=ring, flags=v.FLAG_STAGED)
+                for u in range(W):
+                    assert to_np(st[u]).tobytes() == want[u].tobytes(), f"AR staged {op} {u}"
+                    assert to_np(rs_st[u]).tobytes() == rs_want[u].tobytes(), f"RS staged {op} {u}"
 
 
 @pytest.mark.parametrize("W", [2, 3, 8])
