@@ -33,7 +33,10 @@
  *    on the host before anything is enqueued.  vcoll_last_error() returns a
  *    thread-local message for the last failure on the calling thread.
  *  - Types: VCOLL_F32 and VCOLL_BF16.  Arithmetic is fp32 for both; bf16
- *    inputs are widened exactly and outputs rounded to nearest even once.
+ *    inputs are widened exactly and outputs rounded to nearest even once (a
+ *    NaN keeps its sign and top payload bits and is made quiet: the
+ *    canonical fp32 NaN becomes 0x7FC0).  Subnormals are kept (no flush to
+ *    zero).
  *  - Ops: VCOLL_SUM, VCOLL_MAX, VCOLL_AVG (sum times fl32(1/W), applied once
  *    to the finished sum), VCOLL_MIN, VCOLL_PROD (one fp32 multiply per hop).
  *    max: a NaN operand gives the canonical quiet NaN; +0 wins over -0;
@@ -270,7 +273,10 @@ int vcoll_fusion_allreduce_buffered(const void* const* in, void* const* out,
  * NULL).  threshold mode: the entries with |x| > threshold survive (and
  * x != 0); top-K mode: the K = ceil(threshold * n) entries (threshold in
  * [0, 1], computed in fp32 as SINGA does) with the largest values survive,
- * ties broken toward the lower index.  With accum, accum[u] becomes x minus
+ * ties broken toward the lower index; values are ordered by their bits (-0
+ * just below +0, NaNs beyond the infinities by sign -- with accum, where a
+ * NaN comes from the sum in + accum its sign is the GPU's, which IEEE 754
+ * leaves open).  With accum, accum[u] becomes x minus
  * the sent values: x elsewhere; where an entry survived, x - x in threshold
  * mode and x - (0 + x) in top-K mode (the sent values are scattered into
  * zeros first): zero for a finite x (-0 for a kept -0 in top-K mode), NaN for
