@@ -531,6 +531,20 @@ def test_max_min_special_values(v, W, n, dtype, shift):
                     assert to_np(rs_st[u]).tobytes() == rs_want[u].tobytes(), f"RS staged {op} {u}"
 
 
+@pytest.mark.parametrize("W", [17, 64])
+@pytest.mark.parametrize("frac", [0.01, 0.3])
+def test_sparse_many_ranks(v, W, frac):
+    # up to the largest rank count: per-rank states, candidate lists and
+    # output folds over several groups of eight ranks (list route at 1 %,
+    # band at 30 %), with and without accumulations; threshold mode too
+    n = 50_003
+    ins = _sparse_inputs(W, n, 70 + W)
+    acc = [t * 0.3 for t in _sparse_inputs(W, n, 71 + W)]
+    _check_sparse(v, ins, acc, frac, True)
+    _check_sparse(v, ins, None, frac, True)
+    _check_sparse(v, ins, [torch.zeros(n, device="cuda") for _ in range(W)], 1.5, False)
+
+
 @pytest.mark.parametrize("W", [2, 3, 8])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("shift", [0, 1])
