@@ -504,7 +504,7 @@ def _special_inputs(W, n, dtype, seed, shift):
     return outs
 
 
-@pytest.mark.parametrize("W", [2, 3, 4, 8])
+@pytest.mark.parametrize("W", [2, 3, 4, 8, 12, 16])
 @pytest.mark.parametrize("n", [4099, 65541])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("shift", [0, 1])
@@ -523,7 +523,7 @@ def test_max_min_special_values(v, W, n, dtype, shift):
             for u in range(W):
                 assert to_np(got[u]).tobytes() == want[u].tobytes(), f"AR {op} ring={ring} rank {u}"
                 assert to_np(rs[u]).tobytes() == rs_want[u].tobytes(), f"RS {op} ring={ring} {u}"
-            if W in (2, 4, 8):  # the TMA-staged forms
+            if W in (2, 4, 8, 16):  # the TMA-staged forms
                 st = v.allreduce(ins, op=op, ring_order=ring, flags=v.FLAG_STAGED)
                 rs_st = v.reduce_scatter(ins, op=op, ring_order=ring, flags=v.FLAG_STAGED)
                 for u in range(W):
