@@ -54,7 +54,7 @@ def _check(got, want, s, W, op, ring, what):
         assert_close_fast(got, want, s, W, op, what)
 
 
-@pytest.mark.parametrize("case", range(48))
+@pytest.mark.parametrize("case", range(160))
 def test_random_collectives(v, case):
     rng = np.random.default_rng(7000 + case)
     W = int(rng.choice(WS))
@@ -92,7 +92,7 @@ def test_random_collectives(v, case):
         assert to_np(outs[0]).tobytes() == to_np(cat).tobytes(), "AR = RS + AG " + what
 
 
-@pytest.mark.parametrize("case", range(12))
+@pytest.mark.parametrize("case", range(24))
 def test_random_allgatherv(v, case):
     rng = np.random.default_rng(7500 + case)
     W = int(rng.choice(WS))
@@ -106,7 +106,7 @@ def test_random_allgatherv(v, case):
         assert to_np(outs[u]).tobytes() == want[u].tobytes(), f"AGV W={W} counts={counts[:6]}"
 
 
-@pytest.mark.parametrize("case", range(12))
+@pytest.mark.parametrize("case", range(24))
 def test_random_wire(v, case):
     rng = np.random.default_rng(7700 + case)
     W = int(rng.choice(WS[:-1]))
@@ -122,7 +122,7 @@ def test_random_wire(v, case):
         assert_bit_exact(to_np(ring[u]), want[u], f"wire W={W} n={n} {wire} {op}")
 
 
-@pytest.mark.parametrize("case", range(16))
+@pytest.mark.parametrize("case", range(40))
 def test_random_sparse(v, case):
     rng = np.random.default_rng(7900 + case)
     W = int(rng.choice(WS))
