@@ -2,7 +2,8 @@
 oracle: rank counts from 1 to 64, sizes around the tile boundaries, 16-byte
 phases shared or different per rank, fp32 and bf16, every op, ring and
 fastest order, in place, the TMA-staged forms, allgather(v), the
-reduced-precision wire allreduce and the sparsified allreduce.  Ring order,
+reduced-precision wire allreduce, the sparsified allreduce, tensor fusion and
+user ring permutations.  Ring order,
 max, min and bit copies must match bit for bit; the fastest order within
 the reordering bound (tests/parity.py)."""
 import numpy as np
@@ -152,3 +153,69 @@ def test_random_sparse(v, case):
         if acc is not None:
             assert_bit_exact(to_np(acc[u]), acc_np[u], "sparse accum " + what)
     assert nnz.cpu().tolist() == list(want_nnz), "sparse nnz " + what
+
+
+@pytest.mark.parametrize("case", range(24))
+def test_random_fusion(v, case):
+    # Horovod tensor fusion: random tensor lists (empty and one-element
+    # tensors among them, each tensor at its own 16-byte phase), a threshold
+    # that makes several batches, through the fusion buffers and in one pass
+    rng = np.random.default_rng(8100 + case)
+    W = int(rng.choice([1, 2, 3, 4, 8, 16]))
+    T = int(rng.integers(1, 60))
+    dtype = str(rng.choice(["f32", "bf16"]))
+    op = str(rng.choice(["sum", "avg", "max", "min"]))
+    ring = bool(rng.integers(2))
+    counts = [int(rng.choice([0, 1, 2, 3, 5, 17, 255, 1023, 4097, 20000])) for _ in range(T)]
+    es = 4 if dtype == "f32" else 2
+    thr = int(rng.choice([64, 4096, 40_000, 1 << 26])) * es
+    g = torch.Generator(device="cuda")
+    g.manual_seed(int(rng.integers(1 << 30)))
+    tens = []
+    for u in range(W):
+        row = []
+        for c in counts:
+            sh = int(rng.integers(4))
+            base = torch.randn(c + 4, generator=g, device="cuda") * (10.0 ** torch.randint(
+                -2, 3, (c + 4,), generator=g, device="cuda").float())
+            row.append(base.to(DT[dtype])[sh:sh + c])
+        tens.append(row)
+    begin = oracle.fuse_plan(counts, ODT[dtype], thr)
+    biggest = max(sum(counts[begin[b]:begin[b + 1]]) for b in range(len(begin) - 1))
+    fused = [torch.empty(max(1, biggest), dtype=DT[dtype], device="cuda") for _ in range(W)]
+    outs = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+    v.fusion_allreduce(tens, outs, fused, op=op, ring_order=ring, threshold_bytes=thr)
+    one = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+    v.FusionPlan(tens, one, op=op, ring_order=ring, threshold_bytes=thr)()
+    what = f"W={W} T={T} {dtype} {op} ring={ring} thr={thr}"
+    for u in range(W):
+        for t in range(T):
+            assert to_np(one[u][t]).tobytes() == to_np(outs[u][t]).tobytes(), f"one pass vs pipeline {what} {t}"
+    if ring or op in ("max", "min"):
+        want = oracle.fusion_allreduce([[to_np(x) for x in tens[u]] for u in range(W)], counts, op,
+                                       ODT[dtype], thr)
+        for u in range(W):
+            for t in range(T):
+                assert_bit_exact(to_np(outs[u][t]), want[u][t], f"fusion {what} tensor {t}")
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_random_user_ring(v, case):
+    # the ring order of a permuted ring (NCCL userFromRing)
+    rng = np.random.default_rng(8300 + case)
+    W = int(rng.choice([2, 3, 4, 5, 8, 12, 16, 64]))
+    n = int(rng.choice(NS[1:]))
+    dtype = str(rng.choice(["f32", "bf16"]))
+    op = str(rng.choice(["sum", "avg", "prod"]))
+    ring = [int(x) for x in rng.permutation(W)]
+    shifts = [int(x) for x in rng.integers(0, 4, W)] if rng.integers(2) else [0] * W
+    ins = _inputs(rng, W, n, dtype, shifts, op)
+    ins_np = [to_np(t) for t in ins]
+    want = oracle.allreduce(ins_np, op, ODT[dtype], ring)
+    rs_want = oracle.reduce_scatter(ins_np, op, ODT[dtype], ring)
+    ar = v.allreduce(ins, op=op, user_from_ring=ring)
+    rs = v.reduce_scatter(ins, op=op, user_from_ring=ring)
+    what = f"W={W} n={n} {dtype} {op} ring={ring[:6]}"
+    for u in range(W):
+        assert_bit_exact(to_np(ar[u]), want[u], "AR " + what)
+        assert_bit_exact(to_np(rs[u]), rs_want[u], "RS " + what)
