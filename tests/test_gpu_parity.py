@@ -1237,3 +1237,65 @@ def test_full_tiles_runtime_w_and_uneven(v, W, n):
     ag = v.allgather(segs, n)
     for u in (0, W - 1):
         assert_bit_exact(to_np(ag[u]), ag_want[u], f"AG full tiles W={W} n={n}")
+
+
+def test_every_entry_point_in_a_cuda_graph(v):
+    # each call captured in a CUDA graph on a side stream (no host sync, no
+    # allocation inside), replayed after the inputs change in place, against
+    # the same calls made directly
+    W, n = 4, 70_001
+    ins = make_inputs(W, n, "f32", 9100)
+    segs = [torch.empty(oracle.segment(n, W, j)[1], device="cuda") for j in range(W)]
+    ar = [torch.empty(n, device="cuda") for _ in range(W)]
+    ar_st = [torch.empty(n, device="cuda") for _ in range(W)]
+    ag = [torch.empty(n, device="cuda") for _ in range(W)]
+    wire = [torch.empty(n, device="cuda") for _ in range(W)]
+    rs_ring = [torch.empty_like(s) for s in segs]
+    counts = [5000, 1, 0, 12345, 777]
+    pieces = [t[:c] for t, c in zip(ins, [100, 2000, 0, 70_001])]
+    agv = [torch.empty(sum(p.numel() for p in pieces), device="cuda") for _ in range(W)]
+    tens = [[torch.randn(c, device="cuda") for c in counts] for _ in range(W)]
+    t_one = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+    t_buf = [[torch.empty_like(t) for t in tens[u]] for u in range(W)]
+    fused = [torch.empty(sum(counts), device="cuda") for _ in range(W)]
+    one_plan = v.FusionPlan(tens, t_one, op="avg", threshold_bytes=4 * 6000)
+    buf_plan = v.FusionBufferPlan(tens, t_buf, fused, op="avg", threshold_bytes=4 * 6000)
+    ring = [2, 0, 3, 1]
+
+    def calls(s):
+        v.reduce_scatter(ins, segs, op="sum", ring_order=True, stream=s)
+        v.allgather(segs, n, ag, stream=s)
+        v.allreduce(ins, ar, op="max", stream=s)
+        v.allreduce(ins, ar_st, op="avg", flags=v.FLAG_STAGED, stream=s)
+        v.allreduce_wire(ins, wire, wire="bf16", op="sum", ring_order=True, stream=s)
+        v.reduce_scatter(ins, rs_ring, op="sum", user_from_ring=ring, stream=s)
+        v.allgatherv(pieces, agv, stream=s)
+        one_plan(s)
+        buf_plan(s)
+
+    def results():
+        return [t.clone() for t in segs + ag + ar + ar_st + wire + rs_ring + agv] + \
+            [t.clone() for u in range(W) for t in t_one[u] + t_buf[u]]
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        calls(s)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls(s)
+    for step in range(2):
+        for t in ins:
+            t.mul_(-1.5).add_(0.25)
+        for row in tens:
+            for t in row:
+                t.mul_(0.5).add_(1.0)
+        g.replay()
+        torch.cuda.synchronize()
+        got = results()
+        calls(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        want = results()
+        for a, b in zip(got, want):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32)), f"graph replay {step}"
