@@ -1239,8 +1239,8 @@ def test_full_tiles_runtime_w_and_uneven(v, W, n):
         assert_bit_exact(to_np(ag[u]), ag_want[u], f"AG full tiles W={W} n={n}")
 
 
-def test_every_entry_point_in_a_cuda_graph(v):
-    # each call captured in a CUDA graph on a side stream (no host sync, no
+def test_collectives_and_fusion_in_a_cuda_graph(v):
+    # these calls captured in a CUDA graph on a side stream (no host sync, no
     # allocation inside), replayed after the inputs change in place, against
     # the same calls made directly
     W, n = 4, 70_001
