@@ -1,6 +1,7 @@
-"""The benchmark's JSON line, checked on the CPU: the reference arm (the oracle
-timed on host cores) prints one line with the keys the benchmark contract
-names, and the host-side helpers that combine ranks behave as documented."""
+"""The benchmark's JSON line: the reference arm (the oracle timed on host
+cores, checked on the CPU) and the library's own arm (on the GPU) print one
+line with the keys the benchmark contract names, and the host-side helpers
+that combine ranks behave as documented."""
 import json
 import os
 import subprocess
@@ -63,3 +64,32 @@ def test_reference_arm_under_torchrun_prints_once_from_rank_0():
     assert len(lines) == 1, r.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2
+
+
+@pytest.mark.gpu
+def test_gpu_arm_line_has_the_contract_keys():
+    # the library's own arm on its default workload (W = 8, 2^26 per rank),
+    # few steps and a short oracle sample, with every key the benchmark
+    # contract names: roofline, CPU baseline, end-to-end figure with its
+    # copied bytes, clocks sampled during the timed region, launch count
+    d = _run("--steps", "3", "--warmup", "3", "--no-extras", "--cpu-seconds", "1")
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches"):
+        assert key in d, key
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
+    assert d["scaling"] == "weak" and d["vs_baseline"] is None
+    assert "workload" in d["config"] and "model" not in d["config"]
+    rf = d["roofline"]
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in rf, key
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s"
+    assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"], rel=1e-3)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] > 0 and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == e2e["d2h_bytes_per_step"] == 8 * (1 << 26) * 4
+    assert d["clocks"]["sm_mhz"] > 0 and isinstance(d["clocks"]["reasons"], list)
+    assert d["gpu_launches"] == 3  # one allreduce kernel per timed step
