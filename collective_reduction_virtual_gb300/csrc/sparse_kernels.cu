@@ -34,7 +34,9 @@
 // takes the passes over the whole array instead; the choice is made on the
 // device.  The candidate pass also stores x = in + acc back into acc, so the
 // later passes read one array (without accumulations a separate form of the
-// pass, vc_topk_filter_raw, tests the raw input bits).  With only a lower bound (small K) the lists
+// pass, vc_topk_filter_raw, tests the raw input bits; the list route launches
+// a form of it without the band's bodies).  With only a lower bound (small K)
+// the lists
 // hold every kept entry, grouped by tile, and the output is built from them
 // (vc_topk_list_out) instead of by the dense apply pass -- unless a rank fell
 // back, which the kernels see on the device.  On that route a second pass
@@ -43,7 +45,10 @@
 // the residual of every candidate above it at once, so the output pass
 // revisits the accumulation only for the kept entries at or below it (and
 // when a rank falls back, a restore pass puts x back from the lists before
-// the passes over the whole array read it).
+// the passes over the whole array read it).  With a band the same second
+// pass narrows both band bounds to 22 bits when they lie in one first-digit
+// bin, so the lists hold about the band's sampled width rather than whole
+// quarter-octave bins.
 //
 // The histograms (W x 2048 counters), the per-rank selection state, the
 // per-tile tie counts and list offsets and the candidate lists live in a
