@@ -17,8 +17,7 @@ import torch
 
 import oracle
 from collective_reduction_virtual_gb300 import inputs as I
-from parity import (assert_bit_exact, assert_close_fast, fp32_bound, to_np,
-                    topk_sparse_definition, widen)
+from parity import assert_bit_exact, assert_close_fast, to_np, topk_sparse_definition, widen
 
 pytestmark = pytest.mark.gpu
 
