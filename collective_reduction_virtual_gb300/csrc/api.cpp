@@ -438,6 +438,21 @@ int sparse_launch(SparseParams& prm, int topk, void* workspace, size_t workspace
   return VCOLL_OK;
 }
 
+// The TMA bulk copies of the staged forms run only on device memory: when a
+// buffer is elsewhere (pinned host memory, managed memory) a staged request
+// runs the direct kernels, which give the same bits.
+bool all_device_memory(const void* const* p, int W) {
+  for (int u = 0; u < W; ++u) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p[u]) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return false;
+    }
+    if (a.type != cudaMemoryTypeDevice) return false;
+  }
+  return true;
+}
+
 // wire >= 0: the reduced-precision allreduce (fp32 buffers, arithmetic rounded
 // to the 16-bit wire type every hop); -1: the plain collectives.
 int reduce_common(int kind, const void* const* in, void* const* out, int W, int64_t n, int dtype,
@@ -460,6 +475,9 @@ int reduce_common(int kind, const void* const* in, void* const* out, int W, int6
   if ((rc = check_ptrs(in, W, "in", es, in_len))) return rc;
   if ((rc = check_ptrs((const void* const*)out, W, "out", es, out_len))) return rc;
   if (n == 0) return VCOLL_OK;
+  if ((flags & VCOLL_FLAG_STAGED) &&
+      !(all_device_memory(in, W) && all_device_memory((const void* const*)out, W)))
+    flags &= ~VCOLL_FLAG_STAGED;
 
   std::vector<Buf> bufs;
   for (int u = 0; u < W; ++u) {
@@ -724,7 +742,8 @@ static int gather_common(const void* const* in, void* const* out, int W, const i
   prm.num_tiles = tps * W;
   // TMA variant only when asked for: with one CTA per tile the direct kernel
   // is ahead at every W measured (2-16)
-  const bool tma = (flags & VCOLL_FLAG_STAGED) != 0;
+  const bool tma = (flags & VCOLL_FLAG_STAGED) != 0 && all_device_memory(in, W) &&
+                   all_device_memory((const void* const*)out, W);
   if (tma && vec && !small) {
     // TMA variant: bulk loads into shared memory, W bulk stores per tile
     prm.tile_elems = kGatherTmaTileBytes / es;

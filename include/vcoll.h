@@ -103,7 +103,9 @@ typedef enum {
 /* Force the variant that stages the W input tiles through shared memory with
  * bulk asynchronous copies (TMA), or the variant that loads straight into
  * registers.  Without either flag the library picks by message size.  Both
- * give identical bits. */
+ * give identical bits.  The staged variant runs on device memory only: when
+ * any buffer is pinned host or managed memory (cudaPointerGetAttributes), a
+ * staged request runs the direct kernels. */
 #define VCOLL_FLAG_STAGED 0x2u
 #define VCOLL_FLAG_DIRECT 0x4u
 

@@ -766,6 +766,29 @@ def test_pinned_host_buffers(v, dtype):
         assert to_np(h_out[u]).tobytes() == to_np(ring[u]).tobytes()
 
 
+def test_staged_request_on_host_buffers_runs_the_direct_kernels(v):
+    # the TMA bulk copies of the staged forms run only on device memory; with
+    # pinned host buffers a staged request gives the direct kernels' bits
+    W, n = 8, 300_007
+    ins = make_inputs(W, n, "f32", 62)
+    h_in = [t.cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(n, pin_memory=True) for _ in range(W)]
+    d = v.allreduce(ins, op="sum", flags=v.FLAG_DIRECT)
+    v.allreduce(h_in, h_out, op="sum", flags=v.FLAG_STAGED)
+    torch.cuda.synchronize()
+    for u in range(W):
+        assert to_np(h_out[u]).tobytes() == to_np(d[u]).tobytes()
+    segs = [torch.empty(v.segment(n, W, j)[1], pin_memory=True) for j in range(W)]
+    v.reduce_scatter(h_in, segs, op="sum", ring_order=True, flags=v.FLAG_STAGED)
+    ag = [torch.empty(n, pin_memory=True) for _ in range(W)]
+    v.allgather(segs, n, ag, flags=v.FLAG_STAGED)
+    torch.cuda.synchronize()
+    ring = v.allreduce(ins, op="sum", ring_order=True)
+    for u in range(W):
+        assert to_np(ag[u]).tobytes() == to_np(ring[u]).tobytes()
+    assert v.device_errors(clear=True) == 0
+
+
 @pytest.mark.parametrize("W", [2, 3, 8, 16])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("n", [100_003, (1 << 22) + 6, 3 << 22])
